@@ -1,0 +1,293 @@
+"""fp64 CPU oracle for the Kimi Delta Attention (KDA) forward path.
+
+TEST INFRASTRUCTURE ONLY.  The product library never imports, links or calls
+anything here; only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may.  It shares no code with the CUDA path: the arithmetic
+lives in ``kda_oracle.c`` (plain C, double precision) and in the small numpy
+brute-force helpers below, each citing the passage it follows:
+
+  [K3-7] "Kimi K3 模型结构（7）：结构决定系统"
+  [K3-2] "Kimi K3 模型结构（2）：序列维度（下），chunkwise 并行与下界衰减"
+  [SA]   "Kimi K3: the Manos, the Mythos ..." (SemiAnalysis), "FlashKDA 算法"
+
+Every array argument is converted to contiguous float64 before the call, so a
+caller that passes the exact bf16 / fp32 values given to the GPU gets those
+values widened to double.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+G_MIN = -5.0  # [K3-2] "K3 的改动：下界衰减": gate_lower_bound = -5.0
+
+
+def build(force: bool = False) -> str:
+    """Compile ``kda_oracle.c`` into ``liboracle.so`` with gcc (plain -O2, IEEE math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC,
+                               "-lpthread", "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _configure(lib):
+    P = ctypes.c_void_p
+    I, L, D = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    lib.oracle_gate.argtypes = [D, D, D]
+    lib.oracle_gate.restype = D
+    lib.oracle_gate_array.argtypes = [D, P, P, L, I, I, P]
+    lib.oracle_kda_recurrent.argtypes = [P, P, P, P, P, P, P, I, I, I, I, D, P, P, P, I]
+    lib.oracle_kda_recurrent.restype = I
+    lib.oracle_kda_chunk.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, D, P, P, P, I]
+    lib.oracle_kda_chunk.restype = I
+    lib.oracle_kda_pair.argtypes = [P, P, P, P, P, L, L, I, I, I, I, D, P, P, P, P, P]
+    lib.oracle_compose.argtypes = [P, P, P, P, I, I, P, P]
+    lib.oracle_kda_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P,
+                                           I, I, I, I, I, D, P, I]
+    lib.oracle_kda_decode_step.restype = I
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _configure(ctypes.CDLL(_LIB))
+    return _lib
+
+
+class use_library:
+    """Context manager that points this module at another build of the oracle
+    source (used by the mutation tests, which compile deliberately broken copies)."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        _load()
+        self._saved = _lib
+        _lib = _configure(ctypes.CDLL(self.path))
+        return _lib
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self._saved
+        return False
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # a torch tensor: widen its exact values
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _cu(cu_seqlens, T):
+    if cu_seqlens is None:
+        return np.array([0, T], dtype=np.int64)
+    if hasattr(cu_seqlens, "detach"):
+        cu_seqlens = cu_seqlens.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+
+
+def gate(z, A, g_min=G_MIN):
+    """g = g_min * sigmoid(exp(A_h) * z) elementwise over z [T, H, dk]."""
+    z = _f64(z)
+    A = _f64(A)
+    T, H, dk = z.shape
+    out = np.empty_like(z)
+    _load().oracle_gate_array(g_min, _ptr(A), _ptr(z), T, H, dk, _ptr(out))
+    return out
+
+
+def recurrent(q, k, v, z, A, beta, cu_seqlens=None, init_state=None, g_min=G_MIN,
+              n_threads=0, return_threads=False):
+    """Token-by-token recurrence ([K3-7] eq. (1) in the delta form of [SA]).
+
+    Shapes: q, k, z [T, H, dk]; v [T, H, dv]; beta [T, H]; A [H];
+    cu_seqlens [n+1] or None (one sequence); init_state [n, H, dk, dv] or None.
+    Returns (o [T, H, dv], final_state [n, H, dk, dv]).
+    """
+    q, k, v, z, A, beta = map(_f64, (q, k, v, z, A, beta))
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    cu = _cu(cu_seqlens, T)
+    n = len(cu) - 1
+    init = _f64(init_state)
+    o = np.zeros((T, H, dv))
+    fin = np.zeros((n, H, dk, dv))
+    used = _load().oracle_kda_recurrent(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta),
+                                        _ptr(cu), n, H, dk, dv, g_min, _ptr(init),
+                                        _ptr(o), _ptr(fin), int(n_threads))
+    if return_threads:
+        return o, fin, used
+    return o, fin
+
+
+def chunk_form(q, k, v, z, A, beta, C, cu_seqlens=None, init_state=None, g_min=G_MIN,
+               n_threads=0):
+    """fp64 chunk form of [SA] "算法" / [K3-2] eqs. (4), (8) with chunk length C <= 64."""
+    q, k, v, z, A, beta = map(_f64, (q, k, v, z, A, beta))
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    cu = _cu(cu_seqlens, T)
+    n = len(cu) - 1
+    init = _f64(init_state)
+    o = np.zeros((T, H, dv))
+    fin = np.zeros((n, H, dk, dv))
+    rc = _load().oracle_kda_chunk(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta),
+                                  _ptr(cu), n, H, dk, dv, int(C), g_min, _ptr(init),
+                                  _ptr(o), _ptr(fin), int(n_threads))
+    if rc < 0:
+        raise ValueError("chunk length must be in 1..64")
+    return o, fin
+
+
+def doc_flags(cu_seqlens, T):
+    """(doc_start_flag [T] uint8, doc_of [T] int64) from cu_seqlens."""
+    cu = _cu(cu_seqlens, T)
+    flag = np.zeros(T, dtype=np.uint8)
+    doc_of = np.zeros(T, dtype=np.int64)
+    for d in range(len(cu) - 1):
+        if cu[d] < cu[d + 1]:
+            flag[cu[d]] = 1
+        doc_of[cu[d]:cu[d + 1]] = d
+    return flag, doc_of
+
+
+def pair(k, v, z, A, beta, t_begin, t_end, h, cu_seqlens=None, init_state=None,
+         g_min=G_MIN, reset_at_begin=None):
+    """Affine pair (M, S~) of head h over tokens [t_begin, t_end) ([K3-7] eq. (17)).
+
+    Document starts inside the range (or at t_begin) reset the pair, following
+    [K3-7] "文档边界".  With cu_seqlens None the range is treated as the middle
+    of one document (no reset) unless reset_at_begin is True.
+    """
+    k, v, z, A, beta = map(_f64, (k, v, z, A, beta))
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    if cu_seqlens is None:
+        flag = np.zeros(T, dtype=np.uint8)
+        if reset_at_begin:
+            flag[t_begin] = 1
+        doc_of = np.zeros(T, dtype=np.int64)
+    else:
+        flag, doc_of = doc_flags(cu_seqlens, T)
+    init = _f64(init_state)
+    M = np.zeros((dk, dk))
+    S = np.zeros((dk, dv))
+    _load().oracle_kda_pair(_ptr(k), _ptr(v), _ptr(z), _ptr(A), _ptr(beta), int(t_begin),
+                            int(t_end), int(h), H, dk, dv, g_min, _ptr(flag), _ptr(doc_of),
+                            _ptr(init), _ptr(M), _ptr(S))
+    return M, S
+
+
+def compose(M2, S2, M1, S1):
+    """(M2, S2) o (M1, S1) = (M2 M1, M2 S1 + S2)  ([K3-7] derivation, step 2)."""
+    M2, S2, M1, S1 = map(_f64, (M2, S2, M1, S1))
+    dk, dv = S1.shape
+    Mo = np.zeros((dk, dk))
+    So = np.zeros((dk, dv))
+    _load().oracle_compose(_ptr(M2), _ptr(S2), _ptr(M1), _ptr(S1), dk, dv, _ptr(Mo), _ptr(So))
+    return Mo, So
+
+
+def decode_step(state, q, k, v, z, beta, A, cache_q, cache_k, cache_v, cache_z, cache_beta,
+                num_accepted=None, g_min=G_MIN, n_threads=0):
+    """One decode step with MTP replay ([K3-7] decode paragraph).
+
+    state [N, H, dk, dv]; new inputs q, k, z [N, W, H, dk], v [N, W, H, dv], beta [N, W, H];
+    cache_* [N, W-1, H, *]; num_accepted [N] in 0..W-1 or None.
+    Returns (o [N, W, H, dv], new_state, (cache_q, cache_k, cache_v, cache_z, cache_beta)),
+    all fresh arrays (inputs are not modified).
+    """
+    st = _f64(state).copy()
+    q, k, v, z, beta, A = map(_f64, (q, k, v, z, beta, A))
+    cq, ck, cv, cz, cb = (_f64(x).copy() for x in (cache_q, cache_k, cache_v, cache_z, cache_beta))
+    N, W, H, dk = q.shape
+    dv = v.shape[3]
+    nacc = None
+    if num_accepted is not None:
+        if hasattr(num_accepted, "detach"):
+            num_accepted = num_accepted.detach().cpu().numpy()
+        nacc = np.ascontiguousarray(np.asarray(num_accepted, dtype=np.int64))
+    o = np.zeros((N, W, H, dv))
+    rc = _load().oracle_kda_decode_step(_ptr(st), _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta),
+                                        _ptr(A), _ptr(cq), _ptr(ck), _ptr(cv), _ptr(cz), _ptr(cb),
+                                        _ptr(nacc), N, H, dk, dv, W, g_min, _ptr(o), int(n_threads))
+    if rc < 0:
+        raise ValueError("bad window")
+    return o, st, (cq, ck, cv, cz, cb)
+
+
+# --------------------------------------------------------------------------
+# Brute-force forms for tiny inputs (numpy, used only by the self-pins).
+# --------------------------------------------------------------------------
+
+def transition_matrices(k, z, A, beta, h, g_min=G_MIN):
+    """Dense M_t = (I - b_t k_t k_t^T) Diag(alpha_t) for every token of head h ([K3-7] eq. (1))."""
+    k, z, A, beta = map(_f64, (k, z, A, beta))
+    alpha = np.exp(gate(z, A, g_min))
+    T, H, dk = k.shape
+    out = []
+    for t in range(T):
+        kt = k[t, h]
+        out.append((np.eye(dk) - beta[t, h] * np.outer(kt, kt)) @ np.diag(alpha[t, h]))
+    return out
+
+
+def brute_P_H(k, v, z, A, beta, h, g_min=G_MIN):
+    """P^T and H^T by explicit dense products ([K3-2] "块内展开：P 和 H")."""
+    k, v = _f64(k), _f64(v)
+    Ms = transition_matrices(k, z, A, beta, h, g_min)
+    beta = _f64(beta)
+    T, H, dk = k.shape
+    P = np.eye(dk)
+    Hm = np.zeros((dk, v.shape[2]))
+    for t in range(T):
+        P = Ms[t] @ P
+        Hm = Ms[t] @ Hm + beta[t, h] * np.outer(k[t, h], v[t, h])
+    return P, Hm
+
+
+def wy_vectors(k, v, z, A, beta, h, g_min=G_MIN):
+    """WY auxiliary vectors w^r, u^r by their triangular recurrences
+    ([K3-2] "WY 表示"), with the decay between positions i < r equal to
+    gamma^r / gamma^i (exclusive of alpha^i)."""
+    k, v, z, A, beta = map(_f64, (k, v, z, A, beta))
+    g = gate(z, A, g_min)[:, h]
+    T = k.shape[0]
+    Gc = np.cumsum(g, axis=0)
+    gam = np.exp(Gc)  # gamma^r, inclusive
+    w = []
+    u = []
+    for r in range(T):
+        kr = k[r, h]
+        wr = gam[r] * kr
+        ur = v[r, h].copy()
+        for i in range(r):
+            coef = k[i, h] @ (np.exp(Gc[r] - Gc[i]) * kr)
+            wr = wr - w[i] * coef
+            ur = ur - u[i] * coef
+        w.append(beta[r, h] * wr)
+        u.append(beta[r, h] * ur)
+    return np.array(w), np.array(u), gam, Gc

@@ -1,0 +1,392 @@
+"""Self-pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each test ties one part of the oracle to something other than the oracle's own
+formula: closed forms, brute-force dense products on tiny inputs, algebraic
+invariants, special cases, and constants the pages print
+(tests/golden/pages_constants.json).  A plausible mistake in the oracle (a
+dropped term, a wrong sign or index, a transposed operand, an exclusive /
+inclusive decay mix-up) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "pages_constants.json")
+G_MIN = -5.0
+
+
+def rnd_inputs(T, H, dk, dv, seed, z_mean=0.0, z_std=1.0, beta_mean=0.0, A_std=0.5):
+    r = np.random.default_rng(seed)
+    q = r.standard_normal((T, H, dk))
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k = r.standard_normal((T, H, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = r.standard_normal((T, H, dv))
+    z = z_mean + z_std * r.standard_normal((T, H, dk))
+    A = A_std * r.standard_normal(H)
+    beta = 1.0 / (1.0 + np.exp(-(beta_mean + r.standard_normal((T, H)))))
+    return q, k, v, z, A, beta
+
+
+def rel(a, b):
+    return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)
+
+
+# ---------------------------------------------------------------- gate (P10)
+
+def test_gate_special_values_and_symmetry():
+    # z = 0: sigmoid(0) = 1/2 exactly, for every A.
+    for A in (-1.0, 0.0, 0.7):
+        assert oracle._load().oracle_gate(G_MIN, A, 0.0) == G_MIN / 2
+    # sigmoid(x) + sigmoid(-x) = 1  ->  g(z) + g(-z) = g_min.
+    for z in (0.3, 1.7, -2.2, 6.0):
+        s = oracle._load().oracle_gate(G_MIN, 0.4, z) + oracle._load().oracle_gate(G_MIN, 0.4, -z)
+        assert abs(s - G_MIN) < 1e-14
+    # A only rescales the abscissa: g(A, z) = g(0, e^A z).
+    for A, z in ((0.5, 1.3), (-0.8, -2.0)):
+        assert abs(oracle._load().oracle_gate(G_MIN, A, z)
+                   - oracle._load().oracle_gate(G_MIN, 0.0, math.exp(A) * z)) < 1e-14
+    # slope at 0 is g_min * e^A / 4 (sigmoid'(0) = 1/4), sign and scale pinned.
+    A, h = 0.3, 1e-6
+    d = (oracle._load().oracle_gate(G_MIN, A, h) - oracle._load().oracle_gate(G_MIN, A, -h)) / (2 * h)
+    assert abs(d - G_MIN * math.exp(A) / 4) < 1e-8
+
+
+def test_gate_bounds_match_pages():
+    gold = json.load(open(GOLDEN))
+    g_min = gold["gate_lower_bound"]["value"]
+    z = np.linspace(-30, 30, 2001).reshape(1, 1, -1)
+    g = oracle.gate(z, np.array([0.0]), g_min)
+    assert np.all(g < 0) and np.all(g > g_min)
+    assert np.all(np.diff(g.ravel()) <= 0)  # decreasing in z
+    # limits: z -> +inf pins to g_min, z -> -inf pins to 0
+    assert abs(oracle.gate(np.full((1, 1, 1), 60.0), np.array([0.0]), g_min)[0, 0, 0] - g_min) < 1e-12
+    assert abs(oracle.gate(np.full((1, 1, 1), -60.0), np.array([0.0]), g_min)[0, 0, 0]) < 1e-12
+    # fastest forgetting: alpha > e^{g_min} ~ 0.67 % per step (printed on the page)
+    m = gold["min_alpha_per_step"]
+    assert abs(math.exp(g_min) - m["value"]) / m["value"] < m["rel_tol"]
+    # 16-token sub-tile: accumulated log decay > 16 * g_min = -80, e^80 ~ 5.5e34 < bf16 max
+    n = gold["subtile_tokens"]["value"]
+    assert n * g_min == gold["subtile_log_decay_bound"]["value"]
+    e80 = gold["exp80"]
+    assert abs(math.exp(-n * g_min) - e80["value"]) / e80["value"] < e80["rel_tol"]
+    assert math.exp(-n * g_min) < gold["bf16_max"]["value"]
+
+
+# ---------------------------------------------------------------- P1: beta = 0
+
+def test_beta_zero_is_pure_channel_decay():
+    T, H, dk, dv = 37, 2, 16, 12
+    q, k, v, z, A, beta = rnd_inputs(T, H, dk, dv, 1)
+    beta[:] = 0.0
+    S0 = np.random.default_rng(2).standard_normal((1, H, dk, dv))
+    o, fin = oracle.recurrent(q, k, v, z, A, beta, init_state=S0)
+    g = oracle.gate(z, A)
+    cum = np.cumsum(g, axis=0)  # [T, H, dk], inclusive
+    for h in range(H):
+        for t in range(T):
+            St = np.exp(cum[t, h])[:, None] * S0[0, h]
+            assert rel(o[t, h], St.T @ q[t, h]) < 1e-12
+        assert rel(fin[0, h], np.exp(cum[-1, h])[:, None] * S0[0, h]) < 1e-12
+
+
+# ---------------------------------------------------------------- P2: brute force, T <= 16
+
+@pytest.mark.parametrize("T", [1, 5, 16])
+def test_recurrence_equals_dense_transition_products(T):
+    H, dk, dv = 2, 8, 6
+    q, k, v, z, A, beta = rnd_inputs(T, H, dk, dv, 10 + T)
+    S0 = np.random.default_rng(3).standard_normal((1, H, dk, dv))
+    o, fin = oracle.recurrent(q, k, v, z, A, beta, init_state=S0)
+    for h in range(H):
+        Ms = oracle.transition_matrices(k, z, A, beta, h)
+        S = S0[0, h].copy()
+        for t in range(T):
+            S = Ms[t] @ S + beta[t, h] * np.outer(k[t, h], v[t, h])  # eq. (1), dense
+            assert rel(o[t, h], S.T @ q[t, h]) < 1e-12
+        P, Hm = oracle.brute_P_H(k, v, z, A, beta, h)
+        assert rel(fin[0, h], P @ S0[0, h] + Hm) < 1e-12
+        assert rel(S, fin[0, h]) < 1e-12
+
+
+@pytest.mark.parametrize("T", [2, 7, 16])
+def test_wy_and_ut_match_brute_force(T):
+    """WY (P = Diag(gamma) - sum Diag(gamma^{i->r}) k w^T, H = sum Diag(..) k u^T) and the
+    UT transform M = (I + StrictTril(Diag(beta)(Gamma.K)(K/Gamma)^T))^-1 Diag(beta),
+    W = M (Gamma.K), U = M V, against dense products.  The decay between i and r is
+    gamma^r / gamma^i; the inclusive reading (gamma^r / gamma^{i-1}) fails here."""
+    H, dk, dv = 1, 8, 5
+    q, k, v, z, A, beta = rnd_inputs(T, H, dk, dv, 20 + T)
+    h = 0
+    w, u, gam, Gc = oracle.wy_vectors(k, v, z, A, beta, h)
+    P, Hm = oracle.brute_P_H(k, v, z, A, beta, h)
+    Pw = np.diag(gam[-1]).copy()
+    Hw = np.zeros((dk, dv))
+    for i in range(T):
+        d = np.exp(Gc[-1] - Gc[i])
+        Pw -= np.outer(d * k[i, h], w[i])
+        Hw += np.outer(d * k[i, h], u[i])
+    assert rel(Pw, P) < 1e-12
+    assert rel(Hw, Hm) < 1e-12
+    # UT transform
+    GK = gam * k[:, h]
+    KG = k[:, h] / gam
+    Lm = np.tril(np.diag(beta[:, h]) @ GK @ KG.T, -1)
+    M = np.linalg.solve(np.eye(T) + Lm, np.diag(beta[:, h]))
+    assert rel(M @ GK, w) < 1e-12
+    assert rel(M @ v[:, h], u) < 1e-12
+
+
+# ---------------------------------------------------------------- P3: chunk form == recurrence
+
+@pytest.mark.parametrize("C", [16, 32, 64])
+def test_chunk_form_equals_recurrence(C):
+    T, H, dk, dv = 203, 2, 32, 24
+    q, k, v, z, A, beta = rnd_inputs(T, H, dk, dv, 30 + C)
+    cu = np.array([0, 70, 71, 203])  # includes a one-token document
+    S0 = 0.1 * np.random.default_rng(4).standard_normal((3, H, dk, dv))
+    o_r, f_r = oracle.recurrent(q, k, v, z, A, beta, cu_seqlens=cu, init_state=S0)
+    o_c, f_c = oracle.chunk_form(q, k, v, z, A, beta, C, cu_seqlens=cu, init_state=S0)
+    assert rel(o_c, o_r) < 1e-12
+    assert rel(f_c, f_r) < 1e-12
+
+
+def test_chunk_form_strong_gate_range():
+    """Gate near its lower bound over a whole 64-token chunk: |G| up to 320, still exact in fp64."""
+    T, H, dk, dv = 128, 1, 16, 16
+    q, k, v, z, A, beta = rnd_inputs(T, H, dk, dv, 5, z_mean=8.0)
+    o_r, f_r = oracle.recurrent(q, k, v, z, A, beta)
+    o_c, f_c = oracle.chunk_form(q, k, v, z, A, beta, 64)
+    assert rel(o_c, o_r) < 1e-11
+    assert rel(f_c, f_r) < 1e-11
+
+
+# ---------------------------------------------------------------- P4: eq. (17) composition
+
+def _stress(T, H, dk, dv, seed):
+    # slow decay (z ~ N(-10, 1): g ~ -2e-4) and small beta keep M far from zero
+    return rnd_inputs(T, H, dk, dv, seed, z_mean=-10.0, beta_mean=-4.0)
+
+
+@pytest.mark.parametrize("stress", [False, True])
+def test_segment_composition_equals_unsplit(stress):
+    T, H, dk, dv = 300, 2, 16, 12
+    gen = _stress if stress else (lambda *a: rnd_inputs(*a))
+    q, k, v, z, A, beta = gen(T, H, dk, dv, 40)
+    S0 = np.random.default_rng(5).standard_normal((1, H, dk, dv))
+    o_ref, f_ref = oracle.recurrent(q, k, v, z, A, beta, init_state=S0)
+    cuts = [0, 64, 77, 200, 300]
+    for h in range(H):
+        S = S0[0, h]
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            M, St = oracle.pair(k, v, z, A, beta, a, b, h)
+            # matrix-free check of M: the recurrence from X with v = 0 gives M X
+            X = np.random.default_rng(a).standard_normal((1, 1, dk, dv))
+            _, fx = oracle.recurrent(q[a:b, h:h + 1], k[a:b, h:h + 1], np.zeros((b - a, 1, dv)),
+                                     z[a:b, h:h + 1], A[h:h + 1], beta[a:b, h:h + 1], init_state=X)
+            assert rel(M @ X[0, 0], fx[0, 0]) < 1e-12
+            S_next = M @ S + St
+            if stress:
+                # non-vacuous: the carried-in part is a large share of the exit state
+                assert np.linalg.norm(M @ S) / np.linalg.norm(S_next) > 0.1
+            # re-running the segment from the composed entering state reproduces o
+            o_seg, f_seg = oracle.recurrent(q[a:b, h:h + 1], k[a:b, h:h + 1], v[a:b, h:h + 1],
+                                            z[a:b, h:h + 1], A[h:h + 1], beta[a:b, h:h + 1],
+                                            init_state=S[None, None])
+            assert rel(o_seg[:, 0], o_ref[a:b, h]) < 1e-11
+            S = S_next
+        assert rel(S, f_ref[0, h]) < 1e-11
+
+
+def test_composition_associative_not_commutative():
+    r = np.random.default_rng(6)
+    dk, dv = 8, 5
+    ps = [(r.standard_normal((dk, dk)), r.standard_normal((dk, dv))) for _ in range(3)]
+    (M1, S1), (M2, S2), (M3, S3) = ps
+    a = oracle.compose(*oracle.compose(M3, S3, M2, S2), M1, S1)
+    b = oracle.compose(M3, S3, *oracle.compose(M2, S2, M1, S1))
+    assert rel(a[0], b[0]) < 1e-13 and rel(a[1], b[1]) < 1e-13
+    c = oracle.compose(M1, S1, M2, S2)
+    d = oracle.compose(M2, S2, M1, S1)
+    assert rel(c[1], d[1]) > 1e-3
+    # the page's formula, written out: (M2 M1, M2 S1 + S2)
+    assert rel(d[0], M2 @ M1) < 1e-14 and rel(d[1], M2 @ S1 + S2) < 1e-14
+
+
+def test_linear_attention_limit_is_addition():
+    """M = I (plain linear attention): composition adds and commutes ([K3-7] step 2)."""
+    r = np.random.default_rng(7)
+    dk, dv = 6, 4
+    S1, S2 = r.standard_normal((dk, dv)), r.standard_normal((dk, dv))
+    I = np.eye(dk)
+    a = oracle.compose(I, S2, I, S1)
+    b = oracle.compose(I, S1, I, S2)
+    assert rel(a[1], S1 + S2) < 1e-15 and rel(a[1], b[1]) < 1e-15
+
+
+def test_identity_pair_when_nothing_happens():
+    """beta = 0 and alpha -> 1 (z = -50): the pair is (I, 0), the unit of composition."""
+    T, H, dk, dv = 40, 1, 8, 8
+    q, k, v, z, A, beta = rnd_inputs(T, H, dk, dv, 8)
+    z[:] = -50.0
+    A[:] = 0.0
+    beta[:] = 0.0
+    M, St = oracle.pair(k, v, z, A, beta, 0, T, 0)
+    assert np.array_equal(M, np.eye(dk)) and np.all(St == 0)
+
+
+def test_document_start_inside_segment_resets_pair():
+    T, H, dk, dv = 120, 1, 8, 8
+    q, k, v, z, A, beta = rnd_inputs(T, H, dk, dv, 9)
+    cu = np.array([0, 50, 120])
+    init = np.random.default_rng(10).standard_normal((2, H, dk, dv))
+    M, St = oracle.pair(k, v, z, A, beta, 30, 120, 0, cu_seqlens=cu, init_state=init)
+    assert np.all(M == 0)
+    _, f = oracle.recurrent(q, k, v, z, A, beta, cu_seqlens=cu, init_state=init)
+    assert rel(St, f[1, 0]) < 1e-12
+
+
+# ---------------------------------------------------------------- P5: delta rule exactness
+
+def test_delta_rule_recalls_orthonormal_keys():
+    T, H, dk, dv = 24, 1, 32, 10
+    r = np.random.default_rng(11)
+    Qm, _ = np.linalg.qr(r.standard_normal((dk, dk)))
+    k = Qm[:, :T].T.reshape(T, 1, dk).copy()
+    k[20, 0] = k[3, 0]  # a repeated key overwrites its slot
+    v = r.standard_normal((T, H, dv))
+    q = k.copy()
+    z = np.full((T, H, dk), -50.0)  # alpha = 1 to double precision
+    A = np.zeros(H)
+    beta = np.ones((T, H))
+    o, fin = oracle.recurrent(q, k, v, z, A, beta)
+    S = fin[0, 0]
+    for j in range(T):
+        expect = v[20, 0] if j == 3 else v[j, 0]
+        assert rel(S.T @ k[j, 0], expect) < 1e-12
+        assert rel(o[j, 0], v[j, 0]) < 1e-12  # the token reads its own write
+
+
+# ---------------------------------------------------------------- P7 / P8: linearity, resume, varlen
+
+def test_linearity_in_values_and_state():
+    T, H, dk, dv = 90, 2, 16, 8
+    q, k, v, z, A, beta = rnd_inputs(T, H, dk, dv, 12)
+    r = np.random.default_rng(13)
+    v2 = r.standard_normal(v.shape)
+    S1 = r.standard_normal((1, H, dk, dv))
+    S2 = r.standard_normal((1, H, dk, dv))
+    o1, f1 = oracle.recurrent(q, k, v, z, A, beta, init_state=S1)
+    o2, f2 = oracle.recurrent(q, k, v2, z, A, beta, init_state=S2)
+    o3, f3 = oracle.recurrent(q, k, v + v2, z, A, beta, init_state=S1 + S2)
+    assert rel(o3, o1 + o2) < 1e-12 and rel(f3, f1 + f2) < 1e-12
+    o4, f4 = oracle.recurrent(q, k, 2.5 * v, z, A, beta, init_state=2.5 * S1)
+    assert rel(o4, 2.5 * o1) < 1e-13 and rel(f4, 2.5 * f1) < 1e-13
+
+
+def test_resume_and_packed_documents():
+    T, H, dk, dv = 150, 2, 16, 8
+    q, k, v, z, A, beta = rnd_inputs(T, H, dk, dv, 14)
+    S0 = np.random.default_rng(15).standard_normal((1, H, dk, dv))
+    o, f = oracle.recurrent(q, k, v, z, A, beta, init_state=S0)
+    t = 61
+    oa, fa = oracle.recurrent(q[:t], k[:t], v[:t], z[:t], A, beta[:t], init_state=S0)
+    ob, fb = oracle.recurrent(q[t:], k[t:], v[t:], z[t:], A, beta[t:], init_state=fa)
+    assert rel(np.concatenate([oa, ob]), o) < 1e-13 and rel(fb, f) < 1e-13
+    # packed = separate runs with their own initial states
+    cu = np.array([0, 40, 41, 150])
+    S = np.random.default_rng(16).standard_normal((3, H, dk, dv))
+    op, fp = oracle.recurrent(q, k, v, z, A, beta, cu_seqlens=cu, init_state=S)
+    for d in range(3):
+        a, b = cu[d], cu[d + 1]
+        od, fd = oracle.recurrent(q[a:b], k[a:b], v[a:b], z[a:b], A, beta[a:b],
+                                  init_state=S[d:d + 1])
+        assert rel(op[a:b], od) < 1e-14 and rel(fp[d], fd[0]) < 1e-14
+
+
+def test_empty_document_keeps_initial_state():
+    T, H, dk, dv = 20, 1, 8, 8
+    q, k, v, z, A, beta = rnd_inputs(T, H, dk, dv, 17)
+    cu = np.array([0, 10, 10, 20])
+    S = np.random.default_rng(18).standard_normal((3, H, dk, dv))
+    _, fp = oracle.recurrent(q, k, v, z, A, beta, cu_seqlens=cu, init_state=S)
+    assert np.array_equal(fp[1], S[1])
+
+
+# ---------------------------------------------------------------- P9: decode replay
+
+def test_decode_replay_equals_committed_stream():
+    N, W, H, dk, dv = 5, 5, 2, 16, 8
+    r = np.random.default_rng(19)
+
+    def window():
+        q = r.standard_normal((N, W, H, dk))
+        q /= np.linalg.norm(q, axis=-1, keepdims=True)
+        k = r.standard_normal((N, W, H, dk))
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+        return (q, k, r.standard_normal((N, W, H, dv)), r.standard_normal((N, W, H, dk)),
+                1 / (1 + np.exp(-r.standard_normal((N, W, H)))))
+
+    A = 0.3 * r.standard_normal(H)
+    S0 = 0.05 * r.standard_normal((N, H, dk, dv))
+    cache = (np.zeros((N, W - 1, H, dk)), np.zeros((N, W - 1, H, dk)), np.zeros((N, W - 1, H, dv)),
+             np.zeros((N, W - 1, H, dk)), np.zeros((N, W - 1, H)))
+    w1 = window()
+    o1, S1, cache = oracle.decode_step(S0, *w1, A, *cache, num_accepted=None)
+    w2 = window()
+    nacc = np.array([0, 4, 2, 1, 3])
+    o2, S2, cache2 = oracle.decode_step(S1, *w2, A, *cache, num_accepted=nacc)
+    for b in range(N):
+        n = nacc[b]
+        # committed stream: t0 of window 1, its first n drafts, t0 of window 2
+        idx1 = list(range(0, n + 1))
+        seqs = [np.concatenate([w1[i][b, idx1], w2[i][b, :1]]) for i in range(5)]
+        # then the speculative drafts of window 2
+        seqs = [np.concatenate([s, w2[i][b, 1:]]) for s, i in zip(seqs, range(5))]
+        q, k, v, z, beta = seqs
+        o_ref, _ = oracle.recurrent(q, k, v, z, A, beta, init_state=S0[b:b + 1])
+        # committed state = recurrence over t0(1), d1..dn(1), t0(2)
+        _, f_ref = oracle.recurrent(q[:n + 2], k[:n + 2], v[:n + 2], z[:n + 2], A, beta[:n + 2],
+                                    init_state=S0[b:b + 1])
+        assert rel(S2[b], f_ref[0]) < 1e-12
+        # window-2 outputs: t0 then drafts continue the committed stream
+        assert rel(o2[b], o_ref[n + 1:]) < 1e-12
+        # window-1 outputs: t0 and all drafts in order
+        o1_ref, _ = oracle.recurrent(w1[0][b], w1[1][b], w1[2][b], w1[3][b], A, w1[4][b],
+                                     init_state=S0[b:b + 1])
+        assert rel(o1[b], o1_ref) < 1e-12
+    # the cache now holds window 2's drafts
+    assert np.array_equal(cache2[1], w2[1][:, 1:])
+
+
+def test_decode_replay_equals_snapshot_rollback():
+    """Replaying the accepted prefix equals keeping a state snapshot after every draft and
+    rolling back to the one at the accepted length ([K3-7] decode paragraph)."""
+    N, W, H, dk, dv = 3, 5, 1, 8, 8
+    r = np.random.default_rng(21)
+    q = r.standard_normal((N, W, H, dk)); q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k = r.standard_normal((N, W, H, dk)); k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = r.standard_normal((N, W, H, dv)); z = r.standard_normal((N, W, H, dk))
+    beta = 1 / (1 + np.exp(-r.standard_normal((N, W, H))))
+    A = np.zeros(H)
+    S0 = r.standard_normal((N, H, dk, dv))
+    empty = (np.zeros((N, W - 1, H, dk)),) * 2 + (np.zeros((N, W - 1, H, dv)),
+                                                  np.zeros((N, W - 1, H, dk)), np.zeros((N, W - 1, H)))
+    _, S1, cache = oracle.decode_step(S0, q, k, v, z, beta, A, *empty)
+    nacc = np.array([4, 0, 2])
+    w2 = [x.copy() for x in (q, k, v, z, beta)]
+    _, S2, _ = oracle.decode_step(S1, *w2, A, *cache, num_accepted=nacc)
+    for b in range(N):
+        snaps = [S1[b]]
+        for j in range(1, W):
+            _, f = oracle.recurrent(q[b, j:j + 1], k[b, j:j + 1], v[b, j:j + 1], z[b, j:j + 1], A,
+                                    beta[b, j:j + 1], init_state=snaps[-1][None])
+            snaps.append(f[0])
+        _, f = oracle.recurrent(w2[0][b, :1], w2[1][b, :1], w2[2][b, :1], w2[3][b, :1], A,
+                                w2[4][b, :1], init_state=snaps[nacc[b]][None])
+        assert rel(S2[b], f[0]) < 1e-13
