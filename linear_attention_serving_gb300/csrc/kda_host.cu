@@ -1,0 +1,260 @@
+// kda_host.cu -- the C ABI (include/kda.h): argument checks, workspace layout,
+// chunk planning and the launch sequence of every entry point.
+#include <cstdint>
+#include <cstring>
+
+#include "kda_internal.cuh"
+
+using namespace kda;
+
+// ---------------------------------------------------------------- diagnostics
+namespace {
+constexpr int PROF_MAX = 256;
+bool g_prof = false;
+bool g_prof_ready = false;
+cudaEvent_t g_ev[PROF_MAX];
+const char *g_name[PROF_MAX];
+int g_nmarks = 0;
+unsigned long long g_launches = 0;
+
+void prof_mark(const char *name, cudaStream_t s) {
+    if (!g_prof || !g_prof_ready || g_nmarks >= PROF_MAX) return;
+    if (cudaEventRecord(g_ev[g_nmarks], s) == cudaSuccess) g_name[g_nmarks++] = name;
+}
+}  // namespace
+
+namespace kda {
+void note_launch(const char *name, cudaStream_t s) {
+    __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
+    prof_mark(name, s);
+}
+void note_begin(cudaStream_t s) { prof_mark("begin", s); }
+}  // namespace kda
+
+namespace {
+
+bool aligned16(const void *p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+// Validation shared by kda_chunk_fwd and kda_segment_scan.
+int check_prefill(const void *q, const void *k, const void *v, const float *z, const float *A,
+                  const float *beta, const int32_t *cu, int n_seqs, int64_t T_total, int H, int Dm,
+                  int dtype, float g_min, const void *o) {
+    if (Dm != D) return KDA_ERR_UNSUPPORTED;
+    if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
+    if (H < 1 || n_seqs < 1 || T_total < 0 || T_total >= (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
+    if (!(g_min >= -5.0f && g_min < 0.0f)) return KDA_ERR_INVALID_ARG;
+    if (T_total > 0 && (!q || !k || !v || !z || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (!A) return KDA_ERR_INVALID_ARG;
+    if (!cu && (T_total % n_seqs) != 0) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(z) || !aligned16(o))
+        return KDA_ERR_INVALID_ARG;
+    // the largest element offset of a [T, H, 128] tensor must fit the kernels' 64-bit math;
+    // the chunk count must fit an int
+    if ((int64_t)(T_total / C + n_seqs) >= (int64_t)INT32_MAX / 2) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+// Chunk plan: arithmetic for equal-length documents, a device table otherwise.
+int make_plan(const int32_t *cu, int n_seqs, int64_t T_total, void *ws, const Workspace &w,
+              cudaStream_t s, Plan &p) {
+    memset(&p, 0, sizeof(p));
+    char *base = (char *)ws;
+    p.n_seqs = n_seqs;
+    p.err = (int32_t *)base;
+    p.table = (const ChunkInfo *)(base + w.off_table);
+    p.doc_off = (const int32_t *)(base + w.off_doc);
+    p.n_chunks = (const int32_t *)(base + 4);
+    int rc = cuda_status(cudaMemsetAsync(base, 0, 8, s));
+    if (rc) return rc;
+    if (!cu) {
+        p.uniform = 1;
+        p.seq_len = (int)(T_total / n_seqs);
+        p.chunks_per_seq = (p.seq_len + C - 1) / C;
+        p.max_chunks = n_seqs * p.chunks_per_seq;
+        return KDA_OK;
+    }
+    p.uniform = 0;
+    p.max_chunks = w.max_chunks;
+    return launch_plan(cu, n_seqs, T_total, ws, w, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        case KDA_ERR_DEVICE_CHECK: return "KDA_ERR_DEVICE_CHECK";
+        default: return "KDA_ERR_UNKNOWN";
+    }
+}
+
+int kda_version(void) { return 100; }
+
+int kda_profile_enable(int on) {
+    if (on && !g_prof_ready) {
+        for (int i = 0; i < PROF_MAX; ++i)
+            if (cudaEventCreate(&g_ev[i]) != cudaSuccess) return KDA_ERR_CUDA;
+        g_prof_ready = true;
+    }
+    g_prof = on != 0;
+    g_nmarks = 0;
+    return KDA_OK;
+}
+
+int kda_profile_collect(const char **names, float *ms, int max) {
+    if (!g_prof_ready || g_nmarks == 0) {
+        g_nmarks = 0;
+        return 0;
+    }
+    if (cudaEventSynchronize(g_ev[g_nmarks - 1]) != cudaSuccess) return -KDA_ERR_CUDA;
+    int n = 0;
+    for (int i = 1; i < g_nmarks && n < max; ++i) {
+        if (strcmp(g_name[i], "begin") == 0) continue;
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, g_ev[i - 1], g_ev[i]) != cudaSuccess) return -KDA_ERR_CUDA;
+        if (names) names[n] = g_name[i];
+        if (ms) ms[n] = t;
+        ++n;
+    }
+    g_nmarks = 0;
+    return n;
+}
+
+long long kda_launch_count(void) { return (long long)__atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+size_t kda_chunk_fwd_workspace_size(int64_t T_total, int H, int n_seqs, int dtype) {
+    if (T_total < 0 || H < 1 || n_seqs < 1) return 0;
+    return workspace_layout(T_total, H, n_seqs, 0, dtype).total;
+}
+
+size_t kda_segment_scan_workspace_size(int64_t T_total, int H, int n_seqs, int n_segments,
+                                       int dtype) {
+    if (T_total < 0 || H < 1 || n_seqs < 1 || n_segments < 1) return 0;
+    return workspace_layout(T_total, H, n_seqs, n_segments, dtype).total;
+}
+
+int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *z, const float *A,
+                  const float *beta, const int32_t *cu_seqlens, int n_seqs, int64_t T_total, int H,
+                  int Dm, int dtype, float g_min, const float *init_state, void *o,
+                  float *final_state, void *workspace, size_t workspace_bytes,
+                  kda_stream_t stream) {
+    int rc = check_prefill(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, Dm, dtype, g_min, o);
+    if (rc) return rc;
+    const Workspace w = workspace_layout(T_total, H, n_seqs, 0, dtype);
+    if (!workspace || workspace_bytes < w.total || ((uintptr_t)workspace & 255u)) return KDA_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    note_begin(s);
+    Plan p;
+    if ((rc = make_plan(cu_seqlens, n_seqs, T_total, workspace, w, s, p))) return rc;
+    void *records = (char *)workspace + w.off_rec;
+    if ((rc = launch_prep_simt(q, k, v, z, A, beta, H, dtype, g_min, p, records, s))) return rc;
+    ScanArgs a;
+    memset(&a, 0, sizeof(a));
+    a.plan = p;
+    a.H = H;
+    a.records = records;
+    a.mode = SCAN_DOCS;
+    a.n_units = n_seqs;
+    a.ncols = D;
+    a.phase = 0;
+    a.init_state = init_state;
+    a.o = o;
+    a.final_state = final_state;
+    return launch_scan_simt(a, dtype, s);
+}
+
+int kda_segment_scan(const void *q, const void *k, const void *v, const float *z, const float *A,
+                     const float *beta, const int32_t *cu_seqlens, int n_seqs, int64_t T_total,
+                     int H, int Dm, int dtype, float g_min, const float *init_state, int n_segments,
+                     float *pairs_M, float *pairs_S, void *o, float *final_state, void *workspace,
+                     size_t workspace_bytes, kda_stream_t stream) {
+    int rc = check_prefill(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, Dm, dtype, g_min, o);
+    if (rc) return rc;
+    if (n_segments < 1 || n_segments > (1 << 20)) return KDA_ERR_INVALID_ARG;
+    const Workspace w = workspace_layout(T_total, H, n_seqs, n_segments, dtype);
+    if (!workspace || workspace_bytes < w.total || ((uintptr_t)workspace & 255u)) return KDA_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    note_begin(s);
+    Plan p;
+    if ((rc = make_plan(cu_seqlens, n_seqs, T_total, workspace, w, s, p))) return rc;
+    char *base = (char *)workspace;
+    void *records = base + w.off_rec;
+    float *pairs = (float *)(base + w.off_pairs);
+    float *s_enter = (float *)(base + w.off_enter);
+    if ((rc = launch_prep_simt(q, k, v, z, A, beta, H, dtype, g_min, p, records, s))) return rc;
+
+    ScanArgs a;
+    memset(&a, 0, sizeof(a));
+    a.plan = p;
+    a.H = H;
+    a.records = records;
+    a.mode = SCAN_SEGMENTS;
+    a.n_units = n_segments;
+    a.n_seg = n_segments;
+    a.init_state = init_state;
+    a.s_enter = s_enter;
+    a.pairs = pairs;
+    // phase 1: pairs (M, S~) of every (head, segment) from zero / identity
+    a.ncols = 2 * D;
+    a.phase = 1;
+    if ((rc = launch_scan_simt(a, dtype, s))) return rc;
+    // phase 2: entering states by sequential composition
+    if ((rc = launch_compose(p, H, n_segments, pairs, s_enter, s))) return rc;
+    // phase 3: every segment from its exact entering state
+    a.ncols = D;
+    a.phase = 3;
+    a.o = o;
+    a.final_state = final_state;
+    if ((rc = launch_scan_simt(a, dtype, s))) return rc;
+    if ((rc = launch_empty_docs(p, H, init_state, final_state, s))) return rc;
+    const size_t mat = sizeof(float) * (size_t)H * n_segments * D * D;
+    if (pairs_M && (rc = cuda_status(cudaMemcpyAsync(pairs_M, pairs, mat, cudaMemcpyDeviceToDevice, s))))
+        return rc;
+    if (pairs_S &&
+        (rc = cuda_status(cudaMemcpyAsync(pairs_S, (char *)pairs + mat, mat, cudaMemcpyDeviceToDevice, s))))
+        return rc;
+    return KDA_OK;
+}
+
+int kda_decode_step(float *state, const void *q, const void *k, const void *v, const float *z,
+                    const float *beta, const float *A, void *cache_q, void *cache_k, void *cache_v,
+                    float *cache_z, float *cache_beta, const int32_t *num_accepted, int N, int H,
+                    int Dm, int W, int dtype, float g_min, void *o, int32_t *error_word,
+                    kda_stream_t stream) {
+    if (Dm != D) return KDA_ERR_UNSUPPORTED;
+    if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
+    if (N < 1 || H < 1 || W < 1 || W > 8) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)N * H >= (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
+    if (!(g_min >= -5.0f && g_min < 0.0f)) return KDA_ERR_INVALID_ARG;
+    if (!state || !q || !k || !v || !z || !beta || !A || !o) return KDA_ERR_INVALID_ARG;
+    if (W > 1 && (!cache_q || !cache_k || !cache_v || !cache_z || !cache_beta)) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(z) ||
+        !aligned16(o) || !aligned16(cache_q) || !aligned16(cache_k) || !aligned16(cache_v) ||
+        !aligned16(cache_z))
+        return KDA_ERR_INVALID_ARG;
+    note_begin((cudaStream_t)stream);
+    return launch_decode(state, q, k, v, z, beta, A, cache_q, cache_k, cache_v, cache_z, cache_beta,
+                         num_accepted, N, H, W, dtype, g_min, o, error_word, (cudaStream_t)stream);
+}
+
+int kda_read_device_error(const void *workspace, int32_t *code, kda_stream_t stream) {
+    if (!workspace || !code) return KDA_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    *code = h;
+    return KDA_OK;
+}
+
+}  // extern "C"

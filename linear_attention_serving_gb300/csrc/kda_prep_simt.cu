@@ -1,0 +1,377 @@
+// kda_prep_simt.cu -- per-(chunk, head) preparation in fp32 CUDA cores.
+//
+// Computes, for one 64-token chunk of one head, everything of the chunk form
+// that does not depend on the entering state ("Kimi K3: the Manos, the
+// Mythos ..." (SemiAnalysis), "FlashKDA 算法": a = exp(cumsum g), K_decay,
+// Q_decay, K_inv, K_restore, L, INV = (I+L)^-1, M_qk; "Kimi K3 模型结构（2）",
+// "UT 变换"), and folds them into the record consumed by the scan kernels:
+//   W = INV Diag(beta) K_decay,  U0 = INV Diag(beta) V,
+//   Q' = Q_decay - M_qk W,       O0 = M_qk U0,   K_restore,   a_C.
+//
+// Decay factors follow the 16-token sub-tile factorisation of "Kimi K3 模型
+// 结构（2）", section "数值问题：1/Γ 会溢出": with P_p the cumulative log decay
+// before tile p, r_i = G_i - P_p and e_i = exp(r_i) in (e^-80, 1] (bounded
+// gate, "后果一"), tile totals Delta_p, the pair factor exp(G_i - G_j) for
+// i in tile p, j in tile q <= p is
+//   e_i * F_pq * (exp(Delta_q) / e_j),   F_pp = exp(-Delta_p),
+//   F_pq = prod_{q<t<p} exp(Delta_t)  (q < p),
+// where every factor is at most e^80 and the key factor is at most 1, so no
+// exp(-G) of a whole chunk is ever formed.
+//
+// This kernel serves the fp32 path (exact fp32 arithmetic) and writes either
+// fp32 records or the bf16 tcgen05 operand images.
+#include "kda_internal.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int LD = 132;         // padded row stride of [64][128] fp32 tiles
+constexpr int LDM = 65;         // padded row stride of [64][64] fp32 matrices
+constexpr int PREP_THREADS = 256;
+
+struct PrepSmem {
+    // float offsets
+    static constexpr int xq = 0;
+    static constexpr int xk = xq + C * LD;
+    static constexpr int xf = xk + C * LD;
+    static constexpr int xv = xf + C * LD;
+    static constexpr int xe = xv + C * LD;        // g -> r -> e, later Lm | Mqk
+    static constexpr int inv = xe + C * LD;       // [64][65]
+    static constexpr int tmp = inv + C * LDM;     // [3][16][17]
+    static constexpr int eD = tmp + 3 * 16 * 17;  // [4][128]
+    static constexpr int ePfx = eD + NSUB * D;    // [4][128]
+    static constexpr int eSfx = ePfx + NSUB * D;  // [4][128]
+    static constexpr int F = eSfx + NSUB * D;     // [10][128]
+    static constexpr int aC = F + 10 * D;         // [128]
+    static constexpr int beta = aC + D;           // [64]
+    static constexpr int total = beta + C;
+};
+constexpr size_t PREP_SMEM_BYTES = sizeof(float) * PrepSmem::total;
+
+__device__ __forceinline__ int fpq_index(int p, int q) { return p * (p + 1) / 2 + q; }
+
+template <typename InT, bool BF16_REC>
+__global__ void __launch_bounds__(PREP_THREADS)
+prep_simt_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const InT *__restrict__ v,
+                 const float *__restrict__ z, const float *__restrict__ A,
+                 const float *__restrict__ beta, int H, float g_min, Plan plan,
+                 char *__restrict__ records) {
+    extern __shared__ __align__(16) float sm[];
+    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    if (c >= plan_n_chunks(plan)) return;
+    const ChunkInfo ci = plan_chunk(plan, c);
+    const int t0 = ci.tok, len = ci.len;
+    const float eA = expf(A[h]);
+
+    float *xq = sm + PrepSmem::xq, *xk = sm + PrepSmem::xk, *xf = sm + PrepSmem::xf;
+    float *xv = sm + PrepSmem::xv, *xe = sm + PrepSmem::xe, *INV = sm + PrepSmem::inv;
+    float *tmp = sm + PrepSmem::tmp, *eD = sm + PrepSmem::eD, *ePfx = sm + PrepSmem::ePfx;
+    float *eSfx = sm + PrepSmem::eSfx, *F = sm + PrepSmem::F, *aC = sm + PrepSmem::aC;
+    float *sb = sm + PrepSmem::beta;
+    float *Lm = xe, *Mqk = xe + C * LDM;
+
+    // 1. load the chunk; rows past the end behave as k = q = v = 0, g = 0, beta = 0
+    for (int idx = tid; idx < C * D; idx += PREP_THREADS) {
+        const int r = idx >> 7, col = idx & 127;
+        const bool ok = r < len;
+        const size_t g = ((size_t)(t0 + (ok ? r : 0)) * H + h) * D + col;
+        xq[r * LD + col] = ok ? to_f32(q[g]) : 0.f;
+        xk[r * LD + col] = ok ? to_f32(k[g]) : 0.f;
+        xv[r * LD + col] = ok ? to_f32(v[g]) : 0.f;
+        xe[r * LD + col] = ok ? kda_gate(g_min, eA, z[g]) : 0.f;
+    }
+    if (tid < C) sb[tid] = tid < len ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    // zero INV (its strictly upper blocks stay zero)
+    for (int idx = tid; idx < C * LDM; idx += PREP_THREADS) INV[idx] = 0.f;
+    __syncthreads();
+
+    // 2. per-channel cumulative log decay inside each 16-token tile, and the factors
+    if (tid < D) {
+        const int col = tid;
+        float P = 0.f, Pst[NSUB], Dl[NSUB];
+        for (int p = 0; p < NSUB; ++p) {
+            float acc = 0.f;
+            for (int i = 0; i < SUB; ++i) {
+                acc += xe[(p * SUB + i) * LD + col];
+                xe[(p * SUB + i) * LD + col] = acc;  // r_i
+            }
+            Pst[p] = P;
+            Dl[p] = acc;
+            P += acc;
+        }
+        aC[col] = expf(P);
+        for (int p = 0; p < NSUB; ++p) {
+            eD[p * D + col] = expf(Dl[p]);
+            ePfx[p * D + col] = expf(Pst[p]);
+            eSfx[p * D + col] = expf(P - (Pst[p] + Dl[p]));
+            for (int qq = 0; qq <= p; ++qq) {
+                float f;
+                if (qq == p) {
+                    f = expf(-Dl[p]);
+                } else {
+                    float s = 0.f;
+                    for (int t = qq + 1; t < p; ++t) s += Dl[t];
+                    f = expf(s);
+                }
+                F[fpq_index(p, qq) * D + col] = f;
+            }
+        }
+        for (int i = 0; i < C; ++i) xe[i * LD + col] = expf(xe[i * LD + col]);  // e_i
+    }
+    __syncthreads();
+
+    // 3. factored operands: q*e, k*e (query side), k*exp(Delta_q)/e (key side)
+    for (int idx = tid; idx < C * D; idx += PREP_THREADS) {
+        const int r = idx >> 7, col = idx & 127;
+        const float e = xe[r * LD + col];
+        const float kk = xk[r * LD + col];
+        xq[r * LD + col] *= e;
+        xk[r * LD + col] = kk * e;
+        xf[r * LD + col] = kk * (eD[(r >> 4) * D + col] / e);
+    }
+    __syncthreads();
+
+    // 4. A_qk (lower, diagonal kept) and A_kk (strictly lower), scaled by beta
+    for (int P = tid; P < C * C; P += PREP_THREADS) {
+        const int i = P >> 6, j = P & 63;
+        if (j > i) {
+            Lm[i * LDM + j] = 0.f;
+            Mqk[i * LDM + j] = 0.f;
+            continue;
+        }
+        const float *Fr = F + fpq_index(i >> 4, j >> 4) * D;
+        const float4 *a4 = reinterpret_cast<const float4 *>(xq + i * LD);
+        const float4 *b4 = reinterpret_cast<const float4 *>(xk + i * LD);
+        const float4 *f4 = reinterpret_cast<const float4 *>(xf + j * LD);
+        const float4 *s4 = reinterpret_cast<const float4 *>(Fr);
+        float aqk = 0.f, akk = 0.f;
+#pragma unroll 4
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+            const float4 kf = f4[c4], fs = s4[c4], qa = a4[c4], ka = b4[c4];
+            const float w0 = kf.x * fs.x, w1 = kf.y * fs.y, w2 = kf.z * fs.z, w3 = kf.w * fs.w;
+            aqk = fmaf(qa.x, w0, aqk); aqk = fmaf(qa.y, w1, aqk);
+            aqk = fmaf(qa.z, w2, aqk); aqk = fmaf(qa.w, w3, aqk);
+            akk = fmaf(ka.x, w0, akk); akk = fmaf(ka.y, w1, akk);
+            akk = fmaf(ka.z, w2, akk); akk = fmaf(ka.w, w3, akk);
+        }
+        Mqk[i * LDM + j] = aqk;
+        Lm[i * LDM + j] = (j < i) ? sb[i] * akk : 0.f;
+    }
+    __syncthreads();
+
+    // 5. INV = (I + L)^-1: 16x16 diagonal blocks by forward substitution,
+    //    then X_pq = -X_pp sum_{q<=r<p} L_pr X_rq level by level.
+    if (tid < C) {
+        const int p = tid >> 4, col = tid & 15;
+        float x[SUB];
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) {
+            float val = (i == col) ? 1.f : 0.f;
+#pragma unroll
+            for (int s = 0; s < i; ++s) val = fmaf(-Lm[(p * SUB + i) * LDM + p * SUB + s], x[s], val);
+            x[i] = val;
+        }
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) INV[(p * SUB + i) * LDM + p * SUB + col] = x[i];
+    }
+    __syncthreads();
+    for (int lvl = 1; lvl < NSUB; ++lvl) {
+        const int nblk = NSUB - lvl;
+        for (int e = tid; e < nblk * 256; e += PREP_THREADS) {
+            const int b = e >> 8, i = (e >> 4) & 15, jj = e & 15;
+            const int p = lvl + b, qb = b;
+            float acc = 0.f;
+            for (int r = qb; r < p; ++r)
+                for (int s = 0; s < SUB; ++s)
+                    acc = fmaf(Lm[(p * SUB + i) * LDM + r * SUB + s], INV[(r * SUB + s) * LDM + qb * SUB + jj], acc);
+            tmp[(b * 16 + i) * 17 + jj] = acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < nblk * 256; e += PREP_THREADS) {
+            const int b = e >> 8, i = (e >> 4) & 15, jj = e & 15;
+            const int p = lvl + b, qb = b;
+            float acc = 0.f;
+            for (int s = 0; s < SUB; ++s)
+                acc = fmaf(INV[(p * SUB + i) * LDM + p * SUB + s], tmp[(b * 16 + s) * 17 + jj], acc);
+            INV[(p * SUB + i) * LDM + qb * SUB + jj] = -acc;
+        }
+        __syncthreads();
+    }
+
+    char *rec = records + ((size_t)c * H + h) * (BF16_REC ? REC_BF16_BYTES : REC_F32_BYTES);
+
+    // 6. B1 = Diag(beta) K_decay (K_decay = ePfx * k*e), B2 = Diag(beta) V,
+    //    K_restore = exp(G_last - G_j) k_j = eSfx * (key-side factored k)
+    if (BF16_REC) {
+        // K_restore^T image: row = channel, column = token, 8 tokens per 16-byte store
+        for (int it = tid; it < D * (C / 8); it += PREP_THREADS) {
+            const int ch = it & 127, j0 = (it >> 7) * 8;
+            __align__(16) __nv_bfloat16 vals[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = j0 + u;
+                vals[u] = __float2bfloat16_rn(eSfx[(j >> 4) * D + ch] * xf[j * LD + ch]);
+            }
+            *reinterpret_cast<uint4 *>(rec + REC_BF16_KRT + sw128_offset(ch, j0, 128)) =
+                *reinterpret_cast<const uint4 *>(vals);
+        }
+    } else {
+        float *kr = reinterpret_cast<float *>(rec + REC_F32_KR);
+        for (int idx = tid; idx < C * D; idx += PREP_THREADS) {
+            const int r = idx >> 7, col = idx & 127;
+            kr[idx] = eSfx[(r >> 4) * D + col] * xf[r * LD + col];
+        }
+    }
+    for (int idx = tid; idx < C * D; idx += PREP_THREADS) {
+        const int r = idx >> 7, col = idx & 127;
+        xk[r * LD + col] = sb[r] * ePfx[(r >> 4) * D + col] * xk[r * LD + col];
+        xv[r * LD + col] = sb[r] * xv[r * LD + col];
+        // Q_decay = ePfx * (q*e), kept in xq
+        xq[r * LD + col] = ePfx[(r >> 4) * D + col] * xq[r * LD + col];
+    }
+    if (tid < D) {
+        float *ac = reinterpret_cast<float *>(rec + (BF16_REC ? REC_BF16_AC : REC_F32_AC));
+        ac[tid] = aC[tid];
+    }
+    __syncthreads();
+
+    // thread tile of the 64 x 128 products: 4 rows x 8 columns
+    const int r0 = (tid >> 4) * 4, c0 = (tid & 15) * 8;
+
+    // 7. W = INV B1 -> xf
+    {
+        float acc[4][8] = {};
+        for (int s = 0; s <= r0 + 3; ++s) {
+            const float4 b0 = *reinterpret_cast<const float4 *>(xk + s * LD + c0);
+            const float4 b1 = *reinterpret_cast<const float4 *>(xk + s * LD + c0 + 4);
+            const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float a = INV[(r0 + i) * LDM + s];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a, bb[j], acc[i][j]);
+            }
+        }
+        __syncthreads();  // every read of xf as the key operand finished long ago; keep order simple
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) xf[(r0 + i) * LD + c0 + j] = acc[i][j];
+    }
+    __syncthreads();
+    // 8. U0 = INV B2 -> xk (B1 no longer needed)
+    {
+        float acc[4][8] = {};
+        for (int s = 0; s <= r0 + 3; ++s) {
+            const float4 b0 = *reinterpret_cast<const float4 *>(xv + s * LD + c0);
+            const float4 b1 = *reinterpret_cast<const float4 *>(xv + s * LD + c0 + 4);
+            const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float a = INV[(r0 + i) * LDM + s];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a, bb[j], acc[i][j]);
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) xk[(r0 + i) * LD + c0 + j] = acc[i][j];
+    }
+    __syncthreads();
+
+    // 9. Q' = Q_decay - M_qk W,  O0 = M_qk U0;  write W, Q', U0, O0
+    {
+        float aw[4][8] = {}, au[4][8] = {};
+        for (int s = 0; s <= r0 + 3; ++s) {
+            const float4 w0 = *reinterpret_cast<const float4 *>(xf + s * LD + c0);
+            const float4 w1 = *reinterpret_cast<const float4 *>(xf + s * LD + c0 + 4);
+            const float4 u0 = *reinterpret_cast<const float4 *>(xk + s * LD + c0);
+            const float4 u1 = *reinterpret_cast<const float4 *>(xk + s * LD + c0 + 4);
+            const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float a = Mqk[(r0 + i) * LDM + s];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    aw[i][j] = fmaf(a, ww[j], aw[i][j]);
+                    au[i][j] = fmaf(a, uu[j], au[i][j]);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = r0 + i;
+            float wv[8], qv[8], uv[8], ov[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                wv[j] = xf[r * LD + c0 + j];
+                qv[j] = xq[r * LD + c0 + j] - aw[i][j];
+                uv[j] = xk[r * LD + c0 + j];
+                ov[j] = au[i][j];
+            }
+            if (BF16_REC) {
+                __align__(16) __nv_bfloat16 bw[8], bq[8], bu[8], bo[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    bw[j] = __float2bfloat16_rn(wv[j]);
+                    bq[j] = __float2bfloat16_rn(qv[j]);
+                    bu[j] = __float2bfloat16_rn(uv[j]);
+                    bo[j] = __float2bfloat16_rn(ov[j]);
+                }
+                *reinterpret_cast<uint4 *>(rec + REC_BF16_A1 + sw128_offset(r, c0, 128)) =
+                    *reinterpret_cast<const uint4 *>(bw);
+                *reinterpret_cast<uint4 *>(rec + REC_BF16_A1 + sw128_offset(64 + r, c0, 128)) =
+                    *reinterpret_cast<const uint4 *>(bq);
+                *reinterpret_cast<uint4 *>(rec + REC_BF16_U0 + (size_t)(r * D + c0) * 2) =
+                    *reinterpret_cast<const uint4 *>(bu);
+                *reinterpret_cast<uint4 *>(rec + REC_BF16_O0 + (size_t)(r * D + c0) * 2) =
+                    *reinterpret_cast<const uint4 *>(bo);
+            } else {
+                float *W = reinterpret_cast<float *>(rec + REC_F32_W) + r * D + c0;
+                float *Q = reinterpret_cast<float *>(rec + REC_F32_Q) + r * D + c0;
+                float *U = reinterpret_cast<float *>(rec + REC_F32_U0) + r * D + c0;
+                float *O = reinterpret_cast<float *>(rec + REC_F32_O0) + r * D + c0;
+#pragma unroll
+                for (int j = 0; j < 8; j += 4) {
+                    *reinterpret_cast<float4 *>(W + j) = make_float4(wv[j], wv[j + 1], wv[j + 2], wv[j + 3]);
+                    *reinterpret_cast<float4 *>(Q + j) = make_float4(qv[j], qv[j + 1], qv[j + 2], qv[j + 3]);
+                    *reinterpret_cast<float4 *>(U + j) = make_float4(uv[j], uv[j + 1], uv[j + 2], uv[j + 3]);
+                    *reinterpret_cast<float4 *>(O + j) = make_float4(ov[j], ov[j + 1], ov[j + 2], ov[j + 3]);
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+int launch_prep_simt(const void *q, const void *k, const void *v, const float *z, const float *A,
+                     const float *beta, int H, int dtype, float g_min, const Plan &p, void *records,
+                     cudaStream_t s) {
+    if (p.max_chunks == 0) return KDA_OK;
+    dim3 grid(p.max_chunks, H);
+    cudaError_t e;
+    if (dtype == KDA_BF16) {
+        auto kern = prep_simt_kernel<__nv_bfloat16, true>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PREP_SMEM_BYTES);
+        if (e != cudaSuccess) return KDA_ERR_CUDA;
+        kern<<<grid, PREP_THREADS, PREP_SMEM_BYTES, s>>>(
+            (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, z, A, beta, H,
+            g_min, p, (char *)records);
+    } else {
+        auto kern = prep_simt_kernel<float, false>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PREP_SMEM_BYTES);
+        if (e != cudaSuccess) return KDA_ERR_CUDA;
+        kern<<<grid, PREP_THREADS, PREP_SMEM_BYTES, s>>>((const float *)q, (const float *)k,
+                                                         (const float *)v, z, A, beta, H, g_min, p,
+                                                         (char *)records);
+    }
+    note_launch("prep_simt", s);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace kda

@@ -1,0 +1,105 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol that
+include/kda.h declares, and rejects bad arguments before launching anything
+(no GPU needed: argument validation happens before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_serving_gb300 as kda
+from linear_attention_serving_gb300 import kda as kb
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kda.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("kda_chunk_fwd", "kda_segment_scan", "kda_decode_step"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    kda.load()
+    lib = ctypes.CDLL(kb.library_path())
+    for n in declared_functions():
+        assert hasattr(lib, n), f"libkda.so does not export {n}"
+
+
+def test_status_strings_and_version():
+    lib = kda.load()
+    assert lib.kda_version() >= 100
+    for code, name in [(0, b"KDA_OK"), (1, b"KDA_ERR_INVALID_ARG"), (2, b"KDA_ERR_UNSUPPORTED"),
+                       (3, b"KDA_ERR_CUDA"), (4, b"KDA_ERR_TIMEOUT"), (5, b"KDA_ERR_WORKSPACE"),
+                       (6, b"KDA_ERR_DEVICE_CHECK")]:
+        assert lib.kda_status_string(code) == name
+    assert lib.kda_status_string(99) == b"KDA_ERR_UNKNOWN"
+
+
+def test_workspace_sizes_grow_with_work():
+    s1 = kda.chunk_fwd_workspace_size(8192, 16, 1)
+    s2 = kda.chunk_fwd_workspace_size(16384, 16, 1)
+    assert 0 < s1 < s2
+    assert kda.segment_scan_workspace_size(8192, 16, 1, 4) > s1
+    lib = kda.load()
+    assert lib.kda_chunk_fwd_workspace_size(-1, 16, 1, 0) == 0
+    assert lib.kda_segment_scan_workspace_size(64, 1, 1, 0, 0) == 0
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # aligned dummy address; never dereferenced on these paths
+
+
+def _chunk(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, z=FAKE, A=FAKE, beta=FAKE, cu=None, n=1, T=128, H=2, D=128, dt=0,
+             g_min=-5.0, init=None, o=FAKE, fin=None, ws=None, wsb=0, s=None)
+    a.update(kw)
+    return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["z"], a["A"], a["beta"], a["cu"], a["n"], a["T"],
+                             a["H"], a["D"], a["dt"], a["g_min"], a["init"], a["o"], a["fin"], a["ws"],
+                             a["wsb"], a["s"])
+
+
+def test_chunk_fwd_rejects_bad_arguments_before_launch():
+    lib = kda.load()
+    assert _chunk(lib, D=64) == kb.KDA_OK + 2                       # unsupported head dim
+    assert _chunk(lib, dt=7) == 1
+    assert _chunk(lib, H=0) == 1
+    assert _chunk(lib, g_min=-6.0) == 1                             # below the pages' bound
+    assert _chunk(lib, g_min=0.0) == 1
+    assert _chunk(lib, q=None) == 1
+    assert _chunk(lib, A=None) == 1
+    assert _chunk(lib, q=ctypes.c_void_p((1 << 20) + 2)) == 1       # misaligned
+    assert _chunk(lib, n=3, T=128) == 1                             # T not divisible without cu_seqlens
+    assert _chunk(lib, ws=None) == 5                                # no workspace
+    assert _chunk(lib, ws=ctypes.c_void_p(1 << 20), wsb=16) == 5    # too small
+
+
+def test_segment_scan_and_decode_reject_bad_arguments():
+    lib = kda.load()
+    r = lib.kda_segment_scan(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 128, 2, 128, 0, -5.0, None, 0,
+                             None, None, FAKE, None, None, 0, None)
+    assert r == 1  # zero segments
+    r = lib.kda_segment_scan(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 128, 2, 96, 0, -5.0, None, 4,
+                             None, None, FAKE, None, None, 0, None)
+    assert r == 2
+    dec = lambda **kw: lib.kda_decode_step(
+        kw.get("state", FAKE), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, kw.get("cq", FAKE), FAKE, FAKE, FAKE,
+        FAKE, None, kw.get("N", 4), 2, kw.get("D", 128), kw.get("W", 5), 1, -5.0, FAKE, None, None)
+    assert dec(D=64) == 2
+    assert dec(W=9) == 1
+    assert dec(W=0) == 1
+    assert dec(N=0) == 1
+    assert dec(state=None) == 1
+    assert dec(cq=None) == 1
+
+
+def test_binding_rejects_wrong_dtypes_on_cpu_tensors():
+    import torch
+    q = torch.zeros(4, 1, 128, dtype=torch.float16)
+    with pytest.raises(kda.KDAError):
+        kb._dtype_code(q)

@@ -1,0 +1,135 @@
+"""Parity of kda_chunk_fwd (CUDA, through the C ABI) with the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import kda_synth
+import linear_attention_serving_gb300 as kda
+import oracle
+from kda_testutil import TOL, rel_fro, to_dev
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run_both(inp, n_seqs=1):
+    d = to_dev(inp, DEV)
+    o, fin = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"],
+                           cu_seqlens=d["cu_seqlens"], init_state=d["init_state"], n_seqs=n_seqs)
+    torch.cuda.synchronize()
+    cu = inp["cu_seqlens"]
+    if cu is None and n_seqs > 1:
+        T = inp["q"].shape[0]
+        cu = torch.arange(0, T + 1, T // n_seqs, dtype=torch.int32)
+    o_ref, f_ref = oracle.recurrent(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"],
+                                    cu_seqlens=cu, init_state=inp["init_state"])
+    return o, fin, o_ref, f_ref
+
+
+def check(o, fin, o_ref, f_ref, dtype):
+    to, tf = TOL[dtype]
+    eo, ef = rel_fro(o, o_ref), rel_fro(fin, f_ref)
+    assert np.isfinite(eo) and np.isfinite(ef)
+    assert eo <= to, f"o rel err {eo:.3e} > {to}"
+    assert ef <= tf, f"final_state rel err {ef:.3e} > {tf}"
+    return eo, ef
+
+
+def test_tiny_fp32_workload():
+    """B=1, H=2, T=256, fp32, z~N(0,1), A=0, zero init, seed 0."""
+    inp = kda_synth.workload_inputs("tiny_fp32")
+    check(*run_both(inp), "f32")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 200, 333])
+def test_ragged_lengths(dtype, T):
+    inp = kda_synth.prefill_inputs(T, 3, dtype, seed=100 + T, z_std=1.5, A_std=0.5, init_std=0.05)
+    check(*run_both(inp), dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_slow_decay_carries_state_across_chunks(dtype):
+    """z ~ N(-10, 1): g ~ -2e-4 per token, small beta: the state entering a chunk
+    dominates its outputs, so the inter-chunk path is exercised (not washed out)."""
+    inp = kda_synth.prefill_inputs(700, 2, dtype, seed=7, z_mean=-10.0, beta_mean=-4.0, init_std=0.5)
+    check(*run_both(inp), dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gate_at_lower_bound(dtype):
+    """z ~ N(8, 1): g close to g_min = -5 everywhere; the 16-token sub-tile factors
+    reach e^{+-80} and must stay finite."""
+    inp = kda_synth.prefill_inputs(256, 2, dtype, seed=8, z_mean=8.0, init_std=0.05)
+    check(*run_both(inp), dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_packed_documents_with_empty_and_short_docs(dtype):
+    lens = [100, 0, 1, 64, 130, 0, 77]
+    cu = kda_synth.cu_from_lengths(lens)
+    inp = kda_synth.prefill_inputs(sum(lens), 2, dtype, seed=9, cu_seqlens=cu, init_std=0.05)
+    check(*run_both(inp), dtype)
+
+
+def test_equal_length_batch_without_cu_seqlens():
+    inp = kda_synth.prefill_inputs(4 * 96, 2, "bf16", seed=10, init_std=0.05, n_init=4)
+    check(*run_both(inp, n_seqs=4), "bf16")
+
+
+def test_prefill_h16_t8k_full_size():
+    """Full size prefill: B=1, H=16, T=8192, bf16, z~N(0,1.5), A~N(0,0.5)."""
+    inp = kda_synth.workload_inputs("prefill_h16_t8k")
+    eo, ef = check(*run_both(inp), "bf16")
+    print(f"prefill_h16_t8k: o {eo:.3e}, final_state {ef:.3e}")
+
+
+def test_varlen_32k_h32_full_size():
+    inp = kda_synth.workload_inputs("varlen_32k_h32")
+    eo, ef = check(*run_both(inp), "bf16")
+    print(f"varlen_32k_h32: o {eo:.3e}, final_state {ef:.3e}")
+
+
+def test_bitwise_deterministic():
+    inp = to_dev(kda_synth.prefill_inputs(1000, 4, "bf16", seed=11, init_std=0.05), DEV)
+    a = kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"], init_state=inp["init_state"])
+    b = kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"], init_state=inp["init_state"])
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_linearity_in_values_and_initial_state():
+    """o and S are linear in (V, S0) for fixed q, k, z, beta."""
+    base = kda_synth.prefill_inputs(300, 2, "f32", seed=12, init_std=0.1)
+    other = kda_synth.prefill_inputs(300, 2, "f32", seed=13, init_std=0.1)
+    d = to_dev(base, DEV)
+    v2, s2 = other["v"].to(DEV), other["init_state"].to(DEV)
+    f = lambda v, s: kda.chunk_fwd(d["q"], d["k"], v, d["z"], d["A"], d["beta"], init_state=s)
+    o1, f1 = f(d["v"], d["init_state"])
+    o2, f2 = f(v2, s2)
+    o3, f3 = f(d["v"] + v2, d["init_state"] + s2)
+    assert rel_fro(o3, o1 + o2) < 1e-5 and rel_fro(f3, f1 + f2) < 1e-5
+
+
+def test_resume_from_final_state():
+    inp = kda_synth.prefill_inputs(640, 2, "f32", seed=14, init_std=0.1)
+    d = to_dev(inp, DEV)
+    o, f = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], init_state=d["init_state"])
+    t = 192
+    sl = lambda x, a, b: x[a:b].contiguous()
+    oa, fa = kda.chunk_fwd(*(sl(d[n], 0, t) for n in ("q", "k", "v", "z")), d["A"], sl(d["beta"], 0, t),
+                           init_state=d["init_state"])
+    ob, fb = kda.chunk_fwd(*(sl(d[n], t, 640) for n in ("q", "k", "v", "z")), d["A"], sl(d["beta"], t, 640),
+                           init_state=fa)
+    assert rel_fro(torch.cat([oa, ob]), o) < 1e-5 and rel_fro(fb, f) < 1e-5
+
+
+def test_invalid_cu_seqlens_is_reported_on_device():
+    inp = to_dev(kda_synth.prefill_inputs(256, 1, "bf16", seed=15), DEV)
+    bad = torch.tensor([0, 200, 100, 256], dtype=torch.int32, device=DEV)  # decreasing
+    ws = torch.empty(kda.chunk_fwd_workspace_size(256, 1, 3), dtype=torch.uint8, device=DEV)
+    o = torch.full_like(inp["q"], 7.0)
+    fin_sentinel = None
+    kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"], cu_seqlens=bad,
+                  workspace=ws, out=o, output_final_state=False)
+    assert kda.read_device_error(ws) & 1
+    assert torch.all(o == 7.0)  # nothing written

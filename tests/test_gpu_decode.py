@@ -1,0 +1,78 @@
+"""Parity of kda_decode_step (CUDA, through the C ABI) with the fp64 oracle."""
+import pytest
+import torch
+
+import kda_synth
+import linear_attention_serving_gb300 as kda
+import oracle
+from kda_testutil import TOL, rel_fro
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def empty_cache(N, W, H, dtype):
+    t = kda_synth.TORCH_DTYPE[dtype]
+    z = lambda: torch.zeros((N, W - 1, H, 128), dtype=t, device=DEV)
+    return (z(), z(), z(), torch.zeros((N, W - 1, H, 128), device=DEV),
+            torch.zeros((N, W - 1, H), device=DEV))
+
+
+def run_steps(N, H, W, dtype, steps, seed, sample=None, A_std=0.5):
+    state = kda_synth.decode_state(N, H, seed, std=0.05, device=DEV)
+    A = kda_synth.decode_A(H, seed, A_std=A_std, device=DEV)
+    cache = empty_cache(N, W, H, dtype)
+    ref_state = state.cpu()
+    ref_cache = tuple(c.cpu() for c in cache)
+    idx = torch.arange(N) if sample is None else torch.tensor(sample)
+    ref_state = ref_state[idx]
+    ref_cache = tuple(c[idx] for c in ref_cache)
+    tol_o, tol_s = (1e-4, 1e-4) if dtype == "f32" else TOL["bf16"]
+    for step in range(steps):
+        w = kda_synth.decode_window(N, W, H, step, seed, dtype, z_std=1.5, device=DEV)
+        nacc = None if step == 0 else w["num_accepted"]
+        o = kda.decode_step(state, w["q"], w["k"], w["v"], w["z"], w["beta"], A, cache, num_accepted=nacc)
+        torch.cuda.synchronize()
+        sel = lambda x: x.cpu()[idx]
+        o_ref, ref_state, ref_cache = oracle.decode_step(
+            ref_state, sel(w["q"]), sel(w["k"]), sel(w["v"]), sel(w["z"]), sel(w["beta"]), A.cpu(),
+            *ref_cache, num_accepted=None if nacc is None else sel(nacc))
+        assert rel_fro(o.cpu()[idx], o_ref) <= tol_o, f"step {step}: o"
+        assert rel_fro(state.cpu()[idx], ref_state) <= tol_s, f"step {step}: state"
+        for c, rc in zip(cache, ref_cache):
+            assert torch.equal(c.cpu()[idx].double(), torch.from_numpy(rc)), f"step {step}: cache"
+    return state
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_steps_small(dtype):
+    run_steps(N=7, H=3, W=5, dtype=dtype, steps=4, seed=40)
+
+
+@pytest.mark.parametrize("W", [1, 2, 8])
+def test_decode_window_sizes(W):
+    run_steps(N=5, H=2, W=W, dtype="f32", steps=3, seed=41 + W)
+
+
+def test_decode_mtp_b256_h96_full_size():
+    """N=256, H=96, W=5 (1 + 4 drafts), fp32: full-size launch, sampled sequences
+    checked against the oracle over several steps."""
+    run_steps(N=256, H=96, W=5, dtype="f32", steps=3, seed=5, sample=[0, 1, 77, 128, 200, 255],
+              A_std=0.0)
+
+
+def test_num_accepted_out_of_range_sets_error_and_skips():
+    N, H, W = 4, 2, 5
+    state = kda_synth.decode_state(N, H, 50, device=DEV)
+    before = state.clone()
+    A = torch.zeros(H, device=DEV)
+    cache = empty_cache(N, W, H, "f32")
+    w = kda_synth.decode_window(N, W, H, 0, 50, "f32", device=DEV)
+    nacc = torch.tensor([0, 9, -1, 4], dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda.decode_step(state, w["q"], w["k"], w["v"], w["z"], w["beta"], A, cache, num_accepted=nacc,
+                    error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 2
+    assert torch.equal(state[1], before[1]) and torch.equal(state[2], before[2])
+    assert not torch.equal(state[0], before[0])
