@@ -24,6 +24,19 @@ void prof_mark(const char *name, cudaStream_t s) {
 }  // namespace
 
 namespace kda {
+// SM count of the current device, queried once per device.
+int device_sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
 void note_launch(const char *name, cudaStream_t s) {
     __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
     prof_mark(name, s);
@@ -54,6 +67,13 @@ int check_prefill(const void *q, const void *k, const void *v, const float *z, c
     // the chunk count must fit an int
     if ((int64_t)(T_total / C + n_seqs) >= (int64_t)INT32_MAX / 2) return KDA_ERR_INVALID_ARG;
     return KDA_OK;
+}
+
+// Scan launch by input type: tcgen05 tensor cores for bf16 operands, exact
+// fp32 CUDA cores for fp32 inputs.
+int launch_scan(const ScanArgs &a, int dtype, cudaStream_t s) {
+    if (dtype == KDA_BF16) return launch_scan_tc(a, device_sm_count(), s);
+    return launch_scan_simt(a, dtype, s);
 }
 
 // Chunk plan: arithmetic for equal-length documents, a device table otherwise.
@@ -169,7 +189,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *z, c
     a.init_state = init_state;
     a.o = o;
     a.final_state = final_state;
-    return launch_scan_simt(a, dtype, s);
+    return launch_scan(a, dtype, s);
 }
 
 int kda_segment_scan(const void *q, const void *k, const void *v, const float *z, const float *A,
@@ -206,7 +226,7 @@ int kda_segment_scan(const void *q, const void *k, const void *v, const float *z
     // phase 1: pairs (M, S~) of every (head, segment) from zero / identity
     a.ncols = 2 * D;
     a.phase = 1;
-    if ((rc = launch_scan_simt(a, dtype, s))) return rc;
+    if ((rc = launch_scan(a, dtype, s))) return rc;
     // phase 2: entering states by sequential composition
     if ((rc = launch_compose(p, H, n_segments, pairs, s_enter, s))) return rc;
     // phase 3: every segment from its exact entering state
@@ -214,7 +234,7 @@ int kda_segment_scan(const void *q, const void *k, const void *v, const float *z
     a.phase = 3;
     a.o = o;
     a.final_state = final_state;
-    if ((rc = launch_scan_simt(a, dtype, s))) return rc;
+    if ((rc = launch_scan(a, dtype, s))) return rc;
     if ((rc = launch_empty_docs(p, H, init_state, final_state, s))) return rc;
     const size_t mat = sizeof(float) * (size_t)H * n_segments * D * D;
     if (pairs_M && (rc = cuda_status(cudaMemcpyAsync(pairs_M, pairs, mat, cudaMemcpyDeviceToDevice, s))))

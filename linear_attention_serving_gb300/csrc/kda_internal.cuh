@@ -217,6 +217,8 @@ constexpr int SCAN_DOCS = 0;
 constexpr int SCAN_SEGMENTS = 1;
 
 int launch_scan_simt(const ScanArgs &a, int dtype, cudaStream_t s);
+int launch_scan_tc(const ScanArgs &a, int n_sm, cudaStream_t s);
+int device_sm_count();
 int launch_compose(const Plan &p, int H, int n_seg, const float *pairs, float *s_enter,
                    cudaStream_t s);
 int launch_decode(float *state, const void *q, const void *k, const void *v, const float *z,
