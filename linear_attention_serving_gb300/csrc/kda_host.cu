@@ -69,6 +69,15 @@ int check_prefill(const void *q, const void *k, const void *v, const float *z, c
     return KDA_OK;
 }
 
+// Prep launch by input type: tcgen05 tensor cores for bf16 inputs, exact fp32
+// CUDA cores for fp32 inputs.
+int launch_prep(const void *q, const void *k, const void *v, const float *z, const float *A,
+                const float *beta, int H, int dtype, float g_min, const Plan &p, void *records,
+                cudaStream_t s) {
+    if (dtype == KDA_BF16) return launch_prep_tc(q, k, v, z, A, beta, H, g_min, p, records, device_sm_count(), s);
+    return launch_prep_simt(q, k, v, z, A, beta, H, dtype, g_min, p, records, s);
+}
+
 // Scan launch by input type: tcgen05 tensor cores for bf16 operands, exact
 // fp32 CUDA cores for fp32 inputs.
 int launch_scan(const ScanArgs &a, int dtype, cudaStream_t s) {
@@ -176,7 +185,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *z, c
     Plan p;
     if ((rc = make_plan(cu_seqlens, n_seqs, T_total, workspace, w, s, p))) return rc;
     void *records = (char *)workspace + w.off_rec;
-    if ((rc = launch_prep_simt(q, k, v, z, A, beta, H, dtype, g_min, p, records, s))) return rc;
+    if ((rc = launch_prep(q, k, v, z, A, beta, H, dtype, g_min, p, records, s))) return rc;
     ScanArgs a;
     memset(&a, 0, sizeof(a));
     a.plan = p;
@@ -210,7 +219,7 @@ int kda_segment_scan(const void *q, const void *k, const void *v, const float *z
     void *records = base + w.off_rec;
     float *pairs = (float *)(base + w.off_pairs);
     float *s_enter = (float *)(base + w.off_enter);
-    if ((rc = launch_prep_simt(q, k, v, z, A, beta, H, dtype, g_min, p, records, s))) return rc;
+    if ((rc = launch_prep(q, k, v, z, A, beta, H, dtype, g_min, p, records, s))) return rc;
 
     ScanArgs a;
     memset(&a, 0, sizeof(a));

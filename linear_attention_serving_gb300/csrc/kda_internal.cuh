@@ -104,15 +104,24 @@ __host__ __device__ __forceinline__ void segment_range(int n, int nseg, int i, i
 //   [0, 32768)      A1 = [W ; Q'] 128 x 128 bf16, K-major, 128B-swizzled,
 //                   two 64-column k-blocks of 128 rows x 128 B
 //   [32768, 49152)  K_restore^T 128 (channel) x 64 (token) bf16, K-major, 128B-swizzled
-//   [49152, 65536)  U0 [64 tok][128] bf16 row-major
-//   [65536, 81920)  O0 [64 tok][128] bf16 row-major
-//   [81920, 82432)  a_C [128] fp32
+//   [49152, 49664)  a_C [128] fp32
+//   [49664, 66048)  U0 in 16-column slices: [8][64 tok][16] bf16
+//   [66048, 82432)  O0 in 16-column slices: [8][64 tok][16] bf16
+// The first 49664 bytes are what every state column needs; a block that owns
+// columns [16 s, 16 (s + n)) copies n adjacent 2 KB slices of U0 and of O0.
 constexpr size_t REC_BF16_A1 = 0;
 constexpr size_t REC_BF16_KRT = 32768;
-constexpr size_t REC_BF16_U0 = 49152;
-constexpr size_t REC_BF16_O0 = 65536;
-constexpr size_t REC_BF16_AC = 81920;
+constexpr size_t REC_BF16_AC = 49152;
+constexpr size_t REC_BF16_SHARED = 49664;
+constexpr size_t REC_BF16_U0 = 49664;
+constexpr size_t REC_BF16_O0 = 66048;
+constexpr size_t REC_BF16_SLICE = 2048;
 constexpr size_t REC_BF16_BYTES = 82432;
+
+// Byte offset of U0 / O0 element (token r, column col) inside its region.
+__host__ __device__ __forceinline__ uint32_t slice_offset(int r, int col) {
+    return (uint32_t)((col >> 4) * REC_BF16_SLICE + r * 32 + (col & 15) * 2);
+}
 
 // fp32 record of one (chunk, head), plain row-major, for the exact path.
 //   W, Q', K_restore, U0, O0: [64][128] fp32 each;  a_C [128] fp32
@@ -216,6 +225,9 @@ struct ScanArgs {
 constexpr int SCAN_DOCS = 0;
 constexpr int SCAN_SEGMENTS = 1;
 
+int launch_prep_tc(const void *q, const void *k, const void *v, const float *z, const float *A,
+                   const float *beta, int H, float g_min, const Plan &p, void *records, int n_sm,
+                   cudaStream_t s);
 int launch_scan_simt(const ScanArgs &a, int dtype, cudaStream_t s);
 int launch_scan_tc(const ScanArgs &a, int n_sm, cudaStream_t s);
 int device_sm_count();

@@ -326,9 +326,9 @@ prep_simt_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const InT
                     *reinterpret_cast<const uint4 *>(bw);
                 *reinterpret_cast<uint4 *>(rec + REC_BF16_A1 + sw128_offset(64 + r, c0, 128)) =
                     *reinterpret_cast<const uint4 *>(bq);
-                *reinterpret_cast<uint4 *>(rec + REC_BF16_U0 + (size_t)(r * D + c0) * 2) =
+                *reinterpret_cast<uint4 *>(rec + REC_BF16_U0 + slice_offset(r, c0)) =
                     *reinterpret_cast<const uint4 *>(bu);
-                *reinterpret_cast<uint4 *>(rec + REC_BF16_O0 + (size_t)(r * D + c0) * 2) =
+                *reinterpret_cast<uint4 *>(rec + REC_BF16_O0 + slice_offset(r, c0)) =
                     *reinterpret_cast<const uint4 *>(bo);
             } else {
                 float *W = reinterpret_cast<float *>(rec + REC_F32_W) + r * D + c0;

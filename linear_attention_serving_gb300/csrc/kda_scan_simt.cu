@@ -66,13 +66,13 @@ __device__ __forceinline__ void load_record(const char *rec, float *a1, float *k
 template <bool BF16_REC>
 __device__ __forceinline__ float rec_u0(const char *rec, int r, int col) {
     if (BF16_REC)
-        return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(rec + REC_BF16_U0)[r * 128 + col]);
+        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(rec + REC_BF16_U0 + slice_offset(r, col)));
     return reinterpret_cast<const float *>(rec + REC_F32_U0)[r * 128 + col];
 }
 template <bool BF16_REC>
 __device__ __forceinline__ float rec_o0(const char *rec, int r, int col) {
     if (BF16_REC)
-        return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(rec + REC_BF16_O0)[r * 128 + col]);
+        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(rec + REC_BF16_O0 + slice_offset(r, col)));
     return reinterpret_cast<const float *>(rec + REC_F32_O0)[r * 128 + col];
 }
 

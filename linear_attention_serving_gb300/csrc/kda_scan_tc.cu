@@ -30,12 +30,17 @@ namespace {
 
 using namespace tc;
 
-constexpr int STAGE_BYTES = 49152;  // A1 image (32 KB) + K_restore^T image (16 KB)
 constexpr int CONSUMERS = 128;
 constexpr int THREADS = CONSUMERS + 32;
 
+// One pipeline stage: the shared part of a record (A1, K_restore^T, a_C) and
+// this block's U0 / O0 column slices.
 template <int N>
 struct TcSmem {
+    static constexpr int NS = N / 16;                          // 16-column slices
+    static constexpr int U0 = (int)REC_BF16_SHARED;            // stage offset of the U0 slices
+    static constexpr int O0 = U0 + NS * (int)REC_BF16_SLICE;   // stage offset of the O0 slices
+    static constexpr int STAGE = ((O0 + NS * (int)REC_BF16_SLICE) + 1023) / 1024 * 1024;
     static constexpr int SOP = 2 * N * 128;  // S^T operand: 2 k-blocks x N rows x 128 B
     static constexpr int UOP = N * 128;      // U^T operand: 1 k-block x N rows x 128 B
     static constexpr int NCOLS = (2 * N <= 32) ? 32 : (2 * N <= 64 ? 64 : (2 * N <= 128 ? 128 : 256));
@@ -43,7 +48,7 @@ struct TcSmem {
 
 template <int N, int STAGES>
 constexpr size_t scan_tc_smem_bytes() {
-    return (size_t)STAGES * STAGE_BYTES + TcSmem<N>::SOP + TcSmem<N>::UOP + 1024;
+    return (size_t)STAGES * TcSmem<N>::STAGE + TcSmem<N>::SOP + TcSmem<N>::UOP + 1024;
 }
 
 __device__ __forceinline__ float state_init(const ScanArgs &a, int unit, int h, int r, int g) {
@@ -68,11 +73,12 @@ __device__ __forceinline__ void write_sop(uint8_t *sop, int t, const float *s) {
         *reinterpret_cast<__nv_bfloat16 *>(sop + sw128_offset(n, t, N)) = __float2bfloat16_rn(s[n]);
 }
 
+// N bf16 values of token row r from consecutive 16-column slices (2 KB apart)
 template <int N>
-__device__ __forceinline__ void load_row_bf16(const char *src, float *out) {
+__device__ __forceinline__ void load_row_slices(const uint8_t *base, int r, float *out) {
 #pragma unroll
     for (int j = 0; j < N; j += 8) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(src + j * 2);
+        const uint4 u = *reinterpret_cast<const uint4 *>(base + slice_offset(r, j));
         const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -105,6 +111,7 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
     }
     const int nchunks = c1 - c0;
 
+    constexpr int STAGE_BYTES = TcSmem<N>::STAGE;
     uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
     uint8_t *sop = sm + STAGES * STAGE_BYTES;
     uint8_t *uop = sop + TcSmem<N>::SOP;
@@ -138,9 +145,16 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
                 const uint32_t ph = (uint32_t)((i / STAGES) & 1);
                 if (!mbar_wait(&empty_bar[stage], ph ^ 1u)) { timed_out = true; break; }
                 if (*(volatile int *)&abort_flag) break;
-                mbar_expect_tx(&full_bar[stage], STAGE_BYTES);
-                bulk_g2s(sm + stage * STAGE_BYTES, records + (size_t)(c0 + i) * rec_stride + (size_t)h * REC_BF16_BYTES,
-                         STAGE_BYTES, &full_bar[stage]);
+                const char *rec = records + (size_t)(c0 + i) * rec_stride + (size_t)h * REC_BF16_BYTES;
+                uint8_t *st = sm + stage * STAGE_BYTES;
+                const uint32_t slices = value_cols ? (uint32_t)(TcSmem<N>::NS * REC_BF16_SLICE) : 0u;
+                mbar_expect_tx(&full_bar[stage], (uint32_t)REC_BF16_SHARED + 2u * slices);
+                bulk_g2s(st, rec, (uint32_t)REC_BF16_SHARED, &full_bar[stage]);
+                if (value_cols) {
+                    const size_t so = (size_t)(col0 / 16) * REC_BF16_SLICE;
+                    bulk_g2s(st + TcSmem<N>::U0, rec + REC_BF16_U0 + so, slices, &full_bar[stage]);
+                    bulk_g2s(st + TcSmem<N>::O0, rec + REC_BF16_O0 + so, slices, &full_bar[stage]);
+                }
                 issued = i + 1;
             }
             if (timed_out || *(volatile int *)&abort_flag) {
@@ -168,34 +182,15 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
         fence_async_smem();
         bool aborted = bar_or(1, CONSUMERS, false);
 
-        // per-chunk values of the next chunk, loaded one chunk ahead
         ChunkInfo ci_next;
-        float x_next[N];  // U0 row (t < 64) or O0 row (t >= 64)
-        float ac_next = 0.f;
-        auto prefetch = [&](int c) {
-            ci_next = plan_chunk(p, c);
-            const char *rec = records + (size_t)c * rec_stride + (size_t)h * REC_BF16_BYTES;
-            ac_next = reinterpret_cast<const float *>(rec + REC_BF16_AC)[t];
-            if (value_cols) {
-                const size_t off = t < C ? REC_BF16_U0 + ((size_t)t * D + col0) * 2
-                                         : REC_BF16_O0 + ((size_t)(t - C) * D + col0) * 2;
-                load_row_bf16<N>(rec + off, x_next);
-            } else {
-#pragma unroll
-                for (int j = 0; j < N; ++j) x_next[j] = 0.f;
-            }
-        };
-        if (nchunks > 0) prefetch(c0);
+        if (nchunks > 0) ci_next = plan_chunk(p, c0);
 
         constexpr uint32_t IDESC = idesc_bf16_f32(128, N);
         for (int i = 0; i < nchunks && !aborted; ++i) {
             const int stage = i % STAGES;
             const uint32_t ph = (uint32_t)((i / STAGES) & 1);
             const ChunkInfo ci = ci_next;
-            float x[N];
-#pragma unroll
-            for (int j = 0; j < N; ++j) x[j] = x_next[j];
-            const float ac = ac_next;
+            if (i + 1 < nchunks) ci_next = plan_chunk(p, c0 + i + 1);
             if (a.mode == SCAN_SEGMENTS && (ci.flags & CHUNK_FIRST)) {
                 // a document starts here: the state restarts (uniform branch)
 #pragma unroll
@@ -221,9 +216,18 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
                 }
             }
             // ---- D1 -> U (rows 0..63), O (rows 64..127)
-            const bool ok1 = !bad && mbar_wait(&mma1_bar, (uint32_t)(i & 1));
+            const bool ok1 = !bad && mbar_wait(&mma1_bar, (uint32_t)(i & 1)) && mbar_wait(&full_bar[stage], ph);
             __syncwarp();
             tc_fence_after();
+            // everything this thread needs from the stage, read before the stage is released
+            const uint8_t *stg = sm + stage * STAGE_BYTES;
+            const float ac = reinterpret_cast<const float *>(stg + REC_BF16_AC)[t];
+            float x[N];
+            if (value_cols)
+                load_row_slices<N>(stg + (t < C ? TcSmem<N>::U0 : TcSmem<N>::O0), t < C ? t : t - C, x);
+            else
+#pragma unroll
+                for (int j = 0; j < N; ++j) x[j] = 0.f;
             float d[N];
 #pragma unroll
             for (int j = 0; j < N; j += 16) tmem_ld16(tmem_d1 + lane_off + j, d + j);
@@ -249,7 +253,7 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
             // ---- D2 = K_restore^T U
             if (t == 0) {
                 tc_fence_after();
-                uint8_t *kr = sm + stage * STAGE_BYTES + 32768;
+                uint8_t *kr = sm + stage * STAGE_BYTES + REC_BF16_KRT;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const uint64_t ad = sdesc_sw128(smem_u32(kr + k * 32));
@@ -259,7 +263,6 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
                 mma_commit(&mma2_bar);
                 mma_commit(&empty_bar[stage]);
             }
-            if (i + 1 < nchunks) prefetch(c0 + i + 1);
             const bool ok2 = mbar_wait(&mma2_bar, (uint32_t)(i & 1));
             __syncwarp();
             tc_fence_after();
@@ -317,7 +320,7 @@ int launch_scan_tc(const ScanArgs &a, int n_sm, cudaStream_t s) {
     // SMs.  Many: wider blocks, two per SM, amortise the per-chunk latency.
     const long long slices16 = (long long)a.n_units * a.H * (a.ncols / 16);
     if (slices16 <= 2LL * n_sm) return launch_n<16, 3>(a, s);
-    return launch_n<32, 2>(a, s);
+    return launch_n<64, 2>(a, s);
 }
 
 }  // namespace kda
