@@ -43,7 +43,10 @@ struct TcSmem {
     static constexpr int STAGE = ((O0 + NS * (int)REC_BF16_SLICE) + 1023) / 1024 * 1024;
     static constexpr int SOP = 2 * N * 128;  // S^T operand: 2 k-blocks x N rows x 128 B
     static constexpr int UOP = N * 128;      // U^T operand: 1 k-block x N rows x 128 B
-    static constexpr int NCOLS = (2 * N <= 32) ? 32 : (2 * N <= 64 ? 64 : (2 * N <= 128 ? 128 : 256));
+    // TMEM: D1 in P1 partial accumulators, D2 in P2 (independent MMA chains overlap)
+    static constexpr int P1 = 4, P2 = 2;
+    static constexpr int COLS = (P1 + P2) * N;
+    static constexpr int NCOLS = COLS <= 32 ? 32 : (COLS <= 64 ? 64 : (COLS <= 128 ? 128 : (COLS <= 256 ? 256 : 512)));
 };
 
 template <int N, int STAGES>
@@ -71,6 +74,25 @@ __device__ __forceinline__ void write_sop(uint8_t *sop, int t, const float *s) {
 #pragma unroll
     for (int n = 0; n < N; ++n)
         *reinterpret_cast<__nv_bfloat16 *>(sop + sw128_offset(n, t, N)) = __float2bfloat16_rn(s[n]);
+}
+
+// Sum of P partial accumulators (N columns each, N apart) of this thread's TMEM lane.
+template <int N, int P>
+__device__ __forceinline__ void tmem_sum(uint32_t taddr, float *out) {
+#pragma unroll
+    for (int j = 0; j < N; j += 16) {
+        float part[P][16];
+#pragma unroll
+        for (int pp = 0; pp < P; ++pp) tmem_ld16(taddr + pp * N + j, part[pp]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            float acc = part[0][e];
+#pragma unroll
+            for (int pp = 1; pp < P; ++pp) acc += part[pp][e];
+            out[j + e] = acc;
+        }
+    }
 }
 
 // N bf16 values of token row r from consecutive 16-column slices (2 KB apart)
@@ -133,7 +155,8 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    const uint32_t tmem_d1 = tmem, tmem_d2 = tmem + N;
+    constexpr int P1 = TcSmem<N>::P1, P2 = TcSmem<N>::P2;
+    const uint32_t tmem_d1 = tmem, tmem_d2 = tmem + P1 * N;
 
     if (warp == CONSUMERS / 32) {
         // ------------------------------------------------------------ producer
@@ -208,7 +231,7 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
                     for (int k = 0; k < 8; ++k) {
                         const uint64_t ad = sdesc_sw128(smem_u32(st + (k >> 2) * 16384 + (k & 3) * 32));
                         const uint64_t bd = sdesc_sw128(smem_u32(sop + (k >> 2) * (N * 128) + (k & 3) * 32));
-                        mma_bf16(tmem_d1, ad, bd, IDESC, k > 0);
+                        mma_bf16(tmem_d1 + (k % P1) * N, ad, bd, IDESC, k >= P1);
                     }
                     mma_commit(&mma1_bar);
                 } else {
@@ -229,9 +252,7 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
 #pragma unroll
                 for (int j = 0; j < N; ++j) x[j] = 0.f;
             float d[N];
-#pragma unroll
-            for (int j = 0; j < N; j += 16) tmem_ld16(tmem_d1 + lane_off + j, d + j);
-            tmem_ld_wait();
+            tmem_sum<N, P1>(tmem_d1 + lane_off, d);
             if (t < C) {
 #pragma unroll
                 for (int n = 0; n < N; ++n)
@@ -258,7 +279,7 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
                 for (int k = 0; k < 4; ++k) {
                     const uint64_t ad = sdesc_sw128(smem_u32(kr + k * 32));
                     const uint64_t bd = sdesc_sw128(smem_u32(uop + k * 32));
-                    mma_bf16(tmem_d2, ad, bd, IDESC, k > 0);
+                    mma_bf16(tmem_d2 + (k % P2) * N, ad, bd, IDESC, k >= P2);
                 }
                 mma_commit(&mma2_bar);
                 mma_commit(&empty_bar[stage]);
@@ -266,9 +287,7 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
             const bool ok2 = mbar_wait(&mma2_bar, (uint32_t)(i & 1));
             __syncwarp();
             tc_fence_after();
-#pragma unroll
-            for (int j = 0; j < N; j += 16) tmem_ld16(tmem_d2 + lane_off + j, d + j);
-            tmem_ld_wait();
+            tmem_sum<N, P2>(tmem_d2 + lane_off, d);
 #pragma unroll
             for (int j = 0; j < N; ++j) s[j] = fmaf(ac, s[j], d[j]);
             write_sop<N>(sop, t, s);
