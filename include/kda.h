@@ -116,6 +116,38 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v,
                   void *workspace, size_t workspace_bytes, kda_stream_t stream);
 
 /* --------------------------------------------------------------------------
+ * kda_chunk_fwd_noalloc -- kda_chunk_fwd without a caller-provided workspace.
+ * The pages have no counterpart: this is an interface for callers that cannot
+ * allocate device memory at call time (an engine that reserved the whole
+ * device for its own pool, or a latency-critical path that cannot afford the
+ * device synchronisation a cudaMalloc may imply).
+ *
+ * Same arguments, checks and results as kda_chunk_fwd, without workspace and
+ * workspace_bytes.  The workspace is a fixed array of
+ * KDA_NOALLOC_SCRATCH_BYTES bytes in device global memory owned by the library
+ * (every GPU that loads the library holds it until exit); the call allocates
+ * nothing and calls no allocating routine.
+ *   - A call whose kda_chunk_fwd_workspace_size(T_total, H, n_seqs, dtype)
+ *     exceeds KDA_NOALLOC_SCRATCH_BYTES returns KDA_ERR_WORKSPACE before any
+ *     launch (about 800 (chunk, head) pairs in bf16, 400 in fp32).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call uses the same array: calls whose executions overlap on the
+ *     GPU race.  Order them, e.g. by issuing them on one stream.
+ *   - Device-side errors (bad cu_seqlens) are recorded in the array's first
+ *     word, which the next call clears.
+ * ------------------------------------------------------------------------ */
+#define KDA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+
+int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                          const float *z, const float *A, const float *beta,
+                          const int32_t *cu_seqlens, int n_seqs,
+                          int64_t T_total, int H, int D, int dtype, float g_min,
+                          const float *init_state, void *o, float *final_state,
+                          kda_stream_t stream);
+
+/* --------------------------------------------------------------------------
  * kda_segment_scan -- intra-device context parallelism over one long packed
  * token stream ("Kimi K3 模型结构（7）", section "KDA：三种执行形态" (SM-level
  * CP of long prefill), eq. (17) and "公式 (17) 的推导": segments are affine

@@ -1,0 +1,119 @@
+// kda_noalloc.cu -- kda_chunk_fwd for callers that cannot allocate device memory.
+//
+// Some callers have no way to obtain a device workspace at call time: an
+// engine that reserved the whole device for its own memory pool before this
+// library was loaded, or host code on a latency-critical path where a
+// cudaMalloc (which may synchronise the device) is not acceptable.  For them
+// kda_chunk_fwd_noalloc runs the same kernels as kda_chunk_fwd with the
+// workspace taken from a fixed array in device global memory that the library
+// module itself owns.  The array is KDA_NOALLOC_SCRATCH_BYTES long and every
+// GPU that loads the library holds it until the process exits.
+//
+// Nothing here allocates: the device address of the array is looked up once
+// per device (the first call on that device, with that device current) and
+// cached; every later call only launches kernels and issues one
+// cudaMemsetAsync of the workspace header.  All calls share the one array, so
+// calls whose executions overlap on the GPU race on it; the caller must order
+// them (for example by issuing them on one stream).
+#include <cstring>
+#include <mutex>
+
+#include "kda_internal.cuh"
+
+using namespace kda;
+
+namespace {
+
+// The scratch array.  In host code this name is only a stand-in for the
+// device symbol; kernels must be given the address cudaGetSymbolAddress returns.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int MAX_DEVICES = 64;
+void *g_scratch_addr[MAX_DEVICES] = {nullptr};
+std::mutex g_scratch_mu;
+
+// Device address of the scratch array on the current device, looked up once.
+int scratch_address(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KDA_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return KDA_OK;
+}
+
+bool aligned16(const void *p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+
+extern "C" int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *z,
+                                     const float *A, const float *beta, const int32_t *cu_seqlens,
+                                     int n_seqs, int64_t T_total, int H, int Dm, int dtype, float g_min,
+                                     const float *init_state, void *o, float *final_state,
+                                     kda_stream_t stream) {
+    // the same argument checks as kda_chunk_fwd
+    if (Dm != D) return KDA_ERR_UNSUPPORTED;
+    if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
+    if (H < 1 || n_seqs < 1 || T_total < 0 || T_total >= (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
+    if (!(g_min >= -5.0f && g_min < 0.0f)) return KDA_ERR_INVALID_ARG;
+    if (T_total > 0 && (!q || !k || !v || !z || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    if (!A) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens && (T_total % n_seqs) != 0) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(z) || !aligned16(o))
+        return KDA_ERR_INVALID_ARG;
+    if ((int64_t)(T_total / C + n_seqs) >= (int64_t)INT32_MAX / 2) return KDA_ERR_INVALID_ARG;
+    // the call must fit the fixed scratch array
+    const Workspace w = workspace_layout(T_total, H, n_seqs, 0, dtype);
+    if (w.total > (size_t)KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
+
+    void *ws = nullptr;
+    int rc = scratch_address(&ws);
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    note_begin(s);
+
+    // chunk plan; the header (error word, chunk count) is cleared because the
+    // array keeps whatever the previous call left in it
+    Plan p;
+    memset(&p, 0, sizeof(p));
+    char *base = (char *)ws;
+    p.n_seqs = n_seqs;
+    p.err = (int32_t *)base;
+    p.table = (const ChunkInfo *)(base + w.off_table);
+    p.doc_off = (const int32_t *)(base + w.off_doc);
+    p.n_chunks = (const int32_t *)(base + 4);
+    if (cudaMemsetAsync(base, 0, 8, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (!cu_seqlens) {
+        p.uniform = 1;
+        p.seq_len = (int)(T_total / n_seqs);
+        p.chunks_per_seq = (p.seq_len + C - 1) / C;
+        p.max_chunks = n_seqs * p.chunks_per_seq;
+    } else {
+        p.max_chunks = w.max_chunks;
+        if ((rc = launch_plan(cu_seqlens, n_seqs, T_total, ws, w, s))) return rc;
+    }
+
+    void *records = base + w.off_rec;
+    if (dtype == KDA_BF16)
+        rc = launch_prep_tc(q, k, v, z, A, beta, H, g_min, p, records, device_sm_count(), s);
+    else
+        rc = launch_prep_simt(q, k, v, z, A, beta, H, dtype, g_min, p, records, s);
+    if (rc) return rc;
+    ScanArgs a;
+    memset(&a, 0, sizeof(a));
+    a.plan = p;
+    a.H = H;
+    a.records = records;
+    a.mode = SCAN_DOCS;
+    a.n_units = n_seqs;
+    a.ncols = D;
+    a.phase = 0;
+    a.init_state = init_state;
+    a.o = o;
+    a.final_state = final_state;
+    return dtype == KDA_BF16 ? launch_scan_tc(a, device_sm_count(), s) : launch_scan_simt(a, dtype, s);
+}
