@@ -8,10 +8,13 @@
 // delta form of "Kimi K3: the Manos, the Mythos ..." (SemiAnalysis),
 // "FlashKDA 算法":  S <- D_t S;  u = beta (v - S^T k);  S <- S + k u^T;  o = S^T q.
 //
-// Mapping: one block per (sequence b, head h); thread (column j, part p) keeps
-// rows [p*R, p*R + R) of state column j in registers, so the d_k reductions
-// are a register sum plus one shuffle, and the fp32 state is read and written
-// exactly once per step with coalesced 64-byte row segments.
+// Mapping: persistent blocks walk the (sequence b, head h) items; thread
+// (column j, part p) keeps rows [p*R, p*R + R) of state column j in registers,
+// so the d_k reductions are a register sum plus one shuffle.  The fp32 state
+// is read and written exactly once per step.  While an item computes, one
+// thread has already started bulk copies (cp.async.bulk + mbarrier) of the
+// next item's state and token rows into shared memory, so the HBM stream
+// never waits for the arithmetic.
 //
 // The per-channel decay is applied lazily: with s_t = prod_{tau<=t} alpha_tau
 // (per row, over this step's tokens) the kernel keeps S = Diag(s_t) S^ and
@@ -21,19 +24,84 @@
 // 2W - 1 <= 15 tokens run per step, so s_t >= e^{5 * 15} = e^-75 stays a
 // normal fp32 number (bounded gate, "Kimi K3 模型结构（2）", "后果一").
 #include "kda_internal.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 
 namespace {
 
+using namespace tc;
+
 constexpr int MAX_W = 8;
-constexpr int MAX_TOK = 2 * MAX_W - 1;
 constexpr int DEC_TPC = 2;                  // threads per state column
 constexpr int DEC_R = D / DEC_TPC;          // rows per thread
 constexpr int DEC_THREADS = D * DEC_TPC;    // 256
 constexpr int VPAD = D + 4;                 // padded vector stride (second half shifted by 4)
+constexpr int ROW_SLOT = 4 * 512;           // raw bytes per token: q | k | v | z rows, 512 B each
 
 __device__ __forceinline__ int vidx(int r) { return r + (r >= DEC_R ? 4 : 0); }
+
+struct DecSmem {
+    int ntok_max;
+    size_t state, raw, kt, kh, qt, vt, total;
+    __host__ __device__ DecSmem(int W) {
+        ntok_max = 2 * W - 1;
+        state = 0;                                        // [128][128] fp32
+        raw = state + (size_t)D * D * 4;                  // [ntok][q | k | v | z]
+        kt = raw + (size_t)ntok_max * ROW_SLOT;           // s_t . k    [ntok][VPAD]
+        kh = kt + (size_t)ntok_max * VPAD * 4;            // k / s_t    [ntok][VPAD]
+        qt = kh + (size_t)ntok_max * VPAD * 4;            // s_t . q    [ntok][VPAD]
+        vt = qt + (size_t)ntok_max * VPAD * 4;            // v          [ntok][D]
+        total = vt + (size_t)ntok_max * D * 4;
+    }
+};
+
+// One thread starts the bulk copies of item `item` (its state and token rows)
+// into shared memory; completion is counted on `bar`.  `nacc` was read ahead of
+// time; when it is out of range nothing is copied and the barrier completes
+// without data.
+template <typename InT>
+__device__ __forceinline__ void issue_item(int item, int nacc, int H, int W, const float *__restrict__ state,
+                                           const InT *__restrict__ q, const InT *__restrict__ k,
+                                           const InT *__restrict__ v, const float *__restrict__ z,
+                                           const InT *__restrict__ ck, const InT *__restrict__ cv,
+                                           const float *__restrict__ cz, uint8_t *sm, const DecSmem &L,
+                                           uint64_t *bar) {
+    if (nacc < 0 || nacc > W - 1) {
+        mbar_arrive(bar);
+        return;
+    }
+    const int b = item / H, h = item - b * H;
+    const int ntok = nacc + W;
+    const uint32_t rowb = (uint32_t)(D * sizeof(InT));
+    const uint32_t bytes = (uint32_t)(D * D * 4) + (uint32_t)nacc * (2 * rowb + 512) + (uint32_t)W * (3 * rowb + 512);
+    mbar_expect_tx(bar, bytes);
+    bulk_g2s(sm + L.state, state + (size_t)item * D * D, D * D * 4, bar);
+    for (int t = 0; t < ntok; ++t) {
+        uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
+        if (t < nacc) {
+            const size_t row = ((size_t)b * (W - 1) + t) * H + h;
+            bulk_g2s(slot + 512, ck + row * D, rowb, bar);
+            bulk_g2s(slot + 1024, cv + row * D, rowb, bar);
+            bulk_g2s(slot + 1536, cz + row * D, 512, bar);
+        } else {
+            const size_t row = ((size_t)b * W + (t - nacc)) * H + h;
+            bulk_g2s(slot, q + row * D, rowb, bar);
+            bulk_g2s(slot + 512, k + row * D, rowb, bar);
+            bulk_g2s(slot + 1024, v + row * D, rowb, bar);
+            bulk_g2s(slot + 1536, z + row * D, 512, bar);
+        }
+    }
+}
+
+// beta of token slot t of item `item` for either accepted count: thread t < W-1
+// holds the cached draft's beta in `bc`, thread t < W the window's in `bw`.
+__device__ __forceinline__ void load_betas(int item, int H, int W, int tid, const float *__restrict__ beta,
+                                           const float *__restrict__ cb, float &bc, float &bw) {
+    const int b = item / H, h = item - b * H;
+    bc = (tid < W - 1) ? cb[((size_t)b * (W - 1) + tid) * H + h] : 0.f;
+    bw = (tid < W) ? beta[((size_t)b * W + tid) * H + h] : 0.f;
+}
 
 template <typename InT>
 __global__ void __launch_bounds__(DEC_THREADS, 2)
@@ -41,134 +109,175 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
               const InT *__restrict__ v, const float *__restrict__ z, const float *__restrict__ beta,
               const float *__restrict__ A, InT *__restrict__ cq, InT *__restrict__ ck,
               InT *__restrict__ cv, float *__restrict__ cz, float *__restrict__ cb,
-              const int32_t *__restrict__ nacc_p, int H, int W, float g_min, InT *__restrict__ o,
+              const int32_t *__restrict__ nacc_p, int N, int H, int W, float g_min, InT *__restrict__ o,
               int32_t *__restrict__ err) {
-    __shared__ __align__(16) float kt[MAX_TOK][VPAD];  // s_t . k
-    __shared__ __align__(16) float kh[MAX_TOK][VPAD];  // k / s_t
-    __shared__ __align__(16) float qt[MAX_TOK][VPAD];  // s_t . q
-    __shared__ float vt[MAX_TOK][D];
-    __shared__ float bt[MAX_TOK];
+    extern __shared__ __align__(128) uint8_t smdyn[];
+    __shared__ uint64_t full_bar;
+    __shared__ float sbeta[2][2 * MAX_W];
     __shared__ float scommit[VPAD];
 
-    const int bh = blockIdx.x;
-    const int b = bh / H, h = bh - b * H;
+    const DecSmem L(W);
+    uint8_t *sm = smdyn;
+    float *sS = reinterpret_cast<float *>(sm + L.state);
+    float(*kt)[VPAD] = reinterpret_cast<float(*)[VPAD]>(sm + L.kt);
+    float(*kh)[VPAD] = reinterpret_cast<float(*)[VPAD]>(sm + L.kh);
+    float(*qt)[VPAD] = reinterpret_cast<float(*)[VPAD]>(sm + L.qt);
+    float(*vt)[D] = reinterpret_cast<float(*)[D]>(sm + L.vt);
+
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int col = warp * (32 / DEC_TPC) + (lane & (32 / DEC_TPC - 1));
     const int part = lane / (32 / DEC_TPC);
     const int rbase = part * DEC_R;
+    const int n_items = N * H;
 
-    const int nacc = nacc_p ? nacc_p[b] : 0;
-    if (nacc < 0 || nacc > W - 1) {
-        if (tid == 0 && err) atomicOr(err, KDA_DEVERR_NUM_ACCEPTED);
-        return;
-    }
-    const int ntok = nacc + W;
-
-    // 1. issue the state loads first; they are in flight during the prologue
-    float *Sg = state + (size_t)bh * D * D;
-    float s[DEC_R];
-#pragma unroll
-    for (int i = 0; i < DEC_R; ++i) s[i] = Sg[(size_t)(rbase + i) * D + col];
-
-    // 2. token inputs: replayed drafts from the cache, then the window
-    const float eA = expf(A[h]);
-    for (int idx = tid; idx < ntok * D; idx += DEC_THREADS) {
-        const int t = idx >> 7, c = idx & 127;
-        size_t row;
-        float kk, qq, vv, zz;
-        if (t < nacc) {
-            row = ((size_t)b * (W - 1) + t) * H + h;
-            kk = to_f32(ck[row * D + c]);
-            qq = 0.f;
-            vv = to_f32(cv[row * D + c]);
-            zz = cz[row * D + c];
-        } else {
-            row = ((size_t)b * W + (t - nacc)) * H + h;
-            kk = to_f32(k[row * D + c]);
-            qq = to_f32(q[row * D + c]);
-            vv = to_f32(v[row * D + c]);
-            zz = z[row * D + c];
-        }
-        kt[t][vidx(c)] = kk;
-        qt[t][vidx(c)] = qq;
-        kh[t][vidx(c)] = expf(kda_gate(g_min, eA, zz));  // alpha, scaled below
-        vt[t][c] = vv;
-    }
-    if (tid < ntok) {
-        const int t = tid;
-        bt[t] = t < nacc ? cb[((size_t)b * (W - 1) + t) * H + h] : beta[((size_t)b * W + (t - nacc)) * H + h];
+    if (tid == 0) {
+        mbar_init(&full_bar, 1);
+        mbar_fence_init();
     }
     __syncthreads();
-    if (tid < D) {
-        const int c = vidx(tid);
-        float sc = 1.f;
+    int item = blockIdx.x;
+    // per-item scalars read one item ahead: accepted count and the betas
+    int nacc_cur = 0;
+    float bc_cur = 0.f, bw_cur = 0.f;
+    if (item < n_items) {
+        nacc_cur = nacc_p ? nacc_p[item / H] : 0;
+        load_betas(item, H, W, tid, beta, cb, bc_cur, bw_cur);
+        if (tid == 0) issue_item<InT>(item, nacc_cur, H, W, state, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
+    }
+    bool timed_out = false;
+    for (int it = 0; item < n_items; item += gridDim.x, ++it) {
+        const int b = item / H, h = item - b * H;
+        const int next = item + gridDim.x;
+        int nacc_next = 0;
+        float bc_next = 0.f, bw_next = 0.f;
+        if (next < n_items) {
+            nacc_next = nacc_p ? nacc_p[next / H] : 0;
+            load_betas(next, H, W, tid, beta, cb, bc_next, bw_next);
+        }
+        const int nacc = nacc_cur;
+        if (!mbar_wait(&full_bar, (uint32_t)(it & 1))) timed_out = true;
+        if (__syncthreads_or(timed_out)) {
+            if (tid == 0) atomicOr(err, KDA_DEVERR_TIMEOUT);
+            break;
+        }
+        if (nacc < 0 || nacc > W - 1) {
+            // out-of-range accepted count: this sequence is left untouched
+            if (tid == 0) {
+                atomicOr(err, KDA_DEVERR_NUM_ACCEPTED);
+                if (next < n_items)
+                    issue_item<InT>(next, nacc_next, H, W, state, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
+            }
+            nacc_cur = nacc_next;
+            bc_cur = bc_next;
+            bw_cur = bw_next;
+            continue;
+        }
+        const int ntok = nacc + W;
+        float *Sg = state + (size_t)item * D * D;
+        float *sbt = sbeta[it & 1];
+        if (tid < nacc) sbt[tid] = bc_cur;
+        if (tid < W) sbt[nacc + tid] = bw_cur;
+
+        // state and token rows of this item: shared memory -> registers / vectors
+        float s[DEC_R];
+#pragma unroll
+        for (int i = 0; i < DEC_R; ++i) s[i] = sS[(rbase + i) * D + col];
+        const float eA = expf(A[h]);
+        for (int idx = tid; idx < ntok * D; idx += DEC_THREADS) {
+            const int t = idx >> 7, c = idx & 127;
+            const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
+            const float qq = t < nacc ? 0.f : to_f32(reinterpret_cast<const InT *>(slot)[c]);
+            const float kk = to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
+            const float vv = to_f32(reinterpret_cast<const InT *>(slot + 1024)[c]);
+            const float zz = reinterpret_cast<const float *>(slot + 1536)[c];
+            kt[t][vidx(c)] = kk;
+            qt[t][vidx(c)] = qq;
+            kh[t][vidx(c)] = expf(kda_gate(g_min, eA, zz));  // alpha, scaled below
+            vt[t][c] = vv;
+            // the new drafts' projected inputs replace this sequence's cache slots
+            if (t > nacc) {
+                const size_t dst = (((size_t)b * (W - 1) + (t - nacc - 1)) * H + h) * D + c;
+                cq[dst] = reinterpret_cast<const InT *>(slot)[c];
+                ck[dst] = reinterpret_cast<const InT *>(slot + 512)[c];
+                cv[dst] = reinterpret_cast<const InT *>(slot + 1024)[c];
+                cz[dst] = zz;
+            }
+        }
+        __syncthreads();
+        if (tid < W - 1) cb[((size_t)b * (W - 1) + tid) * H + h] = sbt[nacc + 1 + tid];
+        // shared state and row buffers are free: start the next item's copies now
+        if (tid == 0 && next < n_items)
+            issue_item<InT>(next, nacc_next, H, W, state, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
+        if (tid < D) {
+            // cumulative decay s_t over the step's tokens, in registers
+            const int c = vidx(tid);
+            float sc = 1.f;
+            for (int t = 0; t < ntok; ++t) {
+                const float al = kh[t][c], kk = kt[t][c], qq = qt[t][c];
+                sc *= al;
+                const float inv = __frcp_rn(sc);
+                kt[t][c] = kk * sc;
+                kh[t][c] = kk * inv;
+                qt[t][c] = qq * sc;
+                if (t == nacc) scommit[c] = sc;
+            }
+        }
+        __syncthreads();
+
+        // the recurrence over replay + bonus + drafts
+        const float *bt = sbt;
         for (int t = 0; t < ntok; ++t) {
-            sc *= kh[t][c];
-            const float kk = kt[t][c];
-            kt[t][c] = kk * sc;
-            kh[t][c] = kk / sc;
-            qt[t][c] *= sc;
-            if (t == nacc) scommit[c] = sc;
-        }
-    }
-    __syncthreads();
-
-    // 3. the recurrence over replay + bonus + drafts
-    for (int t = 0; t < ntok; ++t) {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < DEC_R; i += 4) {
-            const float4 kv = *reinterpret_cast<const float4 *>(&kt[t][vidx(rbase + i)]);
-            acc = fmaf(s[i], kv.x, acc);
-            acc = fmaf(s[i + 1], kv.y, acc);
-            acc = fmaf(s[i + 2], kv.z, acc);
-            acc = fmaf(s[i + 3], kv.w, acc);
-        }
-#pragma unroll
-        for (int m = 32 / DEC_TPC; m < 32; m <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-        const float u = bt[t] * (vt[t][col] - acc);
-#pragma unroll
-        for (int i = 0; i < DEC_R; i += 4) {
-            const float4 kv = *reinterpret_cast<const float4 *>(&kh[t][vidx(rbase + i)]);
-            s[i] = fmaf(kv.x, u, s[i]);
-            s[i + 1] = fmaf(kv.y, u, s[i + 1]);
-            s[i + 2] = fmaf(kv.z, u, s[i + 2]);
-            s[i + 3] = fmaf(kv.w, u, s[i + 3]);
-        }
-        if (t >= nacc) {
-            float ao = 0.f;
+            // four independent partial sums keep the FMA chain short
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
             for (int i = 0; i < DEC_R; i += 4) {
-                const float4 qv = *reinterpret_cast<const float4 *>(&qt[t][vidx(rbase + i)]);
-                ao = fmaf(s[i], qv.x, ao);
-                ao = fmaf(s[i + 1], qv.y, ao);
-                ao = fmaf(s[i + 2], qv.z, ao);
-                ao = fmaf(s[i + 3], qv.w, ao);
+                const float4 kv = *reinterpret_cast<const float4 *>(&kt[t][vidx(rbase + i)]);
+                a0 = fmaf(s[i], kv.x, a0);
+                a1 = fmaf(s[i + 1], kv.y, a1);
+                a2 = fmaf(s[i + 2], kv.z, a2);
+                a3 = fmaf(s[i + 3], kv.w, a3);
             }
+            float acc = (a0 + a1) + (a2 + a3);
 #pragma unroll
-            for (int m = 32 / DEC_TPC; m < 32; m <<= 1) ao += __shfl_xor_sync(0xffffffffu, ao, m);
-            if (part == 0) o[(((size_t)b * W + (t - nacc)) * H + h) * D + col] = from_f32<InT>(ao);
-        }
-        if (t == nacc) {
-            // commit: S = Diag(s_t) S^, written back in place
+            for (int m = 32 / DEC_TPC; m < 32; m <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+            const float u = bt[t] * (vt[t][col] - acc);
 #pragma unroll
-            for (int i = 0; i < DEC_R; ++i)
-                Sg[(size_t)(rbase + i) * D + col] = s[i] * scommit[vidx(rbase + i)];
+            for (int i = 0; i < DEC_R; i += 4) {
+                const float4 kv = *reinterpret_cast<const float4 *>(&kh[t][vidx(rbase + i)]);
+                s[i] = fmaf(kv.x, u, s[i]);
+                s[i + 1] = fmaf(kv.y, u, s[i + 1]);
+                s[i + 2] = fmaf(kv.z, u, s[i + 2]);
+                s[i + 3] = fmaf(kv.w, u, s[i + 3]);
+            }
+            if (t >= nacc) {
+                float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+#pragma unroll
+                for (int i = 0; i < DEC_R; i += 4) {
+                    const float4 qv = *reinterpret_cast<const float4 *>(&qt[t][vidx(rbase + i)]);
+                    b0 = fmaf(s[i], qv.x, b0);
+                    b1 = fmaf(s[i + 1], qv.y, b1);
+                    b2 = fmaf(s[i + 2], qv.z, b2);
+                    b3 = fmaf(s[i + 3], qv.w, b3);
+                }
+                float ao = (b0 + b1) + (b2 + b3);
+#pragma unroll
+                for (int m = 32 / DEC_TPC; m < 32; m <<= 1) ao += __shfl_xor_sync(0xffffffffu, ao, m);
+                if (part == 0) o[(((size_t)b * W + (t - nacc)) * H + h) * D + col] = from_f32<InT>(ao);
+            }
+            if (t == nacc) {
+                // commit: S = Diag(s_t) S^, written back in place
+#pragma unroll
+                for (int i = 0; i < DEC_R; ++i)
+                    Sg[(size_t)(rbase + i) * D + col] = s[i] * scommit[vidx(rbase + i)];
+            }
         }
-    }
 
-    // 4. the new drafts' projected inputs replace the cache (all cache reads are done)
-    for (int idx = tid; idx < (W - 1) * D; idx += DEC_THREADS) {
-        const int j = idx >> 7, c = idx & 127;
-        const size_t src = (((size_t)b * W + (j + 1)) * H + h) * D + c;
-        const size_t dst = (((size_t)b * (W - 1) + j) * H + h) * D + c;
-        cq[dst] = q[src];
-        ck[dst] = k[src];
-        cv[dst] = v[src];
-        cz[dst] = z[src];
+        nacc_cur = nacc_next;
+        bc_cur = bc_next;
+        bw_cur = bw_next;
+        __syncthreads();  // vectors are rewritten by the next item
     }
-    if (tid < W - 1) cb[((size_t)b * (W - 1) + tid) * H + h] = beta[((size_t)b * W + tid + 1) * H + h];
 }
 
 }  // namespace
@@ -177,18 +286,32 @@ int launch_decode(float *state, const void *q, const void *k, const void *v, con
                   const float *beta, const float *A, void *cq, void *ck, void *cv, float *cz,
                   float *cb, const int32_t *nacc, int N, int H, int W, int dtype, float g_min,
                   void *o, int32_t *err, cudaStream_t s) {
-    const int64_t blocks = (int64_t)N * H;
-    if (blocks <= 0) return KDA_OK;
+    const long long items = (long long)N * H;
+    if (items <= 0) return KDA_OK;
     if (W > MAX_W) return KDA_ERR_UNSUPPORTED;
+    const DecSmem L(W);
+    const int smem = (int)L.total;
+    int per_sm = 1, n_sm = device_sm_count();
+    int grid;
     if (dtype == KDA_BF16) {
-        decode_kernel<__nv_bfloat16><<<(unsigned)blocks, DEC_THREADS, 0, s>>>(
-            state, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, z, beta,
-            A, (__nv_bfloat16 *)cq, (__nv_bfloat16 *)ck, (__nv_bfloat16 *)cv, cz, cb, nacc, H, W, g_min,
+        auto kern = decode_kernel<__nv_bfloat16>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DEC_THREADS, smem);
+        grid = (int)(items < (long long)n_sm * (per_sm > 0 ? per_sm : 1) ? items : (long long)n_sm * (per_sm > 0 ? per_sm : 1));
+        kern<<<grid, DEC_THREADS, smem, s>>>(
+            state, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, z, beta, A,
+            (__nv_bfloat16 *)cq, (__nv_bfloat16 *)ck, (__nv_bfloat16 *)cv, cz, cb, nacc, N, H, W, g_min,
             (__nv_bfloat16 *)o, err);
     } else {
-        decode_kernel<float><<<(unsigned)blocks, DEC_THREADS, 0, s>>>(
-            state, (const float *)q, (const float *)k, (const float *)v, z, beta, A, (float *)cq,
-            (float *)ck, (float *)cv, cz, cb, nacc, H, W, g_min, (float *)o, err);
+        auto kern = decode_kernel<float>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DEC_THREADS, smem);
+        grid = (int)(items < (long long)n_sm * (per_sm > 0 ? per_sm : 1) ? items : (long long)n_sm * (per_sm > 0 ? per_sm : 1));
+        kern<<<grid, DEC_THREADS, smem, s>>>(state, (const float *)q, (const float *)k, (const float *)v, z,
+                                             beta, A, (float *)cq, (float *)ck, (float *)cv, cz, cb, nacc, N,
+                                             H, W, g_min, (float *)o, err);
     }
     note_launch("decode", s);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
