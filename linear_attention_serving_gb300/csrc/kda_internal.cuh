@@ -100,27 +100,33 @@ __host__ __device__ __forceinline__ void segment_range(int n, int nseg, int i, i
 }
 
 // ---------------------------------------------------------------- records
-// bf16 record of one (chunk, head): operand images ready for tcgen05.
-//   [0, 32768)      A1 = [W ; Q'] 128 x 128 bf16, K-major, 128B-swizzled,
-//                   two 64-column k-blocks of 128 rows x 128 B
-//   [32768, 49152)  K_restore^T 128 (channel) x 64 (token) bf16, K-major, 128B-swizzled
-//   [49152, 49664)  a_C [128] fp32
-//   [49664, 66048)  U0 in 16-column slices: [8][64 tok][16] bf16
-//   [66048, 82432)  O0 in 16-column slices: [8][64 tok][16] bf16
-// The first 49664 bytes are what every state column needs; a block that owns
-// columns [16 s, 16 (s + n)) copies n adjacent 2 KB slices of U0 and of O0.
-constexpr size_t REC_BF16_A1 = 0;
-constexpr size_t REC_BF16_KRT = 32768;
-constexpr size_t REC_BF16_AC = 49152;
-constexpr size_t REC_BF16_SHARED = 49664;
-constexpr size_t REC_BF16_U0 = 49664;
-constexpr size_t REC_BF16_O0 = 66048;
-constexpr size_t REC_BF16_SLICE = 2048;
-constexpr size_t REC_BF16_BYTES = 82432;
+// bf16 record of one (chunk, head), written by the tcgen05 prep kernel and
+// streamed by the tcgen05 scan.  With G = K_restore^T W and H = K_restore^T U0
+// the state update of a chunk is one product, S <- Diag(a_C) S + H - G S, and
+// the output O = O0 + Q' S comes off that chain.
+//   [0, 32768)      G: 128 x 128 bf16 image, K-major, 128-byte swizzle, two
+//                   64-column k-blocks of 128 rows x 128 B
+//   [32768, 33280)  a_C [128] fp32
+//   [33792, 50176)  Q': 64 x 128 bf16 image, two k-blocks of 64 rows x 128 B
+//   [50176, 82944)  H in 16-column slices: [8][128 rows][16] bf16
+//   [82944, 99328)  O0 in 16-column slices: [8][64 rows][16] bf16
+// Every state-column block needs [0, 33280); a block that owns columns
+// [16 s, 16 (s + n)) of the values copies Q', n adjacent H slices and n
+// adjacent O0 slices.
+constexpr size_t REC_BF16_G = 0;
+constexpr size_t REC_BF16_AC = 32768;
+constexpr size_t REC_BF16_SHARED = 33280;
+constexpr size_t REC_BF16_QP = 33792;
+constexpr size_t REC_BF16_H = 50176;
+constexpr size_t REC_BF16_HSLICE = 4096;
+constexpr size_t REC_BF16_O0 = 82944;
+constexpr size_t REC_BF16_OSLICE = 2048;
+constexpr size_t REC_BF16_BYTES = 99328;
 
-// Byte offset of U0 / O0 element (token r, column col) inside its region.
-__host__ __device__ __forceinline__ uint32_t slice_offset(int r, int col) {
-    return (uint32_t)((col >> 4) * REC_BF16_SLICE + r * 32 + (col & 15) * 2);
+// Byte offset of element (row r, column col) inside a 16-column slice region
+// whose slices hold `rows` rows.
+__host__ __device__ __forceinline__ uint32_t slice_offset(int r, int col, int rows) {
+    return (uint32_t)((col >> 4) * rows * 32 + r * 32 + (col & 15) * 2);
 }
 
 // fp32 record of one (chunk, head), plain row-major, for the exact path.

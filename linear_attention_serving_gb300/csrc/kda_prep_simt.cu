@@ -18,8 +18,7 @@
 // where every factor is at most e^80 and the key factor is at most 1, so no
 // exp(-G) of a whole chunk is ever formed.
 //
-// This kernel serves the fp32 path (exact fp32 arithmetic) and writes either
-// fp32 records or the bf16 tcgen05 operand images.
+// This kernel serves the fp32 path: exact fp32 arithmetic, fp32 records.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -51,9 +50,8 @@ constexpr size_t PREP_SMEM_BYTES = sizeof(float) * PrepSmem::total;
 
 __device__ __forceinline__ int fpq_index(int p, int q) { return p * (p + 1) / 2 + q; }
 
-template <typename InT, bool BF16_REC>
 __global__ void __launch_bounds__(PREP_THREADS)
-prep_simt_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const InT *__restrict__ v,
+prep_simt_kernel(const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
                  const float *__restrict__ z, const float *__restrict__ A,
                  const float *__restrict__ beta, int H, float g_min, Plan plan,
                  char *__restrict__ records) {
@@ -199,24 +197,11 @@ prep_simt_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const InT
         __syncthreads();
     }
 
-    char *rec = records + ((size_t)c * H + h) * (BF16_REC ? REC_BF16_BYTES : REC_F32_BYTES);
+    char *rec = records + ((size_t)c * H + h) * REC_F32_BYTES;
 
     // 6. B1 = Diag(beta) K_decay (K_decay = ePfx * k*e), B2 = Diag(beta) V,
     //    K_restore = exp(G_last - G_j) k_j = eSfx * (key-side factored k)
-    if (BF16_REC) {
-        // K_restore^T image: row = channel, column = token, 8 tokens per 16-byte store
-        for (int it = tid; it < D * (C / 8); it += PREP_THREADS) {
-            const int ch = it & 127, j0 = (it >> 7) * 8;
-            __align__(16) __nv_bfloat16 vals[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int j = j0 + u;
-                vals[u] = __float2bfloat16_rn(eSfx[(j >> 4) * D + ch] * xf[j * LD + ch]);
-            }
-            *reinterpret_cast<uint4 *>(rec + REC_BF16_KRT + sw128_offset(ch, j0, 128)) =
-                *reinterpret_cast<const uint4 *>(vals);
-        }
-    } else {
+    {
         float *kr = reinterpret_cast<float *>(rec + REC_F32_KR);
         for (int idx = tid; idx < C * D; idx += PREP_THREADS) {
             const int r = idx >> 7, col = idx & 127;
@@ -231,7 +216,7 @@ prep_simt_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const InT
         xq[r * LD + col] = ePfx[(r >> 4) * D + col] * xq[r * LD + col];
     }
     if (tid < D) {
-        float *ac = reinterpret_cast<float *>(rec + (BF16_REC ? REC_BF16_AC : REC_F32_AC));
+        float *ac = reinterpret_cast<float *>(rec + REC_F32_AC);
         ac[tid] = aC[tid];
     }
     __syncthreads();
@@ -313,24 +298,7 @@ prep_simt_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const InT
                 uv[j] = xk[r * LD + c0 + j];
                 ov[j] = au[i][j];
             }
-            if (BF16_REC) {
-                __align__(16) __nv_bfloat16 bw[8], bq[8], bu[8], bo[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    bw[j] = __float2bfloat16_rn(wv[j]);
-                    bq[j] = __float2bfloat16_rn(qv[j]);
-                    bu[j] = __float2bfloat16_rn(uv[j]);
-                    bo[j] = __float2bfloat16_rn(ov[j]);
-                }
-                *reinterpret_cast<uint4 *>(rec + REC_BF16_A1 + sw128_offset(r, c0, 128)) =
-                    *reinterpret_cast<const uint4 *>(bw);
-                *reinterpret_cast<uint4 *>(rec + REC_BF16_A1 + sw128_offset(64 + r, c0, 128)) =
-                    *reinterpret_cast<const uint4 *>(bq);
-                *reinterpret_cast<uint4 *>(rec + REC_BF16_U0 + slice_offset(r, c0)) =
-                    *reinterpret_cast<const uint4 *>(bu);
-                *reinterpret_cast<uint4 *>(rec + REC_BF16_O0 + slice_offset(r, c0)) =
-                    *reinterpret_cast<const uint4 *>(bo);
-            } else {
+            {
                 float *W = reinterpret_cast<float *>(rec + REC_F32_W) + r * D + c0;
                 float *Q = reinterpret_cast<float *>(rec + REC_F32_Q) + r * D + c0;
                 float *U = reinterpret_cast<float *>(rec + REC_F32_U0) + r * D + c0;
@@ -353,23 +321,14 @@ int launch_prep_simt(const void *q, const void *k, const void *v, const float *z
                      const float *beta, int H, int dtype, float g_min, const Plan &p, void *records,
                      cudaStream_t s) {
     if (p.max_chunks == 0) return KDA_OK;
+    if (dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
     dim3 grid(p.max_chunks, H);
-    cudaError_t e;
-    if (dtype == KDA_BF16) {
-        auto kern = prep_simt_kernel<__nv_bfloat16, true>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PREP_SMEM_BYTES);
-        if (e != cudaSuccess) return KDA_ERR_CUDA;
-        kern<<<grid, PREP_THREADS, PREP_SMEM_BYTES, s>>>(
-            (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, z, A, beta, H,
-            g_min, p, (char *)records);
-    } else {
-        auto kern = prep_simt_kernel<float, false>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PREP_SMEM_BYTES);
-        if (e != cudaSuccess) return KDA_ERR_CUDA;
-        kern<<<grid, PREP_THREADS, PREP_SMEM_BYTES, s>>>((const float *)q, (const float *)k,
-                                                         (const float *)v, z, A, beta, H, g_min, p,
-                                                         (char *)records);
-    }
+    if (cudaFuncSetAttribute(prep_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PREP_SMEM_BYTES) !=
+        cudaSuccess)
+        return KDA_ERR_CUDA;
+    prep_simt_kernel<<<grid, PREP_THREADS, PREP_SMEM_BYTES, s>>>((const float *)q, (const float *)k,
+                                                                  (const float *)v, z, A, beta, H, g_min, p,
+                                                                  (char *)records);
     note_launch("prep_simt", s);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

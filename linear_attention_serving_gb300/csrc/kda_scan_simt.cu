@@ -12,8 +12,7 @@
 // "Kimi K3 模型结构（7）" eq. (17) (M I = M), giving the segment pair (M, S~).
 // Document starts reset the state ("文档边界").
 //
-// This is the exact-fp32 scan used for fp32 inputs; it also reads the bf16
-// operand images, which lets tests cross-check the tensor-core scan.
+// This is the exact-fp32 scan used for fp32 inputs (fp32 records).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -35,44 +34,23 @@ struct ScanSmem {
 };
 constexpr size_t SCAN_SMEM_BYTES = sizeof(float) * ScanSmem::total;
 
-template <bool BF16_REC>
 __device__ __forceinline__ void load_record(const char *rec, float *a1, float *kr, float *ac, int tid) {
-    if (BF16_REC) {
-        for (int idx = tid; idx < 128 * 128; idx += SCAN_THREADS) {
-            const int r = idx >> 7, col = idx & 127;
-            a1[r * LDA + col] = __bfloat162float(
-                *reinterpret_cast<const __nv_bfloat16 *>(rec + REC_BF16_A1 + sw128_offset(r, col, 128)));
-        }
-        for (int idx = tid; idx < 64 * 128; idx += SCAN_THREADS) {
-            const int j = idx & 63, ch = idx >> 6;  // K_restore^T image: row = channel, col = token
-            kr[j * LDA + ch] = __bfloat162float(
-                *reinterpret_cast<const __nv_bfloat16 *>(rec + REC_BF16_KRT + sw128_offset(ch, j, 128)));
-        }
-        if (tid < 128) ac[tid] = reinterpret_cast<const float *>(rec + REC_BF16_AC)[tid];
-    } else {
-        const float *W = reinterpret_cast<const float *>(rec + REC_F32_W);
-        const float *Q = reinterpret_cast<const float *>(rec + REC_F32_Q);
-        const float *K = reinterpret_cast<const float *>(rec + REC_F32_KR);
-        for (int idx = tid; idx < 64 * 32; idx += SCAN_THREADS) {
-            const int r = idx >> 5, c4 = (idx & 31) * 4;
-            *reinterpret_cast<float4 *>(a1 + r * LDA + c4) = *reinterpret_cast<const float4 *>(W + r * 128 + c4);
-            *reinterpret_cast<float4 *>(a1 + (64 + r) * LDA + c4) = *reinterpret_cast<const float4 *>(Q + r * 128 + c4);
-            *reinterpret_cast<float4 *>(kr + r * LDA + c4) = *reinterpret_cast<const float4 *>(K + r * 128 + c4);
-        }
-        if (tid < 128) ac[tid] = reinterpret_cast<const float *>(rec + REC_F32_AC)[tid];
+    const float *W = reinterpret_cast<const float *>(rec + REC_F32_W);
+    const float *Q = reinterpret_cast<const float *>(rec + REC_F32_Q);
+    const float *K = reinterpret_cast<const float *>(rec + REC_F32_KR);
+    for (int idx = tid; idx < 64 * 32; idx += SCAN_THREADS) {
+        const int r = idx >> 5, c4 = (idx & 31) * 4;
+        *reinterpret_cast<float4 *>(a1 + r * LDA + c4) = *reinterpret_cast<const float4 *>(W + r * 128 + c4);
+        *reinterpret_cast<float4 *>(a1 + (64 + r) * LDA + c4) = *reinterpret_cast<const float4 *>(Q + r * 128 + c4);
+        *reinterpret_cast<float4 *>(kr + r * LDA + c4) = *reinterpret_cast<const float4 *>(K + r * 128 + c4);
     }
+    if (tid < 128) ac[tid] = reinterpret_cast<const float *>(rec + REC_F32_AC)[tid];
 }
 
-template <bool BF16_REC>
 __device__ __forceinline__ float rec_u0(const char *rec, int r, int col) {
-    if (BF16_REC)
-        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(rec + REC_BF16_U0 + slice_offset(r, col)));
     return reinterpret_cast<const float *>(rec + REC_F32_U0)[r * 128 + col];
 }
-template <bool BF16_REC>
 __device__ __forceinline__ float rec_o0(const char *rec, int r, int col) {
-    if (BF16_REC)
-        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(rec + REC_BF16_O0 + slice_offset(r, col)));
     return reinterpret_cast<const float *>(rec + REC_F32_O0)[r * 128 + col];
 }
 
@@ -82,7 +60,6 @@ __device__ __forceinline__ float state_reset(const ScanArgs &a, int doc, int h, 
     return a.init_state ? a.init_state[(((size_t)doc * a.H + h) * D + r) * D + gcol] : 0.f;
 }
 
-template <typename OutT, bool BF16_REC>
 __global__ void __launch_bounds__(SCAN_THREADS) scan_simt_kernel(ScanArgs a) {
     extern __shared__ __align__(16) float sm[];
     const int unit = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
@@ -125,7 +102,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_simt_kernel(ScanArgs a) {
     for (int c = c0; c < c1; ++c) {
         const ChunkInfo ci = plan_chunk(p, c);
         const char *rec = (const char *)a.records +
-                          ((size_t)c * a.H + h) * (BF16_REC ? REC_BF16_BYTES : REC_F32_BYTES);
+                          ((size_t)c * a.H + h) * REC_F32_BYTES;
         __syncthreads();  // previous chunk finished with a1 / kr / S
         if (a.mode == SCAN_SEGMENTS && (ci.flags & CHUNK_FIRST)) {
             for (int idx = tid; idx < 128 * NC; idx += SCAN_THREADS) {
@@ -133,7 +110,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_simt_kernel(ScanArgs a) {
                 S[r * LDS + j] = state_reset(a, ci.doc, h, r, col0 + j);
             }
         }
-        load_record<BF16_REC>(rec, a1, kr, ac, tid);
+        load_record(rec, a1, kr, ac, tid);
         __syncthreads();
 
         // D1 = [W ; Q'] S   (row < 64: W S, row >= 64: Q' S)
@@ -149,15 +126,15 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_simt_kernel(ScanArgs a) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int g = col0 + cc + j;
-                const float u0 = (g < D) ? rec_u0<BF16_REC>(rec, row, g) : 0.f;
+                const float u0 = (g < D) ? rec_u0(rec, row, g) : 0.f;
                 U[row * LDS + cc + j] = u0 - acc[j];
             }
         } else if (value_cols && a.o && a.phase != 1 && row - C < ci.len) {
             const int r = row - C;
-            OutT *orow = reinterpret_cast<OutT *>(a.o) + ((size_t)(ci.tok + r) * a.H + h) * D + col0 + cc;
+            float *orow = reinterpret_cast<float *>(a.o) + ((size_t)(ci.tok + r) * a.H + h) * D + col0 + cc;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                orow[j] = from_f32<OutT>(rec_o0<BF16_REC>(rec, r, col0 + cc + j) + acc[j]);
+                orow[j] = rec_o0(rec, r, col0 + cc + j) + acc[j];
         }
         __syncthreads();
 
@@ -199,19 +176,12 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_simt_kernel(ScanArgs a) {
 
 int launch_scan_simt(const ScanArgs &a, int dtype, cudaStream_t s) {
     if (a.n_units == 0) return KDA_OK;
+    if (dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
     dim3 grid(a.n_units, a.H, a.ncols / NC);
-    cudaError_t e;
-    if (dtype == KDA_BF16) {
-        auto kern = scan_simt_kernel<__nv_bfloat16, true>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SCAN_SMEM_BYTES);
-        if (e != cudaSuccess) return KDA_ERR_CUDA;
-        kern<<<grid, SCAN_THREADS, SCAN_SMEM_BYTES, s>>>(a);
-    } else {
-        auto kern = scan_simt_kernel<float, false>;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SCAN_SMEM_BYTES);
-        if (e != cudaSuccess) return KDA_ERR_CUDA;
-        kern<<<grid, SCAN_THREADS, SCAN_SMEM_BYTES, s>>>(a);
-    }
+    if (cudaFuncSetAttribute(scan_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SCAN_SMEM_BYTES) !=
+        cudaSuccess)
+        return KDA_ERR_CUDA;
+    scan_simt_kernel<<<grid, SCAN_THREADS, SCAN_SMEM_BYTES, s>>>(a);
     note_launch("scan_simt", s);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -1,26 +1,28 @@
 // kda_scan_tc.cu -- the sequential chunk scan on tcgen05 tensor cores.
 //
-// Per chunk ("Kimi K3: the Manos, the Mythos ..." (SemiAnalysis),
-// "FlashKDA 算法", the K2 recurrence, with the state-independent products
-// folded by the prep kernel into W, U0, Q', O0):
-//   D1 = [W ; Q'] S          (one M = 128 MMA: rows 0..63 W S, rows 64..127 Q' S)
-//   U  = U0 - D1[0:64],  O = O0 + D1[64:128]
-//   D2 = K_restore^T U       (one M = 128 MMA over the chunk's 64 tokens)
-//   S <- Diag(a_C) S + D2
-// The fp32 state master lives in registers (thread t owns state row t); its
-// bf16 copy in shared memory is the B operand of the next chunk's first MMA,
-// and U's bf16 copy is the B operand of the second.  Accumulators live in
-// TMEM.  The chunk operands (A1 = [W ; Q'] and K_restore^T, 48 KB per chunk,
-// stored by the prep kernel as ready-swizzled images) stream in through a
-// multi-stage bulk-copy pipeline driven by a producer warp.
+// With the record of the prep kernel (G = K_restore^T W, H = K_restore^T U0,
+// Q' = Q_decay - M_qk W, O0 = M_qk U0, a_C), one chunk of the scan is
+//   S <- Diag(a_C) S + H - G S          (the chain: one M = 128 MMA per chunk)
+//   O  = O0 + Q' S                      (off the chain)
+// which is "Kimi K3: the Manos, the Mythos ..." (SemiAnalysis), "FlashKDA 算法"
+// K2 (U = INV Diag(beta)(V - K_decay S), O = Q_decay S + M_qk U,
+// S = Diag(a[-1]) S + K_restore^T U) with its products regrouped so that only
+// one tensor-core round trip sits on the sequential path.
 //
-// A block owns N state columns (they evolve independently); with 256 state
-// columns the extra 128 start from the identity and see V = 0, which carries
+// A block owns N state columns (columns evolve independently).  With 256
+// state columns the extra 128 start from the identity with H = 0: they carry
 // the transition M of "Kimi K3 模型结构（7）" eq. (17) for the segment pairs.
 //
-// Warps 0-3: epilogue (TMEM lane = warp * 32 + lane), thread 0 issues the MMAs.
-// Warp 4: producer.  Every wait is bounded; on a timeout the block records
-// KDA_DEVERR_TIMEOUT, leaves its loop, and frees its TMEM.
+// Warps 0-3 (chain): thread t owns state row t (TMEM lane t); the fp32 state
+//   master lives in registers, its bf16 copy (double buffered) in shared
+//   memory is the B operand of the next chunk's MMAs; thread 0 issues them.
+// Warps 4-5 (output): one of their threads issues O = Q' S into a
+//   double-buffered TMEM accumulator as soon as the chain has published S,
+//   and the two warps drain O0 + Q' S while the chain moves on.
+// Warp 6 (producer): streams each chunk's record (G, a_C, Q', the block's H
+//   and O0 column slices) through a bulk-copy pipeline.
+// Every wait is bounded; on a timeout the block records KDA_DEVERR_TIMEOUT,
+// leaves its loops, and frees its TMEM.
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 
@@ -30,28 +32,28 @@ namespace {
 
 using namespace tc;
 
-constexpr int CONSUMERS = 128;
-constexpr int THREADS = CONSUMERS + 32;
+constexpr int CHAIN = 128;          // warps 0-3
+constexpr int PRODUCER_WARP = 6;
+constexpr int THREADS = 224;
 
-// One pipeline stage: the shared part of a record (A1, K_restore^T, a_C) and
-// this block's U0 / O0 column slices.
+// pipeline stage: G (32 KB) | a_C | Q' (16 KB) | H slices | O0 slices
 template <int N>
-struct TcSmem {
-    static constexpr int NS = N / 16;                          // 16-column slices
-    static constexpr int U0 = (int)REC_BF16_SHARED;            // stage offset of the U0 slices
-    static constexpr int O0 = U0 + NS * (int)REC_BF16_SLICE;   // stage offset of the O0 slices
-    static constexpr int STAGE = ((O0 + NS * (int)REC_BF16_SLICE) + 1023) / 1024 * 1024;
-    static constexpr int SOP = 2 * N * 128;  // S^T operand: 2 k-blocks x N rows x 128 B
-    static constexpr int UOP = N * 128;      // U^T operand: 1 k-block x N rows x 128 B
-    // TMEM: D1 in P1 partial accumulators, D2 in P2 (independent MMA chains overlap)
-    static constexpr int P1 = 4, P2 = 2;
-    static constexpr int COLS = (P1 + P2) * N;
-    static constexpr int NCOLS = COLS <= 32 ? 32 : (COLS <= 64 ? 64 : (COLS <= 128 ? 128 : (COLS <= 256 ? 256 : 512)));
+struct Stage {
+    static constexpr int NS = N / 16;
+    static constexpr int G = 0;
+    static constexpr int AC = (int)REC_BF16_AC;
+    static constexpr int QP = (int)REC_BF16_QP;
+    static constexpr int H = (int)REC_BF16_H;
+    static constexpr int O0 = H + NS * (int)REC_BF16_HSLICE;
+    static constexpr int BYTES = ((O0 + NS * (int)REC_BF16_OSLICE) + 1023) / 1024 * 1024;
+    static constexpr int SOP = 2 * N * 128;  // one bf16 S operand: 2 k-blocks x N rows x 128 B
+    static constexpr int COLS = 3 * N;       // TMEM: chain accumulator + two output accumulators
+    static constexpr int NCOLS = COLS <= 32 ? 32 : (COLS <= 64 ? 64 : (COLS <= 128 ? 128 : 256));
 };
 
 template <int N, int STAGES>
 constexpr size_t scan_tc_smem_bytes() {
-    return (size_t)STAGES * TcSmem<N>::STAGE + TcSmem<N>::SOP + TcSmem<N>::UOP + 1024;
+    return (size_t)STAGES * Stage<N>::BYTES + 2 * Stage<N>::SOP + 1024;
 }
 
 __device__ __forceinline__ float state_init(const ScanArgs &a, int unit, int h, int r, int g) {
@@ -68,7 +70,7 @@ __device__ __forceinline__ float state_reset(const ScanArgs &a, int doc, int h, 
     return a.init_state ? a.init_state[(((size_t)doc * a.H + h) * D + r) * D + g] : 0.f;
 }
 
-// bf16 copy of this thread's state row into the K-major S^T operand (row n = column, k = state row t)
+// bf16 copy of this thread's state row into the K-major S operand (row n = column, k = state row t)
 template <int N>
 __device__ __forceinline__ void write_sop(uint8_t *sop, int t, const float *s) {
 #pragma unroll
@@ -76,31 +78,12 @@ __device__ __forceinline__ void write_sop(uint8_t *sop, int t, const float *s) {
         *reinterpret_cast<__nv_bfloat16 *>(sop + sw128_offset(n, t, N)) = __float2bfloat16_rn(s[n]);
 }
 
-// Sum of P partial accumulators (N columns each, N apart) of this thread's TMEM lane.
-template <int N, int P>
-__device__ __forceinline__ void tmem_sum(uint32_t taddr, float *out) {
-#pragma unroll
-    for (int j = 0; j < N; j += 16) {
-        float part[P][16];
-#pragma unroll
-        for (int pp = 0; pp < P; ++pp) tmem_ld16(taddr + pp * N + j, part[pp]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            float acc = part[0][e];
-#pragma unroll
-            for (int pp = 1; pp < P; ++pp) acc += part[pp][e];
-            out[j + e] = acc;
-        }
-    }
-}
-
-// N bf16 values of token row r from consecutive 16-column slices (2 KB apart)
+// N bf16 values of row r from consecutive 16-column slices of `rows` rows each
 template <int N>
-__device__ __forceinline__ void load_row_slices(const uint8_t *base, int r, float *out) {
+__device__ __forceinline__ void load_slices(const uint8_t *base, int r, int rows, float *out) {
 #pragma unroll
     for (int j = 0; j < N; j += 8) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(base + slice_offset(r, j));
+        const uint4 u = *reinterpret_cast<const uint4 *>(base + slice_offset(r, j, rows));
         const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -111,10 +94,18 @@ __device__ __forceinline__ void load_row_slices(const uint8_t *base, int r, floa
     }
 }
 
+template <int N>
+__device__ __forceinline__ void tmem_row(uint32_t taddr, float *out) {
+#pragma unroll
+    for (int j = 0; j < N; j += 16) tmem_ld16(taddr + j, out + j);
+    tmem_ld_wait();
+}
+
 template <int N, int STAGES>
 __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
+    using ST = Stage<N>;
     extern __shared__ uint8_t smraw[];
-    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], mma1_bar, mma2_bar;
+    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], g_bar, o_bar[2], sready_bar[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -122,6 +113,7 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
     const int warp = tid >> 5, lane = tid & 31;
     const int col0 = blockIdx.z * N;
     const bool value_cols = col0 < D;
+    const bool emit_o = value_cols && a.o && a.phase != 1;
     const Plan &p = a.plan;
     if (plan_failed(p)) return;
     int c0, c1;
@@ -133,50 +125,56 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
     }
     const int nchunks = c1 - c0;
 
-    constexpr int STAGE_BYTES = TcSmem<N>::STAGE;
     uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
-    uint8_t *sop = sm + STAGES * STAGE_BYTES;
-    uint8_t *uop = sop + TcSmem<N>::SOP;
+    uint8_t *sop0 = sm + STAGES * ST::BYTES;
     const char *records = (const char *)a.records;
     const size_t rec_stride = (size_t)a.H * REC_BF16_BYTES;
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);
+            // released by: the chain MMA (commit), the chain warps, and when the
+            // output is emitted the output MMA (commit) and the output warps
+            mbar_init(&empty_bar[s], emit_o ? 4 : 2);
         }
-        mbar_init(&mma1_bar, 1);
-        mbar_init(&mma2_bar, 1);
+        mbar_init(&g_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&o_bar[b], 1);
+            mbar_init(&sready_bar[b], 1);  // the S operand of buffer b holds the entering state
+        }
         abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(&tmem_slot, TcSmem<N>::NCOLS);
+    if (warp == 0) tmem_alloc(&tmem_slot, ST::NCOLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    constexpr int P1 = TcSmem<N>::P1, P2 = TcSmem<N>::P2;
-    const uint32_t tmem_d1 = tmem, tmem_d2 = tmem + P1 * N;
+    const uint32_t tmem_g = tmem, tmem_o = tmem + N;  // output accumulators at tmem_o + b * N
 
-    if (warp == CONSUMERS / 32) {
+    if (warp == PRODUCER_WARP) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             int issued = 0;
             bool timed_out = false;
+            const uint32_t bytes = (uint32_t)REC_BF16_SHARED +
+                                   (value_cols ? (uint32_t)(16384 + ST::NS * (REC_BF16_HSLICE + REC_BF16_OSLICE)) : 0u);
             for (int i = 0; i < nchunks; ++i) {
                 const int stage = i % STAGES;
                 const uint32_t ph = (uint32_t)((i / STAGES) & 1);
                 if (!mbar_wait(&empty_bar[stage], ph ^ 1u)) { timed_out = true; break; }
                 if (*(volatile int *)&abort_flag) break;
                 const char *rec = records + (size_t)(c0 + i) * rec_stride + (size_t)h * REC_BF16_BYTES;
-                uint8_t *st = sm + stage * STAGE_BYTES;
-                const uint32_t slices = value_cols ? (uint32_t)(TcSmem<N>::NS * REC_BF16_SLICE) : 0u;
-                mbar_expect_tx(&full_bar[stage], (uint32_t)REC_BF16_SHARED + 2u * slices);
+                uint8_t *st = sm + stage * ST::BYTES;
+                mbar_expect_tx(&full_bar[stage], bytes);
                 bulk_g2s(st, rec, (uint32_t)REC_BF16_SHARED, &full_bar[stage]);
                 if (value_cols) {
-                    const size_t so = (size_t)(col0 / 16) * REC_BF16_SLICE;
-                    bulk_g2s(st + TcSmem<N>::U0, rec + REC_BF16_U0 + so, slices, &full_bar[stage]);
-                    bulk_g2s(st + TcSmem<N>::O0, rec + REC_BF16_O0 + so, slices, &full_bar[stage]);
+                    const int s0 = col0 / 16;
+                    bulk_g2s(st + ST::QP, rec + REC_BF16_QP, 16384, &full_bar[stage]);
+                    bulk_g2s(st + ST::H, rec + REC_BF16_H + (size_t)s0 * REC_BF16_HSLICE,
+                             (uint32_t)(ST::NS * REC_BF16_HSLICE), &full_bar[stage]);
+                    bulk_g2s(st + ST::O0, rec + REC_BF16_O0 + (size_t)s0 * REC_BF16_OSLICE,
+                             (uint32_t)(ST::NS * REC_BF16_OSLICE), &full_bar[stage]);
                 }
                 issued = i + 1;
             }
@@ -187,110 +185,125 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
                 if (timed_out) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
             }
         }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ output warps
+        if (emit_o) {
+            const int r = tid - CHAIN;  // token row of the chunk = TMEM lane
+            const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+            constexpr uint32_t IDESC = idesc_bf16_f32(128, N);
+            for (int i = 0; i < nchunks; ++i) {
+                const int stage = i % STAGES, b = i & 1;
+                const uint32_t ph = (uint32_t)((i / STAGES) & 1);
+                const ChunkInfo ci = plan_chunk(p, c0 + i);
+                bool ok = true;
+                if (r == 0) {
+                    // O = Q' S of this chunk, once its stage has landed and the chain has
+                    // published the entering state in S operand buffer b
+                    ok = mbar_wait(&full_bar[stage], ph) && mbar_wait(&sready_bar[b], (uint32_t)((i >> 1) & 1));
+                    if (ok) {
+                        tc_fence_after();
+                        const uint8_t *st = sm + stage * ST::BYTES;
+                        const uint8_t *sop = sop0 + b * ST::SOP;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const uint64_t ad = sdesc_sw128(smem_u32(st + ST::QP + (k >> 2) * 8192 + (k & 3) * 32));
+                            const uint64_t bd = sdesc_sw128(smem_u32(sop + (k >> 2) * (N * 128) + (k & 3) * 32));
+                            mma_bf16(tmem_o + b * N, ad, bd, IDESC, k > 0);
+                        }
+                        mma_commit(&o_bar[b]);
+                        mma_commit(&empty_bar[stage]);
+                    }
+                }
+                ok = ok && mbar_wait(&o_bar[b], (uint32_t)((i >> 1) & 1)) && mbar_wait(&full_bar[stage], ph);
+                __syncwarp();
+                tc_fence_after();
+                float d[N], x[N];
+                tmem_row<N>(tmem_o + b * N + lane_off, d);
+                load_slices<N>(sm + stage * ST::BYTES + ST::O0, r, 64, x);
+                tc_fence_before();
+                // both output warps are done with this accumulator and stage (or both give up)
+                if (bar_or(2, 64, !ok || *(volatile int *)&abort_flag)) break;
+                if (r == 0) mbar_arrive(&empty_bar[stage]);
+                if (r < ci.len) {
+                    __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(a.o) + ((size_t)(ci.tok + r) * a.H + h) * D + col0;
+#pragma unroll
+                    for (int j = 0; j < N; j += 8) {
+                        __align__(16) __nv_bfloat16 ob[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ob[e] = __float2bfloat16_rn(x[j + e] + d[j + e]);
+                        *reinterpret_cast<uint4 *>(orow + j) = *reinterpret_cast<const uint4 *>(ob);
+                    }
+                }
+            }
+        }
     } else {
-        // ------------------------------------------------------------ epilogue + MMA issue
-        const int t = tid;  // TMEM lane == state row (D2) == token row (D1)
+        // ------------------------------------------------------------ chain warps
+        const int t = tid;  // state row == TMEM lane
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         float s[N];
 #pragma unroll
         for (int j = 0; j < N; ++j) s[j] = state_init(a, unit, h, t, col0 + j);
-        if (a.mode == SCAN_DOCS && nchunks == 0) {
-            if (value_cols && a.final_state) {
-                float *f = a.final_state + (((size_t)unit * a.H + h) * D + t) * D + col0;
+        if (a.mode == SCAN_DOCS && nchunks == 0 && value_cols && a.final_state) {
+            float *f = a.final_state + (((size_t)unit * a.H + h) * D + t) * D + col0;
 #pragma unroll
-                for (int j = 0; j < N; j += 4) *reinterpret_cast<float4 *>(f + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
-            }
+            for (int j = 0; j < N; j += 4) *reinterpret_cast<float4 *>(f + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
         }
-        write_sop<N>(sop, t, s);
+        write_sop<N>(sop0, t, s);
         fence_async_smem();
-        bool aborted = bar_or(1, CONSUMERS, false);
-
+        bool aborted = bar_or(1, CHAIN, false);
         ChunkInfo ci_next;
         if (nchunks > 0) ci_next = plan_chunk(p, c0);
-
         constexpr uint32_t IDESC = idesc_bf16_f32(128, N);
         for (int i = 0; i < nchunks && !aborted; ++i) {
             const int stage = i % STAGES;
             const uint32_t ph = (uint32_t)((i / STAGES) & 1);
             const ChunkInfo ci = ci_next;
             if (i + 1 < nchunks) ci_next = plan_chunk(p, c0 + i + 1);
+            uint8_t *sop = sop0 + (i & 1) * ST::SOP;
             if (a.mode == SCAN_SEGMENTS && (ci.flags & CHUNK_FIRST)) {
                 // a document starts here: the state restarts (uniform branch)
 #pragma unroll
                 for (int j = 0; j < N; ++j) s[j] = state_reset(a, ci.doc, h, t, col0 + j);
                 write_sop<N>(sop, t, s);
                 fence_async_smem();
-                bar_or(1, CONSUMERS, false);
+                bar_or(1, CHAIN, false);
             }
             bool bad = false;
             if (t == 0) {
                 if (mbar_wait(&full_bar[stage], ph)) {
                     tc_fence_after();
-                    uint8_t *st = sm + stage * STAGE_BYTES;
+                    uint8_t *st = sm + stage * ST::BYTES;
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const uint64_t ad = sdesc_sw128(smem_u32(st + (k >> 2) * 16384 + (k & 3) * 32));
+                        const uint64_t ad = sdesc_sw128(smem_u32(st + ST::G + (k >> 2) * 16384 + (k & 3) * 32));
                         const uint64_t bd = sdesc_sw128(smem_u32(sop + (k >> 2) * (N * 128) + (k & 3) * 32));
-                        mma_bf16(tmem_d1 + (k % P1) * N, ad, bd, IDESC, k >= P1);
+                        mma_bf16(tmem_g, ad, bd, IDESC, k > 0);
                     }
-                    mma_commit(&mma1_bar);
+                    mma_commit(&g_bar);
+                    mma_commit(&empty_bar[stage]);
+                    // the S operand of this chunk is final: the output MMA may read it
+                    if (emit_o) mbar_arrive(&sready_bar[i & 1]);
                 } else {
                     bad = true;
                 }
             }
-            // ---- D1 -> U (rows 0..63), O (rows 64..127)
-            const bool ok1 = !bad && mbar_wait(&mma1_bar, (uint32_t)(i & 1)) && mbar_wait(&full_bar[stage], ph);
+            // ---- S <- Diag(a_C) S + H - G S
+            const bool ok = !bad && mbar_wait(&g_bar, (uint32_t)(i & 1)) && mbar_wait(&full_bar[stage], ph);
             __syncwarp();
             tc_fence_after();
-            // everything this thread needs from the stage, read before the stage is released
-            const uint8_t *stg = sm + stage * STAGE_BYTES;
-            const float ac = reinterpret_cast<const float *>(stg + REC_BF16_AC)[t];
-            float x[N];
-            if (value_cols)
-                load_row_slices<N>(stg + (t < C ? TcSmem<N>::U0 : TcSmem<N>::O0), t < C ? t : t - C, x);
+            const uint8_t *stg = sm + stage * ST::BYTES;
+            const float ac = reinterpret_cast<const float *>(stg + ST::AC)[t];
+            float d[N], hv[N];
+            tmem_row<N>(tmem_g + lane_off, d);
+            if (value_cols) load_slices<N>(stg + ST::H, t, 128, hv);
             else
 #pragma unroll
-                for (int j = 0; j < N; ++j) x[j] = 0.f;
-            float d[N];
-            tmem_sum<N, P1>(tmem_d1 + lane_off, d);
-            if (t < C) {
+                for (int j = 0; j < N; ++j) hv[j] = 0.f;
 #pragma unroll
-                for (int n = 0; n < N; ++n)
-                    *reinterpret_cast<__nv_bfloat16 *>(uop + sw128_offset(n, t, N)) = __float2bfloat16_rn(x[n] - d[n]);
-            } else if (value_cols && a.o && a.phase != 1 && (t - C) < ci.len) {
-                __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(a.o) + ((size_t)(ci.tok + t - C) * a.H + h) * D + col0;
-#pragma unroll
-                for (int j = 0; j < N; j += 8) {
-                    __align__(16) __nv_bfloat16 ob[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) ob[e] = __float2bfloat16_rn(x[j + e] + d[j + e]);
-                    *reinterpret_cast<uint4 *>(orow + j) = *reinterpret_cast<const uint4 *>(ob);
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            aborted = bar_or(1, CONSUMERS, !ok1);
-            if (aborted) break;
-            // ---- D2 = K_restore^T U
-            if (t == 0) {
-                tc_fence_after();
-                uint8_t *kr = sm + stage * STAGE_BYTES + REC_BF16_KRT;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint64_t ad = sdesc_sw128(smem_u32(kr + k * 32));
-                    const uint64_t bd = sdesc_sw128(smem_u32(uop + k * 32));
-                    mma_bf16(tmem_d2 + (k % P2) * N, ad, bd, IDESC, k >= P2);
-                }
-                mma_commit(&mma2_bar);
-                mma_commit(&empty_bar[stage]);
-            }
-            const bool ok2 = mbar_wait(&mma2_bar, (uint32_t)(i & 1));
-            __syncwarp();
-            tc_fence_after();
-            tmem_sum<N, P2>(tmem_d2 + lane_off, d);
-#pragma unroll
-            for (int j = 0; j < N; ++j) s[j] = fmaf(ac, s[j], d[j]);
-            write_sop<N>(sop, t, s);
+            for (int j = 0; j < N; ++j) s[j] = fmaf(ac, s[j], hv[j] - d[j]);
+            // buffer (i+1)&1 was last read by chunk i-1's output MMA, which must be done
+            const bool ok_o = !emit_o || i < 1 || mbar_wait(&o_bar[(i + 1) & 1], (uint32_t)(((i - 1) >> 1) & 1));
+            write_sop<N>(sop0 + ((i + 1) & 1) * ST::SOP, t, s);
             if (value_cols && a.final_state && a.phase != 1 && (ci.flags & CHUNK_LAST)) {
                 float *f = a.final_state + (((size_t)ci.doc * a.H + h) * D + t) * D + col0;
 #pragma unroll
@@ -298,7 +311,8 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
             }
             fence_async_smem();
             tc_fence_before();
-            aborted = bar_or(1, CONSUMERS, !ok2);
+            aborted = bar_or(1, CHAIN, !ok || !ok_o);
+            if (t == 0 && !aborted) mbar_arrive(&empty_bar[stage]);
         }
         if (aborted) {
             if (t == 0) {
@@ -316,7 +330,7 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, TcSmem<N>::NCOLS);
+    if (warp == 0) tmem_dealloc(tmem, ST::NCOLS);
 }
 
 template <int N, int STAGES>
@@ -335,8 +349,8 @@ int launch_n(const ScanArgs &a, cudaStream_t s) {
 
 int launch_scan_tc(const ScanArgs &a, int n_sm, cudaStream_t s) {
     if (a.n_units == 0) return KDA_OK;
-    // Few independent column slices: narrow blocks spread the chain over more
-    // SMs.  Many: wider blocks, two per SM, amortise the per-chunk latency.
+    // Few independent column slices: narrow blocks spread the chains over more
+    // SMs.  Many: wider blocks amortise the per-chunk latency.
     const long long slices16 = (long long)a.n_units * a.H * (a.ncols / 16);
     if (slices16 <= 2LL * n_sm) return launch_n<16, 3>(a, s);
     return launch_n<64, 2>(a, s);
