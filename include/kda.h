@@ -129,7 +129,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v,
  * nothing and calls no allocating routine.
  *   - A call whose kda_chunk_fwd_workspace_size(T_total, H, n_seqs, dtype)
  *     exceeds KDA_NOALLOC_SCRATCH_BYTES returns KDA_ERR_WORKSPACE before any
- *     launch (about 800 (chunk, head) pairs in bf16, 400 in fp32).
+ *     launch (about 500 (chunk, head) pairs in bf16, 400 in fp32).
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture.

@@ -100,19 +100,22 @@ __host__ __device__ __forceinline__ void segment_range(int n, int nseg, int i, i
 }
 
 // ---------------------------------------------------------------- records
-// bf16 record of one (chunk, head), written by the tcgen05 prep kernel and
-// streamed by the tcgen05 scan.  With G = K_restore^T W and H = K_restore^T U0
-// the state update of a chunk is one product, S <- Diag(a_C) S + H - G S, and
-// the output O = O0 + Q' S comes off that chain.
-//   [0, 32768)      G: 128 x 128 bf16 image, K-major, 128-byte swizzle, two
-//                   64-column k-blocks of 128 rows x 128 B
-//   [32768, 33280)  a_C [128] fp32
-//   [33792, 50176)  Q': 64 x 128 bf16 image, two k-blocks of 64 rows x 128 B
-//   [50176, 82944)  H in 16-column slices: [8][128 rows][16] bf16
-//   [82944, 99328)  O0 in 16-column slices: [8][64 rows][16] bf16
-// Every state-column block needs [0, 33280); a block that owns columns
-// [16 s, 16 (s + n)) of the values copies Q', n adjacent H slices and n
-// adjacent O0 slices.
+// bf16 record of one (chunk, head), written by the tcgen05 prep kernel, read
+// by the tcgen05 scan (the state chain) and by the output kernel.  With
+// G = K_restore^T W and H = K_restore^T U0 the state update of a chunk is one
+// product, S <- Diag(a_C) S + H - G S; the output O = O0 + Q' S needs the
+// entering state S, which the scan stores into the record.
+//   [0, 32768)       G: 128 x 128 bf16 image, K-major, 128-byte swizzle, two
+//                    64-column k-blocks of 128 rows x 128 B
+//   [32768, 33280)   a_C [128] fp32
+//   [33792, 50176)   Q': 64 x 128 bf16 image, two k-blocks of 64 rows x 128 B
+//   [50176, 82944)   H in 16-column slices: [8][128 rows][16] bf16
+//   [82944, 99328)   O0 in 16-column slices: [8][64 rows][16] bf16
+//   [99328, 132096)  S entering the chunk, bf16, MN-major with the 32-byte
+//                    swizzle: [8 column blocks][128 rows][16], the two 16-byte
+//                    halves of row r swapped when (r >> 2) is odd
+// A scan block that owns state columns [16 s, 16 (s + n)) copies [0, 33280)
+// and n adjacent H slices, and writes n adjacent S blocks.
 constexpr size_t REC_BF16_G = 0;
 constexpr size_t REC_BF16_AC = 32768;
 constexpr size_t REC_BF16_SHARED = 33280;
@@ -121,7 +124,9 @@ constexpr size_t REC_BF16_H = 50176;
 constexpr size_t REC_BF16_HSLICE = 4096;
 constexpr size_t REC_BF16_O0 = 82944;
 constexpr size_t REC_BF16_OSLICE = 2048;
-constexpr size_t REC_BF16_BYTES = 99328;
+constexpr size_t REC_BF16_S = 99328;
+constexpr size_t REC_BF16_SBLOCK = 4096;
+constexpr size_t REC_BF16_BYTES = 132096;
 
 // Byte offset of element (row r, column col) inside a 16-column slice region
 // whose slices hold `rows` rows.
@@ -236,6 +241,7 @@ int launch_prep_tc(const void *q, const void *k, const void *v, const float *z, 
                    cudaStream_t s);
 int launch_scan_simt(const ScanArgs &a, int dtype, cudaStream_t s);
 int launch_scan_tc(const ScanArgs &a, int n_sm, cudaStream_t s);
+int launch_out_tc(const Plan &p, int H, const void *records, void *o, int n_sm, cudaStream_t s);
 int device_sm_count();
 int launch_compose(const Plan &p, int H, int n_seg, const float *pairs, float *s_enter,
                    cudaStream_t s);

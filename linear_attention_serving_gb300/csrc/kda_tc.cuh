@@ -121,6 +121,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *out) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 2^x by the hardware approximation (PTX ex2.approx.ftz).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// TMEM lane of row m of an M = 64 accumulator (cta_group::1): rows 16 q .. 16 q + 15
+// sit in lanes 32 q .. 32 q + 15 (checked against a host product).
+__host__ __device__ constexpr int m64_lane(int m) { return (m >> 4) * 32 + (m & 15); }
+
 // ---------------------------------------------------------------- MMA
 // Shared-memory matrix descriptor of a K-major operand with the 128-byte
 // swizzle: rows of 128 B, 8-row groups 1024 B apart, base 1024-byte aligned.
@@ -133,10 +144,31 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
     d |= (uint64_t)2 << 61;                   // 128-byte swizzle
     return d;
 }
+// Descriptor of an MN-major operand (rows of the contraction index k, the M or
+// N index contiguous within a row):
+//   mode SWZ_128B: blocks 64 elements (128 B) wide, 16-byte chunk c of row k
+//                  stored at chunk c ^ (k & 7);
+//   mode SWZ_32B:  blocks 16 elements (32 B) wide, chunk c stored at
+//                  c ^ ((k >> 2) & 1);
+// lbo = byte stride between consecutive blocks along M/N, sbo = byte stride
+// between consecutive 8-row groups along k.  Checked against a host product
+// for both modes, N = 16 .. 128.
+constexpr uint32_t SWZ_128B = 2, SWZ_32B = 6;
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t mode) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)mode << 61;
+    return d;
+}
 // Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// The same with the B operand MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) { return idesc_bf16_f32(M, N) | (1u << 16); }
 // D[tmem] (+)= A[smem] * B[smem]^T, one K = 16 step; issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          bool accumulate) {

@@ -1,73 +1,136 @@
 // kda_tri.cuh -- the UT-transform inverse of one chunk, in fp32 CUDA cores.
 //
 // "Kimi K3 模型结构（2）：序列维度（下），chunkwise 并行与下界衰减", section
-// "UT 变换": I + L is unit lower triangular, so its inverse is unique and is
-// obtained by forward substitution.  Here the 64 x 64 matrix is handled as
-// 4 x 4 blocks of 16: the diagonal blocks by forward substitution, then
-// X_pq = -X_pp sum_{q<=r<p} L_pr X_rq one block diagonal at a time.  Every
-// loop bound is a compile-time constant so the shared-memory loads are issued
-// ahead of the FMA chains, which use two partial sums.
+// "UT 变换": I + L is unit lower triangular, so its inverse is unique.  The
+// 64 x 64 matrix is split twice by the block rule
+//   [[P, 0], [R, Q]]^-1 = [[P^-1, 0], [-Q^-1 R P^-1, Q^-1]]:
+//   D.  the four 16 x 16 diagonal blocks by forward substitution;
+//   1.  the two 32 x 32 diagonal blocks: X_10 = -X_11 (L_10 X_00) and
+//       X_32 = -X_33 (L_32 X_22);
+//   2.  the lower-left 32 x 32 block: -X_B (L_BA X_A), X_A and X_B the inverses
+//       of the two 32 x 32 diagonal blocks.
+// Phases 1 and 2 are products of small dense blocks; each thread forms four
+// adjacent outputs of a row, so one 16-byte shared load of the right operand
+// serves four multiply-adds (two paired fp32 FMAs).
 #pragma once
 
 namespace kda {
 
-constexpr int TRI_LD = 65;  // row stride of the 64 x 64 fp32 matrices
+constexpr int TRI_LD = 68;  // row stride (floats) of the 64 x 64 fp32 matrices; 16-byte rows
 
-// INV (zeroed above its diagonal blocks by the caller), L strictly lower with
-// beta folded in, tmp [3][16][17].  All NT threads of the block call this; it
-// synchronises internally and ends with a barrier.
+// L: strictly lower with beta folded in.  Only its lower blocks are read: the
+// strictly lower part of the diagonal blocks and the whole of the blocks below
+// them.  INV is written in full (zeros above the block diagonal).  T is scratch
+// of at least 32 x TRI_LD floats.  All NT >= 512 threads of the block call
+// this; it synchronises internally and ends with a barrier.
 template <int NT>
 __device__ __forceinline__ void tri_inverse(const float *__restrict__ L, float *__restrict__ INV,
-                                            float *__restrict__ tmp, int tid) {
-    if (tid < 64) {
-        const int p = tid >> 4, col = tid & 15;
-        float x[16];
+                                            float *__restrict__ T, int tid) {
+    static_assert(NT >= 512, "tri_inverse wants at least 512 threads");
+    const int warp = tid >> 5, lane = tid & 31;
+    // ---- D: warp p inverts diagonal block p, one column per lane; the other
+    // warps clear the six blocks above the block diagonal
+    if (warp < 4) {
+        if (lane < 16) {
+            const int p = warp, col = lane;
+            const float *Lp = L + (16 * p) * TRI_LD + 16 * p;
+            float x[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float v0 = (i == col) ? 1.f : 0.f, v1 = 0.f;
+            for (int i = 0; i < 16; ++i) {
+                float a0 = (i == col) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int s = 0; s < i; s += 2) {
-                v0 = fmaf(-L[(p * 16 + i) * TRI_LD + p * 16 + s], x[s], v0);
-                if (s + 1 < i) v1 = fmaf(-L[(p * 16 + i) * TRI_LD + p * 16 + s + 1], x[s + 1], v1);
+                for (int s = 0; s < i; s += 4) {
+                    a0 = fmaf(-Lp[i * TRI_LD + s], x[s], a0);
+                    if (s + 1 < i) a1 = fmaf(-Lp[i * TRI_LD + s + 1], x[s + 1], a1);
+                    if (s + 2 < i) a2 = fmaf(-Lp[i * TRI_LD + s + 2], x[s + 2], a2);
+                    if (s + 3 < i) a3 = fmaf(-Lp[i * TRI_LD + s + 3], x[s + 3], a3);
+                }
+                x[i] = (a0 + a1) + (a2 + a3);
             }
-            x[i] = v0 + v1;
-        }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) INV[(p * 16 + i) * TRI_LD + p * 16 + col] = x[i];
+            for (int i = 0; i < 16; ++i) INV[(16 * p + i) * TRI_LD + 16 * p + col] = x[i];
+        }
+    } else {
+        for (int idx = tid - 128; idx < 6 * 64; idx += NT - 128) {
+            const int blk = idx >> 6, w = idx & 63;
+            const int p = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+            const int q = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            *reinterpret_cast<float4 *>(INV + (16 * p + (w >> 2)) * TRI_LD + 16 * q + 4 * (w & 3)) =
+                make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
     __syncthreads();
+
+    // ---- 1a: T_b = L_pq X_qq for (p, q) = (1, 0), (3, 2)
+    if (tid < 128) {
+        const int b = tid >> 6, row = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+        const int p = 2 * b + 1, q = 2 * b;
+        const float *Lr = L + (16 * p + row) * TRI_LD + 16 * q;
+        const float *X = INV + (16 * q) * TRI_LD + 16 * q + c4;
+        float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int lvl = 1; lvl < 4; ++lvl) {
-        const int nblk = 4 - lvl;
-        for (int e = tid; e < nblk * 256; e += NT) {
-            const int b = e >> 8, i = (e >> 4) & 15, jj = e & 15;
-            const int p = lvl + b, qb = b;
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int rr = 0; rr < lvl; ++rr) {
-                const int r = qb + rr;
-#pragma unroll
-                for (int s = 0; s < 16; s += 2) {
-                    a0 = fmaf(L[(p * 16 + i) * TRI_LD + r * 16 + s], INV[(r * 16 + s) * TRI_LD + qb * 16 + jj], a0);
-                    a1 = fmaf(L[(p * 16 + i) * TRI_LD + r * 16 + s + 1], INV[(r * 16 + s + 1) * TRI_LD + qb * 16 + jj], a1);
-                }
-            }
-            tmp[(b * 16 + i) * 17 + jj] = a0 + a1;
+        for (int s = 0; s < 16; ++s) {
+            const float l = Lr[s];
+            const float4 x = *reinterpret_cast<const float4 *>(X + s * TRI_LD);
+            acc01 = __ffma2_rn(make_float2(l, l), make_float2(x.x, x.y), acc01);
+            acc23 = __ffma2_rn(make_float2(l, l), make_float2(x.z, x.w), acc23);
         }
-        __syncthreads();
-        for (int e = tid; e < nblk * 256; e += NT) {
-            const int b = e >> 8, i = (e >> 4) & 15, jj = e & 15;
-            const int p = lvl + b, qb = b;
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int s = 0; s < 16; s += 2) {
-                a0 = fmaf(INV[(p * 16 + i) * TRI_LD + p * 16 + s], tmp[(b * 16 + s) * 17 + jj], a0);
-                a1 = fmaf(INV[(p * 16 + i) * TRI_LD + p * 16 + s + 1], tmp[(b * 16 + s + 1) * 17 + jj], a1);
-            }
-            INV[(p * 16 + i) * TRI_LD + qb * 16 + jj] = -(a0 + a1);
-        }
-        __syncthreads();
+        *reinterpret_cast<float4 *>(T + (16 * b + row) * TRI_LD + c4) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
     }
+    __syncthreads();
+    // ---- 1b: X_pq = -X_pp T_b
+    if (tid < 128) {
+        const int b = tid >> 6, row = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+        const int p = 2 * b + 1, q = 2 * b;
+        const float *Xr = INV + (16 * p + row) * TRI_LD + 16 * p;
+        const float *Tb = T + (16 * b) * TRI_LD + c4;
+        float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+            const float l = Xr[s];
+            const float4 t = *reinterpret_cast<const float4 *>(Tb + s * TRI_LD);
+            acc01 = __ffma2_rn(make_float2(l, l), make_float2(t.x, t.y), acc01);
+            acc23 = __ffma2_rn(make_float2(l, l), make_float2(t.z, t.w), acc23);
+        }
+        *reinterpret_cast<float4 *>(INV + (16 * p + row) * TRI_LD + 16 * q + c4) =
+            make_float4(-acc01.x, -acc01.y, -acc23.x, -acc23.y);
+    }
+    __syncthreads();
+
+    // ---- 2a: P = L[32:64, 0:32] X_A  (X_A lower triangular, zeros above)
+    if (tid < 256) {
+        const int row = tid >> 3, c4 = 4 * (tid & 7);
+        const float *Lr = L + (32 + row) * TRI_LD;
+        const float *X = INV + c4;
+        float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
+#pragma unroll 8
+        for (int s = 0; s < 32; ++s) {
+            const float l = Lr[s];
+            const float4 x = *reinterpret_cast<const float4 *>(X + s * TRI_LD);
+            acc01 = __ffma2_rn(make_float2(l, l), make_float2(x.x, x.y), acc01);
+            acc23 = __ffma2_rn(make_float2(l, l), make_float2(x.z, x.w), acc23);
+        }
+        *reinterpret_cast<float4 *>(T + row * TRI_LD + c4) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
+    }
+    __syncthreads();
+    // ---- 2b: INV[32:64, 0:32] = -X_B P; row r of X_B is zero beyond column r,
+    // and a warp's rows end at 4 (warp + 1), so that bounds its loop
+    if (tid < 256) {
+        const int row = tid >> 3, c4 = 4 * (tid & 7);
+        const int smax = 4 * ((tid >> 5) + 1);
+        const float *Xr = INV + (32 + row) * TRI_LD + 32;
+        const float *P = T + c4;
+        float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
+#pragma unroll 4
+        for (int s = 0; s < smax; ++s) {
+            const float l = Xr[s];
+            const float4 t = *reinterpret_cast<const float4 *>(P + s * TRI_LD);
+            acc01 = __ffma2_rn(make_float2(l, l), make_float2(t.x, t.y), acc01);
+            acc23 = __ffma2_rn(make_float2(l, l), make_float2(t.z, t.w), acc23);
+        }
+        *reinterpret_cast<float4 *>(INV + (32 + row) * TRI_LD + c4) = make_float4(-acc01.x, -acc01.y, -acc23.x, -acc23.y);
+    }
+    __syncthreads();
 }
 
 }  // namespace kda
