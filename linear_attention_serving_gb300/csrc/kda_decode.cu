@@ -57,26 +57,32 @@ struct DecSmem {
 };
 
 // One thread starts the bulk copies of item `item` (its state and token rows)
-// into shared memory; completion is counted on `bar`.  `nacc` was read ahead of
-// time; when it is out of range nothing is copied and the barrier completes
-// without data.
-template <typename InT>
-__device__ __forceinline__ void issue_item(int item, int nacc, int H, int W, const float *__restrict__ state,
-                                           const InT *__restrict__ q, const InT *__restrict__ k,
-                                           const InT *__restrict__ v, const float *__restrict__ z,
-                                           const InT *__restrict__ ck, const InT *__restrict__ cv,
-                                           const float *__restrict__ cz, uint8_t *sm, const DecSmem &L,
-                                           uint64_t *bar) {
+// into shared memory; completion is counted on `bar`, in two parts so that the
+// state copy can start as soon as the state buffer is free and the rows copy
+// as soon as the row buffer is.  `nacc` was read ahead of time; when it is out
+// of range nothing is copied and the barrier completes without data.
+__device__ __forceinline__ uint32_t item_bytes(int nacc, int W, uint32_t rowb) {
+    return (uint32_t)(D * D * 4) + (uint32_t)nacc * (2 * rowb + 512) + (uint32_t)W * (3 * rowb + 512);
+}
+__device__ __forceinline__ void issue_state(int item, int nacc, int W, uint32_t rowb, const float *__restrict__ state,
+                                            uint8_t *sm, const DecSmem &L, uint64_t *bar) {
     if (nacc < 0 || nacc > W - 1) {
         mbar_arrive(bar);
         return;
     }
+    mbar_expect_tx(bar, item_bytes(nacc, W, rowb));
+    bulk_g2s(sm + L.state, state + (size_t)item * D * D, D * D * 4, bar);
+}
+template <typename InT>
+__device__ __forceinline__ void issue_rows(int item, int nacc, int H, int W, const InT *__restrict__ q,
+                                           const InT *__restrict__ k, const InT *__restrict__ v,
+                                           const float *__restrict__ z, const InT *__restrict__ ck,
+                                           const InT *__restrict__ cv, const float *__restrict__ cz, uint8_t *sm,
+                                           const DecSmem &L, uint64_t *bar) {
+    if (nacc < 0 || nacc > W - 1) return;
     const int b = item / H, h = item - b * H;
     const int ntok = nacc + W;
     const uint32_t rowb = (uint32_t)(D * sizeof(InT));
-    const uint32_t bytes = (uint32_t)(D * D * 4) + (uint32_t)nacc * (2 * rowb + 512) + (uint32_t)W * (3 * rowb + 512);
-    mbar_expect_tx(bar, bytes);
-    bulk_g2s(sm + L.state, state + (size_t)item * D * D, D * D * 4, bar);
     for (int t = 0; t < ntok; ++t) {
         uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
         if (t < nacc) {
@@ -130,6 +136,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
     const int part = lane / (32 / DEC_TPC);
     const int rbase = part * DEC_R;
     const int n_items = N * H;
+    const uint32_t rowb = (uint32_t)(D * sizeof(InT));
 
     if (tid == 0) {
         mbar_init(&full_bar, 1);
@@ -143,7 +150,10 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
     if (item < n_items) {
         nacc_cur = nacc_p ? nacc_p[item / H] : 0;
         load_betas(item, H, W, tid, beta, cb, bc_cur, bw_cur);
-        if (tid == 0) issue_item<InT>(item, nacc_cur, H, W, state, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
+        if (tid == 0) {
+            issue_state(item, nacc_cur, W, rowb, state, sm, L, &full_bar);
+            issue_rows<InT>(item, nacc_cur, H, W, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
+        }
     }
     bool timed_out = false;
     for (int it = 0; item < n_items; item += gridDim.x, ++it) {
@@ -165,8 +175,10 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
             // out-of-range accepted count: this sequence is left untouched
             if (tid == 0) {
                 atomicOr(err, KDA_DEVERR_NUM_ACCEPTED);
-                if (next < n_items)
-                    issue_item<InT>(next, nacc_next, H, W, state, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
+                if (next < n_items) {
+                    issue_state(next, nacc_next, W, rowb, state, sm, L, &full_bar);
+                    issue_rows<InT>(next, nacc_next, H, W, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
+                }
             }
             nacc_cur = nacc_next;
             bc_cur = bc_next;
@@ -179,51 +191,49 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
         if (tid < nacc) sbt[tid] = bc_cur;
         if (tid < W) sbt[nacc + tid] = bw_cur;
 
-        // state and token rows of this item: shared memory -> registers / vectors
+        // state of this item: shared memory -> registers; then the state buffer
+        // takes the next item's state while the token rows are still in use
         float s[DEC_R];
 #pragma unroll
         for (int i = 0; i < DEC_R; ++i) s[i] = sS[(rbase + i) * D + col];
-        const float eA = expf(A[h]);
-        for (int idx = tid; idx < ntok * D; idx += DEC_THREADS) {
-            const int t = idx >> 7, c = idx & 127;
-            const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
-            const float qq = t < nacc ? 0.f : to_f32(reinterpret_cast<const InT *>(slot)[c]);
-            const float kk = to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
-            const float vv = to_f32(reinterpret_cast<const InT *>(slot + 1024)[c]);
-            const float zz = reinterpret_cast<const float *>(slot + 1536)[c];
-            kt[t][vidx(c)] = kk;
-            qt[t][vidx(c)] = qq;
-            kh[t][vidx(c)] = expf(kda_gate(g_min, eA, zz));  // alpha, scaled below
-            vt[t][c] = vv;
-            // the new drafts' projected inputs replace this sequence's cache slots
-            if (t > nacc) {
-                const size_t dst = (((size_t)b * (W - 1) + (t - nacc - 1)) * H + h) * D + c;
-                cq[dst] = reinterpret_cast<const InT *>(slot)[c];
-                ck[dst] = reinterpret_cast<const InT *>(slot + 512)[c];
-                cv[dst] = reinterpret_cast<const InT *>(slot + 1024)[c];
-                cz[dst] = zz;
-            }
-        }
         __syncthreads();
-        if (tid < W - 1) cb[((size_t)b * (W - 1) + tid) * H + h] = sbt[nacc + 1 + tid];
-        // shared state and row buffers are free: start the next item's copies now
-        if (tid == 0 && next < n_items)
-            issue_item<InT>(next, nacc_next, H, W, state, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
+        if (tid == 0 && next < n_items) issue_state(next, nacc_next, W, rowb, state, sm, L, &full_bar);
+        const float eA = expf(A[h]);
         if (tid < D) {
-            // cumulative decay s_t over the step's tokens, in registers
-            const int c = vidx(tid);
+            // channel c of every token: inputs, the cumulative decay s_t over the
+            // step's tokens, and the scaled vectors s_t k, k / s_t, s_t q
+            const int c = tid, vc = vidx(c);
             float sc = 1.f;
             for (int t = 0; t < ntok; ++t) {
-                const float al = kh[t][c], kk = kt[t][c], qq = qt[t][c];
-                sc *= al;
-                const float inv = __frcp_rn(sc);
-                kt[t][c] = kk * sc;
-                kh[t][c] = kk * inv;
-                qt[t][c] = qq * sc;
-                if (t == nacc) scommit[c] = sc;
+                const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
+                const float qq = t < nacc ? 0.f : to_f32(reinterpret_cast<const InT *>(slot)[c]);
+                const float kk = to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
+                const float zz = reinterpret_cast<const float *>(slot + 1536)[c];
+                sc *= expf(kda_gate(g_min, eA, zz));
+                kt[t][vc] = kk * sc;
+                kh[t][vc] = __fdividef(kk, sc);
+                qt[t][vc] = qq * sc;
+                vt[t][c] = to_f32(reinterpret_cast<const InT *>(slot + 1024)[c]);
+                if (t == nacc) scommit[vc] = sc;
             }
+        } else if (tid == D) {
+            // the new drafts' projected inputs replace this sequence's cache slots
+            for (int t = nacc + 1; t < ntok; ++t) {
+                const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
+                const size_t row = ((size_t)b * (W - 1) + (t - nacc - 1)) * H + h;
+                bulk_s2g(cq + row * D, slot, rowb);
+                bulk_s2g(ck + row * D, slot + 512, rowb);
+                bulk_s2g(cv + row * D, slot + 1024, rowb);
+                bulk_s2g(cz + row * D, slot + 1536, 512);
+            }
+            bulk_commit();
         }
+        if (tid < W - 1) cb[((size_t)b * (W - 1) + tid) * H + h] = sbt[nacc + 1 + tid];
         __syncthreads();
+        // the row buffers are free once the cache copies have read them: the next item's token rows
+        if (tid == D) bulk_wait_read_all();
+        if (tid == D && next < n_items)
+            issue_rows<InT>(next, nacc_next, H, W, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
 
         // the recurrence over replay + bonus + drafts
         const float *bt = sbt;
@@ -269,7 +279,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                 // commit: S = Diag(s_t) S^, written back in place
 #pragma unroll
                 for (int i = 0; i < DEC_R; ++i)
-                    Sg[(size_t)(rbase + i) * D + col] = s[i] * scommit[vidx(rbase + i)];
+                    __stcs(&Sg[(size_t)(rbase + i) * D + col], s[i] * scommit[vidx(rbase + i)]);
             }
         }
 
@@ -278,6 +288,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
         bw_cur = bw_next;
         __syncthreads();  // vectors are rewritten by the next item
     }
+    if (tid == D) bulk_wait_all();  // the cache copies have landed before the block exits
 }
 
 }  // namespace

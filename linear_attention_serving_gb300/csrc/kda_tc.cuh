@@ -177,7 +177,23 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64
             tmem_d),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate));
 }
-// Arrive once on `bar` when every previously issued tcgen05.mma of this thread completes.
+// The same with A in TMEM (lane m = row m, K packed two bf16 per 32-bit column,
+// 8 columns per K = 16 step).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                            bool accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
+            tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate));
+}
+// Copy 128 rows x 32 bytes (one K = 16 step of a K-major bf16 A operand,
+// described like an MMA operand) from shared memory into TMEM lanes 0-127,
+// 8 columns from taddr; it lands in the layout mma_bf16_ta reads (checked
+// against a host product).  Ordered with this thread's MMAs.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// Arrive once on `bar` when every previously issued tcgen05.mma / tcgen05.cp of this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
