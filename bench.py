@@ -45,6 +45,7 @@ KERNEL_SOURCES = {
     "scan_simt": "linear_attention_serving_gb300/csrc/kda_scan_simt.cu",
     "prep_tc": "linear_attention_serving_gb300/csrc/kda_prep_tc.cu",
     "scan_tc": "linear_attention_serving_gb300/csrc/kda_scan_tc.cu",
+    "out_tc": "linear_attention_serving_gb300/csrc/kda_out_tc.cu",
     "decode": "linear_attention_serving_gb300/csrc/kda_decode.cu",
 }
 
@@ -368,7 +369,8 @@ def main():
     dom = max(tot, key=tot.get) if tot else None
     chunk_heads = H * ((T + 63) // 64)
     algo = {"prep_simt": roofline.prep_bytes_per_chunk_head(), "prep_tc": roofline.prep_bytes_per_chunk_head(),
-            "scan_simt": roofline.scan_bytes_per_chunk_head(), "scan_tc": roofline.scan_bytes_per_chunk_head()}
+            "scan_simt": roofline.scan_bytes_per_chunk_head(), "scan_tc": roofline.scan_bytes_per_chunk_head(),
+            "out_tc": roofline.out_bytes_per_chunk_head()}
     roof = None
     if dom is not None:
         avg_ms = statistics.mean(kt[dom])

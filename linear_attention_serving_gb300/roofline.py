@@ -34,6 +34,13 @@ def scan_bytes_per_chunk_head(C: int = C, D: int = D) -> int:
     return 10 * C * D + 4 * C ** 2
 
 
+def out_bytes_per_chunk_head(C: int = C, D: int = D) -> int:
+    """The output kernel of this library (not a kernel of the pages' split): it
+    reads Q' and O0 (bf16, C x D each) and the entering state (bf16, D x D) and
+    writes O (bf16, C x D)."""
+    return 3 * 2 * C * D + 2 * D * D
+
+
 def prefill_kernel_bytes(T: int, heads: int, n_seqs: int = 1, C: int = C, D: int = D) -> float:
     """Whole-call traffic by the pages' kernel-level count, pro-rated by tokens
     (padding earns nothing): (T / C)(8 C^2 + 22 C D) per head + 8 D^2 per (sequence, head)."""
