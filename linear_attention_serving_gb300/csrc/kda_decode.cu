@@ -120,7 +120,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
     extern __shared__ __align__(128) uint8_t smdyn[];
     __shared__ uint64_t full_bar;
     __shared__ float sbeta[2][2 * MAX_W];
-    __shared__ float scommit[VPAD];
+    __shared__ __align__(16) float scommit[VPAD];
 
     const DecSmem L(W);
     uint8_t *sm = smdyn;
@@ -144,12 +144,17 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
     }
     __syncthreads();
     int item = blockIdx.x;
-    // per-item scalars read one item ahead: accepted count and the betas
-    int nacc_cur = 0;
-    float bc_cur = 0.f, bw_cur = 0.f;
+    // per-item scalars (accepted count and betas) are read two items ahead, so
+    // their global-load latency never sits in front of a bulk-copy issue
+    int nacc_cur = 0, nacc_nx = 0;
+    float bc_cur = 0.f, bw_cur = 0.f, bc_nx = 0.f, bw_nx = 0.f;
     if (item < n_items) {
         nacc_cur = nacc_p ? nacc_p[item / H] : 0;
         load_betas(item, H, W, tid, beta, cb, bc_cur, bw_cur);
+        if (item + (int)gridDim.x < n_items) {
+            nacc_nx = nacc_p ? nacc_p[(item + gridDim.x) / H] : 0;
+            load_betas(item + gridDim.x, H, W, tid, beta, cb, bc_nx, bw_nx);
+        }
         if (tid == 0) {
             issue_state(item, nacc_cur, W, rowb, state, sm, L, &full_bar);
             issue_rows<InT>(item, nacc_cur, H, W, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
@@ -158,12 +163,13 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
     bool timed_out = false;
     for (int it = 0; item < n_items; item += gridDim.x, ++it) {
         const int b = item / H, h = item - b * H;
-        const int next = item + gridDim.x;
-        int nacc_next = 0;
-        float bc_next = 0.f, bw_next = 0.f;
-        if (next < n_items) {
-            nacc_next = nacc_p ? nacc_p[next / H] : 0;
-            load_betas(next, H, W, tid, beta, cb, bc_next, bw_next);
+        const int next = item + gridDim.x, next2 = next + gridDim.x;
+        const int nacc_next = nacc_nx;
+        int nacc_nn = 0;
+        float bc_nn = 0.f, bw_nn = 0.f;
+        if (next2 < n_items) {
+            nacc_nn = nacc_p ? nacc_p[next2 / H] : 0;
+            load_betas(next2, H, W, tid, beta, cb, bc_nn, bw_nn);
         }
         const int nacc = nacc_cur;
         if (!mbar_wait(&full_bar, (uint32_t)(it & 1))) timed_out = true;
@@ -180,9 +186,12 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                     issue_rows<InT>(next, nacc_next, H, W, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
                 }
             }
-            nacc_cur = nacc_next;
-            bc_cur = bc_next;
-            bw_cur = bw_next;
+            nacc_cur = nacc_nx;
+            bc_cur = bc_nx;
+            bw_cur = bw_nx;
+            nacc_nx = nacc_nn;
+            bc_nx = bc_nn;
+            bw_nx = bw_nn;
             continue;
         }
         const int ntok = nacc + W;
@@ -278,14 +287,22 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
             if (t == nacc) {
                 // commit: S = Diag(s_t) S^, written back in place
 #pragma unroll
-                for (int i = 0; i < DEC_R; ++i)
-                    __stcs(&Sg[(size_t)(rbase + i) * D + col], s[i] * scommit[vidx(rbase + i)]);
+                for (int i = 0; i < DEC_R; i += 4) {
+                    const float4 sc4 = *reinterpret_cast<const float4 *>(&scommit[vidx(rbase + i)]);
+                    __stcs(&Sg[(size_t)(rbase + i) * D + col], s[i] * sc4.x);
+                    __stcs(&Sg[(size_t)(rbase + i + 1) * D + col], s[i + 1] * sc4.y);
+                    __stcs(&Sg[(size_t)(rbase + i + 2) * D + col], s[i + 2] * sc4.z);
+                    __stcs(&Sg[(size_t)(rbase + i + 3) * D + col], s[i + 3] * sc4.w);
+                }
             }
         }
 
-        nacc_cur = nacc_next;
-        bc_cur = bc_next;
-        bw_cur = bw_next;
+        nacc_cur = nacc_nx;
+        bc_cur = bc_nx;
+        bw_cur = bw_nx;
+        nacc_nx = nacc_nn;
+        bc_nx = bc_nn;
+        bw_nx = bw_nn;
         __syncthreads();  // vectors are rewritten by the next item
     }
     if (tid == D) bulk_wait_all();  // the cache copies have landed before the block exits
