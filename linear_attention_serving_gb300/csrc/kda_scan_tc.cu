@@ -17,10 +17,11 @@
 //
 // Warps 0-3 (chain): thread t owns state row t (TMEM lane t); the fp32 state
 //   master lives in registers, its bf16 copy (double buffered) in shared
-//   memory is the B operand (MN-major) of the next chunk's MMA, which thread 0
-//   issues.  The per-chunk path is kept short: descriptors are precomputed,
-//   a_C and H are read while the MMA runs, and the stage is released by a
-//   plain arrival once every chain thread has read it.
+//   memory is the B operand (MN-major) of the next chunk's MMA.  Each warp
+//   publishes its 32 rows of that operand on an mbarrier, so the warps never
+//   wait for one another; a_C and H are read while the MMA runs.
+// Warp 5 (MMA): waits for all four warps' rows and the chunk's stage, issues
+//   the chunk's MMA and commits it.
 // Warp 4 (producer): streams each chunk's G, a_C and the block's H slices
 //   through a bulk-copy pipeline.
 // Every wait is bounded; on a timeout the block records KDA_DEVERR_TIMEOUT,
@@ -34,9 +35,9 @@ namespace {
 
 using namespace tc;
 
-constexpr int CHAIN = 128;  // warps 0-3
 constexpr int PRODUCER_WARP = 4;
-constexpr int THREADS = 160;
+constexpr int MMA_WARP = 5;
+constexpr int THREADS = 192;
 
 // pipeline stage: G (32 KB) | a_C | H slices
 template <int N>
@@ -88,27 +89,33 @@ struct SOp {
     static constexpr uint32_t MODE = N == 16 ? SWZ_32B : SWZ_128B;
 };
 
-// bf16 copy of this thread's state row t into the S operand
+// bf16 pairs of this thread's state row
 template <int N>
-__device__ __forceinline__ void write_sop(uint8_t *sop, int t, const float *s) {
+__device__ __forceinline__ void pack_row(const float *s, uint4 *pk) {
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c) pk[c] = pack8f(s + 8 * c);
+}
+
+// the packed row t into the S operand
+template <int N>
+__device__ __forceinline__ void write_sop(uint8_t *sop, int t, const uint4 *pk) {
     uint8_t *row = sop + t * SOp<N>::ROW;
 #pragma unroll
     for (int c = 0; c < N / 8; ++c) {
         const int sc = N == 16 ? (c ^ ((t >> 2) & 1)) : (c ^ (t & 7));
-        *reinterpret_cast<uint4 *>(row + sc * 16) = pack8f(s + 8 * c);
+        *reinterpret_cast<uint4 *>(row + sc * 16) = pk[c];
     }
 }
 
-// bf16 copy of this thread's state row t into the record's S field (32-byte
-// swizzled 16-column blocks), the same values as the S operand
+// the packed row t into the record's S field (32-byte swizzled 16-column
+// blocks): the same values as the S operand
 template <int N>
-__device__ __forceinline__ void store_s(char *rec, int col0, int t, const float *s) {
+__device__ __forceinline__ void store_s(char *rec, int col0, int t, const uint4 *pk) {
 #pragma unroll
     for (int blk = 0; blk < N / 16; ++blk) {
         char *row = rec + REC_BF16_S + (size_t)(col0 / 16 + blk) * REC_BF16_SBLOCK + t * 32;
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-            *reinterpret_cast<uint4 *>(row + ((c ^ ((t >> 2) & 1)) << 4)) = pack8f(s + 16 * blk + 8 * c);
+        for (int c = 0; c < 2; ++c) *reinterpret_cast<uint4 *>(row + ((c ^ ((t >> 2) & 1)) << 4)) = pk[2 * blk + c];
     }
 }
 
@@ -144,7 +151,7 @@ template <int N, int STAGES>
 __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
     using ST = Stage<N>;
     extern __shared__ uint8_t smraw[];
-    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], g_bar;
+    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], g_bar, sop_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -172,9 +179,10 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);  // released by chain thread 0 once all chain threads read it
+            mbar_init(&empty_bar[s], 4);  // released by the four chain warps once they read it
         }
         mbar_init(&g_bar, 1);
+        mbar_init(&sop_bar, 4);  // the four chain warps' rows of the next S operand
         abort_flag = 0;
         mbar_fence_init();
     }
@@ -215,10 +223,41 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
                 if (timed_out) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
             }
         }
+    } else if (warp == MMA_WARP) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_bf16_f32_bmn(128, N);
+            const uint64_t gd0 = sdesc_sw128(smem_u32(sm + ST::G));
+            const uint64_t sd0 = sop_desc<N>(sop0);
+            int stage = 0;
+            uint32_t ph = 0;
+            for (int i = 0; i < nchunks; ++i) {
+                const int b = i & 1;
+                // chunk i's S operand is complete (and the accumulator of chunk i - 1 read)
+                if (!mbar_wait(&sop_bar, (uint32_t)(i & 1)) || !mbar_wait(&full_bar[stage], ph) ||
+                    *(volatile int *)&abort_flag) {
+                    abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t gd = gd0 + (uint64_t)((stage * ST::BYTES) >> 4);
+                const uint64_t sd = sd0 + (uint64_t)((b * ST::SOP) >> 4);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16(tmem_g, gd + (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                             sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDESC, k > 0);
+                mma_commit(&g_bar);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
     } else if (warp < 4) {
         // ------------------------------------------------------------ chain warps
         const int t = tid;  // state row == TMEM lane
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const bool segs = a.mode == SCAN_SEGMENTS;
         float s[N];
 #pragma unroll
         for (int j = 0; j < N; ++j) s[j] = state_init(a, unit, h, t, col0 + j);
@@ -227,54 +266,43 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
 #pragma unroll
             for (int j = 0; j < N; j += 4) *reinterpret_cast<float4 *>(f + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
         }
-        write_sop<N>(sop0, t, s);
-        fence_async_smem();
-        bool aborted = bar_or(1, CHAIN, false);
-        const bool segs = a.mode == SCAN_SEGMENTS;
         ChunkInfo ci_next;
-        if (segs && nchunks > 0) ci_next = plan_chunk(p, c0);
-        constexpr uint32_t IDESC = idesc_bf16_f32_bmn(128, N);
-        const uint64_t gd0 = sdesc_sw128(smem_u32(sm + ST::G));
-        const uint64_t sd0 = sop_desc<N>(sop0);
+        if (segs && nchunks > 0) {
+            ci_next = plan_chunk(p, c0);
+            if (ci_next.flags & CHUNK_FIRST) {
+                // a document starts at the segment's first chunk
+#pragma unroll
+                for (int j = 0; j < N; ++j) s[j] = state_reset(a, ci_next.doc, h, t, col0 + j);
+            }
+        }
+        uint4 pk[N / 8];  // bf16 copy of the state row entering the current chunk
+        pack_row<N>(s, pk);
+        write_sop<N>(sop0, t, pk);
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sop_bar);
         const bool write_final = value_cols && a.final_state && a.phase != 1;
+        bool ok = true;
         int stage = 0;
         uint32_t ph = 0;
-        for (int i = 0; i < nchunks && !aborted; ++i) {
+        for (int i = 0; i < nchunks; ++i) {
             const int b = i & 1;
             int doc = unit;
             bool last = i == nchunks - 1;
+            bool next_first = false;
             if (segs) {
                 const ChunkInfo ci = ci_next;
-                if (i + 1 < nchunks) ci_next = plan_chunk(p, c0 + i + 1);
+                if (i + 1 < nchunks) {
+                    ci_next = plan_chunk(p, c0 + i + 1);
+                    next_first = (ci_next.flags & CHUNK_FIRST) != 0;
+                }
                 doc = ci.doc;
                 last = (ci.flags & CHUNK_LAST) != 0;
-                if (ci.flags & CHUNK_FIRST) {
-                    // a document starts here: the state restarts (uniform branch)
-#pragma unroll
-                    for (int j = 0; j < N; ++j) s[j] = state_reset(a, ci.doc, h, t, col0 + j);
-                    write_sop<N>(sop0 + b * ST::SOP, t, s);
-                    fence_async_smem();
-                    bar_or(1, CHAIN, false);
-                }
             }
-            bool ok = true;
-            if (t == 0) {
-                ok = mbar_wait(&full_bar[stage], ph);
-                if (ok) {
-                    tc_fence_after();
-                    const uint64_t gd = gd0 + (uint64_t)((stage * ST::BYTES) >> 4);
-                    const uint64_t sd = sd0 + (uint64_t)((b * ST::SOP) >> 4);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        mma_bf16(tmem_g, gd + (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
-                                 sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDESC, k > 0);
-                    mma_commit(&g_bar);
-                }
-            } else {
-                ok = mbar_wait(&full_bar[stage], ph);
-            }
+            ok = mbar_wait(&full_bar[stage], ph);
             // the entering state of this chunk, for the output kernel
-            if (emit_s) store_s<N>(records + (size_t)(c0 + i) * rec_stride + (size_t)h * REC_BF16_BYTES, col0, t, s);
+            if (emit_s) store_s<N>(records + (size_t)(c0 + i) * rec_stride + (size_t)h * REC_BF16_BYTES, col0, t, pk);
             // ---- S <- Diag(a_C) S + H - G S; a_C and H are read while the MMA runs
             const uint8_t *stg = sm + stage * ST::BYTES;
             const float ac = reinterpret_cast<const float *>(stg + ST::AC)[t];
@@ -284,7 +312,11 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
 #pragma unroll
                 for (int j = 0; j < N; ++j) hv[j] = 0.f;
             ok = ok && mbar_wait(&g_bar, (uint32_t)(i & 1));
-            __syncwarp();
+            // a warp stops as a whole; the others then run out of their bounded waits
+            if (!__all_sync(0xffffffffu, ok) || *(volatile int *)&abort_flag) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             float d[N];
             tmem_row<N>(tmem_g + lane_off, d);
@@ -295,23 +327,34 @@ __global__ void __launch_bounds__(THREADS, 1) scan_tc_kernel(ScanArgs a) {
                 s[j] = r2.x;
                 s[j + 1] = r2.y;
             }
-            write_sop<N>(sop0 + (b ^ 1) * ST::SOP, t, s);
             if (write_final && last) {
                 float *f = a.final_state + (((size_t)doc * a.H + h) * D + t) * D + col0;
 #pragma unroll
                 for (int j = 0; j < N; j += 4) *reinterpret_cast<float4 *>(f + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
             }
-            fence_async_smem();
+            if (next_first) {
+                // a document starts at the next chunk: the state restarts there
+#pragma unroll
+                for (int j = 0; j < N; ++j) s[j] = state_reset(a, ci_next.doc, h, t, col0 + j);
+            }
+            pack_row<N>(s, pk);
+            if (i + 1 < nchunks) {
+                write_sop<N>(sop0 + (b ^ 1) * ST::SOP, t, pk);
+                fence_async_smem();
+            }
             tc_fence_before();
-            aborted = bar_or(1, CHAIN, !ok);
-            if (t == 0 && !aborted) mbar_arrive(&empty_bar[stage]);
+            __syncwarp();
+            if (lane == 0) {
+                if (i + 1 < nchunks) mbar_arrive(&sop_bar);
+                mbar_arrive(&empty_bar[stage]);
+            }
             if (++stage == STAGES) {
                 stage = 0;
                 ph ^= 1u;
             }
         }
-        if (aborted) {
-            if (t == 0) {
+        if (!ok) {
+            if (lane == 0) {
                 abort_flag = 1;
                 atomicOr(p.err, KDA_DEVERR_TIMEOUT);
             }
