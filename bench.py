@@ -41,12 +41,14 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "KDA prefill tokens/s (H=16,T=8K) & decode tokens/s (B=256); % of roofline"
 KERNEL_SOURCES = {
-    "prep_simt": "linear_attention_serving_gb300/csrc/kda_prep_simt.cu",
-    "scan_simt": "linear_attention_serving_gb300/csrc/kda_scan_simt.cu",
-    "prep_tc": "linear_attention_serving_gb300/csrc/kda_prep_tc.cu",
-    "scan_tc": "linear_attention_serving_gb300/csrc/kda_scan_tc.cu",
-    "out_tc": "linear_attention_serving_gb300/csrc/kda_out_tc.cu",
-    "decode": "linear_attention_serving_gb300/csrc/kda_decode.cu",
+    "prep_simt": ["linear_attention_serving_gb300/csrc/kda_prep_simt.cu"],
+    "scan_simt": ["linear_attention_serving_gb300/csrc/kda_scan_simt.cu"],
+    "prep_tc": ["linear_attention_serving_gb300/csrc/kda_prep_tc.cu", "linear_attention_serving_gb300/csrc/kda_prep_body.cuh"],
+    "scan_tc": ["linear_attention_serving_gb300/csrc/kda_scan_tc.cu", "linear_attention_serving_gb300/csrc/kda_scan_body.cuh"],
+    "fused_tc": ["linear_attention_serving_gb300/csrc/kda_fused_tc.cu", "linear_attention_serving_gb300/csrc/kda_prep_body.cuh",
+                 "linear_attention_serving_gb300/csrc/kda_scan_body.cuh"],
+    "out_tc": ["linear_attention_serving_gb300/csrc/kda_out_tc.cu"],
+    "decode": ["linear_attention_serving_gb300/csrc/kda_decode.cu"],
 }
 
 
@@ -67,11 +69,14 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def src_sha(path):
-    full = os.path.join(ROOT, path)
-    if not os.path.exists(full):
-        return None
-    return hashlib.sha256(open(full, "rb").read()).hexdigest()[:16]
+def src_sha(paths):
+    h = hashlib.sha256()
+    for path in paths:
+        full = os.path.join(ROOT, path)
+        if not os.path.exists(full):
+            return None
+        h.update(open(full, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def traffic_for(kernel):
@@ -81,7 +86,7 @@ def traffic_for(kernel):
         t = json.load(open(TRAFFIC_FILE))[kernel]
     except Exception:
         return None
-    if t.get("src_sha") != src_sha(KERNEL_SOURCES.get(kernel, "")):
+    if t.get("src_sha") != src_sha(KERNEL_SOURCES.get(kernel, [])):
         return None
     return t.get("bytes_per_launch")
 
@@ -370,7 +375,8 @@ def main():
     chunk_heads = H * ((T + 63) // 64)
     algo = {"prep_simt": roofline.prep_bytes_per_chunk_head(), "prep_tc": roofline.prep_bytes_per_chunk_head(),
             "scan_simt": roofline.scan_bytes_per_chunk_head(), "scan_tc": roofline.scan_bytes_per_chunk_head(),
-            "out_tc": roofline.out_bytes_per_chunk_head()}
+            "out_tc": roofline.out_bytes_per_chunk_head(),
+            "fused_tc": roofline.prep_bytes_per_chunk_head() + roofline.scan_bytes_per_chunk_head()}
     roof = None
     if dom is not None:
         avg_ms = statistics.mean(kt[dom])

@@ -160,7 +160,7 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int 
 // (segment scan) pairs       fp32 [2][H][n_seg][D][D]  (M then S~)
 // (segment scan) s_enter     fp32 [H][n_seg][D][D]
 struct Workspace {
-    size_t off_table, off_doc, off_rec, off_pairs, off_enter, total;
+    size_t off_table, off_doc, off_rec, off_ready, off_pairs, off_enter, total;
     int max_chunks;
     size_t rec_bytes;
 };
@@ -178,6 +178,8 @@ static inline Workspace workspace_layout(int64_t T_total, int H, int n_seqs, int
     off = align_up(off + sizeof(int32_t) * (size_t)(n_seqs + 1), 1024);
     w.off_rec = off;
     off = align_up(off + w.rec_bytes * (size_t)w.max_chunks * (size_t)H, 1024);
+    w.off_ready = off;  // one record-ready flag per (chunk, head) for the fused prefill
+    off = align_up(off + sizeof(int) * (size_t)w.max_chunks * (size_t)H, 256);
     w.off_pairs = off;
     if (n_seg > 0) off = align_up(off + sizeof(float) * 2 * (size_t)H * n_seg * D * D, 1024);
     w.off_enter = off;
@@ -242,6 +244,9 @@ int launch_prep_tc(const void *q, const void *k, const void *v, const float *z, 
 int launch_scan_simt(const ScanArgs &a, int dtype, cudaStream_t s);
 int launch_scan_tc(const ScanArgs &a, int n_sm, cudaStream_t s);
 int launch_out_tc(const Plan &p, int H, const void *records, void *o, int n_sm, cudaStream_t s);
+int launch_fused_tc(const void *q, const void *k, const void *v, const float *z, const float *A,
+                    const float *beta, int H, float g_min, const ScanArgs &sa, int *ready, int n_sm,
+                    cudaStream_t s, bool *used);
 int device_sm_count();
 int launch_compose(const Plan &p, int H, int n_seg, const float *pairs, float *s_enter,
                    cudaStream_t s);

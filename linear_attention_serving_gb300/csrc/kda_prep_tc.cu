@@ -1,540 +1,17 @@
-// kda_prep_tc.cu -- per-(chunk, head) preparation for bf16 inputs, with the
-// contractions on tcgen05 tensor cores.
-//
-// For one 64-token chunk of one head this computes everything of the chunk
-// form that does not depend on the entering state ("Kimi K3: the Manos, the
-// Mythos ..." (SemiAnalysis), "FlashKDA 算法": a = exp(cumsum g), K_decay,
-// Q_decay, K_inv, K_restore, L, INV = (I+L)^-1, M_qk), and folds it into the
-// record the scan consumes:
-//   W = INV Diag(beta) K_decay,  U0 = INV Diag(beta) V,  Q' = Q_decay - M_qk W,
-//   O0 = M_qk U0,  G = K_restore^T W,  H = K_restore^T U0,  a_C,
-// so that a chunk of the scan is S <- Diag(a_C) S + H - G S and O = O0 + Q' S,
-// which is the pages' U = INV Diag(beta)(V - K_decay S), O = Q_decay S + M_qk U,
-// S <- Diag(a[-1]) S + K_restore^T U with the products regrouped.
-//
-// One block per SM walks (chunk, head) units with 512 threads:
-//  1. operand build, thread = (2 channels, 8 tokens): q, k, v, z of its
-//     channels and tokens (the next unit's are prefetched while the current one
-//     computes); gate of "Kimi K3 模型结构（2）" eq. (5) in base-2 log space;
-//     cumulative log decay inside each 16-token sub-tile ("数值问题：1/Γ 会溢出");
-//     e_i = exp(G_i - G_{tile start}) in (e^-80, 1]; and every MMA operand of
-//     the chunk, in bf16 with the 128-byte swizzle: for key tile q the
-//     query-side rows x_i e_i F_pq (x = q and x = k, rows of tiles p >= q) and
-//     the key side k_j exp(Delta_q) / e_j, with F_pp = exp(-Delta_p) <= e^80 and
-//     F_pq = prod_{q<t<p} exp(Delta_t) <= 1; Q_decay; and the token-contiguous
-//     Diag(beta) K_decay, Diag(beta) V, K_restore^T;
-//  2. four block-column MMAs (M = 128 for key tiles 0 and 1, M = 64 for tiles 2
-//     and 3, whose images have at most 64 rows) give M_qk and A_kk, from which
-//     L = StrictTril(Diag(beta) A_kk) (fp32) and the bf16 operand M_qk;
-//  3. INV = (I + L)^-1 in fp32 CUDA cores ("UT 变换"), stored as a bf16 operand;
-//  4. one M = 64, N = 256, K = 64 MMA: INV [Diag(beta) K_decay | Diag(beta) V]
-//     = [W | U0];
-//  5. [W | U0] becomes the MN-major operand of the MMAs issued together:
-//     K_restore^T [W | U0] = [G | H] (M = 128) and, with M = 64,
-//     Q' = I Q_decay + (-M_qk) W and O0 = M_qk U0; G, H, Q', O0 go to the record.
-// The record is staged in shared memory and written with bulk copies that
-// overlap the next unit.  Every wait is bounded; a timeout records
-// KDA_DEVERR_TIMEOUT and ends the block.
-#include "kda_internal.cuh"
-#include "kda_tc.cuh"
-#include "kda_tri.cuh"
+// kda_prep_tc.cu -- the prep kernel for bf16 inputs (device code in
+// kda_prep_body.cuh): persistent blocks, one per SM, over all (chunk, head) units.
+#include "kda_prep_body.cuh"
 
 namespace kda {
 
 namespace {
-
-using namespace tc;
-
-constexpr int PT_THREADS = 512;
-constexpr int PT_TMEM_COLS = 512;
-constexpr float LOG2E = 1.4426950408889634f;
-
-// shared-memory map (bytes from a 1024-aligned base)
-constexpr int SM_AREG = 0;           // A_q images (2 k-blocks x 320 rows x 128 B); after their MMA,
-                                     // fp32 L | INV | scratch, then the record staging.  A read of
-                                     // an image past its valid rows runs into the following bytes;
-                                     // those rows are ignored.
-constexpr int SM_AREG_KB = 40960;    // offset of the second k-block of the A_q images
-constexpr int SM_BQ = 81920;         // key-side images, 4 x (2 k-blocks x 16 rows x 128 B)
-constexpr int SM_B2 = 98304;         // [Diag(beta) K_decay | Diag(beta) V]^T (256 rows x 64 tokens);
-                                     // later [W | U0] MN-major (4 blocks of 64 columns x 64 tokens)
-constexpr int SM_A2 = 131072;        // INV (64 rows x 64), then O0 staging
-constexpr int SM_KRT = 147456;       // K_restore^T: 128 channels x 64 tokens
-constexpr int SM_QD = 163840;        // Q_decay, MN-major (2 blocks of 64 channels x 64 tokens)
-constexpr int SM_MQ = 180224;        // M_qk (64 rows x 64)
-constexpr int SM_ID = 188416;        // identity (64 rows x 64), written once
-constexpr int SM_MISC = 196608;      // beta [64] | partial log2-decay sums [8][128]
-constexpr int SM_BYTES = SM_MISC + 256 + 4096;
-constexpr size_t PREP_TC_SMEM = SM_BYTES + 1024;
-
-// staging of the output record: written after the last MMA has read its
-// operands, read by the bulk stores while the next unit builds B2, KRT, BQ, QD
-constexpr int ST_G = SM_AREG;          // 32 KB
-constexpr int ST_H = SM_AREG + 32768;  // 32 KB
-constexpr int ST_QP = SM_AREG + 65536; // 16 KB
-constexpr int ST_O0 = SM_A2;           // 16 KB
-
-// fp32 matrices inside SM_AREG (row stride TRI_LD floats), below ST_QP
-constexpr int MAT_BYTES = 64 * TRI_LD * 4;
-constexpr int SM_L = 0;
-constexpr int SM_INV = MAT_BYTES;
-constexpr int SM_TMP = 2 * MAT_BYTES;
-static_assert(3 * MAT_BYTES <= 65536, "fp32 work matrices overlap the Q' staging");
-
-__device__ __forceinline__ int arow_base(int q) { return q == 0 ? 0 : (q == 1 ? 128 : (q == 2 ? 224 : 288)); }
-
-// byte offset of (row, cc) in a 128-byte-swizzled k-block; cc < 64
-__device__ __forceinline__ uint32_t swz(int row, int cc) {
-    return (uint32_t)(row * 128 + ((((cc >> 3) ^ (row & 7)) & 7) << 4) + (cc & 7) * 2);
-}
-// byte offset of 16-byte chunk g8 of row `row` in a 128-byte-swizzled k-block
-__device__ __forceinline__ uint32_t swz_chunk(int row, int g8) {
-    return (uint32_t)(row * 128 + (((g8 ^ (row & 7)) & 7) << 4));
-}
-
-// inputs of the operand build: channels 2 cp, 2 cp + 1 of tokens 8 rg .. 8 rg + 7
-struct BuildIn {
-    __nv_bfloat162 q[8], k[8], v[8];
-    float2 z[8];
-};
-// The next unit's inputs are fetched in three parts, each issued right after an
-// MMA so that the loads overlap the tensor-core work instead of the build.
-template <int PART>
-__device__ __forceinline__ void load_part(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                                          const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z, int H,
-                                          int h, int t0, int len, int rg, int cp, BuildIn &in) {
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const int i = 8 * rg + r;
-        const size_t a = ((size_t)(t0 + i) * H + h) * D + 2 * cp;
-        const bool ok = i < len;
-        if (PART == 0) in.z[r] = ok ? *reinterpret_cast<const float2 *>(z + a) : make_float2(0.f, 0.f);
-        if (PART == 1) {
-            in.q[r] = ok ? *reinterpret_cast<const __nv_bfloat162 *>(q + a) : __float2bfloat162_rn(0.f);
-            in.k[r] = ok ? *reinterpret_cast<const __nv_bfloat162 *>(k + a) : __float2bfloat162_rn(0.f);
-        }
-        if (PART == 2) in.v[r] = ok ? *reinterpret_cast<const __nv_bfloat162 *>(v + a) : __float2bfloat162_rn(0.f);
-    }
-}
-
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
-__device__ __forceinline__ float2 ex2x2(float2 a) { return make_float2(ex2(a.x), ex2(a.y)); }
-// Gate of "Kimi K3 模型结构（2）" eq. (5) in base-2 log space, g log2(e) =
-// g_min log2(e) sigmoid(e^{A_h} z), and its running sums over this thread's tokens.
-__device__ __forceinline__ void gate_sums(const BuildIn &in, float A_h, float gm2, int first, int len, float2 *rl) {
-    const float c1 = -ex2(A_h * 1.4426950408889634f) * 1.4426950408889634f;  // exp(-e^{A_h} z) = 2^(c1 z)
-    float2 hs = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const float2 uu = make_float2(ex2(in.z[r].x * c1), ex2(in.z[r].y * c1));
-        const float2 den = __fadd2_rn(uu, make_float2(1.f, 1.f));
-        const float2 g2 = first + r < len ? make_float2(__fdividef(gm2, den.x), __fdividef(gm2, den.y)) : make_float2(0.f, 0.f);
-        hs = __fadd2_rn(hs, g2);
-        rl[r] = hs;
-    }
-}
-
-__device__ __forceinline__ uint32_t bf2(float2 a) {
-    const __nv_bfloat162 b = __float22bfloat162_rn(a);
-    return *reinterpret_cast<const uint32_t *>(&b);
-}
-__device__ __forceinline__ uint4 pack8(const float *f) {
-    uint4 u;
-    u.x = bf2(make_float2(f[0], f[1]));
-    u.y = bf2(make_float2(f[2], f[3]));
-    u.z = bf2(make_float2(f[4], f[5]));
-    u.w = bf2(make_float2(f[6], f[7]));
-    return u;
-}
 
 __global__ void __launch_bounds__(PT_THREADS, 1)
 prep_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z, const float *__restrict__ A,
                const float *__restrict__ beta, int H, float g_min, Plan plan, char *__restrict__ records) {
     extern __shared__ uint8_t smraw[];
-    __shared__ uint64_t mbar_p, mbar_w, mbar_g;
-    __shared__ uint32_t tmem_slot;
-
-    if (plan_failed(plan)) return;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int cp = tid & 63, rg = tid >> 6;      // build phase: channel pair, 8-token group
-    const int tile = rg >> 1;                    // the 16-token sub-tile of this thread's tokens
-    const int kb = cp >> 5, cc = (2 * cp) & 63;  // k-block and column of the channel pair in K-major images
-    uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
-    float *sbeta = reinterpret_cast<float *>(sm + SM_MISC);
-    float *sHalf = sbeta + 64;  // [8][128] log2-decay sums of each 8-token group
-    const float gm2 = g_min * LOG2E;
-
-    if (tid == 0) {
-        mbar_init(&mbar_p, 1);
-        mbar_init(&mbar_w, 1);
-        mbar_init(&mbar_g, 1);
-        mbar_fence_init();
-    }
-    if (warp == 0) tmem_alloc(&tmem_slot, PT_TMEM_COLS);
-    {
-        // identity operand: row m has its 1 at k = m
-        const int m = tid >> 3, g8 = tid & 7;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if ((m >> 3) == g8) {
-            uint32_t *wp = reinterpret_cast<uint32_t *>(&w);
-            wp[(m & 7) >> 1] = (m & 1) ? 0x3F800000u : 0x00003F80u;
-        }
-        *reinterpret_cast<uint4 *>(sm + SM_ID + swz_chunk(m, g8)) = w;
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_slot;
-    const int lg = warp & 3;  // TMEM lane quadrant of this warp
-    const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
-    const int qt = warp >> 2;  // column quarter / block read by this warp
-
-    const int n_units = plan_n_chunks(plan) * H;
-    BuildIn cin;
-    float b_next = 0.f, a_next = 0.f;
-    int u = blockIdx.x;
-    ChunkInfo ci;
-    if (u < n_units) {
-        ci = plan_chunk(plan, u / H);
-        load_part<0>(q, k, v, z, H, u % H, ci.tok, ci.len, rg, cp, cin);
-        load_part<1>(q, k, v, z, H, u % H, ci.tok, ci.len, rg, cp, cin);
-        load_part<2>(q, k, v, z, H, u % H, ci.tok, ci.len, rg, cp, cin);
-        if (tid < 64 && tid < ci.len) b_next = beta[(size_t)(ci.tok + tid) * H + u % H];
-        a_next = A[u % H];
-    }
-    bool timed_out = false;
-    for (int it = 0; u < n_units && !timed_out; u += gridDim.x, ++it) {
-        const int cidx = u / H, h = u - cidx * H;
-        char *rec = records + ((size_t)cidx * H + h) * REC_BF16_BYTES;
-
-        // ---- 1. gate, partial log2-decay sums of each 8-token group, and beta
-        float2 rl[8];
-        gate_sums(cin, a_next, gm2, 8 * rg, ci.len, rl);
-        *reinterpret_cast<float2 *>(sHalf + rg * 128 + 2 * cp) = rl[7];
-        if (tid < 64) sbeta[tid] = b_next;
-        __syncthreads();
-
-        // tile sums Delta_t (log2), exp(Delta_t), and this thread's carry into its tile
-        float2 Dl = make_float2(0.f, 0.f), carry = make_float2(0.f, 0.f), eD[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const float2 a0 = *reinterpret_cast<const float2 *>(sHalf + (2 * t) * 128 + 2 * cp);
-            const float2 a1 = *reinterpret_cast<const float2 *>(sHalf + (2 * t + 1) * 128 + 2 * cp);
-            const float2 st = add2(a0, a1);
-            eD[t] = ex2x2(st);
-            if (t == tile) {
-                Dl = st;
-                if (rg & 1) carry = a0;
-            }
-        }
-        float2 ePfx = make_float2(1.f, 1.f), eSfx = make_float2(1.f, 1.f);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            if (t < tile) ePfx = mul2(ePfx, eD[t]);
-            if (t > tile) eSfx = mul2(eSfx, eD[t]);
-        }
-        if (rg == 0)
-            *reinterpret_cast<float2 *>(rec + REC_BF16_AC + 8 * cp) = mul2(mul2(eD[0], eD[1]), mul2(eD[2], eD[3]));
-
-        // ---- 1b. per-token operands that do not touch the staging area
-        float2 qe[8], ke[8];
-        {
-            // token-contiguous images, two tokens per packed word: [channel][token pair]
-            uint32_t bkd[2][4], bv[2][4], bkr[2][4];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int i = 8 * rg + r;
-                const float2 qf = __bfloat1622float2(cin.q[r]);
-                const float2 kf = __bfloat1622float2(cin.k[r]);
-                const float2 vf = __bfloat1622float2(cin.v[r]);
-                const float2 c2 = add2(carry, rl[r]);
-                const float2 e = ex2x2(c2);
-                const float2 x = ex2x2(add2(Dl, make_float2(-c2.x, -c2.y)));  // exp(Delta_p) / e_i
-                const float b = sbeta[i];
-                qe[r] = mul2(qf, e);
-                ke[r] = mul2(kf, e);
-                const float2 kx = mul2(kf, x);
-                const float2 vbkd = mul2(mul2(ePfx, make_float2(b, b)), ke[r]);  // Diag(beta) K_decay
-                const float2 vbv = mul2(vf, make_float2(b, b));                  // Diag(beta) V
-                const float2 vbkr = mul2(eSfx, kx);                              // K_restore = exp(G_last - G_i) k_i
-                {
-                    // channel j of this token -> low (even token) or high (odd token) half of a word
-                    const uint32_t w0 = bf2(make_float2(vbkd.x, vbkd.y)), w1 = bf2(make_float2(vbv.x, vbv.y)),
-                                   w2 = bf2(make_float2(vbkr.x, vbkr.y));
-                    const int pr = r >> 1;
-                    if ((r & 1) == 0) {
-                        bkd[0][pr] = w0 & 0xFFFFu;
-                        bkd[1][pr] = w0 >> 16;
-                        bv[0][pr] = w1 & 0xFFFFu;
-                        bv[1][pr] = w1 >> 16;
-                        bkr[0][pr] = w2 & 0xFFFFu;
-                        bkr[1][pr] = w2 >> 16;
-                    } else {
-                        bkd[0][pr] |= w0 << 16;
-                        bkd[1][pr] |= w0 & 0xFFFF0000u;
-                        bv[0][pr] |= w1 << 16;
-                        bv[1][pr] |= w1 & 0xFFFF0000u;
-                        bkr[0][pr] |= w2 << 16;
-                        bkr[1][pr] |= w2 & 0xFFFF0000u;
-                    }
-                }
-                // key side of key tile p, and Q_decay
-                *reinterpret_cast<uint32_t *>(sm + SM_BQ + tile * 4096 + kb * 2048 + swz(i - 16 * tile, cc)) = bf2(kx);
-                *reinterpret_cast<uint32_t *>(sm + SM_QD + kb * 8192 + swz(i, cc)) = bf2(mul2(ePfx, qe[r]));
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int c = 2 * cp + j;
-                const uint32_t sw = (uint32_t)(((rg ^ (c & 7)) & 7) << 4);
-                *reinterpret_cast<uint4 *>(sm + SM_B2 + c * 128 + sw) = make_uint4(bkd[j][0], bkd[j][1], bkd[j][2], bkd[j][3]);
-                *reinterpret_cast<uint4 *>(sm + SM_B2 + (128 + c) * 128 + sw) = make_uint4(bv[j][0], bv[j][1], bv[j][2], bv[j][3]);
-                *reinterpret_cast<uint4 *>(sm + SM_KRT + c * 128 + sw) = make_uint4(bkr[j][0], bkr[j][1], bkr[j][2], bkr[j][3]);
-            }
-        }
-        if (tid == 0) bulk_wait_read_all();  // the previous unit's record has left the staging area
-        __syncthreads();
-
-        // ---- 1c. query-side rows of the A_q images
-        {
-            uint8_t *abase = sm + SM_AREG + kb * SM_AREG_KB;
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                if (qq > tile) continue;
-                float2 F = make_float2(1.f, 1.f);
-#pragma unroll
-                for (int t = 0; t < 4; ++t)
-                    if (t > qq && t < tile) F = mul2(F, eD[t]);
-                if (qq == tile) F = make_float2(__fdividef(1.f, eD[tile].x), __fdividef(1.f, eD[tile].y));
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int i = 8 * rg + r;
-                    const int rowQ = arow_base(qq) + (i - 16 * qq);
-                    const int rowK = rowQ + 16 * (4 - qq);
-                    *reinterpret_cast<uint32_t *>(abase + swz(rowQ, cc)) = bf2(mul2(qe[r], F));
-                    *reinterpret_cast<uint32_t *>(abase + swz(rowK, cc)) = bf2(mul2(ke[r], F));
-                }
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- 2. A_qk / A_kk block columns on the tensor cores
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t ID128 = idesc_bf16_f32(128, 16), ID64 = idesc_bf16_f32(64, 16);
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const int kbs = s >> 2, w = s & 3;
-                    const uint64_t ad = sdesc_sw128(smem_u32(sm + SM_AREG + kbs * SM_AREG_KB + arow_base(qq) * 128 + w * 32));
-                    const uint64_t bd = sdesc_sw128(smem_u32(sm + SM_BQ + qq * 4096 + kbs * 2048 + w * 32));
-                    mma_bf16(tmem + 16 * qq, ad, bd, qq < 2 ? ID128 : ID64, s > 0);
-                }
-            }
-            mma_commit(&mbar_p);
-        }
-        // next unit: its gate inputs now, q and k after the next MMA, v after the last
-        const int u_next = u + gridDim.x;
-        const bool has_next = u_next < n_units;
-        ChunkInfo ci_next = ci;
-        if (has_next) {
-            ci_next = plan_chunk(plan, u_next / H);
-            load_part<0>(q, k, v, z, H, u_next % H, ci_next.tok, ci_next.len, rg, cp, cin);
-            if (tid < 64) b_next = tid < ci_next.len ? beta[(size_t)(ci_next.tok + tid) * H + u_next % H] : 0.f;
-            a_next = A[u_next % H];
-        }
-        bool ok = mbar_wait(&mbar_p, (uint32_t)(it & 1));
-        __syncwarp();
-        tc_fence_after();
-        float *Lm = reinterpret_cast<float *>(sm + SM_AREG + SM_L);
-        float *INV = reinterpret_cast<float *>(sm + SM_AREG + SM_INV);
-        float *tmp = reinterpret_cast<float *>(sm + SM_AREG + SM_TMP);
-        {
-            // block column qq: image rows < nq are M_qk rows, rows nq .. 2 nq - 1 are A_kk rows
-            const int qq = qt;
-            float d[16];
-            tmem_ld16(tmem + lane_off + 16 * qq, d);
-            tmem_ld_wait();
-            const int nq = 16 * (4 - qq);
-            const int r = qq < 2 ? lg * 32 + lane : (lane < 16 ? lg * 16 + lane : 1 << 20);
-            if (r < nq) {
-                const int i = 16 * qq + r;
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) d[jj] = (16 * qq + jj <= i) ? d[jj] : 0.f;
-                *reinterpret_cast<uint4 *>(sm + SM_MQ + swz_chunk(i, 2 * qq)) = pack8(d);
-                *reinterpret_cast<uint4 *>(sm + SM_MQ + swz_chunk(i, 2 * qq + 1)) = pack8(d + 8);
-            } else if (r < 2 * nq) {
-                const int i = 16 * qq + (r - nq);
-                const float b = sbeta[i];
-                float *dst = Lm + i * TRI_LD + 16 * qq;
-#pragma unroll
-                for (int j4 = 0; j4 < 16; j4 += 4) {
-                    float4 t;
-                    t.x = (16 * qq + j4 < i) ? b * d[j4] : 0.f;
-                    t.y = (16 * qq + j4 + 1 < i) ? b * d[j4 + 1] : 0.f;
-                    t.z = (16 * qq + j4 + 2 < i) ? b * d[j4 + 2] : 0.f;
-                    t.w = (16 * qq + j4 + 3 < i) ? b * d[j4 + 3] : 0.f;
-                    *reinterpret_cast<float4 *>(dst + j4) = t;
-                }
-            }
-        }
-        if (tid < 256) {
-            // M_qk is zero above its block diagonal: row i, 16-column block t > tile(i)
-            const int i = tid >> 2, t = tid & 3;
-            if (t > (i >> 4)) {
-                const uint4 zz = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(sm + SM_MQ + swz_chunk(i, 2 * t)) = zz;
-                *reinterpret_cast<uint4 *>(sm + SM_MQ + swz_chunk(i, 2 * t + 1)) = zz;
-            }
-        }
-        tc_fence_before();
-        ok = !__syncthreads_or(!ok);
-        if (!ok) { timed_out = true; break; }
-
-        // ---- 3. INV = (I + L)^-1, then its bf16 image (row i, k = s)
-        tri_inverse<PT_THREADS>(Lm, INV, tmp, tid);
-        {
-            const int i = tid >> 3, g8 = tid & 7;
-            const float4 a = *reinterpret_cast<const float4 *>(INV + i * TRI_LD + 8 * g8);
-            const float4 b = *reinterpret_cast<const float4 *>(INV + i * TRI_LD + 8 * g8 + 4);
-            uint4 w;
-            w.x = bf2(make_float2(a.x, a.y));
-            w.y = bf2(make_float2(a.z, a.w));
-            w.z = bf2(make_float2(b.x, b.y));
-            w.w = bf2(make_float2(b.z, b.w));
-            *reinterpret_cast<uint4 *>(sm + SM_A2 + swz_chunk(i, g8)) = w;
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---- 4. INV [Diag(beta) K_decay | Diag(beta) V] = [W | U0]  (M = 64, N = 256, K = 64)
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t IDW = idesc_bf16_f32(64, 256);
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t ad = sdesc_sw128(smem_u32(sm + SM_A2 + s * 32));
-                const uint64_t bd = sdesc_sw128(smem_u32(sm + SM_B2 + s * 32));
-                mma_bf16(tmem, ad, bd, IDW, s > 0);
-            }
-            mma_commit(&mbar_w);
-        }
-        if (has_next) load_part<1>(q, k, v, z, H, u_next % H, ci_next.tok, ci_next.len, rg, cp, cin);
-        ok = mbar_wait(&mbar_w, (uint32_t)(it & 1));
-        __syncwarp();
-        tc_fence_after();
-        {
-            // token m = 16 lg + lane (lanes < 16) -> [W | U0] MN-major, 64-column block qt
-            const int m = 16 * lg + lane;
-#pragma unroll
-            for (int cb = 0; cb < 4; cb += 2) {
-                float d[32];
-                tmem_ld16(tmem + lane_off + 64 * qt + 16 * cb, d);
-                tmem_ld16(tmem + lane_off + 64 * qt + 16 * cb + 16, d + 16);
-                tmem_ld_wait();
-                if (lane < 16) {
-#pragma unroll
-                    for (int h8 = 0; h8 < 4; ++h8)
-                        *reinterpret_cast<uint4 *>(sm + SM_B2 + qt * 8192 + swz_chunk(m, 2 * cb + h8)) = pack8(d + 8 * h8);
-                }
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        ok = !__syncthreads_or(!ok);
-        if (!ok) { timed_out = true; break; }
-
-        // ---- 5. K_restore^T [W | U0] = [G | H] (M = 128), and with M = 64
-        //         Q' = Q_decay - M_qk W (as I Q_decay + (-M_qk) W) and O0 = M_qk U0
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t IDG = idesc_bf16_f32_bmn(128, 256), IDM = idesc_bf16_f32_bmn(64, 128);
-            constexpr uint32_t NEG_A = 1u << 13;
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint32_t b0 = smem_u32(sm + SM_B2 + s * 2048);
-                const uint64_t am = sdesc_sw128(smem_u32(sm + SM_MQ + s * 32));
-                mma_bf16(tmem, sdesc_sw128(smem_u32(sm + SM_KRT + s * 32)), sdesc_mn(b0, 8192, 1024, SWZ_128B), IDG, s > 0);
-                mma_bf16(tmem + 256, am, sdesc_mn(b0, 8192, 1024, SWZ_128B), IDM | NEG_A, s > 0);
-                mma_bf16(tmem + 384, am, sdesc_mn(b0 + 16384, 8192, 1024, SWZ_128B), IDM, s > 0);
-            }
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tmem + 256, sdesc_sw128(smem_u32(sm + SM_ID + s * 32)),
-                         sdesc_mn(smem_u32(sm + SM_QD + s * 2048), 8192, 1024, SWZ_128B), IDM, true);
-            mma_commit(&mbar_g);
-        }
-        if (has_next) load_part<2>(q, k, v, z, H, u_next % H, ci_next.tok, ci_next.len, rg, cp, cin);
-        ok = mbar_wait(&mbar_g, (uint32_t)(it & 1));
-        __syncwarp();
-        tc_fence_after();
-        {
-            const int c = lg * 32 + lane;  // state row (channel) of [G | H]
-            const int m = 16 * lg + lane;  // token of [M_qk W | O0] (lanes < 16)
-#pragma unroll
-            for (int cb = 0; cb < 4; cb += 2) {
-                const int col = 64 * qt + 16 * cb;
-                float d[32];
-                tmem_ld16(tmem + lane_off + col, d);
-                tmem_ld16(tmem + lane_off + col + 16, d + 16);
-                tmem_ld_wait();
-                if (qt < 2) {
-#pragma unroll
-                    for (int h8 = 0; h8 < 4; ++h8)
-                        *reinterpret_cast<uint4 *>(sm + ST_G + sw128_offset(c, col + 8 * h8, 128)) = pack8(d + 8 * h8);
-                } else {
-#pragma unroll
-                    for (int h16 = 0; h16 < 2; ++h16) {
-                        uint8_t *dst = sm + ST_H + slice_offset(c, col + 16 * h16 - 128, 128);
-                        *reinterpret_cast<uint4 *>(dst) = pack8(d + 16 * h16);
-                        *reinterpret_cast<uint4 *>(dst + 16) = pack8(d + 16 * h16 + 8);
-                    }
-                }
-                tmem_ld16(tmem + lane_off + 256 + col, d);
-                tmem_ld16(tmem + lane_off + 256 + col + 16, d + 16);
-                tmem_ld_wait();
-                if (lane < 16) {
-                    if (qt < 2) {
-#pragma unroll
-                        for (int h8 = 0; h8 < 4; ++h8)
-                            *reinterpret_cast<uint4 *>(sm + ST_QP + sw128_offset(m, col + 8 * h8, 64)) = pack8(d + 8 * h8);
-                    } else {
-#pragma unroll
-                        for (int h16 = 0; h16 < 2; ++h16) {
-                            uint8_t *dst = sm + ST_O0 + slice_offset(m, col + 16 * h16 - 128, 64);
-                            *reinterpret_cast<uint4 *>(dst) = pack8(d + 16 * h16);
-                            *reinterpret_cast<uint4 *>(dst + 16) = pack8(d + 16 * h16 + 8);
-                        }
-                    }
-                }
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        ok = !__syncthreads_or(!ok);
-        if (!ok) { timed_out = true; break; }
-        if (tid == 0) {
-            bulk_s2g(rec + REC_BF16_G, sm + ST_G, 32768);
-            bulk_s2g(rec + REC_BF16_QP, sm + ST_QP, 16384);
-            bulk_s2g(rec + REC_BF16_H, sm + ST_H, 32768);
-            bulk_s2g(rec + REC_BF16_O0, sm + ST_O0, 16384);
-            bulk_commit();
-        }
-        ci = ci_next;
-    }
-    if (tid == 0) {
-        bulk_wait_all();
-        if (timed_out) atomicOr(plan.err, KDA_DEVERR_TIMEOUT);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, PT_TMEM_COLS);
+    prep_blocks(q, k, v, z, A, beta, H, g_min, plan, records, smraw, blockIdx.x, gridDim.x, nullptr);
 }
 
 }  // namespace
