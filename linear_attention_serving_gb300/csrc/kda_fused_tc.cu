@@ -10,8 +10,10 @@
 // each finished record with a release flag, and a chain's producer waits for
 // the flag (acquire, bounded) before copying the record.  The launch is
 // cooperative, so every block is resident and a waiting chain cannot starve
-// the prep it waits for; the prep never waits for a chain.  The outputs are
-// formed afterwards by the output kernel.
+// the prep it waits for; the prep never waits for a chain.  The chain blocks
+// also form the outputs O = O0 + Q' S of their columns (an M = 64 MMA issued
+// right after the chain's own, drained by four output warps): a chain keeps up
+// with the prep with time to spare, so the outputs cost no extra pass.
 #include "kda_prep_body.cuh"
 #include "kda_scan_body.cuh"
 
@@ -32,7 +34,7 @@ fused_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
         const int per_doc = H * FUSED_SLICES;
         const int doc = blockIdx.x / per_doc, rem = blockIdx.x - doc * per_doc;
         const int h = rem / FUSED_SLICES, zc = rem - h * FUSED_SLICES;
-        scan_block<FUSED_N, FUSED_STAGES, FUSED_TPR>(sa, doc, h, zc * (FUSED_N / 16), smraw, ready);
+        scan_block<FUSED_N, FUSED_STAGES, FUSED_TPR, true>(sa, doc, h, zc * (FUSED_N / 16), smraw, ready);
     } else {
         prep_blocks(q, k, v, z, A, beta, H, g_min, plan, records, smraw, blockIdx.x - n_chain,
                     gridDim.x - n_chain, ready);
@@ -53,9 +55,9 @@ int launch_fused_tc(const void *q, const void *k, const void *v, const float *z,
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop)
         return KDA_OK;
-    const size_t smem = PREP_TC_SMEM > scan_tc_smem_bytes<FUSED_N, FUSED_STAGES>()
-                            ? PREP_TC_SMEM
-                            : scan_tc_smem_bytes<FUSED_N, FUSED_STAGES>();
+    constexpr size_t chain_smem = scan_tc_smem_bytes<FUSED_N, FUSED_STAGES, true>();
+    static_assert(ScanCfg<FUSED_N, FUSED_TPR, true>::THREADS <= PT_THREADS, "chain block fits the prep's block");
+    const size_t smem = PREP_TC_SMEM > chain_smem ? PREP_TC_SMEM : chain_smem;
     if (cudaFuncSetAttribute(fused_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_tc_kernel, PT_THREADS, smem) != cudaSuccess ||

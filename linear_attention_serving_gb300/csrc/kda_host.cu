@@ -198,12 +198,12 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *z, c
     a.o = o;
     a.final_state = final_state;
     if (dtype == KDA_BF16) {
-        // few (document, head) chains: prep and chains in one launch, then the outputs
+        // few (document, head) chains: prep, chains and outputs in one launch
         bool used = false;
         if ((rc = launch_fused_tc(q, k, v, z, A, beta, H, g_min, a, (int *)((char *)workspace + w.off_ready),
                                   device_sm_count(), s, &used)))
             return rc;
-        if (used) return o ? launch_out_tc(p, H, records, o, device_sm_count(), s) : KDA_OK;
+        if (used) return KDA_OK;
     }
     if ((rc = launch_prep(q, k, v, z, A, beta, H, dtype, g_min, p, records, s))) return rc;
     return launch_scan(a, dtype, s);

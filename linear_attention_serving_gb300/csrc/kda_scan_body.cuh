@@ -40,32 +40,38 @@ using namespace tc;
 
 // Block layout for N state columns with TPR threads per state row: warps
 // 0 .. 4 TPR - 1 run the chain (warp w: rows 32 (w % 4) .., columns
-// (w / 4) N / TPR ..), then the MMA warp, then the producer warp.
-template <int N, int TPR>
+// (w / 4) N / TPR ..), then the MMA warp, the producer warp and, when the
+// block forms the outputs itself (EMIT_O), four output warps.
+template <int N, int TPR, bool EMIT_O = false>
 struct ScanCfg {
     static constexpr int NT = N / TPR;  // state columns per chain thread
     static constexpr int CHAIN_WARPS = 4 * TPR;
     static constexpr int MMA_WARP = CHAIN_WARPS;
     static constexpr int PRODUCER_WARP = CHAIN_WARPS + 1;
-    static constexpr int THREADS = 32 * (CHAIN_WARPS + 2);
+    static constexpr int OUT_WARP0 = CHAIN_WARPS + 2;
+    static constexpr int OUT_WARPS = EMIT_O ? 4 : 0;
+    static constexpr int THREADS = 32 * (CHAIN_WARPS + 2 + OUT_WARPS);
     static_assert(NT % 16 == 0, "a chain thread owns whole 16-column blocks");
 };
 
-// pipeline stage: G (32 KB) | a_C | H slices
-template <int N>
+// pipeline stage: G (32 KB) | a_C | [Q' (16 KB)] | H slices | [O0 slices]
+template <int N, bool EMIT_O = false>
 struct Stage {
     static constexpr int NS = N / 16;
     static constexpr int G = 0;
     static constexpr int AC = (int)REC_BF16_AC;
-    static constexpr int H = (int)REC_BF16_SHARED;  // H slices right after a_C
-    static constexpr int BYTES = ((H + NS * (int)REC_BF16_HSLICE) + 1023) / 1024 * 1024;
+    static constexpr int QP = (int)REC_BF16_QP;  // 1024-aligned, as in the record
+    static constexpr int H = EMIT_O ? QP + 16384 : (int)REC_BF16_SHARED;
+    static constexpr int O0 = H + NS * (int)REC_BF16_HSLICE;
+    static constexpr int BYTES = ((O0 + (EMIT_O ? NS * (int)REC_BF16_OSLICE : 0)) + 1023) / 1024 * 1024;
     static constexpr int SOP = 2 * N * 128;  // one bf16 S operand: 128 rows x N columns
-    static constexpr int NCOLS = N < 32 ? 32 : N;
+    static constexpr int OCOL = N;           // TMEM: output accumulators at N and 2 N
+    static constexpr int NCOLS = EMIT_O ? 256 : (N < 32 ? 32 : N);
 };
 
-template <int N, int STAGES>
+template <int N, int STAGES, bool EMIT_O = false>
 constexpr size_t scan_tc_smem_bytes() {
-    return (size_t)STAGES * Stage<N>::BYTES + 2 * Stage<N>::SOP + 1024;
+    return (size_t)STAGES * Stage<N, EMIT_O>::BYTES + 2 * Stage<N, EMIT_O>::SOP + 1024;
 }
 
 __device__ __forceinline__ float state_init(const ScanArgs &a, int unit, int h, int r, int g) {
@@ -180,13 +186,13 @@ __device__ __forceinline__ void tmem_row(uint32_t taddr, float *out) {
 // `unit` (document or segment).  With `ready` non-null the producer waits,
 // before copying chunk c's record, until ready[c * H + h] is set (the record
 // is written by other blocks of the same launch).
-template <int N, int STAGES, int TPR>
+template <int N, int STAGES, int TPR, bool EMIT_O = false>
 __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, int zc16, uint8_t *smraw,
                                            const int *ready) {
-    using ST = Stage<N>;
-    using CF = ScanCfg<N, TPR>;
+    using ST = Stage<N, EMIT_O>;
+    using CF = ScanCfg<N, TPR, EMIT_O>;
     constexpr int NT = CF::NT;
-    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], g_bar, sop_bar;
+    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], g_bar, sop_bar, o_bar[2], oempty_bar[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -194,7 +200,8 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
     const int warp = tid >> 5, lane = tid & 31;
     const int col0 = zc16 * 16;
     const bool value_cols = col0 < D;
-    const bool emit_s = value_cols && a.o && a.phase != 1;  // the output kernel needs S
+    // the output kernel needs S, unless this block forms the outputs itself
+    const bool emit_s = !EMIT_O && value_cols && a.o && a.phase != 1;
     const Plan &p = a.plan;
     if (plan_failed(p)) return;
     int c0, c1;
@@ -214,10 +221,15 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], CF::CHAIN_WARPS);  // released by the chain warps once they read it
+            // released by the chain warps (and the output warps) once they read it
+            mbar_init(&empty_bar[s], CF::CHAIN_WARPS + CF::OUT_WARPS);
         }
         mbar_init(&g_bar, 1);
         mbar_init(&sop_bar, CF::CHAIN_WARPS);  // the chain warps' parts of the next S operand
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&o_bar[b], 1);                // output accumulator b written
+            mbar_init(&oempty_bar[b], CF::OUT_WARPS > 0 ? CF::OUT_WARPS : 1);  // and read back
+        }
         abort_flag = 0;
         mbar_fence_init();
     }
@@ -232,7 +244,8 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
         if (lane == 0) {
             int issued = 0;
             bool timed_out = false;
-            const uint32_t bytes = (uint32_t)REC_BF16_SHARED + (value_cols ? (uint32_t)(ST::NS * REC_BF16_HSLICE) : 0u);
+            const uint32_t bytes = (uint32_t)REC_BF16_SHARED + (value_cols ? (uint32_t)(ST::NS * REC_BF16_HSLICE) : 0u) +
+                                   (EMIT_O ? (uint32_t)(16384 + ST::NS * REC_BF16_OSLICE) : 0u);
             int stage = 0;
             uint32_t ph = 0;
             for (int i = 0; i < nchunks; ++i) {
@@ -246,6 +259,11 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 if (value_cols)
                     bulk_g2s(st + ST::H, rec + REC_BF16_H + (size_t)(col0 / 16) * REC_BF16_HSLICE,
                              (uint32_t)(ST::NS * REC_BF16_HSLICE), &full_bar[stage]);
+                if (EMIT_O) {
+                    bulk_g2s(st + ST::QP, rec + REC_BF16_QP, 16384, &full_bar[stage]);
+                    bulk_g2s(st + ST::O0, rec + REC_BF16_O0 + (size_t)(col0 / 16) * REC_BF16_OSLICE,
+                             (uint32_t)(ST::NS * REC_BF16_OSLICE), &full_bar[stage]);
+                }
                 issued = i + 1;
                 if (++stage == STAGES) {
                     stage = 0;
@@ -283,6 +301,22 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                     mma_bf16(tmem_g, gd + (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
                              sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDESC, k > 0);
                 mma_commit(&g_bar);
+                if (EMIT_O) {
+                    // O = Q' S_enter of this chunk into output accumulator b, once the
+                    // output warps have read what chunk i - 2 left there
+                    if (i >= 2 && !mbar_wait(&oempty_bar[b], (uint32_t)(((i - 2) >> 1) & 1))) {
+                        abort_flag = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    constexpr uint32_t IDO = idesc_bf16_f32_bmn(64, N);
+                    const uint64_t qd = sdesc_sw128(smem_u32(sm + stage * ST::BYTES + ST::QP));
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mma_bf16(tmem_g + ST::OCOL + b * N, qd + (uint64_t)(((k >> 2) * 8192 + (k & 3) * 32) >> 4),
+                                 sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDO, k > 0);
+                    mma_commit(&o_bar[b]);
+                }
                 if (++stage == STAGES) {
                     stage = 0;
                     ph ^= 1u;
@@ -376,6 +410,14 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 for (int j = 0; j < NT; ++j) s[j] = state_reset(a, ci_next.doc, h, t, pc + j);
             }
             pack_row<NT>(s, pk);
+            if (EMIT_O && i >= 1 && i + 1 < nchunks) {
+                // operand buffer b ^ 1 was also read by chunk i - 1's output MMA
+                const bool okk = mbar_wait(&o_bar[b ^ 1], (uint32_t)(((i - 1) >> 1) & 1));
+                if (!__all_sync(0xffffffffu, okk)) {
+                    ok = false;
+                    break;
+                }
+            }
             if (i + 1 < nchunks) {
                 write_sop<N, NT>(sop0 + (b ^ 1) * ST::SOP, t, part * NT / 16, pk);
                 fence_async_smem();
@@ -402,6 +444,57 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
             float *dst = a.pairs + ((((size_t)which * a.H + h) * a.n_seg + unit) * D + t) * D + pc0;
 #pragma unroll
             for (int j = 0; j < NT; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
+        }
+    }
+    if (EMIT_O && warp >= CF::OUT_WARP0 && warp < CF::OUT_WARP0 + CF::OUT_WARPS) {
+        // ------------------------------------------------------------ output warps
+        // M = 64 accumulator: token r sits in lane 32 (r / 16) + r % 16, so the
+        // warp of lane quadrant q4 drains tokens 16 q4 .. 16 q4 + 15
+        const int q4 = warp & 3, r = 16 * q4 + lane;
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        int stage = 0;
+        uint32_t ph = 0;
+        for (int i = 0; i < nchunks; ++i) {
+            const int b = i & 1;
+            const bool okw = mbar_wait(&full_bar[stage], ph) && mbar_wait(&o_bar[b], (uint32_t)((i >> 1) & 1));
+            if (!__all_sync(0xffffffffu, okw) || *(volatile int *)&abort_flag) {
+                if (lane == 0) abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const ChunkInfo ci = plan_chunk(p, c0 + i);
+            const uint8_t *stg = sm + stage * ST::BYTES;
+#pragma unroll
+            for (int half = 0; half < N / 32; ++half) {
+                float d[32], x[32];
+                tmem_ld16(tmem_g + lane_off + ST::OCOL + b * N + 32 * half, d);
+                tmem_ld16(tmem_g + lane_off + ST::OCOL + b * N + 32 * half + 16, d + 16);
+                tmem_ld_wait();
+                if (a.o && lane < 16 && r < ci.len) {
+                    load_slices<32>(stg + ST::O0 + slice_offset(0, 32 * half, 64), r, 64, x);
+                    __nv_bfloat16 *orow =
+                        reinterpret_cast<__nv_bfloat16 *>(a.o) + ((size_t)(ci.tok + r) * a.H + h) * D + col0 + 32 * half;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 w;
+                        __nv_bfloat162 *wp = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            wp[e] = __floats2bfloat162_rn(x[j + 2 * e] + d[j + 2 * e], x[j + 2 * e + 1] + d[j + 2 * e + 1]);
+                        *reinterpret_cast<uint4 *>(orow + j) = w;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&oempty_bar[b]);
+                mbar_arrive(&empty_bar[stage]);
+            }
+            if (++stage == STAGES) {
+                stage = 0;
+                ph ^= 1u;
+            }
         }
     }
     tc_fence_before();
