@@ -34,7 +34,10 @@
 //     K_restore^T [W | U0] = [G | H] (M = 128) and, with M = 64,
 //     Q' = I Q_decay + (-M_qk) W and O0 = M_qk U0; G, H, Q', O0 go to the record.
 // The record is staged in shared memory and written with bulk copies that
-// overlap the next unit.  Every wait is bounded; a timeout records
+// overlap the next unit.  Where chain blocks consume the records as they
+// appear, the thread that issued the copies waits for them to complete while
+// the next unit's inverse runs on the other threads, then raises the unit's
+// ready flag.  Every wait is bounded; a timeout records
 // KDA_DEVERR_TIMEOUT and ends the block.
 #pragma once
 
@@ -50,6 +53,7 @@ using namespace tc;
 
 constexpr int PT_THREADS = 512;
 constexpr int PT_TMEM_COLS = 512;
+constexpr int PT_STORE_TID = 256;  // issues the bulk stores of a record and publishes it
 constexpr float LOG2E = 1.4426950408889634f;
 
 // shared-memory map (bytes from a 1024-aligned base)
@@ -309,15 +313,8 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
                 *reinterpret_cast<uint4 *>(sm + SM_KRT + c * 128 + sw) = make_uint4(bkr[j][0], bkr[j][1], bkr[j][2], bkr[j][3]);
             }
         }
-        if (tid == 0) {
-            if (ready) {
-                // the previous unit's record is complete in memory: publish it
-                bulk_wait_all();
-                if (u_prev >= 0) publish(ready + u_prev);
-            } else {
-                bulk_wait_read_all();  // the previous unit's record has left the staging area
-            }
-        }
+        // the previous unit's record has left the staging area
+        if (tid == PT_STORE_TID) bulk_wait_read_all();
         __syncthreads();
 
         // ---- 1c. query-side rows of the A_q images
@@ -420,7 +417,15 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         if (!ok) { timed_out = true; break; }
 
         // ---- 3. INV = (I + L)^-1, then its bf16 image (row i, k = s)
-        tri_inverse<PT_THREADS>(Lm, INV, tmp, tid);
+        // the storing thread idles during the inverse's block products: it
+        // waits there for the previous unit's record to be complete in memory
+        // and publishes it
+        tri_inverse<PT_THREADS>(Lm, INV, tmp, tid, [&] {
+            if (tid == PT_STORE_TID && ready && u_prev >= 0) {
+                bulk_wait_all();
+                publish(ready + u_prev);
+            }
+        });
         {
             const int i = tid >> 3, g8 = tid & 7;
             const float4 a = *reinterpret_cast<const float4 *>(INV + i * TRI_LD + 8 * g8);
@@ -542,7 +547,7 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         tc_fence_before();
         ok = !__syncthreads_or(!ok);
         if (!ok) { timed_out = true; break; }
-        if (tid == 0) {
+        if (tid == PT_STORE_TID) {
             bulk_s2g(rec + REC_BF16_G, sm + ST_G, 32768);
             bulk_s2g(rec + REC_BF16_QP, sm + ST_QP, 16384);
             bulk_s2g(rec + REC_BF16_H, sm + ST_H, 32768);
@@ -552,11 +557,11 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         u_prev = u;
         ci = ci_next;
     }
-    if (tid == 0) {
+    if (tid == PT_STORE_TID) {
         bulk_wait_all();
         if (ready && u_prev >= 0 && !timed_out) publish(ready + u_prev);
-        if (timed_out) atomicOr(plan.err, KDA_DEVERR_TIMEOUT);
     }
+    if (tid == 0 && timed_out) atomicOr(plan.err, KDA_DEVERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

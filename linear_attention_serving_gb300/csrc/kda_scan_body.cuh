@@ -16,15 +16,20 @@
 // state columns the extra 128 start from the identity with H = 0: they carry
 // the transition M of "Kimi K3 模型结构（7）" eq. (17) for the segment pairs.
 //
-// Warps 0-3 (chain): thread t owns state row t (TMEM lane t); the fp32 state
-//   master lives in registers, its bf16 copy (double buffered) in shared
-//   memory is the B operand (MN-major) of the next chunk's MMA.  Each warp
-//   publishes its 32 rows of that operand on an mbarrier, so the warps never
-//   wait for one another; a_C and H are read while the MMA runs.
-// Warp 5 (MMA): waits for all four warps' rows and the chunk's stage, issues
-//   the chunk's MMA and commits it.
-// Warp 4 (producer): streams each chunk's G, a_C and the block's H slices
-//   through a bulk-copy pipeline.
+// Chain warps (4 per TPR): thread t of a row group owns state row t (TMEM lane
+//   t) and N / TPR of its columns; the fp32 state master lives in registers,
+//   its bf16 copy (double buffered) in shared memory is the B operand
+//   (MN-major) of the next chunk's MMA.  Each warp publishes its rows of that
+//   operand on an mbarrier, so the warps never wait for one another; a_C and H
+//   are read while the MMA runs.
+// MMA warp: waits for the chain warps' rows and the chunk's stage, issues the
+//   chunk's MMA and commits it; with EMIT_O it then issues the chunk's output
+//   MMA O = Q' S_enter (M = 64) into one of two TMEM accumulators.
+// Producer warp: waits for a chunk's record (its ready flag, when another part
+//   of the launch writes it), then streams G, a_C, [Q'] and the block's H
+//   slices through a bulk-copy pipeline, and the O0 slices through a ring of
+//   their own.
+// Output warps (EMIT_O): read an output accumulator, add O0, store bf16 o.
 // Every wait is bounded; on a timeout the block records KDA_DEVERR_TIMEOUT,
 // leaves its loops, and frees its TMEM.
 #pragma once
@@ -54,7 +59,9 @@ struct ScanCfg {
     static_assert(NT % 16 == 0, "a chain thread owns whole 16-column blocks");
 };
 
-// pipeline stage: G (32 KB) | a_C | [Q' (16 KB)] | H slices | [O0 slices]
+// pipeline stage: G (32 KB) | a_C | [Q' (16 KB)] | H slices.  With EMIT_O the
+// O0 slices ride a ring of their own, read by the output warps only, so that a
+// stage is free again once the chain warps and the output MMA are done with it.
 template <int N, bool EMIT_O = false>
 struct Stage {
     static constexpr int NS = N / 16;
@@ -62,8 +69,9 @@ struct Stage {
     static constexpr int AC = (int)REC_BF16_AC;
     static constexpr int QP = (int)REC_BF16_QP;  // 1024-aligned, as in the record
     static constexpr int H = EMIT_O ? QP + 16384 : (int)REC_BF16_SHARED;
-    static constexpr int O0 = H + NS * (int)REC_BF16_HSLICE;
-    static constexpr int BYTES = ((O0 + (EMIT_O ? NS * (int)REC_BF16_OSLICE : 0)) + 1023) / 1024 * 1024;
+    static constexpr int BYTES = ((H + NS * (int)REC_BF16_HSLICE) + 1023) / 1024 * 1024;
+    static constexpr int OBYTES = EMIT_O ? NS * (int)REC_BF16_OSLICE : 0;  // one O0 ring slot
+    static constexpr int OSTAGES = 3;
     static constexpr int SOP = 2 * N * 128;  // one bf16 S operand: 128 rows x N columns
     static constexpr int OCOL = N;           // TMEM: output accumulators at N and 2 N
     static constexpr int NCOLS = EMIT_O ? 256 : (N < 32 ? 32 : N);
@@ -71,7 +79,8 @@ struct Stage {
 
 template <int N, int STAGES, bool EMIT_O = false>
 constexpr size_t scan_tc_smem_bytes() {
-    return (size_t)STAGES * Stage<N, EMIT_O>::BYTES + 2 * Stage<N, EMIT_O>::SOP + 1024;
+    using ST = Stage<N, EMIT_O>;
+    return (size_t)STAGES * ST::BYTES + (size_t)ST::OSTAGES * ST::OBYTES + 2 * ST::SOP + 1024;
 }
 
 __device__ __forceinline__ float state_init(const ScanArgs &a, int unit, int h, int r, int g) {
@@ -193,6 +202,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
     using CF = ScanCfg<N, TPR, EMIT_O>;
     constexpr int NT = CF::NT;
     __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], g_bar, sop_bar, o_bar[2], oempty_bar[2];
+    __shared__ uint64_t o0full_bar[ST::OSTAGES], o0free_bar[ST::OSTAGES];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -214,21 +224,27 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
     const int nchunks = c1 - c0;
 
     uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
-    uint8_t *sop0 = sm + STAGES * ST::BYTES;
+    uint8_t *o0ring = sm + STAGES * ST::BYTES;
+    uint8_t *sop0 = o0ring + ST::OSTAGES * ST::OBYTES;
     char *records = (char *)a.records;
     const size_t rec_stride = (size_t)a.H * REC_BF16_BYTES;
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
-            // released by the chain warps (and the output warps) once they read it
-            mbar_init(&empty_bar[s], CF::CHAIN_WARPS + CF::OUT_WARPS);
+            // released by the chain warps once they read it (and by the output
+            // MMA's commit, which reads its Q')
+            mbar_init(&empty_bar[s], CF::CHAIN_WARPS + (EMIT_O ? 1 : 0));
         }
         mbar_init(&g_bar, 1);
         mbar_init(&sop_bar, CF::CHAIN_WARPS);  // the chain warps' parts of the next S operand
         for (int b = 0; b < 2; ++b) {
             mbar_init(&o_bar[b], 1);                // output accumulator b written
             mbar_init(&oempty_bar[b], CF::OUT_WARPS > 0 ? CF::OUT_WARPS : 1);  // and read back
+        }
+        for (int s = 0; s < ST::OSTAGES; ++s) {
+            mbar_init(&o0full_bar[s], 1);
+            mbar_init(&o0free_bar[s], CF::OUT_WARPS > 0 ? CF::OUT_WARPS : 1);
         }
         abort_flag = 0;
         mbar_fence_init();
@@ -242,16 +258,17 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
     if (warp == CF::PRODUCER_WARP) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int issued = 0;
+            int issued = 0, o_issued = 0;
             bool timed_out = false;
             const uint32_t bytes = (uint32_t)REC_BF16_SHARED + (value_cols ? (uint32_t)(ST::NS * REC_BF16_HSLICE) : 0u) +
-                                   (EMIT_O ? (uint32_t)(16384 + ST::NS * REC_BF16_OSLICE) : 0u);
+                                   (EMIT_O ? 16384u : 0u);
             int stage = 0;
             uint32_t ph = 0;
             for (int i = 0; i < nchunks; ++i) {
+                // the record first: its flag is read while the stage drains
+                if (ready && !wait_flag(ready + (size_t)(c0 + i) * a.H + h)) { timed_out = true; break; }
                 if (!mbar_wait(&empty_bar[stage], ph ^ 1u)) { timed_out = true; break; }
                 if (*(volatile int *)&abort_flag) break;
-                if (ready && !wait_flag(ready + (size_t)(c0 + i) * a.H + h)) { timed_out = true; break; }
                 const char *rec = records + (size_t)(c0 + i) * rec_stride + (size_t)h * REC_BF16_BYTES;
                 uint8_t *st = sm + stage * ST::BYTES;
                 mbar_expect_tx(&full_bar[stage], bytes);
@@ -259,12 +276,17 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 if (value_cols)
                     bulk_g2s(st + ST::H, rec + REC_BF16_H + (size_t)(col0 / 16) * REC_BF16_HSLICE,
                              (uint32_t)(ST::NS * REC_BF16_HSLICE), &full_bar[stage]);
-                if (EMIT_O) {
-                    bulk_g2s(st + ST::QP, rec + REC_BF16_QP, 16384, &full_bar[stage]);
-                    bulk_g2s(st + ST::O0, rec + REC_BF16_O0 + (size_t)(col0 / 16) * REC_BF16_OSLICE,
-                             (uint32_t)(ST::NS * REC_BF16_OSLICE), &full_bar[stage]);
-                }
+                if (EMIT_O) bulk_g2s(st + ST::QP, rec + REC_BF16_QP, 16384, &full_bar[stage]);
                 issued = i + 1;
+                if (EMIT_O) {
+                    // the O0 slices of the block's columns (an output block owns value columns)
+                    const int os = i % ST::OSTAGES;
+                    if (!mbar_wait(&o0free_bar[os], (uint32_t)(((i / ST::OSTAGES) & 1) ^ 1))) { timed_out = true; break; }
+                    mbar_expect_tx(&o0full_bar[os], (uint32_t)ST::OBYTES);
+                    bulk_g2s(o0ring + os * ST::OBYTES, rec + REC_BF16_O0 + (size_t)(col0 / 16) * REC_BF16_OSLICE,
+                             (uint32_t)ST::OBYTES, &o0full_bar[os]);
+                    o_issued = i + 1;
+                }
                 if (++stage == STAGES) {
                     stage = 0;
                     ph ^= 1u;
@@ -274,6 +296,8 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 // let the copies this thread started land before the block exits
                 for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
                     mbar_wait(&full_bar[i % STAGES], (uint32_t)((i / STAGES) & 1));
+                for (int i = (o_issued > ST::OSTAGES ? o_issued - ST::OSTAGES : 0); i < o_issued; ++i)
+                    mbar_wait(&o0full_bar[i % ST::OSTAGES], (uint32_t)((i / ST::OSTAGES) & 1));
                 if (timed_out) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
             }
         }
@@ -316,6 +340,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                         mma_bf16(tmem_g + ST::OCOL + b * N, qd + (uint64_t)(((k >> 2) * 8192 + (k & 3) * 32) >> 4),
                                  sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDO, k > 0);
                     mma_commit(&o_bar[b]);
+                    mma_commit(&empty_bar[stage]);  // Q' of this stage read
                 }
                 if (++stage == STAGES) {
                     stage = 0;
@@ -452,18 +477,18 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
         // warp of lane quadrant q4 drains tokens 16 q4 .. 16 q4 + 15
         const int q4 = warp & 3, r = 16 * q4 + lane;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        int stage = 0;
-        uint32_t ph = 0;
         for (int i = 0; i < nchunks; ++i) {
             const int b = i & 1;
-            const bool okw = mbar_wait(&full_bar[stage], ph) && mbar_wait(&o_bar[b], (uint32_t)((i >> 1) & 1));
+            const int os = i % ST::OSTAGES;
+            const bool okw = mbar_wait(&o0full_bar[os], (uint32_t)((i / ST::OSTAGES) & 1)) &&
+                             mbar_wait(&o_bar[b], (uint32_t)((i >> 1) & 1));
             if (!__all_sync(0xffffffffu, okw) || *(volatile int *)&abort_flag) {
                 if (lane == 0) abort_flag = 1;
                 break;
             }
             tc_fence_after();
             const ChunkInfo ci = plan_chunk(p, c0 + i);
-            const uint8_t *stg = sm + stage * ST::BYTES;
+            const uint8_t *o0s = o0ring + os * ST::OBYTES;
 #pragma unroll
             for (int half = 0; half < N / 32; ++half) {
                 float d[32], x[32];
@@ -471,7 +496,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 tmem_ld16(tmem_g + lane_off + ST::OCOL + b * N + 32 * half + 16, d + 16);
                 tmem_ld_wait();
                 if (a.o && lane < 16 && r < ci.len) {
-                    load_slices<32>(stg + ST::O0 + slice_offset(0, 32 * half, 64), r, 64, x);
+                    load_slices<32>(o0s + slice_offset(0, 32 * half, 64), r, 64, x);
                     __nv_bfloat16 *orow =
                         reinterpret_cast<__nv_bfloat16 *>(a.o) + ((size_t)(ci.tok + r) * a.H + h) * D + col0 + 32 * half;
 #pragma unroll
@@ -489,11 +514,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&oempty_bar[b]);
-                mbar_arrive(&empty_bar[stage]);
-            }
-            if (++stage == STAGES) {
-                stage = 0;
-                ph ^= 1u;
+                mbar_arrive(&o0free_bar[os]);
             }
         }
     }

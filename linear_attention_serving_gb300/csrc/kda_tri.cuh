@@ -22,10 +22,12 @@ constexpr int TRI_LD = 68;  // row stride (floats) of the 64 x 64 fp32 matrices;
 // strictly lower part of the diagonal blocks and the whole of the blocks below
 // them.  INV is written in full (zeros above the block diagonal).  T is scratch
 // of at least 32 x TRI_LD floats.  All NT >= 512 threads of the block call
-// this; it synchronises internally and ends with a barrier.
-template <int NT>
+// this; it synchronises internally and ends with a block barrier.  Phases 1
+// and 2 run on threads 0-255 only (named barrier 1); threads 256 and up call
+// `idle()` meanwhile and meet the others at the final barrier.
+template <int NT, typename Idle>
 __device__ __forceinline__ void tri_inverse(const float *__restrict__ L, float *__restrict__ INV,
-                                            float *__restrict__ T, int tid) {
+                                            float *__restrict__ T, int tid, Idle &&idle) {
     static_assert(NT >= 512, "tri_inverse wants at least 512 threads");
     const int warp = tid >> 5, lane = tid & 31;
     // ---- D: warp p inverts diagonal block p, one column per lane; the other
@@ -61,74 +63,78 @@ __device__ __forceinline__ void tri_inverse(const float *__restrict__ L, float *
     }
     __syncthreads();
 
-    // ---- 1a: T_b = L_pq X_qq for (p, q) = (1, 0), (3, 2)
-    if (tid < 128) {
-        const int b = tid >> 6, row = (tid >> 2) & 15, c4 = 4 * (tid & 3);
-        const int p = 2 * b + 1, q = 2 * b;
-        const float *Lr = L + (16 * p + row) * TRI_LD + 16 * q;
-        const float *X = INV + (16 * q) * TRI_LD + 16 * q + c4;
-        float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            const float l = Lr[s];
-            const float4 x = *reinterpret_cast<const float4 *>(X + s * TRI_LD);
-            acc01 = __ffma2_rn(make_float2(l, l), make_float2(x.x, x.y), acc01);
-            acc23 = __ffma2_rn(make_float2(l, l), make_float2(x.z, x.w), acc23);
+    if (tid >= 256) {
+        idle();
+    } else {
+        // ---- 1a: T_b = L_pq X_qq for (p, q) = (1, 0), (3, 2)
+        if (tid < 128) {
+            const int b = tid >> 6, row = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+            const int p = 2 * b + 1, q = 2 * b;
+            const float *Lr = L + (16 * p + row) * TRI_LD + 16 * q;
+            const float *X = INV + (16 * q) * TRI_LD + 16 * q + c4;
+            float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
+    #pragma unroll
+            for (int s = 0; s < 16; ++s) {
+                const float l = Lr[s];
+                const float4 x = *reinterpret_cast<const float4 *>(X + s * TRI_LD);
+                acc01 = __ffma2_rn(make_float2(l, l), make_float2(x.x, x.y), acc01);
+                acc23 = __ffma2_rn(make_float2(l, l), make_float2(x.z, x.w), acc23);
+            }
+            *reinterpret_cast<float4 *>(T + (16 * b + row) * TRI_LD + c4) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
         }
-        *reinterpret_cast<float4 *>(T + (16 * b + row) * TRI_LD + c4) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
-    }
-    __syncthreads();
-    // ---- 1b: X_pq = -X_pp T_b
-    if (tid < 128) {
-        const int b = tid >> 6, row = (tid >> 2) & 15, c4 = 4 * (tid & 3);
-        const int p = 2 * b + 1, q = 2 * b;
-        const float *Xr = INV + (16 * p + row) * TRI_LD + 16 * p;
-        const float *Tb = T + (16 * b) * TRI_LD + c4;
-        float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-            const float l = Xr[s];
-            const float4 t = *reinterpret_cast<const float4 *>(Tb + s * TRI_LD);
-            acc01 = __ffma2_rn(make_float2(l, l), make_float2(t.x, t.y), acc01);
-            acc23 = __ffma2_rn(make_float2(l, l), make_float2(t.z, t.w), acc23);
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        // ---- 1b: X_pq = -X_pp T_b
+        if (tid < 128) {
+            const int b = tid >> 6, row = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+            const int p = 2 * b + 1, q = 2 * b;
+            const float *Xr = INV + (16 * p + row) * TRI_LD + 16 * p;
+            const float *Tb = T + (16 * b) * TRI_LD + c4;
+            float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
+    #pragma unroll
+            for (int s = 0; s < 16; ++s) {
+                const float l = Xr[s];
+                const float4 t = *reinterpret_cast<const float4 *>(Tb + s * TRI_LD);
+                acc01 = __ffma2_rn(make_float2(l, l), make_float2(t.x, t.y), acc01);
+                acc23 = __ffma2_rn(make_float2(l, l), make_float2(t.z, t.w), acc23);
+            }
+            *reinterpret_cast<float4 *>(INV + (16 * p + row) * TRI_LD + 16 * q + c4) =
+                make_float4(-acc01.x, -acc01.y, -acc23.x, -acc23.y);
         }
-        *reinterpret_cast<float4 *>(INV + (16 * p + row) * TRI_LD + 16 * q + c4) =
-            make_float4(-acc01.x, -acc01.y, -acc23.x, -acc23.y);
-    }
-    __syncthreads();
+        asm volatile("bar.sync 1, 256;" ::: "memory");
 
-    // ---- 2a: P = L[32:64, 0:32] X_A  (X_A lower triangular, zeros above)
-    if (tid < 256) {
-        const int row = tid >> 3, c4 = 4 * (tid & 7);
-        const float *Lr = L + (32 + row) * TRI_LD;
-        const float *X = INV + c4;
-        float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
-#pragma unroll 8
-        for (int s = 0; s < 32; ++s) {
-            const float l = Lr[s];
-            const float4 x = *reinterpret_cast<const float4 *>(X + s * TRI_LD);
-            acc01 = __ffma2_rn(make_float2(l, l), make_float2(x.x, x.y), acc01);
-            acc23 = __ffma2_rn(make_float2(l, l), make_float2(x.z, x.w), acc23);
+        // ---- 2a: P = L[32:64, 0:32] X_A  (X_A lower triangular, zeros above)
+        if (tid < 256) {
+            const int row = tid >> 3, c4 = 4 * (tid & 7);
+            const float *Lr = L + (32 + row) * TRI_LD;
+            const float *X = INV + c4;
+            float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
+    #pragma unroll 8
+            for (int s = 0; s < 32; ++s) {
+                const float l = Lr[s];
+                const float4 x = *reinterpret_cast<const float4 *>(X + s * TRI_LD);
+                acc01 = __ffma2_rn(make_float2(l, l), make_float2(x.x, x.y), acc01);
+                acc23 = __ffma2_rn(make_float2(l, l), make_float2(x.z, x.w), acc23);
+            }
+            *reinterpret_cast<float4 *>(T + row * TRI_LD + c4) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
         }
-        *reinterpret_cast<float4 *>(T + row * TRI_LD + c4) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
-    }
-    __syncthreads();
-    // ---- 2b: INV[32:64, 0:32] = -X_B P; row r of X_B is zero beyond column r,
-    // and a warp's rows end at 4 (warp + 1), so that bounds its loop
-    if (tid < 256) {
-        const int row = tid >> 3, c4 = 4 * (tid & 7);
-        const int smax = 4 * ((tid >> 5) + 1);
-        const float *Xr = INV + (32 + row) * TRI_LD + 32;
-        const float *P = T + c4;
-        float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
-#pragma unroll 4
-        for (int s = 0; s < smax; ++s) {
-            const float l = Xr[s];
-            const float4 t = *reinterpret_cast<const float4 *>(P + s * TRI_LD);
-            acc01 = __ffma2_rn(make_float2(l, l), make_float2(t.x, t.y), acc01);
-            acc23 = __ffma2_rn(make_float2(l, l), make_float2(t.z, t.w), acc23);
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        // ---- 2b: INV[32:64, 0:32] = -X_B P; row r of X_B is zero beyond column r,
+        // and a warp's rows end at 4 (warp + 1), so that bounds its loop
+        if (tid < 256) {
+            const int row = tid >> 3, c4 = 4 * (tid & 7);
+            const int smax = 4 * ((tid >> 5) + 1);
+            const float *Xr = INV + (32 + row) * TRI_LD + 32;
+            const float *P = T + c4;
+            float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
+    #pragma unroll 4
+            for (int s = 0; s < smax; ++s) {
+                const float l = Xr[s];
+                const float4 t = *reinterpret_cast<const float4 *>(P + s * TRI_LD);
+                acc01 = __ffma2_rn(make_float2(l, l), make_float2(t.x, t.y), acc01);
+                acc23 = __ffma2_rn(make_float2(l, l), make_float2(t.z, t.w), acc23);
+            }
+            *reinterpret_cast<float4 *>(INV + (32 + row) * TRI_LD + c4) = make_float4(-acc01.x, -acc01.y, -acc23.x, -acc23.y);
         }
-        *reinterpret_cast<float4 *>(INV + (32 + row) * TRI_LD + c4) = make_float4(-acc01.x, -acc01.y, -acc23.x, -acc23.y);
     }
     __syncthreads();
 }
