@@ -8,7 +8,9 @@
 // run the chains (64 state columns each, kda_scan_body.cuh) and the others the
 // prep (kda_prep_body.cuh), in chunk-major unit order; a prep block publishes
 // each finished record with a release flag, and a chain's producer waits for
-// the flag (acquire, bounded) before copying the record.  The launch is
+// the flag (acquire, bounded) before copying the record.  The chain blocks
+// start with one prep unit each, since their first records take a unit's
+// time to appear anyway.  The launch is
 // cooperative, so every block is resident and a waiting chain cannot starve
 // the prep it waits for; the prep never waits for a chain.  The chain blocks
 // also form the outputs O = O0 + Q' S of their columns (an M = 64 MMA issued
@@ -21,7 +23,7 @@ namespace kda {
 
 namespace {
 
-constexpr int FUSED_N = 64, FUSED_STAGES = 2, FUSED_TPR = 2;
+constexpr int FUSED_N = 64, FUSED_STAGES = 3, FUSED_TPR = 2;
 constexpr int FUSED_SLICES = D / FUSED_N;  // chain blocks per (document, head)
 
 __global__ void __launch_bounds__(PT_THREADS, 1)
@@ -30,14 +32,20 @@ fused_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
                 const float *__restrict__ beta, int H, float g_min, Plan plan, char *__restrict__ records,
                 ScanArgs sa, int n_chain, int *ready) {
     extern __shared__ uint8_t smraw[];
-    if ((int)blockIdx.x < n_chain) {
+    // A chain would only wait for its first records at the start, so each chain
+    // block first prepares one unit (units 0 .. n_chain - 1); prep block j takes
+    // units n_chain + j, n_chain + j + n_prep, ...  (One call site: the prep
+    // code is inlined once.)
+    const bool chain = (int)blockIdx.x < n_chain;
+    prep_blocks(q, k, v, z, A, beta, H, g_min, plan, records, smraw, blockIdx.x,
+                chain ? (1 << 30) : (int)gridDim.x - n_chain, ready);
+    if (chain) {
+        fence_async_smem();
+        __syncthreads();
         const int per_doc = H * FUSED_SLICES;
         const int doc = blockIdx.x / per_doc, rem = blockIdx.x - doc * per_doc;
         const int h = rem / FUSED_SLICES, zc = rem - h * FUSED_SLICES;
         scan_block<FUSED_N, FUSED_STAGES, FUSED_TPR, true>(sa, doc, h, zc * (FUSED_N / 16), smraw, ready);
-    } else {
-        prep_blocks(q, k, v, z, A, beta, H, g_min, plan, records, smraw, blockIdx.x - n_chain,
-                    gridDim.x - n_chain, ready);
     }
 }
 

@@ -191,7 +191,9 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         mbar_init(&mbar_g, 1);
         mbar_fence_init();
     }
-    if (warp == 0) tmem_alloc(&tmem_slot, PT_TMEM_COLS);
+    // a block that publishes its records may run a chain afterwards, which
+    // allocates TMEM again: it keeps its permit to allocate
+    if (warp == 0) tmem_alloc(&tmem_slot, PT_TMEM_COLS, ready == nullptr);
     {
         // identity operand: row m has its 1 at k = m
         const int m = tid >> 3, g8 = tid & 7;

@@ -26,10 +26,10 @@
 //   chunk's MMA and commits it; with EMIT_O it then issues the chunk's output
 //   MMA O = Q' S_enter (M = 64) into one of two TMEM accumulators.
 // Producer warp: waits for a chunk's record (its ready flag, when another part
-//   of the launch writes it), then streams G, a_C, [Q'] and the block's H
-//   slices through a bulk-copy pipeline, and the O0 slices through a ring of
-//   their own.
-// Output warps (EMIT_O): read an output accumulator, add O0, store bf16 o.
+//   of the launch writes it), then streams G, a_C and the block's H slices
+//   through a bulk-copy pipeline, and (EMIT_O) Q' through a ring of its own.
+// Output warps (EMIT_O): load O0 from the record, read an output accumulator,
+//   add, store bf16 o.
 // Every wait is bounded; on a timeout the block records KDA_DEVERR_TIMEOUT,
 // leaves its loops, and frees its TMEM.
 #pragma once
@@ -59,19 +59,19 @@ struct ScanCfg {
     static_assert(NT % 16 == 0, "a chain thread owns whole 16-column blocks");
 };
 
-// pipeline stage: G (32 KB) | a_C | [Q' (16 KB)] | H slices.  With EMIT_O the
-// O0 slices ride a ring of their own, read by the output warps only, so that a
-// stage is free again once the chain warps and the output MMA are done with it.
+// pipeline stage: G (32 KB) | a_C | H slices, as laid out in the record.  With
+// EMIT_O, Q' (the output MMA's A operand) rides a ring of its own, freed by
+// that MMA's commit, and the output warps read O0 straight from the record, so
+// that the stages the chain waits on stay small enough for a deep pipeline.
 template <int N, bool EMIT_O = false>
 struct Stage {
     static constexpr int NS = N / 16;
     static constexpr int G = 0;
     static constexpr int AC = (int)REC_BF16_AC;
-    static constexpr int QP = (int)REC_BF16_QP;  // 1024-aligned, as in the record
-    static constexpr int H = EMIT_O ? QP + 16384 : (int)REC_BF16_SHARED;
+    static constexpr int H = (int)REC_BF16_SHARED;
     static constexpr int BYTES = ((H + NS * (int)REC_BF16_HSLICE) + 1023) / 1024 * 1024;
-    static constexpr int OBYTES = EMIT_O ? NS * (int)REC_BF16_OSLICE : 0;  // one O0 ring slot
-    static constexpr int OSTAGES = 3;
+    static constexpr int QBYTES = EMIT_O ? 16384 : 0;  // one Q' ring slot (1024-aligned)
+    static constexpr int QSTAGES = 2;
     static constexpr int SOP = 2 * N * 128;  // one bf16 S operand: 128 rows x N columns
     static constexpr int OCOL = N;           // TMEM: output accumulators at N and 2 N
     static constexpr int NCOLS = EMIT_O ? 256 : (N < 32 ? 32 : N);
@@ -80,7 +80,7 @@ struct Stage {
 template <int N, int STAGES, bool EMIT_O = false>
 constexpr size_t scan_tc_smem_bytes() {
     using ST = Stage<N, EMIT_O>;
-    return (size_t)STAGES * ST::BYTES + (size_t)ST::OSTAGES * ST::OBYTES + 2 * ST::SOP + 1024;
+    return (size_t)STAGES * ST::BYTES + (size_t)ST::QSTAGES * ST::QBYTES + 2 * ST::SOP + 1024;
 }
 
 __device__ __forceinline__ float state_init(const ScanArgs &a, int unit, int h, int r, int g) {
@@ -202,7 +202,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
     using CF = ScanCfg<N, TPR, EMIT_O>;
     constexpr int NT = CF::NT;
     __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], g_bar, sop_bar, o_bar[2], oempty_bar[2];
-    __shared__ uint64_t o0full_bar[ST::OSTAGES], o0free_bar[ST::OSTAGES];
+    __shared__ uint64_t qfull_bar[ST::QSTAGES], qfree_bar[ST::QSTAGES];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -224,17 +224,15 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
     const int nchunks = c1 - c0;
 
     uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
-    uint8_t *o0ring = sm + STAGES * ST::BYTES;
-    uint8_t *sop0 = o0ring + ST::OSTAGES * ST::OBYTES;
+    uint8_t *qring = sm + STAGES * ST::BYTES;
+    uint8_t *sop0 = qring + ST::QSTAGES * ST::QBYTES;
     char *records = (char *)a.records;
     const size_t rec_stride = (size_t)a.H * REC_BF16_BYTES;
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
-            // released by the chain warps once they read it (and by the output
-            // MMA's commit, which reads its Q')
-            mbar_init(&empty_bar[s], CF::CHAIN_WARPS + (EMIT_O ? 1 : 0));
+            mbar_init(&empty_bar[s], CF::CHAIN_WARPS);  // released by the chain warps once they read it
         }
         mbar_init(&g_bar, 1);
         mbar_init(&sop_bar, CF::CHAIN_WARPS);  // the chain warps' parts of the next S operand
@@ -242,9 +240,9 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
             mbar_init(&o_bar[b], 1);                // output accumulator b written
             mbar_init(&oempty_bar[b], CF::OUT_WARPS > 0 ? CF::OUT_WARPS : 1);  // and read back
         }
-        for (int s = 0; s < ST::OSTAGES; ++s) {
-            mbar_init(&o0full_bar[s], 1);
-            mbar_init(&o0free_bar[s], CF::OUT_WARPS > 0 ? CF::OUT_WARPS : 1);
+        for (int s = 0; s < ST::QSTAGES; ++s) {
+            mbar_init(&qfull_bar[s], 1);
+            mbar_init(&qfree_bar[s], 1);  // the output MMA's commit
         }
         abort_flag = 0;
         mbar_fence_init();
@@ -258,10 +256,9 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
     if (warp == CF::PRODUCER_WARP) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int issued = 0, o_issued = 0;
+            int issued = 0, q_issued = 0;
             bool timed_out = false;
-            const uint32_t bytes = (uint32_t)REC_BF16_SHARED + (value_cols ? (uint32_t)(ST::NS * REC_BF16_HSLICE) : 0u) +
-                                   (EMIT_O ? 16384u : 0u);
+            const uint32_t bytes = (uint32_t)REC_BF16_SHARED + (value_cols ? (uint32_t)(ST::NS * REC_BF16_HSLICE) : 0u);
             int stage = 0;
             uint32_t ph = 0;
             for (int i = 0; i < nchunks; ++i) {
@@ -276,16 +273,13 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 if (value_cols)
                     bulk_g2s(st + ST::H, rec + REC_BF16_H + (size_t)(col0 / 16) * REC_BF16_HSLICE,
                              (uint32_t)(ST::NS * REC_BF16_HSLICE), &full_bar[stage]);
-                if (EMIT_O) bulk_g2s(st + ST::QP, rec + REC_BF16_QP, 16384, &full_bar[stage]);
                 issued = i + 1;
                 if (EMIT_O) {
-                    // the O0 slices of the block's columns (an output block owns value columns)
-                    const int os = i % ST::OSTAGES;
-                    if (!mbar_wait(&o0free_bar[os], (uint32_t)(((i / ST::OSTAGES) & 1) ^ 1))) { timed_out = true; break; }
-                    mbar_expect_tx(&o0full_bar[os], (uint32_t)ST::OBYTES);
-                    bulk_g2s(o0ring + os * ST::OBYTES, rec + REC_BF16_O0 + (size_t)(col0 / 16) * REC_BF16_OSLICE,
-                             (uint32_t)ST::OBYTES, &o0full_bar[os]);
-                    o_issued = i + 1;
+                    const int qs = i % ST::QSTAGES;
+                    if (!mbar_wait(&qfree_bar[qs], (uint32_t)(((i / ST::QSTAGES) & 1) ^ 1))) { timed_out = true; break; }
+                    mbar_expect_tx(&qfull_bar[qs], (uint32_t)ST::QBYTES);
+                    bulk_g2s(qring + qs * ST::QBYTES, rec + REC_BF16_QP, (uint32_t)ST::QBYTES, &qfull_bar[qs]);
+                    q_issued = i + 1;
                 }
                 if (++stage == STAGES) {
                     stage = 0;
@@ -296,8 +290,8 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 // let the copies this thread started land before the block exits
                 for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
                     mbar_wait(&full_bar[i % STAGES], (uint32_t)((i / STAGES) & 1));
-                for (int i = (o_issued > ST::OSTAGES ? o_issued - ST::OSTAGES : 0); i < o_issued; ++i)
-                    mbar_wait(&o0full_bar[i % ST::OSTAGES], (uint32_t)((i / ST::OSTAGES) & 1));
+                for (int i = (q_issued > ST::QSTAGES ? q_issued - ST::QSTAGES : 0); i < q_issued; ++i)
+                    mbar_wait(&qfull_bar[i % ST::QSTAGES], (uint32_t)((i / ST::QSTAGES) & 1));
                 if (timed_out) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
             }
         }
@@ -328,19 +322,21 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 if (EMIT_O) {
                     // O = Q' S_enter of this chunk into output accumulator b, once the
                     // output warps have read what chunk i - 2 left there
-                    if (i >= 2 && !mbar_wait(&oempty_bar[b], (uint32_t)(((i - 2) >> 1) & 1))) {
+                    const int qs = i % ST::QSTAGES;
+                    if ((i >= 2 && !mbar_wait(&oempty_bar[b], (uint32_t)(((i - 2) >> 1) & 1))) ||
+                        !mbar_wait(&qfull_bar[qs], (uint32_t)((i / ST::QSTAGES) & 1))) {
                         abort_flag = 1;
                         break;
                     }
                     tc_fence_after();
                     constexpr uint32_t IDO = idesc_bf16_f32_bmn(64, N);
-                    const uint64_t qd = sdesc_sw128(smem_u32(sm + stage * ST::BYTES + ST::QP));
+                    const uint64_t qd = sdesc_sw128(smem_u32(qring + qs * ST::QBYTES));
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
                         mma_bf16(tmem_g + ST::OCOL + b * N, qd + (uint64_t)(((k >> 2) * 8192 + (k & 3) * 32) >> 4),
                                  sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDO, k > 0);
                     mma_commit(&o_bar[b]);
-                    mma_commit(&empty_bar[stage]);  // Q' of this stage read
+                    mma_commit(&qfree_bar[qs]);  // Q' read
                 }
                 if (++stage == STAGES) {
                     stage = 0;
@@ -479,43 +475,55 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         for (int i = 0; i < nchunks; ++i) {
             const int b = i & 1;
-            const int os = i % ST::OSTAGES;
-            const bool okw = mbar_wait(&o0full_bar[os], (uint32_t)((i / ST::OSTAGES) & 1)) &&
-                             mbar_wait(&o_bar[b], (uint32_t)((i >> 1) & 1));
+            const int c = c0 + i;
+            const ChunkInfo ci = plan_chunk(p, c);
+            const bool mine = a.o && lane < 16 && r < ci.len;
+            // O0 of this thread's token and the block's columns, read straight from
+            // the record (ST::NS 16-column slices of 64 tokens x 32 bytes), after
+            // the record's ready flag when another part of the launch writes it
+            bool okw = !ready || wait_flag(ready + (size_t)c * a.H + h);
+            uint4 o0v[2 * ST::NS];
+            if (okw && mine) {
+                const char *o0 = records + (size_t)c * rec_stride + (size_t)h * REC_BF16_BYTES + REC_BF16_O0 +
+                                 (size_t)(col0 / 16) * REC_BF16_OSLICE + (size_t)r * 32;
+#pragma unroll
+                for (int sl = 0; sl < ST::NS; ++sl) {
+                    o0v[2 * sl] = *reinterpret_cast<const uint4 *>(o0 + sl * REC_BF16_OSLICE);
+                    o0v[2 * sl + 1] = *reinterpret_cast<const uint4 *>(o0 + sl * REC_BF16_OSLICE + 16);
+                }
+            }
+            okw = okw && mbar_wait(&o_bar[b], (uint32_t)((i >> 1) & 1));
             if (!__all_sync(0xffffffffu, okw) || *(volatile int *)&abort_flag) {
                 if (lane == 0) abort_flag = 1;
                 break;
             }
             tc_fence_after();
-            const ChunkInfo ci = plan_chunk(p, c0 + i);
-            const uint8_t *o0s = o0ring + os * ST::OBYTES;
 #pragma unroll
             for (int half = 0; half < N / 32; ++half) {
-                float d[32], x[32];
+                float d[32];
                 tmem_ld16(tmem_g + lane_off + ST::OCOL + b * N + 32 * half, d);
                 tmem_ld16(tmem_g + lane_off + ST::OCOL + b * N + 32 * half + 16, d + 16);
                 tmem_ld_wait();
-                if (a.o && lane < 16 && r < ci.len) {
-                    load_slices<32>(o0s + slice_offset(0, 32 * half, 64), r, 64, x);
+                if (mine) {
                     __nv_bfloat16 *orow =
                         reinterpret_cast<__nv_bfloat16 *>(a.o) + ((size_t)(ci.tok + r) * a.H + h) * D + col0 + 32 * half;
 #pragma unroll
                     for (int j = 0; j < 32; j += 8) {
+                        const __nv_bfloat162 *x = reinterpret_cast<const __nv_bfloat162 *>(&o0v[(32 * half + j) / 8]);
                         uint4 w;
                         __nv_bfloat162 *wp = reinterpret_cast<__nv_bfloat162 *>(&w);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            wp[e] = __floats2bfloat162_rn(x[j + 2 * e] + d[j + 2 * e], x[j + 2 * e + 1] + d[j + 2 * e + 1]);
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(x[e]);
+                            wp[e] = __floats2bfloat162_rn(f.x + d[j + 2 * e], f.y + d[j + 2 * e + 1]);
+                        }
                         *reinterpret_cast<uint4 *>(orow + j) = w;
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&oempty_bar[b]);
-                mbar_arrive(&o0free_bar[os]);
-            }
+            if (lane == 0) mbar_arrive(&oempty_bar[b]);
         }
     }
     tc_fence_before();

@@ -91,11 +91,13 @@ __device__ __forceinline__ bool bar_or(int id, int nthreads, bool pred) {
 }
 
 // ---------------------------------------------------------------- TMEM
-__device__ __forceinline__ void tmem_alloc(uint32_t *slot_smem, uint32_t ncols) {
+// Allocates ncols TMEM columns (a power of two >= 32).  Unless the block
+// allocates again later, it then gives up its permit to allocate.
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot_smem, uint32_t ncols, bool last_alloc = true) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
                  "r"(ncols)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (last_alloc) asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
