@@ -9,8 +9,10 @@
 // "FlashKDA 算法":  S <- D_t S;  u = beta (v - S^T k);  S <- S + k u^T;  o = S^T q.
 //
 // Mapping: persistent blocks walk the (sequence b, head h) items; thread
-// (column j, part p) keeps rows [p*R, p*R + R) of state column j in registers,
-// so the d_k reductions are a register sum plus one shuffle.  The fp32 state
+// (column pair j, part p) keeps rows [32 p, 32 p + 32) of state columns 2j and
+// 2j + 1 in registers, so the d_k reductions are a register sum plus two
+// shuffles, and every per-token vector element read from shared memory
+// serves two columns.  The fp32 state
 // is read and written exactly once per step.  While an item computes, one
 // thread has already started bulk copies (cp.async.bulk + mbarrier) of the
 // next item's state and token rows into shared memory, so the HBM stream
@@ -33,13 +35,21 @@ namespace {
 using namespace tc;
 
 constexpr int MAX_W = 8;
-constexpr int DEC_TPC = 2;                  // threads per state column
-constexpr int DEC_R = D / DEC_TPC;          // rows per thread
-constexpr int DEC_THREADS = D * DEC_TPC;    // 256
-constexpr int VPAD = D + 4;                 // padded vector stride (second half shifted by 4)
-constexpr int ROW_SLOT = 4 * 512;           // raw bytes per token: q | k | v | z rows, 512 B each
+constexpr int DEC_RP = 4;                     // row parts: threads sharing a pair of state columns
+constexpr int DEC_R = D / DEC_RP;             // rows per thread (32)
+constexpr int DEC_THREADS = D / 2 * DEC_RP;   // 256
+constexpr int VPAD = D + 4 * DEC_RP;          // padded vector stride: row part p shifted by 4 p floats
+constexpr int ROW_SLOT = 4 * 512;             // raw bytes per token: q | k | v | z rows, 512 B each
 
-__device__ __forceinline__ int vidx(int r) { return r + (r >= DEC_R ? 4 : 0); }
+// Row part p of a vector starts 4 p floats further on, in its own 16-byte bank
+// group.  A warp holds 8 column pairs x 4 row parts with the row part in the
+// high lane bits, so each 8-lane phase of a 128-bit load reads one address.
+__device__ __forceinline__ int vidx(int r) { return r + 4 * (r / DEC_R); }
+
+__device__ __forceinline__ void store_pair(float *p, float a, float b) { *reinterpret_cast<float2 *>(p) = make_float2(a, b); }
+__device__ __forceinline__ void store_pair(__nv_bfloat16 *p, float a, float b) {
+    *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
+}
 
 struct DecSmem {
     int ntok_max;
@@ -132,8 +142,8 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int col = warp * (32 / DEC_TPC) + (lane & (32 / DEC_TPC - 1));
-    const int part = lane / (32 / DEC_TPC);
+    const int part = lane >> 3;                                 // row part: lanes 8 p .. 8 p + 7
+    const int col = 2 * (warp * (32 / DEC_RP) + (lane & 7));  // first of this thread's two columns
     const int rbase = part * DEC_R;
     const int n_items = N * H;
     const uint32_t rowb = (uint32_t)(D * sizeof(InT));
@@ -202,9 +212,13 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
 
         // state of this item: shared memory -> registers; then the state buffer
         // takes the next item's state while the token rows are still in use
-        float s[DEC_R];
+        float s0[DEC_R], s1[DEC_R];
 #pragma unroll
-        for (int i = 0; i < DEC_R; ++i) s[i] = sS[(rbase + i) * D + col];
+        for (int i = 0; i < DEC_R; ++i) {
+            const float2 x = *reinterpret_cast<const float2 *>(&sS[(rbase + i) * D + col]);
+            s0[i] = x.x;
+            s1[i] = x.y;
+        }
         __syncthreads();
         if (tid == 0 && next < n_items) issue_state(next, nacc_next, W, rowb, state, sm, L, &full_bar);
         const float eA = expf(A[h]);
@@ -247,52 +261,71 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
         // the recurrence over replay + bonus + drafts
         const float *bt = sbt;
         for (int t = 0; t < ntok; ++t) {
-            // four independent partial sums keep the FMA chain short
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            // two partial sums per column keep the FMA chains short
+            float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
 #pragma unroll
             for (int i = 0; i < DEC_R; i += 4) {
                 const float4 kv = *reinterpret_cast<const float4 *>(&kt[t][vidx(rbase + i)]);
-                a0 = fmaf(s[i], kv.x, a0);
-                a1 = fmaf(s[i + 1], kv.y, a1);
-                a2 = fmaf(s[i + 2], kv.z, a2);
-                a3 = fmaf(s[i + 3], kv.w, a3);
+                a0 = fmaf(s0[i], kv.x, a0);
+                a1 = fmaf(s0[i + 1], kv.y, a1);
+                a0 = fmaf(s0[i + 2], kv.z, a0);
+                a1 = fmaf(s0[i + 3], kv.w, a1);
+                c0 = fmaf(s1[i], kv.x, c0);
+                c1 = fmaf(s1[i + 1], kv.y, c1);
+                c0 = fmaf(s1[i + 2], kv.z, c0);
+                c1 = fmaf(s1[i + 3], kv.w, c1);
             }
-            float acc = (a0 + a1) + (a2 + a3);
+            float acc0 = a0 + a1, acc1 = c0 + c1;
 #pragma unroll
-            for (int m = 32 / DEC_TPC; m < 32; m <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-            const float u = bt[t] * (vt[t][col] - acc);
+            for (int m = 8; m < 32; m <<= 1) {  // the four row parts
+                acc0 += __shfl_xor_sync(0xffffffffu, acc0, m);
+                acc1 += __shfl_xor_sync(0xffffffffu, acc1, m);
+            }
+            const float2 vv = *reinterpret_cast<const float2 *>(&vt[t][col]);
+            const float u0 = bt[t] * (vv.x - acc0), u1 = bt[t] * (vv.y - acc1);
 #pragma unroll
             for (int i = 0; i < DEC_R; i += 4) {
                 const float4 kv = *reinterpret_cast<const float4 *>(&kh[t][vidx(rbase + i)]);
-                s[i] = fmaf(kv.x, u, s[i]);
-                s[i + 1] = fmaf(kv.y, u, s[i + 1]);
-                s[i + 2] = fmaf(kv.z, u, s[i + 2]);
-                s[i + 3] = fmaf(kv.w, u, s[i + 3]);
+                s0[i] = fmaf(kv.x, u0, s0[i]);
+                s0[i + 1] = fmaf(kv.y, u0, s0[i + 1]);
+                s0[i + 2] = fmaf(kv.z, u0, s0[i + 2]);
+                s0[i + 3] = fmaf(kv.w, u0, s0[i + 3]);
+                s1[i] = fmaf(kv.x, u1, s1[i]);
+                s1[i + 1] = fmaf(kv.y, u1, s1[i + 1]);
+                s1[i + 2] = fmaf(kv.z, u1, s1[i + 2]);
+                s1[i + 3] = fmaf(kv.w, u1, s1[i + 3]);
             }
             if (t >= nacc) {
-                float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+                float b0 = 0.f, b1 = 0.f, d0 = 0.f, d1 = 0.f;
 #pragma unroll
                 for (int i = 0; i < DEC_R; i += 4) {
                     const float4 qv = *reinterpret_cast<const float4 *>(&qt[t][vidx(rbase + i)]);
-                    b0 = fmaf(s[i], qv.x, b0);
-                    b1 = fmaf(s[i + 1], qv.y, b1);
-                    b2 = fmaf(s[i + 2], qv.z, b2);
-                    b3 = fmaf(s[i + 3], qv.w, b3);
+                    b0 = fmaf(s0[i], qv.x, b0);
+                    b1 = fmaf(s0[i + 1], qv.y, b1);
+                    b0 = fmaf(s0[i + 2], qv.z, b0);
+                    b1 = fmaf(s0[i + 3], qv.w, b1);
+                    d0 = fmaf(s1[i], qv.x, d0);
+                    d1 = fmaf(s1[i + 1], qv.y, d1);
+                    d0 = fmaf(s1[i + 2], qv.z, d0);
+                    d1 = fmaf(s1[i + 3], qv.w, d1);
                 }
-                float ao = (b0 + b1) + (b2 + b3);
+                float ao0 = b0 + b1, ao1 = d0 + d1;
 #pragma unroll
-                for (int m = 32 / DEC_TPC; m < 32; m <<= 1) ao += __shfl_xor_sync(0xffffffffu, ao, m);
-                if (part == 0) o[(((size_t)b * W + (t - nacc)) * H + h) * D + col] = from_f32<InT>(ao);
+                for (int m = 8; m < 32; m <<= 1) {  // the four row parts
+                    ao0 += __shfl_xor_sync(0xffffffffu, ao0, m);
+                    ao1 += __shfl_xor_sync(0xffffffffu, ao1, m);
+                }
+                if (part == 0) store_pair(o + (((size_t)b * W + (t - nacc)) * H + h) * D + col, ao0, ao1);
             }
             if (t == nacc) {
                 // commit: S = Diag(s_t) S^, written back in place
 #pragma unroll
                 for (int i = 0; i < DEC_R; i += 4) {
                     const float4 sc4 = *reinterpret_cast<const float4 *>(&scommit[vidx(rbase + i)]);
-                    __stcs(&Sg[(size_t)(rbase + i) * D + col], s[i] * sc4.x);
-                    __stcs(&Sg[(size_t)(rbase + i + 1) * D + col], s[i + 1] * sc4.y);
-                    __stcs(&Sg[(size_t)(rbase + i + 2) * D + col], s[i + 2] * sc4.z);
-                    __stcs(&Sg[(size_t)(rbase + i + 3) * D + col], s[i + 3] * sc4.w);
+                    __stcs(reinterpret_cast<float2 *>(&Sg[(size_t)(rbase + i) * D + col]), make_float2(s0[i] * sc4.x, s1[i] * sc4.x));
+                    __stcs(reinterpret_cast<float2 *>(&Sg[(size_t)(rbase + i + 1) * D + col]), make_float2(s0[i + 1] * sc4.y, s1[i + 1] * sc4.y));
+                    __stcs(reinterpret_cast<float2 *>(&Sg[(size_t)(rbase + i + 2) * D + col]), make_float2(s0[i + 2] * sc4.z, s1[i + 2] * sc4.z));
+                    __stcs(reinterpret_cast<float2 *>(&Sg[(size_t)(rbase + i + 3) * D + col]), make_float2(s0[i + 3] * sc4.w, s1[i + 3] * sc4.w));
                 }
             }
         }
