@@ -71,7 +71,6 @@ int launch_fused_tc(const void *q, const void *k, const void *v, const float *z,
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_tc_kernel, PT_THREADS, smem) != cudaSuccess ||
         per_sm < 1)
         return KDA_OK;
-    if (cudaMemsetAsync(ready, 0, sizeof(int) * (size_t)p.max_chunks * H, s) != cudaSuccess) return KDA_ERR_CUDA;
     const __nv_bfloat16 *qb = (const __nv_bfloat16 *)q, *kb = (const __nv_bfloat16 *)k, *vb = (const __nv_bfloat16 *)v;
     char *records = (char *)sa.records;
     Plan plan = p;

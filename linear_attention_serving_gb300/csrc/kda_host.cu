@@ -86,8 +86,10 @@ int launch_scan(const ScanArgs &a, int dtype, cudaStream_t s) {
 }
 
 // Chunk plan: arithmetic for equal-length documents, a device table otherwise.
+// Clears the workspace's first `zero_bytes` (at least the 8-byte header: error
+// word and chunk count) and fills in the chunk plan.
 int make_plan(const int32_t *cu, int n_seqs, int64_t T_total, void *ws, const Workspace &w,
-              cudaStream_t s, Plan &p) {
+              cudaStream_t s, Plan &p, size_t zero_bytes = 8) {
     memset(&p, 0, sizeof(p));
     char *base = (char *)ws;
     p.n_seqs = n_seqs;
@@ -95,7 +97,7 @@ int make_plan(const int32_t *cu, int n_seqs, int64_t T_total, void *ws, const Wo
     p.table = (const ChunkInfo *)(base + w.off_table);
     p.doc_off = (const int32_t *)(base + w.off_doc);
     p.n_chunks = (const int32_t *)(base + 4);
-    int rc = cuda_status(cudaMemsetAsync(base, 0, 8, s));
+    int rc = cuda_status(cudaMemsetAsync(base, 0, zero_bytes, s));
     if (rc) return rc;
     if (!cu) {
         p.uniform = 1;
@@ -183,7 +185,9 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *z, c
     cudaStream_t s = (cudaStream_t)stream;
     note_begin(s);
     Plan p;
-    if ((rc = make_plan(cu_seqlens, n_seqs, T_total, workspace, w, s, p))) return rc;
+    // bf16: the header and the fused launch's ready flags, in one memset
+    const size_t zero = dtype == KDA_BF16 ? w.off_ready + sizeof(int) * (size_t)w.max_chunks * H : 8;
+    if ((rc = make_plan(cu_seqlens, n_seqs, T_total, workspace, w, s, p, zero))) return rc;
     void *records = (char *)workspace + w.off_rec;
     ScanArgs a;
     memset(&a, 0, sizeof(a));

@@ -172,14 +172,15 @@ static inline Workspace workspace_layout(int64_t T_total, int H, int n_seqs, int
     w.max_chunks = (int)(T_total / C + n_seqs);
     w.rec_bytes = dtype == KDA_BF16 ? REC_BF16_BYTES : REC_F32_BYTES;
     size_t off = 256;
+    w.off_ready = off;  // one record-ready flag per (chunk, head) for the fused prefill, right after
+                        // the header so that one memset clears both
+    off = align_up(off + sizeof(int) * (size_t)w.max_chunks * (size_t)H, 256);
     w.off_table = off;
     off = align_up(off + sizeof(ChunkInfo) * (size_t)w.max_chunks, 256);
     w.off_doc = off;
     off = align_up(off + sizeof(int32_t) * (size_t)(n_seqs + 1), 1024);
     w.off_rec = off;
     off = align_up(off + w.rec_bytes * (size_t)w.max_chunks * (size_t)H, 1024);
-    w.off_ready = off;  // one record-ready flag per (chunk, head) for the fused prefill
-    off = align_up(off + sizeof(int) * (size_t)w.max_chunks * (size_t)H, 256);
     w.off_pairs = off;
     if (n_seg > 0) off = align_up(off + sizeof(float) * 2 * (size_t)H * n_seg * D * D, 1024);
     w.off_enter = off;
@@ -244,6 +245,7 @@ int launch_prep_tc(const void *q, const void *k, const void *v, const float *z, 
 int launch_scan_simt(const ScanArgs &a, int dtype, cudaStream_t s);
 int launch_scan_tc(const ScanArgs &a, int n_sm, cudaStream_t s);
 int launch_out_tc(const Plan &p, int H, const void *records, void *o, int n_sm, cudaStream_t s);
+// `ready` holds plan max_chunks x H flags that the caller has zeroed on stream s.
 int launch_fused_tc(const void *q, const void *k, const void *v, const float *z, const float *A,
                     const float *beta, int H, float g_min, const ScanArgs &sa, int *ready, int n_sm,
                     cudaStream_t s, bool *used);
