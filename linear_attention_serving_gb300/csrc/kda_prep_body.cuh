@@ -62,7 +62,7 @@ constexpr int SM_AREG = 0;           // A_q images (2 k-blocks x 320 rows x 128 
                                      // an image past its valid rows runs into the following bytes;
                                      // those rows are ignored.
 constexpr int SM_AREG_KB = 40960;    // offset of the second k-block of the A_q images
-constexpr int SM_BQ = 81920;         // key-side images, 4 x (2 k-blocks x 16 rows x 128 B)
+constexpr int SM_BQ = 81920;         // key-side images, 2 k-blocks x (4 tiles x 16 rows x 128 B)
 constexpr int SM_B2 = 98304;         // [Diag(beta) K_decay | Diag(beta) V]^T (256 rows x 64 tokens);
                                      // later [W | U0] MN-major (4 blocks of 64 columns x 64 tokens)
 constexpr int SM_A2 = 131072;        // INV (64 rows x 64), then O0 staging
@@ -303,7 +303,7 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
                     }
                 }
                 // key side of key tile p, and Q_decay
-                *reinterpret_cast<uint32_t *>(sm + SM_BQ + tile * 4096 + kb * 2048 + swz(i - 16 * tile, cc)) = bf2(kx);
+                *reinterpret_cast<uint32_t *>(sm + SM_BQ + kb * 8192 + tile * 2048 + swz(i - 16 * tile, cc)) = bf2(kx);
                 *reinterpret_cast<uint32_t *>(sm + SM_QD + kb * 8192 + swz(i, cc)) = bf2(mul2(ePfx, qe[r]));
             }
 #pragma unroll
@@ -344,18 +344,22 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         tc_fence_before();
         __syncthreads();
 
-        // ---- 2. A_qk / A_kk block columns on the tensor cores
+        // ---- 2. A_qk / A_kk block columns on the tensor cores.  Key tiles 0 and 1
+        // take one M = 128 MMA each (N = 16); the images of tiles 2 and 3 (64 and
+        // 32 rows) are adjacent, so one M = 128, N = 32 MMA over both key tiles
+        // serves them: the blocks it forms across the two (tile 2's rows against
+        // tile 3's keys and the reverse) are never read.
         if (tid == 0) {
             tc_fence_after();
-            constexpr uint32_t ID128 = idesc_bf16_f32(128, 16), ID64 = idesc_bf16_f32(64, 16);
+            constexpr uint32_t ID16 = idesc_bf16_f32(128, 16), ID32 = idesc_bf16_f32(128, 32);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
+                for (int qq = 0; qq < 3; ++qq) {
                     const int kbs = s >> 2, w = s & 3;
                     const uint64_t ad = sdesc_sw128(smem_u32(sm + SM_AREG + kbs * SM_AREG_KB + arow_base(qq) * 128 + w * 32));
-                    const uint64_t bd = sdesc_sw128(smem_u32(sm + SM_BQ + qq * 4096 + kbs * 2048 + w * 32));
-                    mma_bf16(tmem + 16 * qq, ad, bd, qq < 2 ? ID128 : ID64, s > 0);
+                    const uint64_t bd = sdesc_sw128(smem_u32(sm + SM_BQ + kbs * 8192 + qq * 2048 + w * 32));
+                    mma_bf16(tmem + 16 * qq, ad, bd, qq < 2 ? ID16 : ID32, s > 0);
                 }
             }
             mma_commit(&mbar_p);
@@ -377,13 +381,14 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         float *INV = reinterpret_cast<float *>(sm + SM_AREG + SM_INV);
         float *tmp = reinterpret_cast<float *>(sm + SM_AREG + SM_TMP);
         {
-            // block column qq: image rows < nq are M_qk rows, rows nq .. 2 nq - 1 are A_kk rows
+            // block column qq: image rows < nq are M_qk rows, rows nq .. 2 nq - 1 are
+            // A_kk rows.  Image row r sits in TMEM lane r (tiles 0-2) or 64 + r (tile 3)
             const int qq = qt;
             float d[16];
             tmem_ld16(tmem + lane_off + 16 * qq, d);
             tmem_ld_wait();
             const int nq = 16 * (4 - qq);
-            const int r = qq < 2 ? lg * 32 + lane : (lane < 16 ? lg * 16 + lane : 1 << 20);
+            const int r = qq < 3 ? lg * 32 + lane : (lg == 2 ? lane : 1 << 20);
             if (r < nq) {
                 const int i = 16 * qq + r;
 #pragma unroll
