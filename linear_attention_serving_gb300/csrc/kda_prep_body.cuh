@@ -486,18 +486,20 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         if (!ok) { timed_out = true; break; }
 
         // ---- 5. K_restore^T [W | U0] = [G | H] (M = 128), and with M = 64
-        //         Q' = Q_decay - M_qk W (as I Q_decay + (-M_qk) W) and O0 = M_qk U0
+        //         (-M_qk) [W | U0] = [-M_qk W | -O0] (one N = 256 product), to which
+        //         I Q_decay is added on the left half: Q' = Q_decay - M_qk W.  The
+        //         epilogue flips the sign of the right half back to O0.
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t IDG = idesc_bf16_f32_bmn(128, 256), IDM = idesc_bf16_f32_bmn(64, 128);
+            constexpr uint32_t IDW = idesc_bf16_f32_bmn(64, 256);
             constexpr uint32_t NEG_A = 1u << 13;
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint32_t b0 = smem_u32(sm + SM_B2 + s * 2048);
                 const uint64_t am = sdesc_sw128(smem_u32(sm + SM_MQ + s * 32));
                 mma_bf16(tmem, sdesc_sw128(smem_u32(sm + SM_KRT + s * 32)), sdesc_mn(b0, 8192, 1024, SWZ_128B), IDG, s > 0);
-                mma_bf16(tmem + 256, am, sdesc_mn(b0, 8192, 1024, SWZ_128B), IDM | NEG_A, s > 0);
-                mma_bf16(tmem + 384, am, sdesc_mn(b0 + 16384, 8192, 1024, SWZ_128B), IDM, s > 0);
+                mma_bf16(tmem + 256, am, sdesc_mn(b0, 8192, 1024, SWZ_128B), IDW | NEG_A, s > 0);
             }
 #pragma unroll
             for (int s = 0; s < 4; ++s)
@@ -540,6 +542,8 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
                         for (int h8 = 0; h8 < 4; ++h8)
                             *reinterpret_cast<uint4 *>(sm + ST_QP + sw128_offset(m, col + 8 * h8, 64)) = pack8(d + 8 * h8);
                     } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) d[j] = -d[j];  // -O0 -> O0
 #pragma unroll
                         for (int h16 = 0; h16 < 2; ++h16) {
                             uint8_t *dst = sm + ST_O0 + slice_offset(m, col + 16 * h16 - 128, 64);
