@@ -221,33 +221,60 @@ def bench_prefill(args, dev, ws, kda):
 
 def e2e_prefill(args, dev, kda, inputs):
     """Through the public API with inputs in pinned host memory: every step copies
-    the inputs host -> device, runs kda_chunk_fwd, and reads o and the final state back."""
+    its inputs host -> device, runs kda_chunk_fwd, and reads o and the final state
+    back.  Steps are pipelined the way a serving loop runs them: two device input
+    sets, the host -> device copy of step i on one stream while step i - 1 computes
+    on another, and the device -> host read of step i on a third."""
     q, k, v, z, A, beta, cu, init = inputs
     host = [t.cpu().pin_memory() for t in (q, k, v, z, A, beta)]
-    devb = [torch.empty_like(t) for t in (q, k, v, z, A, beta)]
-    o_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    devb = [[torch.empty_like(t) for t in (q, k, v, z, A, beta)] for _ in range(2)]
     T, H = q.shape[0], q.shape[1]
     n_seqs = 1 if cu is None else cu.numel() - 1
-    f_h = torch.empty((n_seqs, H, 128, 128), dtype=torch.float32).pin_memory()
-    wsp = torch.empty(kda.chunk_fwd_workspace_size(T, H, n_seqs, q.dtype), dtype=torch.uint8, device=dev)
+    o_d = [torch.empty_like(q) for _ in range(2)]
+    o_h = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(2)]
+    f_h = [torch.empty((n_seqs, H, 128, 128), dtype=torch.float32).pin_memory() for _ in range(2)]
+    wsp = [torch.empty(kda.chunk_fwd_workspace_size(T, H, n_seqs, q.dtype), dtype=torch.uint8, device=dev)
+           for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host)
-    d2h = o_h.numel() * o_h.element_size() + f_h.numel() * f_h.element_size()
+    d2h = o_h[0].numel() * o_h[0].element_size() + f_h[0].numel() * f_h[0].element_size()
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_run = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    fins = [None, None]
 
-    def step():
-        for d_, h_ in zip(devb, host):
-            d_.copy_(h_, non_blocking=True)
-        o, fin = kda.chunk_fwd(*devb, cu_seqlens=cu, init_state=init, workspace=wsp)
-        o_h.copy_(o, non_blocking=True)
-        f_h.copy_(fin, non_blocking=True)
+    def step(i):
+        b_ = i & 1
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_run[b_])  # step i - 2 is done reading this input set
+            for d_, h_ in zip(devb[b_], host):
+                d_.copy_(h_, non_blocking=True)
+            ev_in[b_].record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(ev_in[b_])
+            s_run.wait_event(ev_out[b_])  # step i - 2's outputs have been read back
+            _, fins[b_] = kda.chunk_fwd(*devb[b_], cu_seqlens=cu, init_state=init, workspace=wsp[b_], out=o_d[b_])
+            ev_run[b_].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_run[b_])
+            fins[b_].record_stream(s_out)  # allocated on s_run, read here
+            o_h[b_].copy_(o_d[b_], non_blocking=True)
+            f_h[b_].copy_(fins[b_], non_blocking=True)
+            ev_out[b_].record(s_out)
 
-    for _ in range(max(1, args.warmup)):
-        step()
+    for i in range(max(2, args.warmup)):
+        step(i)
     torch.cuda.synchronize()
-    n = max(3, args.steps // 2)
+    n = max(4, args.steps // 2)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
-    for _ in range(n):
-        step()
+    for st in (s_in, s_run, s_out):
+        st.wait_event(a)
+    for i in range(n):
+        step(i)
+    cur = torch.cuda.current_stream()
+    for st in (s_in, s_run, s_out):
+        cur.wait_stream(st)
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / n
