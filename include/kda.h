@@ -108,6 +108,22 @@ int kda_version(void);
  * ------------------------------------------------------------------------ */
 size_t kda_chunk_fwd_workspace_size(int64_t T_total, int H, int n_seqs, int dtype);
 
+/* --------------------------------------------------------------------------
+ * kda_chunk_fwd_plan_segments -- the segment count kda_chunk_fwd picks by
+ * itself ("Kimi K3 模型结构（7）", section "KDA：三种执行形态" (SM-level CP):
+ * when a few (document, head) chains over long documents would leave the
+ * chain, not the parallel preparation, setting the time, kda_chunk_fwd runs
+ * the kda_segment_scan decomposition with this many segments instead; its
+ * results equal the single-chain run up to rounding).
+ *   varlen  nonzero when the call passes cu_seqlens: such calls (document
+ *           lengths only on the device) always take the single-chain path
+ * Returns 0 for the single-chain path, else the segment count (2 .. 64).  The
+ * choice depends on the shape, the dtype (bf16 only) and the current device's
+ * SM count; kda_chunk_fwd_workspace_size already includes the room it needs.
+ * No device work; never fails (invalid shapes return 0).
+ * ------------------------------------------------------------------------ */
+int kda_chunk_fwd_plan_segments(int64_t T_total, int H, int n_seqs, int dtype, int varlen);
+
 int kda_chunk_fwd(const void *q, const void *k, const void *v,
                   const float *z, const float *A, const float *beta,
                   const int32_t *cu_seqlens, int n_seqs,

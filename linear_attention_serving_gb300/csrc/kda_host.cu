@@ -1,6 +1,7 @@
 // kda_host.cu -- the C ABI (include/kda.h): argument checks, workspace layout,
 // chunk planning and the launch sequence of every entry point.
 #include <cstdint>
+#include <cmath>
 #include <cstring>
 
 #include "kda_internal.cuh"
@@ -111,6 +112,84 @@ int make_plan(const int32_t *cu, int n_seqs, int64_t T_total, void *ws, const Wo
     return launch_plan(cu, n_seqs, T_total, ws, w, s);
 }
 
+// Automatic segment count for kda_chunk_fwd ("Kimi K3 模型结构（7）", section
+// "KDA：三种执行形态" (SM-level CP): with few (document, head) chains over a
+// long document the sequential chain, not the parallel preparation, sets the
+// time; cutting the chunk list into segments that run side by side and are
+// then composed shortens it).  Only for equal-length bf16 batches, whose
+// document length is known on the host.  The model, measured on GB300:
+//   one chain        about 1.3 us per chunk (64 state columns per block);
+//   preparation      about 10.3 us per (chunk, head) unit on one SM, on the SMs
+//                    the chains leave free (all SMs without the fused launch);
+//   segments         pay a second pass over the chain and the composition
+//                    (about 25 us per segment), so they win only when the
+//                    chain is over 1.5x the preparation; their count balances
+//                    chain length against composition, n = sqrt(chunks / 18).
+// Returns 0 for one chain per (document, head).
+int plan_segments(int64_t T_total, int H, int n_seqs, bool varlen, int dtype, int n_sm) {
+    if (varlen || dtype != KDA_BF16 || T_total <= 0 || n_seqs < 1 || H < 1) return 0;
+    const int64_t chunks = (T_total / n_seqs + C - 1) / C;  // per document
+    const int64_t total = chunks * n_seqs;
+    const double units = (double)total * H;
+    const int64_t chains = 2LL * n_seqs * H;
+    const int prep_sms = chains <= n_sm / 4 ? n_sm - (int)chains : n_sm;
+    const double prep_us = 10.3 * units / (double)(prep_sms > 0 ? prep_sms : 1);
+    const double chain_us = 1.3 * (double)chunks;
+    if (chain_us <= 1.5 * prep_us) return 0;
+    int64_t n = llround(sqrt((double)total / 18.0));
+    if (n > 64) n = 64;
+    if (n > total / 2) n = total / 2;
+    return n >= 2 ? (int)n : 0;
+}
+
+// The three phases of the segment scan over a workspace laid out for n_segments.
+int run_segment_scan(const void *q, const void *k, const void *v, const float *z, const float *A,
+                     const float *beta, const int32_t *cu_seqlens, int n_seqs, int64_t T_total, int H,
+                     int dtype, float g_min, const float *init_state, int n_segments, float *pairs_M,
+                     float *pairs_S, void *o, float *final_state, void *workspace, const Workspace &w,
+                     cudaStream_t s) {
+    int rc;
+    Plan p;
+    if ((rc = make_plan(cu_seqlens, n_seqs, T_total, workspace, w, s, p))) return rc;
+    char *base = (char *)workspace;
+    void *records = base + w.off_rec;
+    float *pairs = (float *)(base + w.off_pairs);
+    float *s_enter = (float *)(base + w.off_enter);
+    if ((rc = launch_prep(q, k, v, z, A, beta, H, dtype, g_min, p, records, s))) return rc;
+
+    ScanArgs a;
+    memset(&a, 0, sizeof(a));
+    a.plan = p;
+    a.H = H;
+    a.records = records;
+    a.mode = SCAN_SEGMENTS;
+    a.n_units = n_segments;
+    a.n_seg = n_segments;
+    a.init_state = init_state;
+    a.s_enter = s_enter;
+    a.pairs = pairs;
+    // phase 1: pairs (M, S~) of every (head, segment) from zero / identity
+    a.ncols = 2 * D;
+    a.phase = 1;
+    if ((rc = launch_scan(a, dtype, s))) return rc;
+    // phase 2: entering states by sequential composition
+    if ((rc = launch_compose(p, H, n_segments, pairs, s_enter, s))) return rc;
+    // phase 3: every segment from its exact entering state
+    a.ncols = D;
+    a.phase = 3;
+    a.o = o;
+    a.final_state = final_state;
+    if ((rc = launch_scan(a, dtype, s))) return rc;
+    if ((rc = launch_empty_docs(p, H, init_state, final_state, s))) return rc;
+    const size_t mat = sizeof(float) * (size_t)H * n_segments * D * D;
+    if (pairs_M && (rc = cuda_status(cudaMemcpyAsync(pairs_M, pairs, mat, cudaMemcpyDeviceToDevice, s))))
+        return rc;
+    if (pairs_S &&
+        (rc = cuda_status(cudaMemcpyAsync(pairs_S, (char *)pairs + mat, mat, cudaMemcpyDeviceToDevice, s))))
+        return rc;
+    return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -164,7 +243,14 @@ long long kda_launch_count(void) { return (long long)__atomic_load_n(&g_launches
 
 size_t kda_chunk_fwd_workspace_size(int64_t T_total, int H, int n_seqs, int dtype) {
     if (T_total < 0 || H < 1 || n_seqs < 1) return 0;
-    return workspace_layout(T_total, H, n_seqs, 0, dtype).total;
+    // room for the segmented path whenever an equal-length batch of this shape takes it
+    const int n_seg = plan_segments(T_total, H, n_seqs, false, dtype, device_sm_count());
+    return workspace_layout(T_total, H, n_seqs, n_seg, dtype).total;
+}
+
+int kda_chunk_fwd_plan_segments(int64_t T_total, int H, int n_seqs, int dtype, int varlen) {
+    if (T_total < 0 || H < 1 || n_seqs < 1) return 0;
+    return plan_segments(T_total, H, n_seqs, varlen != 0, dtype, device_sm_count());
 }
 
 size_t kda_segment_scan_workspace_size(int64_t T_total, int H, int n_seqs, int n_segments,
@@ -180,10 +266,14 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *z, c
                   kda_stream_t stream) {
     int rc = check_prefill(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, Dm, dtype, g_min, o);
     if (rc) return rc;
-    const Workspace w = workspace_layout(T_total, H, n_seqs, 0, dtype);
+    const int n_seg = plan_segments(T_total, H, n_seqs, cu_seqlens != nullptr, dtype, device_sm_count());
+    const Workspace w = workspace_layout(T_total, H, n_seqs, n_seg, dtype);
     if (!workspace || workspace_bytes < w.total || ((uintptr_t)workspace & 255u)) return KDA_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     note_begin(s);
+    if (n_seg > 0)
+        return run_segment_scan(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, dtype, g_min, init_state,
+                                n_seg, nullptr, nullptr, o, final_state, workspace, w, s);
     Plan p;
     // bf16: the header and the fused launch's ready flags, in one memset
     const size_t zero = dtype == KDA_BF16 ? w.off_ready + sizeof(int) * (size_t)w.max_chunks * H : 8;
@@ -225,45 +315,8 @@ int kda_segment_scan(const void *q, const void *k, const void *v, const float *z
     if (!workspace || workspace_bytes < w.total || ((uintptr_t)workspace & 255u)) return KDA_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     note_begin(s);
-    Plan p;
-    if ((rc = make_plan(cu_seqlens, n_seqs, T_total, workspace, w, s, p))) return rc;
-    char *base = (char *)workspace;
-    void *records = base + w.off_rec;
-    float *pairs = (float *)(base + w.off_pairs);
-    float *s_enter = (float *)(base + w.off_enter);
-    if ((rc = launch_prep(q, k, v, z, A, beta, H, dtype, g_min, p, records, s))) return rc;
-
-    ScanArgs a;
-    memset(&a, 0, sizeof(a));
-    a.plan = p;
-    a.H = H;
-    a.records = records;
-    a.mode = SCAN_SEGMENTS;
-    a.n_units = n_segments;
-    a.n_seg = n_segments;
-    a.init_state = init_state;
-    a.s_enter = s_enter;
-    a.pairs = pairs;
-    // phase 1: pairs (M, S~) of every (head, segment) from zero / identity
-    a.ncols = 2 * D;
-    a.phase = 1;
-    if ((rc = launch_scan(a, dtype, s))) return rc;
-    // phase 2: entering states by sequential composition
-    if ((rc = launch_compose(p, H, n_segments, pairs, s_enter, s))) return rc;
-    // phase 3: every segment from its exact entering state
-    a.ncols = D;
-    a.phase = 3;
-    a.o = o;
-    a.final_state = final_state;
-    if ((rc = launch_scan(a, dtype, s))) return rc;
-    if ((rc = launch_empty_docs(p, H, init_state, final_state, s))) return rc;
-    const size_t mat = sizeof(float) * (size_t)H * n_segments * D * D;
-    if (pairs_M && (rc = cuda_status(cudaMemcpyAsync(pairs_M, pairs, mat, cudaMemcpyDeviceToDevice, s))))
-        return rc;
-    if (pairs_S &&
-        (rc = cuda_status(cudaMemcpyAsync(pairs_S, (char *)pairs + mat, mat, cudaMemcpyDeviceToDevice, s))))
-        return rc;
-    return KDA_OK;
+    return run_segment_scan(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, dtype, g_min, init_state,
+                            n_segments, pairs_M, pairs_S, o, final_state, workspace, w, s);
 }
 
 int kda_decode_step(float *state, const void *q, const void *k, const void *v, const float *z,

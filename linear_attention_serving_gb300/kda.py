@@ -51,6 +51,8 @@ def load(build_if_missing: bool = True):
     lib.kda_chunk_fwd_workspace_size.restype = S
     lib.kda_segment_scan_workspace_size.argtypes = [L, I, I, I, I]
     lib.kda_segment_scan_workspace_size.restype = S
+    lib.kda_chunk_fwd_plan_segments.argtypes = [L, I, I, I, I]
+    lib.kda_chunk_fwd_plan_segments.restype = I
     lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, P, P, P, S, P]
     lib.kda_chunk_fwd.restype = I
     lib.kda_segment_scan.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, I, P, P, P, P, P, S, P]
@@ -93,6 +95,14 @@ def _contig(*ts):
 def chunk_fwd_workspace_size(T_total: int, H: int, n_seqs: int, dtype=torch.bfloat16) -> int:
     code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
     return int(load().kda_chunk_fwd_workspace_size(T_total, H, n_seqs, code))
+
+
+def chunk_fwd_plan_segments(T_total: int, H: int, n_seqs: int = 1, dtype=torch.bfloat16,
+                            varlen: bool = False) -> int:
+    """kda_chunk_fwd_plan_segments: the segment count kda_chunk_fwd uses for this
+    shape on the current device (0 = one chain per (document, head))."""
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    return int(load().kda_chunk_fwd_plan_segments(T_total, H, n_seqs, code, int(varlen)))
 
 
 def segment_scan_workspace_size(T_total: int, H: int, n_seqs: int, n_segments: int,

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import linear_attention_serving_gb300 as kda
 from linear_attention_serving_gb300 import kda as kb
@@ -50,6 +51,24 @@ def test_workspace_sizes_grow_with_work():
     lib = kda.load()
     assert lib.kda_chunk_fwd_workspace_size(-1, 16, 1, 0) == 0
     assert lib.kda_segment_scan_workspace_size(64, 1, 1, 0, 0) == 0
+
+
+def test_segment_planner_host_logic():
+    """kda_chunk_fwd's own segment count: none for the bench's H=16, T=8192
+    (the chains keep pace with the preparation) or for short documents; a few
+    dozen at most for a long document over few heads; never for varlen (document
+    lengths are on the device) or fp32; and the workspace size has room for it."""
+    bf16 = torch.bfloat16
+    assert kda.chunk_fwd_plan_segments(8192, 16, 1, bf16) == 0
+    assert kda.chunk_fwd_plan_segments(333, 3, 1, bf16) == 0
+    n = kda.chunk_fwd_plan_segments(1 << 20, 8, 1, bf16)
+    assert 2 <= n <= 64
+    assert kda.chunk_fwd_plan_segments(1 << 20, 8, 1, bf16, varlen=True) == 0
+    assert kda.chunk_fwd_plan_segments(1 << 20, 8, 1, torch.float32) == 0
+    assert kda.chunk_fwd_plan_segments(-1, 8, 1, bf16) == 0 and kda.chunk_fwd_plan_segments(64, 0, 1, bf16) == 0
+    assert kda.chunk_fwd_workspace_size(1 << 20, 8, 1) >= kda.segment_scan_workspace_size(1 << 20, 8, 1, n)
+    # more heads leave the chain less exposed: the planner never asks for more segments
+    assert kda.chunk_fwd_plan_segments(1 << 20, 64, 1, bf16) <= n
 
 
 FAKE = ctypes.c_void_p(1 << 20)  # aligned dummy address; never dereferenced on these paths

@@ -133,3 +133,13 @@ def test_invalid_cu_seqlens_is_reported_on_device():
                   workspace=ws, out=o, output_final_state=False)
     assert kda.read_device_error(ws) & 1
     assert torch.all(o == 7.0)  # nothing written
+
+
+@pytest.mark.parametrize("T,H,n_seqs", [(8192, 1, 1), (16384, 1, 2)])
+def test_planner_segmented_path(T, H, n_seqs):
+    """Long documents over one head: kda_chunk_fwd cuts the chunk list into
+    segments by itself (kda_chunk_fwd_plan_segments > 0), and still matches the
+    oracle, across the document boundary of the two-document batch too."""
+    assert kda.chunk_fwd_plan_segments(T, H, n_seqs) >= 2
+    inp = kda_synth.prefill_inputs(T, H, "bf16", seed=900 + T, z_std=1.0, init_std=0.05, n_init=n_seqs)
+    check(*run_both(inp, n_seqs=n_seqs), "bf16")
