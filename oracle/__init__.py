@@ -119,6 +119,25 @@ def gate(z, A, g_min=G_MIN):
     return out
 
 
+L2NORM_EPS = 1e-6  # added to the sum of squares under the root; the pages give the flag, not the constant
+
+
+def input_prep(q, k, beta, qk_l2norm=False, beta_sigmoid=False, eps=L2NORM_EPS):
+    """The kernel-side input options of the pages' chunk_kda / fused_recurrent_kda
+    interface ([K3-2] "训练、prefill、decode 各用哪种形式": use_qk_l2norm_in_kernel,
+    use_beta_sigmoid_in_kernel):
+    q and k divided by their L2 norm over the key dimension, q / sqrt(sum(q^2) + eps),
+    per (token, head); beta replaced by its logistic sigmoid 1 / (1 + exp(-beta)).
+    q, k [..., dk]; beta any shape.  Returns fp64 copies (unchanged when a flag is off)."""
+    q, k, beta = _f64(q), _f64(k), _f64(beta)
+    if qk_l2norm:
+        q = q / np.sqrt(np.sum(q * q, axis=-1, keepdims=True) + eps)
+        k = k / np.sqrt(np.sum(k * k, axis=-1, keepdims=True) + eps)
+    if beta_sigmoid:
+        beta = 1.0 / (1.0 + np.exp(-beta))
+    return q, k, beta
+
+
 def recurrent(q, k, v, z, A, beta, cu_seqlens=None, init_state=None, g_min=G_MIN,
               n_threads=0, return_threads=False):
     """Token-by-token recurrence ([K3-7] eq. (1) in the delta form of [SA]).

@@ -390,3 +390,39 @@ def test_decode_replay_equals_snapshot_rollback():
         _, f = oracle.recurrent(w2[0][b, :1], w2[1][b, :1], w2[2][b, :1], w2[3][b, :1], A,
                                 w2[4][b, :1], init_state=snaps[nacc[b]][None])
         assert rel(S2[b], f[0]) < 1e-13
+
+
+# ---------------------------------------------------------------- in-kernel input options
+
+def test_input_prep_l2norm_closed_forms():
+    r = np.random.default_rng(11)
+    q = r.standard_normal((5, 3, 128)) * 3.0
+    k = r.standard_normal((5, 3, 128)) * 0.2
+    qn, kn, _ = oracle.input_prep(q, k, np.zeros((5, 3)), qk_l2norm=True)
+    # unit rows (up to the eps under the root), same directions
+    assert np.allclose(np.linalg.norm(qn, axis=-1), 1.0, atol=1e-6)
+    assert np.allclose(np.linalg.norm(kn, axis=-1), 1.0, atol=1e-4)
+    assert np.allclose(qn * np.linalg.norm(q, axis=-1, keepdims=True), q, atol=1e-6)
+    # scale invariance over the key dimension only (a norm over the wrong axis breaks it)
+    qs, _, _ = oracle.input_prep(q * np.arange(1, 6).reshape(5, 1, 1), k, np.zeros((5, 3)), qk_l2norm=True)
+    assert np.allclose(qs, qn, atol=1e-9)
+    # eps sits under the root: a row of squared norm eps comes out with norm 1/sqrt(2)
+    e = oracle.L2NORM_EPS
+    tiny = np.zeros((1, 1, 128))
+    tiny[0, 0, 7] = math.sqrt(e)
+    t, _, _ = oracle.input_prep(tiny, tiny, np.zeros((1, 1)), qk_l2norm=True)
+    assert abs(np.linalg.norm(t) - 1 / math.sqrt(2)) < 1e-12
+    # the zero row stays zero; flags off leave everything unchanged
+    z0, _, _ = oracle.input_prep(np.zeros((1, 1, 128)), tiny, np.zeros((1, 1)), qk_l2norm=True)
+    assert not z0.any()
+    q2, k2, b2 = oracle.input_prep(q, k, np.ones((5, 3)))
+    assert np.array_equal(q2, q) and np.array_equal(k2, k) and np.array_equal(b2, np.ones((5, 3)))
+
+
+def test_input_prep_beta_sigmoid_closed_forms():
+    x = np.array([[-30.0, -2.0, 0.0, 0.5, 3.0, 30.0]])
+    _, _, b = oracle.input_prep(np.zeros((1, 1, 4)), np.zeros((1, 1, 4)), x, beta_sigmoid=True)
+    assert b[0, 2] == 0.5
+    assert np.allclose(b + oracle.input_prep(np.zeros((1, 1, 4)), np.zeros((1, 1, 4)), -x, beta_sigmoid=True)[2], 1.0)
+    assert abs(b[0, 4] - 1 / (1 + math.exp(-3.0))) < 1e-15
+    assert 0 < b[0, 0] < 1e-12 and 1 - b[0, 5] < 1e-12
