@@ -57,6 +57,15 @@ enum kda_status {
 
 enum kda_dtype { KDA_BF16 = 0, KDA_F32 = 1 };
 
+/* Input options (bit flags), the kernel-side options of the pages' chunk_kda /
+ * fused_recurrent_kda ("Kimi K3 模型结构（2）", section "训练、prefill、decode
+ * 各用哪种形式": use_qk_l2norm_in_kernel, use_beta_sigmoid_in_kernel):
+ *   KDA_FLAG_QK_L2NORM     q and k are divided by their L2 norm over the 128 key
+ *                          channels, x / sqrt(sum(x^2) + 1e-6), per (token, head)
+ *   KDA_FLAG_BETA_SIGMOID  beta holds logits; the kernels use 1 / (1 + exp(-beta))
+ * The decode cache keeps the projected inputs as given (unnormalised, logits). */
+enum kda_flags { KDA_FLAG_QK_L2NORM = 1, KDA_FLAG_BETA_SIGMOID = 2 };
+
 /* Device error codes (bit flags) written into the workspace / error word. */
 enum kda_device_error {
     KDA_DEVERR_NONE = 0,
@@ -86,7 +95,8 @@ int kda_version(void);
  *   q, k, v      (device) [T_total, H, D]  dtype
  *   z            (device) [T_total, H, D]  fp32 gate logits
  *   A            (device) [H]              fp32 per-head log scale A_h
- *   beta         (device) [T_total, H]     fp32, after sigmoid
+ *   beta         (device) [T_total, H]     fp32, after sigmoid (logits with
+ *                KDA_FLAG_BETA_SIGMOID)
  *   cu_seqlens   (device) int32 [n_seqs+1]: document offsets, cu[0] = 0,
  *                non-decreasing, cu[n_seqs] = T_total (empty documents allowed).
  *                NULL: n_seqs equal-length sequences (T_total % n_seqs == 0).
@@ -98,6 +108,7 @@ int kda_version(void);
  *   H            heads (>= 1);  D: must be 128
  *   dtype        KDA_BF16 or KDA_F32
  *   g_min        gate lower bound (the pages fix -5); must be in [-5, 0)
+ *   flags        0 or an OR of KDA_FLAG_* (others: KDA_ERR_INVALID_ARG)
  *   init_state   (device) fp32 [n_seqs, H, D, D] or NULL (zeros)
  *   o            (device) [T_total, H, D] dtype, written
  *   final_state  (device) fp32 [n_seqs, H, D, D] or NULL (not written)
@@ -129,7 +140,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v,
                   const int32_t *cu_seqlens, int n_seqs,
                   int64_t T_total, int H, int D, int dtype, float g_min,
                   const float *init_state, void *o, float *final_state,
-                  void *workspace, size_t workspace_bytes, kda_stream_t stream);
+                  void *workspace, size_t workspace_bytes, int flags, kda_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * kda_chunk_fwd_noalloc -- kda_chunk_fwd without a caller-provided workspace.
@@ -139,7 +150,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v,
  * device synchronisation a cudaMalloc may imply).
  *
  * Same arguments, checks and results as kda_chunk_fwd, without workspace and
- * workspace_bytes.  The workspace is a fixed array of
+ * workspace_bytes (and without the automatic segmentation).  The workspace is a fixed array of
  * KDA_NOALLOC_SCRATCH_BYTES bytes in device global memory owned by the library
  * (every GPU that loads the library holds it until exit); the call allocates
  * nothing and calls no allocating routine.
@@ -161,7 +172,7 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                           const int32_t *cu_seqlens, int n_seqs,
                           int64_t T_total, int H, int D, int dtype, float g_min,
                           const float *init_state, void *o, float *final_state,
-                          kda_stream_t stream);
+                          int flags, kda_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * kda_segment_scan -- intra-device context parallelism over one long packed
@@ -197,7 +208,7 @@ int kda_segment_scan(const void *q, const void *k, const void *v,
                      const float *init_state, int n_segments,
                      float *pairs_M, float *pairs_S,
                      void *o, float *final_state,
-                     void *workspace, size_t workspace_bytes, kda_stream_t stream);
+                     void *workspace, size_t workspace_bytes, int flags, kda_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * kda_decode_step -- one decode step with MTP draft replay ("Kimi K3 模型结构
@@ -217,7 +228,8 @@ int kda_segment_scan(const void *q, const void *k, const void *v,
  *
  *   state        (device) fp32 [N, H, D, D], read and written in place
  *   q, k, v      (device) [N, W, H, D] dtype;  z (device) fp32 [N, W, H, D]
- *   beta         (device) fp32 [N, W, H];      A (device) fp32 [H]
+ *   beta         (device) fp32 [N, W, H] (logits with KDA_FLAG_BETA_SIGMOID);
+ *                A (device) fp32 [H]
  *   cache_q, cache_k, cache_v (device) [N, W-1, H, D] dtype, read and written
  *   cache_z      (device) fp32 [N, W-1, H, D]; cache_beta (device) fp32 [N, W-1, H]
  *                (the cache pointers may be NULL only when W == 1)
@@ -227,6 +239,8 @@ int kda_segment_scan(const void *q, const void *k, const void *v,
  *   error_word   (device) int32 or NULL: KDA_DEVERR_NUM_ACCEPTED is OR-ed in
  *                when a num_accepted value is out of range; that sequence's
  *                state, cache and outputs are then left untouched.
+ *   flags        0 or an OR of KDA_FLAG_*, the same for every step of a
+ *                sequence (the cache holds inputs as given)
  * state, q, k, v, z, o and the caches must be 16-byte aligned.
  * ------------------------------------------------------------------------ */
 int kda_decode_step(float *state,
@@ -236,7 +250,7 @@ int kda_decode_step(float *state,
                     float *cache_z, float *cache_beta,
                     const int32_t *num_accepted,
                     int N, int H, int D, int W, int dtype, float g_min,
-                    void *o, int32_t *error_word, kda_stream_t stream);
+                    void *o, int32_t *error_word, int flags, kda_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * kda_read_device_error -- synchronise `stream` and read the device error

@@ -119,18 +119,23 @@ __device__ __forceinline__ void load_betas(int item, int H, int W, int tid, cons
     bw = (tid < W) ? beta[((size_t)b * W + tid) * H + h] : 0.f;
 }
 
-template <typename InT>
+// OPTS compiles the input options (KDA_FLAG_*) in: a separate instantiation,
+// so that the default path keeps its registers.
+template <typename InT, bool OPTS>
 __global__ void __launch_bounds__(DEC_THREADS, 2)
 decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *__restrict__ k,
               const InT *__restrict__ v, const float *__restrict__ z, const float *__restrict__ beta,
               const float *__restrict__ A, InT *__restrict__ cq, InT *__restrict__ ck,
               InT *__restrict__ cv, float *__restrict__ cz, float *__restrict__ cb,
               const int32_t *__restrict__ nacc_p, int N, int H, int W, float g_min, InT *__restrict__ o,
-              int32_t *__restrict__ err) {
+              int32_t *__restrict__ err, int flags) {
     extern __shared__ __align__(128) uint8_t smdyn[];
     __shared__ uint64_t full_bar;
     __shared__ float sbeta[2][2 * MAX_W];
     __shared__ __align__(16) float scommit[VPAD];
+    __shared__ float snorm[2 * MAX_W][4][2];  // KDA_FLAG_QK_L2NORM: squared norms per token and warp
+    const bool l2norm = OPTS && (flags & KDA_FLAG_QK_L2NORM) != 0;
+    const bool bsig = OPTS && (flags & KDA_FLAG_BETA_SIGMOID) != 0;
 
     const DecSmem L(W);
     uint8_t *sm = smdyn;
@@ -226,11 +231,35 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
             // channel c of every token: inputs, the cumulative decay s_t over the
             // step's tokens, and the scaled vectors s_t k, k / s_t, s_t q
             const int c = tid, vc = vidx(c);
+            if (l2norm) {
+                // input option: squared norms of q and k over the 128 channels
+                // (replayed tokens carry no q)
+                for (int t = 0; t < ntok; ++t) {
+                    const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
+                    const float qq = t < nacc ? 0.f : to_f32(reinterpret_cast<const InT *>(slot)[c]);
+                    const float kk = to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
+                    float pq = qq * qq, pk = kk * kk;
+#pragma unroll
+                    for (int m = 16; m > 0; m >>= 1) {
+                        pq += __shfl_xor_sync(0xffffffffu, pq, m);
+                        pk += __shfl_xor_sync(0xffffffffu, pk, m);
+                    }
+                    if (lane == 0) {
+                        snorm[t][warp][0] = pq;
+                        snorm[t][warp][1] = pk;
+                    }
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");  // the channel threads (warps 0-3) only
+            }
             float sc = 1.f;
             for (int t = 0; t < ntok; ++t) {
                 const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
-                const float qq = t < nacc ? 0.f : to_f32(reinterpret_cast<const InT *>(slot)[c]);
-                const float kk = to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
+                float qq = t < nacc ? 0.f : to_f32(reinterpret_cast<const InT *>(slot)[c]);
+                float kk = to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
+                if (l2norm) {
+                    qq *= rsqrtf(snorm[t][0][0] + snorm[t][1][0] + snorm[t][2][0] + snorm[t][3][0] + L2NORM_EPS);
+                    kk *= rsqrtf(snorm[t][0][1] + snorm[t][1][1] + snorm[t][2][1] + snorm[t][3][1] + L2NORM_EPS);
+                }
                 const float zz = reinterpret_cast<const float *>(slot + 1536)[c];
                 sc *= expf(kda_gate(g_min, eA, zz));
                 kt[t][vc] = kk * sc;
@@ -282,7 +311,8 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                 acc1 += __shfl_xor_sync(0xffffffffu, acc1, m);
             }
             const float2 vv = *reinterpret_cast<const float2 *>(&vt[t][col]);
-            const float u0 = bt[t] * (vv.x - acc0), u1 = bt[t] * (vv.y - acc1);
+            const float bb = bsig ? 1.f / (1.f + __expf(-bt[t])) : bt[t];  // input option: beta logit
+            const float u0 = bb * (vv.x - acc0), u1 = bb * (vv.y - acc1);
 #pragma unroll
             for (int i = 0; i < DEC_R; i += 4) {
                 const float4 kv = *reinterpret_cast<const float4 *>(&kh[t][vidx(rbase + i)]);
@@ -346,7 +376,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
 int launch_decode(float *state, const void *q, const void *k, const void *v, const float *z,
                   const float *beta, const float *A, void *cq, void *ck, void *cv, float *cz,
                   float *cb, const int32_t *nacc, int N, int H, int W, int dtype, float g_min,
-                  void *o, int32_t *err, cudaStream_t s) {
+                  void *o, int32_t *err, int flags, cudaStream_t s) {
     const long long items = (long long)N * H;
     if (items <= 0) return KDA_OK;
     if (W > MAX_W) return KDA_ERR_UNSUPPORTED;
@@ -355,7 +385,7 @@ int launch_decode(float *state, const void *q, const void *k, const void *v, con
     int per_sm = 1, n_sm = device_sm_count();
     int grid;
     if (dtype == KDA_BF16) {
-        auto kern = decode_kernel<__nv_bfloat16>;
+        auto kern = flags ? decode_kernel<__nv_bfloat16, true> : decode_kernel<__nv_bfloat16, false>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return KDA_ERR_CUDA;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DEC_THREADS, smem);
@@ -363,16 +393,16 @@ int launch_decode(float *state, const void *q, const void *k, const void *v, con
         kern<<<grid, DEC_THREADS, smem, s>>>(
             state, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, z, beta, A,
             (__nv_bfloat16 *)cq, (__nv_bfloat16 *)ck, (__nv_bfloat16 *)cv, cz, cb, nacc, N, H, W, g_min,
-            (__nv_bfloat16 *)o, err);
+            (__nv_bfloat16 *)o, err, flags);
     } else {
-        auto kern = decode_kernel<float>;
+        auto kern = flags ? decode_kernel<float, true> : decode_kernel<float, false>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return KDA_ERR_CUDA;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DEC_THREADS, smem);
         grid = (int)(items < (long long)n_sm * (per_sm > 0 ? per_sm : 1) ? items : (long long)n_sm * (per_sm > 0 ? per_sm : 1));
         kern<<<grid, DEC_THREADS, smem, s>>>(state, (const float *)q, (const float *)k, (const float *)v, z,
                                              beta, A, (float *)cq, (float *)ck, (float *)cv, cz, cb, nacc, N,
-                                             H, W, g_min, (float *)o, err);
+                                             H, W, g_min, (float *)o, err, flags);
     }
     note_launch("decode", s);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;

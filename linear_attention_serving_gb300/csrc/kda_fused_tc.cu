@@ -26,6 +26,7 @@ namespace {
 constexpr int FUSED_N = 64, FUSED_STAGES = 3, FUSED_TPR = 2;
 constexpr int FUSED_SLICES = D / FUSED_N;  // chain blocks per (document, head)
 
+template <bool OPTS>
 __global__ void __launch_bounds__(PT_THREADS, 1)
 fused_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z, const float *__restrict__ A,
@@ -37,7 +38,7 @@ fused_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
     // units n_chain + j, n_chain + j + n_prep, ...  (One call site: the prep
     // code is inlined once.)
     const bool chain = (int)blockIdx.x < n_chain;
-    prep_blocks(q, k, v, z, A, beta, H, g_min, plan, records, smraw, blockIdx.x,
+    prep_blocks<OPTS>(q, k, v, z, A, beta, H, g_min, plan, records, smraw, blockIdx.x,
                 chain ? (1 << 30) : (int)gridDim.x - n_chain, ready);
     if (chain) {
         fence_async_smem();
@@ -66,9 +67,10 @@ int launch_fused_tc(const void *q, const void *k, const void *v, const float *z,
     constexpr size_t chain_smem = scan_tc_smem_bytes<FUSED_N, FUSED_STAGES, true>();
     static_assert(ScanCfg<FUSED_N, FUSED_TPR, true>::THREADS <= PT_THREADS, "chain block fits the prep's block");
     const size_t smem = PREP_TC_SMEM > chain_smem ? PREP_TC_SMEM : chain_smem;
-    if (cudaFuncSetAttribute(fused_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    auto kern = p.flags ? fused_tc_kernel<true> : fused_tc_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return KDA_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_tc_kernel, PT_THREADS, smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, PT_THREADS, smem) != cudaSuccess ||
         per_sm < 1)
         return KDA_OK;
     const __nv_bfloat16 *qb = (const __nv_bfloat16 *)q, *kb = (const __nv_bfloat16 *)k, *vb = (const __nv_bfloat16 *)v;
@@ -77,7 +79,7 @@ int launch_fused_tc(const void *q, const void *k, const void *v, const float *z,
     ScanArgs a = sa;
     int nc = (int)n_chain;
     void *args[] = {&qb, &kb, &vb, &z, &A, &beta, &H, &g_min, &plan, &records, &a, &nc, &ready};
-    const cudaError_t e = cudaLaunchCooperativeKernel((const void *)fused_tc_kernel, dim3(n_sm), dim3(PT_THREADS),
+    const cudaError_t e = cudaLaunchCooperativeKernel((const void *)kern, dim3(n_sm), dim3(PT_THREADS),
                                                       args, smem, s);
     if (e != cudaSuccess) {
         cudaGetLastError();  // a cooperative launch that does not fit leaves the three-kernel path

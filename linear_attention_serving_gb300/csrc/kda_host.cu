@@ -54,8 +54,9 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA
 // Validation shared by kda_chunk_fwd and kda_segment_scan.
 int check_prefill(const void *q, const void *k, const void *v, const float *z, const float *A,
                   const float *beta, const int32_t *cu, int n_seqs, int64_t T_total, int H, int Dm,
-                  int dtype, float g_min, const void *o) {
+                  int dtype, float g_min, const void *o, int flags) {
     if (Dm != D) return KDA_ERR_UNSUPPORTED;
+    if (flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BETA_SIGMOID)) return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
     if (H < 1 || n_seqs < 1 || T_total < 0 || T_total >= (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
     if (!(g_min >= -5.0f && g_min < 0.0f)) return KDA_ERR_INVALID_ARG;
@@ -90,8 +91,9 @@ int launch_scan(const ScanArgs &a, int dtype, cudaStream_t s) {
 // Clears the workspace's first `zero_bytes` (at least the 8-byte header: error
 // word and chunk count) and fills in the chunk plan.
 int make_plan(const int32_t *cu, int n_seqs, int64_t T_total, void *ws, const Workspace &w,
-              cudaStream_t s, Plan &p, size_t zero_bytes = 8) {
+              cudaStream_t s, Plan &p, int flags, size_t zero_bytes = 8) {
     memset(&p, 0, sizeof(p));
+    p.flags = flags;
     char *base = (char *)ws;
     p.n_seqs = n_seqs;
     p.err = (int32_t *)base;
@@ -147,10 +149,10 @@ int run_segment_scan(const void *q, const void *k, const void *v, const float *z
                      const float *beta, const int32_t *cu_seqlens, int n_seqs, int64_t T_total, int H,
                      int dtype, float g_min, const float *init_state, int n_segments, float *pairs_M,
                      float *pairs_S, void *o, float *final_state, void *workspace, const Workspace &w,
-                     cudaStream_t s) {
+                     int flags, cudaStream_t s) {
     int rc;
     Plan p;
-    if ((rc = make_plan(cu_seqlens, n_seqs, T_total, workspace, w, s, p))) return rc;
+    if ((rc = make_plan(cu_seqlens, n_seqs, T_total, workspace, w, s, p, flags))) return rc;
     char *base = (char *)workspace;
     void *records = base + w.off_rec;
     float *pairs = (float *)(base + w.off_pairs);
@@ -262,9 +264,9 @@ size_t kda_segment_scan_workspace_size(int64_t T_total, int H, int n_seqs, int n
 int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *z, const float *A,
                   const float *beta, const int32_t *cu_seqlens, int n_seqs, int64_t T_total, int H,
                   int Dm, int dtype, float g_min, const float *init_state, void *o,
-                  float *final_state, void *workspace, size_t workspace_bytes,
+                  float *final_state, void *workspace, size_t workspace_bytes, int flags,
                   kda_stream_t stream) {
-    int rc = check_prefill(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, Dm, dtype, g_min, o);
+    int rc = check_prefill(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, Dm, dtype, g_min, o, flags);
     if (rc) return rc;
     const int n_seg = plan_segments(T_total, H, n_seqs, cu_seqlens != nullptr, dtype, device_sm_count());
     const Workspace w = workspace_layout(T_total, H, n_seqs, n_seg, dtype);
@@ -273,11 +275,11 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *z, c
     note_begin(s);
     if (n_seg > 0)
         return run_segment_scan(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, dtype, g_min, init_state,
-                                n_seg, nullptr, nullptr, o, final_state, workspace, w, s);
+                                n_seg, nullptr, nullptr, o, final_state, workspace, w, flags, s);
     Plan p;
     // bf16: the header and the fused launch's ready flags, in one memset
     const size_t zero = dtype == KDA_BF16 ? w.off_ready + sizeof(int) * (size_t)w.max_chunks * H : 8;
-    if ((rc = make_plan(cu_seqlens, n_seqs, T_total, workspace, w, s, p, zero))) return rc;
+    if ((rc = make_plan(cu_seqlens, n_seqs, T_total, workspace, w, s, p, flags, zero))) return rc;
     void *records = (char *)workspace + w.off_rec;
     ScanArgs a;
     memset(&a, 0, sizeof(a));
@@ -307,8 +309,8 @@ int kda_segment_scan(const void *q, const void *k, const void *v, const float *z
                      const float *beta, const int32_t *cu_seqlens, int n_seqs, int64_t T_total,
                      int H, int Dm, int dtype, float g_min, const float *init_state, int n_segments,
                      float *pairs_M, float *pairs_S, void *o, float *final_state, void *workspace,
-                     size_t workspace_bytes, kda_stream_t stream) {
-    int rc = check_prefill(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, Dm, dtype, g_min, o);
+                     size_t workspace_bytes, int flags, kda_stream_t stream) {
+    int rc = check_prefill(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, Dm, dtype, g_min, o, flags);
     if (rc) return rc;
     if (n_segments < 1 || n_segments > (1 << 20)) return KDA_ERR_INVALID_ARG;
     const Workspace w = workspace_layout(T_total, H, n_seqs, n_segments, dtype);
@@ -316,15 +318,16 @@ int kda_segment_scan(const void *q, const void *k, const void *v, const float *z
     cudaStream_t s = (cudaStream_t)stream;
     note_begin(s);
     return run_segment_scan(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, dtype, g_min, init_state,
-                            n_segments, pairs_M, pairs_S, o, final_state, workspace, w, s);
+                            n_segments, pairs_M, pairs_S, o, final_state, workspace, w, flags, s);
 }
 
 int kda_decode_step(float *state, const void *q, const void *k, const void *v, const float *z,
                     const float *beta, const float *A, void *cache_q, void *cache_k, void *cache_v,
                     float *cache_z, float *cache_beta, const int32_t *num_accepted, int N, int H,
-                    int Dm, int W, int dtype, float g_min, void *o, int32_t *error_word,
+                    int Dm, int W, int dtype, float g_min, void *o, int32_t *error_word, int flags,
                     kda_stream_t stream) {
     if (Dm != D) return KDA_ERR_UNSUPPORTED;
+    if (flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BETA_SIGMOID)) return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
     if (N < 1 || H < 1 || W < 1 || W > 8) return KDA_ERR_INVALID_ARG;
     if ((int64_t)N * H >= (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
@@ -337,7 +340,7 @@ int kda_decode_step(float *state, const void *q, const void *k, const void *v, c
         return KDA_ERR_INVALID_ARG;
     note_begin((cudaStream_t)stream);
     return launch_decode(state, q, k, v, z, beta, A, cache_q, cache_k, cache_v, cache_z, cache_beta,
-                         num_accepted, N, H, W, dtype, g_min, o, error_word, (cudaStream_t)stream);
+                         num_accepted, N, H, W, dtype, g_min, o, error_word, flags, (cudaStream_t)stream);
 }
 
 int kda_read_device_error(const void *workspace, int32_t *code, kda_stream_t stream) {

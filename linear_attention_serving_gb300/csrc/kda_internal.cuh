@@ -57,7 +57,10 @@ struct Plan {
     const int32_t *doc_off;  // table mode: [n_seqs + 1] first chunk of each document
     const int32_t *n_chunks; // table mode: device count
     int32_t *err;            // device error word (bit flags kda_device_error)
+    int flags;               // input options (KDA_FLAG_*) for the preparation kernels
 };
+
+constexpr float L2NORM_EPS = 1e-6f;  // KDA_FLAG_QK_L2NORM: x / sqrt(sum(x^2) + eps)
 
 __device__ __forceinline__ int plan_n_chunks(const Plan &p) {
     return p.uniform ? p.n_seqs * p.chunks_per_seq : *p.n_chunks;
@@ -255,6 +258,6 @@ int launch_compose(const Plan &p, int H, int n_seg, const float *pairs, float *s
 int launch_decode(float *state, const void *q, const void *k, const void *v, const float *z,
                   const float *beta, const float *A, void *cq, void *ck, void *cv, float *cz,
                   float *cb, const int32_t *nacc, int N, int H, int W, int dtype, float g_min,
-                  void *o, int32_t *err, cudaStream_t s);
+                  void *o, int32_t *err, int flags, cudaStream_t s);
 
 }  // namespace kda

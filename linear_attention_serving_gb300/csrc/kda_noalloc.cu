@@ -54,9 +54,10 @@ extern "C" int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v
                                      const float *A, const float *beta, const int32_t *cu_seqlens,
                                      int n_seqs, int64_t T_total, int H, int Dm, int dtype, float g_min,
                                      const float *init_state, void *o, float *final_state,
-                                     kda_stream_t stream) {
+                                     int flags, kda_stream_t stream) {
     // the same argument checks as kda_chunk_fwd
     if (Dm != D) return KDA_ERR_UNSUPPORTED;
+    if (flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BETA_SIGMOID)) return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
     if (H < 1 || n_seqs < 1 || T_total < 0 || T_total >= (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
     if (!(g_min >= -5.0f && g_min < 0.0f)) return KDA_ERR_INVALID_ARG;
@@ -86,6 +87,7 @@ extern "C" int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v
     p.table = (const ChunkInfo *)(base + w.off_table);
     p.doc_off = (const int32_t *)(base + w.off_doc);
     p.n_chunks = (const int32_t *)(base + 4);
+    p.flags = flags;
     if (cudaMemsetAsync(base, 0, 8, s) != cudaSuccess) return KDA_ERR_CUDA;
     if (!cu_seqlens) {
         p.uniform = 1;

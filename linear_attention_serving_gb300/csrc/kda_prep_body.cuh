@@ -70,8 +70,9 @@ constexpr int SM_KRT = 147456;       // K_restore^T: 128 channels x 64 tokens
 constexpr int SM_QD = 163840;        // Q_decay, MN-major (2 blocks of 64 channels x 64 tokens)
 constexpr int SM_MQ = 180224;        // M_qk (64 rows x 64)
 constexpr int SM_ID = 188416;        // identity (64 rows x 64), written once
-constexpr int SM_MISC = 196608;      // beta [64] | partial log2-decay sums [8][128]
-constexpr int SM_BYTES = SM_MISC + 256 + 4096;
+constexpr int SM_MISC = 196608;      // beta [64] | partial log2-decay sums [8][128] |
+                                     // squared norms of q, k per token and warp half [64][4]
+constexpr int SM_BYTES = SM_MISC + 256 + 4096 + 1024;
 constexpr size_t PREP_TC_SMEM = SM_BYTES + 1024;
 
 // staging of the output record: written after the last MMA has read its
@@ -165,8 +166,11 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
 }
 
 // The units first, first + stride, ... of the launch, on one block of
-// PT_THREADS threads.  With `ready` non-null, ready[u] is set (release, after
+// PT_THREADS threads.  OPTS compiles the input options (KDA_FLAG_*, read from
+// the plan) in: a separate instantiation, so that the default path keeps its
+// registers.  With `ready` non-null, ready[u] is set (release, after
 // the record's bulk stores have completed) once unit u's record is in memory.
+template <bool OPTS>
 __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                                             const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z,
                                             const float *__restrict__ A, const float *__restrict__ beta, int H,
@@ -183,6 +187,9 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
     uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
     float *sbeta = reinterpret_cast<float *>(sm + SM_MISC);
     float *sHalf = sbeta + 64;  // [8][128] log2-decay sums of each 8-token group
+    float *snorm = sHalf + 8 * 128;  // [64 tokens][q half 0, q half 1, k half 0, k half 1]
+    const bool l2norm = OPTS && (plan.flags & KDA_FLAG_QK_L2NORM) != 0;
+    const bool bsig = OPTS && (plan.flags & KDA_FLAG_BETA_SIGMOID) != 0;
     const float gm2 = g_min * LOG2E;
 
     if (tid == 0) {
@@ -223,7 +230,10 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         load_part<0>(q, k, v, z, H, u % H, ci.tok, ci.len, rg, cp, cin);
         load_part<1>(q, k, v, z, H, u % H, ci.tok, ci.len, rg, cp, cin);
         load_part<2>(q, k, v, z, H, u % H, ci.tok, ci.len, rg, cp, cin);
-        if (tid < 64 && tid < ci.len) b_next = beta[(size_t)(ci.tok + tid) * H + u % H];
+        if (tid < 64 && tid < ci.len) {
+            b_next = beta[(size_t)(ci.tok + tid) * H + u % H];
+            if (bsig) b_next = 1.f / (1.f + __expf(-b_next));  // input option: beta logit
+        }
         a_next = A[u % H];
     }
     bool timed_out = false;
@@ -235,7 +245,25 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         float2 rl[8];
         gate_sums(cin, a_next, gm2, 8 * rg, ci.len, rl);
         *reinterpret_cast<float2 *>(sHalf + rg * 128 + 2 * cp) = rl[7];
+        // input option: squared norms of q and k over this warp's 64 channels (the
+        // token's other 64 sit in the neighbouring warp)
         if (tid < 64) sbeta[tid] = b_next;
+        if (l2norm) {
+#pragma unroll 1
+            for (int r = 0; r < 8; ++r) {
+                const float2 qf = __bfloat1622float2(cin.q[r]), kf = __bfloat1622float2(cin.k[r]);
+                float pq = qf.x * qf.x + qf.y * qf.y, pk = kf.x * kf.x + kf.y * kf.y;
+#pragma unroll
+                for (int m = 16; m > 0; m >>= 1) {
+                    pq += __shfl_xor_sync(0xffffffffu, pq, m);
+                    pk += __shfl_xor_sync(0xffffffffu, pk, m);
+                }
+                if (lane == 0) {
+                    snorm[4 * (8 * rg + r) + (warp & 1)] = pq;
+                    snorm[4 * (8 * rg + r) + 2 + (warp & 1)] = pk;
+                }
+            }
+        }
         __syncthreads();
 
         // tile sums Delta_t (log2), exp(Delta_t), and this thread's carry into its tile
@@ -261,6 +289,17 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
             *reinterpret_cast<float2 *>(rec + REC_BF16_AC + 8 * cp) = mul2(mul2(eD[0], eD[1]), mul2(eD[2], eD[3]));
 
         // ---- 1b. per-token operands that do not touch the staging area
+        if (l2norm) {
+            // input option: this thread's q and k divided by their tokens' norms
+            // (rounded back to bf16, as the operands they feed are)
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const float4 nn = *reinterpret_cast<const float4 *>(snorm + 4 * (8 * rg + r));
+                const float iq = rsqrtf(nn.x + nn.y + L2NORM_EPS), ik = rsqrtf(nn.z + nn.w + L2NORM_EPS);
+                cin.q[r] = __float22bfloat162_rn(mul2(__bfloat1622float2(cin.q[r]), make_float2(iq, iq)));
+                cin.k[r] = __float22bfloat162_rn(mul2(__bfloat1622float2(cin.k[r]), make_float2(ik, ik)));
+            }
+        }
         float2 qe[8], ke[8];
         {
             // token-contiguous images, two tokens per packed word: [channel][token pair]
@@ -371,7 +410,10 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         if (has_next) {
             ci_next = plan_chunk(plan, u_next / H);
             load_part<0>(q, k, v, z, H, u_next % H, ci_next.tok, ci_next.len, rg, cp, cin);
-            if (tid < 64) b_next = tid < ci_next.len ? beta[(size_t)(ci_next.tok + tid) * H + u_next % H] : 0.f;
+            if (tid < 64) {
+                b_next = tid < ci_next.len ? beta[(size_t)(ci_next.tok + tid) * H + u_next % H] : 0.f;
+                if (bsig && tid < ci_next.len) b_next = 1.f / (1.f + __expf(-b_next));
+            }
             a_next = A[u_next % H];
         }
         bool ok = mbar_wait(&mbar_p, (uint32_t)(it & 1));

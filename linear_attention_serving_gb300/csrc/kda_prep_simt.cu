@@ -79,10 +79,34 @@ prep_simt_kernel(const float *__restrict__ q, const float *__restrict__ k, const
         xv[r * LD + col] = ok ? to_f32(v[g]) : 0.f;
         xe[r * LD + col] = ok ? kda_gate(g_min, eA, z[g]) : 0.f;
     }
-    if (tid < C) sb[tid] = tid < len ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
+    if (tid < C) {
+        const float b = tid < len ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
+        sb[tid] = (plan.flags & KDA_FLAG_BETA_SIGMOID) && tid < len ? 1.f / (1.f + expf(-b)) : b;
+    }
     // zero INV (its strictly upper blocks stay zero)
     for (int idx = tid; idx < C * LDM; idx += PREP_THREADS) INV[idx] = 0.f;
     __syncthreads();
+    if (plan.flags & KDA_FLAG_QK_L2NORM) {
+        // input option: q and k rows divided by their L2 norm over the 128 channels
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int r = warp; r < C; r += PREP_THREADS / 32) {
+            float pq = 0.f, pk = 0.f;
+            for (int col = lane; col < D; col += 32) {
+                pq += xq[r * LD + col] * xq[r * LD + col];
+                pk += xk[r * LD + col] * xk[r * LD + col];
+            }
+            for (int m = 16; m > 0; m >>= 1) {
+                pq += __shfl_xor_sync(0xffffffffu, pq, m);
+                pk += __shfl_xor_sync(0xffffffffu, pk, m);
+            }
+            const float iq = 1.f / sqrtf(pq + L2NORM_EPS), ik = 1.f / sqrtf(pk + L2NORM_EPS);
+            for (int col = lane; col < D; col += 32) {
+                xq[r * LD + col] *= iq;
+                xk[r * LD + col] *= ik;
+            }
+        }
+        __syncthreads();
+    }
 
     // 2. per-channel cumulative log decay inside each 16-token tile, and the factors
     if (tid < D) {

@@ -6,12 +6,13 @@ namespace kda {
 
 namespace {
 
+template <bool OPTS>
 __global__ void __launch_bounds__(PT_THREADS, 1)
 prep_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z, const float *__restrict__ A,
                const float *__restrict__ beta, int H, float g_min, Plan plan, char *__restrict__ records) {
     extern __shared__ uint8_t smraw[];
-    prep_blocks(q, k, v, z, A, beta, H, g_min, plan, records, smraw, blockIdx.x, gridDim.x, nullptr);
+    prep_blocks<OPTS>(q, k, v, z, A, beta, H, g_min, plan, records, smraw, blockIdx.x, gridDim.x, nullptr);
 }
 
 }  // namespace
@@ -21,13 +22,12 @@ int launch_prep_tc(const void *q, const void *k, const void *v, const float *z, 
                    cudaStream_t s) {
     const long long units = (long long)p.max_chunks * H;
     if (units == 0) return KDA_OK;
-    if (cudaFuncSetAttribute(prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PREP_TC_SMEM) !=
-        cudaSuccess)
+    auto kern = p.flags ? prep_tc_kernel<true> : prep_tc_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PREP_TC_SMEM) != cudaSuccess)
         return KDA_ERR_CUDA;
     const int grid = (int)(units < n_sm ? units : n_sm);
-    prep_tc_kernel<<<grid, PT_THREADS, PREP_TC_SMEM, s>>>((const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
-                                                          (const __nv_bfloat16 *)v, z, A, beta, H, g_min, p,
-                                                          (char *)records);
+    kern<<<grid, PT_THREADS, PREP_TC_SMEM, s>>>((const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k,
+                                                (const __nv_bfloat16 *)v, z, A, beta, H, g_min, p, (char *)records);
     note_launch("prep_tc", s);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

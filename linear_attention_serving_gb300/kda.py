@@ -53,11 +53,11 @@ def load(build_if_missing: bool = True):
     lib.kda_segment_scan_workspace_size.restype = S
     lib.kda_chunk_fwd_plan_segments.argtypes = [L, I, I, I, I]
     lib.kda_chunk_fwd_plan_segments.restype = I
-    lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, P, P, P, S, P]
+    lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, P, P, P, S, I, P]
     lib.kda_chunk_fwd.restype = I
-    lib.kda_segment_scan.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, I, P, P, P, P, P, S, P]
+    lib.kda_segment_scan.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, I, P, P, P, P, P, S, I, P]
     lib.kda_segment_scan.restype = I
-    lib.kda_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, P]
+    lib.kda_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, I, P]
     lib.kda_decode_step.restype = I
     lib.kda_read_device_error.argtypes = [P, P, P]
     lib.kda_read_device_error.restype = I
@@ -119,8 +119,17 @@ def _n_seqs(cu_seqlens, n_seqs):
     return n_seqs
 
 
+KDA_FLAG_QK_L2NORM = 1
+KDA_FLAG_BETA_SIGMOID = 2
+
+
+def _flags(qk_l2norm: bool, beta_sigmoid: bool) -> int:
+    return (KDA_FLAG_QK_L2NORM if qk_l2norm else 0) | (KDA_FLAG_BETA_SIGMOID if beta_sigmoid else 0)
+
+
 def chunk_fwd(q, k, v, z, A, beta, cu_seqlens=None, init_state=None, g_min=G_MIN,
-              output_final_state=True, n_seqs=1, workspace=None, out=None):
+              output_final_state=True, n_seqs=1, workspace=None, out=None, qk_l2norm=False,
+              beta_sigmoid=False):
     """kda_chunk_fwd: chunkwise prefill.  q, k, v, z [T, H, 128]; A [H]; beta [T, H];
     cu_seqlens int32 [n+1] (device) or None (n_seqs equal-length sequences).
     Returns (o [T, H, 128] in q's dtype, final_state [n, H, 128, 128] fp32 or None)."""
@@ -136,13 +145,14 @@ def chunk_fwd(q, k, v, z, A, beta, cu_seqlens=None, init_state=None, g_min=G_MIN
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     rc = lib.kda_chunk_fwd(_p(q), _p(k), _p(v), _p(z), _p(A), _p(beta), _p(cu_seqlens), n, T, H, Dm,
                            dt, float(g_min), _p(init_state), _p(o), _p(fin), _p(workspace),
-                           workspace.numel(), _stream(q.device))
+                           workspace.numel(), _flags(qk_l2norm, beta_sigmoid), _stream(q.device))
     _check(rc, "kda_chunk_fwd")
     return o, fin
 
 
 def segment_scan(q, k, v, z, A, beta, n_segments, cu_seqlens=None, init_state=None, g_min=G_MIN,
-                 output_final_state=True, return_pairs=False, n_seqs=1, workspace=None):
+                 output_final_state=True, return_pairs=False, n_seqs=1, workspace=None, qk_l2norm=False,
+                 beta_sigmoid=False):
     """kda_segment_scan: intra-device segment-parallel prefill.
     Returns (o, final_state) or (o, final_state, pairs_M, pairs_S) with pairs [H, n_seg, 128, 128]."""
     lib = load()
@@ -161,7 +171,8 @@ def segment_scan(q, k, v, z, A, beta, n_segments, cu_seqlens=None, init_state=No
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     rc = lib.kda_segment_scan(_p(q), _p(k), _p(v), _p(z), _p(A), _p(beta), _p(cu_seqlens), n, T, H, Dm,
                               dt, float(g_min), _p(init_state), int(n_segments), _p(pm), _p(ps),
-                              _p(o), _p(fin), _p(workspace), workspace.numel(), _stream(q.device))
+                              _p(o), _p(fin), _p(workspace), workspace.numel(), _flags(qk_l2norm, beta_sigmoid),
+                              _stream(q.device))
     _check(rc, "kda_segment_scan")
     if return_pairs:
         return o, fin, pm, ps
@@ -169,7 +180,7 @@ def segment_scan(q, k, v, z, A, beta, n_segments, cu_seqlens=None, init_state=No
 
 
 def decode_step(state, q, k, v, z, beta, A, cache, num_accepted=None, g_min=G_MIN,
-                error_word=None, out=None):
+                error_word=None, out=None, qk_l2norm=False, beta_sigmoid=False):
     """kda_decode_step: in-place state update with MTP replay.
     state [N, H, 128, 128] fp32 (updated in place); q, k, v, z [N, W, H, 128]; beta [N, W, H];
     cache = (cache_q, cache_k, cache_v, cache_z, cache_beta) with W-1 slots (updated in place);
@@ -183,7 +194,8 @@ def decode_step(state, q, k, v, z, beta, A, cache, num_accepted=None, g_min=G_MI
     o = out if out is not None else torch.empty_like(q)
     rc = lib.kda_decode_step(_p(state), _p(q), _p(k), _p(v), _p(z), _p(beta), _p(A), _p(cq), _p(ck),
                              _p(cv), _p(cz), _p(cb), _p(num_accepted), N, H, Dm, W, _dtype_code(q),
-                             float(g_min), _p(o), _p(error_word), _stream(q.device))
+                             float(g_min), _p(o), _p(error_word), _flags(qk_l2norm, beta_sigmoid),
+                             _stream(q.device))
     _check(rc, "kda_decode_step")
     return o
 

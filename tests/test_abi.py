@@ -76,11 +76,11 @@ FAKE = ctypes.c_void_p(1 << 20)  # aligned dummy address; never dereferenced on 
 
 def _chunk(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, z=FAKE, A=FAKE, beta=FAKE, cu=None, n=1, T=128, H=2, D=128, dt=0,
-             g_min=-5.0, init=None, o=FAKE, fin=None, ws=None, wsb=0, s=None)
+             g_min=-5.0, init=None, o=FAKE, fin=None, ws=None, wsb=0, flags=0, s=None)
     a.update(kw)
     return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["z"], a["A"], a["beta"], a["cu"], a["n"], a["T"],
                              a["H"], a["D"], a["dt"], a["g_min"], a["init"], a["o"], a["fin"], a["ws"],
-                             a["wsb"], a["s"])
+                             a["wsb"], a["flags"], a["s"])
 
 
 def test_chunk_fwd_rejects_bad_arguments_before_launch():
@@ -96,25 +96,28 @@ def test_chunk_fwd_rejects_bad_arguments_before_launch():
     assert _chunk(lib, n=3, T=128) == 1                             # T not divisible without cu_seqlens
     assert _chunk(lib, ws=None) == 5                                # no workspace
     assert _chunk(lib, ws=ctypes.c_void_p(1 << 20), wsb=16) == 5    # too small
+    assert _chunk(lib, flags=4) == 1                                # unknown input option
 
 
 def test_segment_scan_and_decode_reject_bad_arguments():
     lib = kda.load()
     r = lib.kda_segment_scan(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 128, 2, 128, 0, -5.0, None, 0,
-                             None, None, FAKE, None, None, 0, None)
+                             None, None, FAKE, None, None, 0, 0, None)
     assert r == 1  # zero segments
     r = lib.kda_segment_scan(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 128, 2, 96, 0, -5.0, None, 4,
-                             None, None, FAKE, None, None, 0, None)
+                             None, None, FAKE, None, None, 0, 0, None)
     assert r == 2
     dec = lambda **kw: lib.kda_decode_step(
         kw.get("state", FAKE), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, kw.get("cq", FAKE), FAKE, FAKE, FAKE,
-        FAKE, None, kw.get("N", 4), 2, kw.get("D", 128), kw.get("W", 5), 1, -5.0, FAKE, None, None)
+        FAKE, None, kw.get("N", 4), 2, kw.get("D", 128), kw.get("W", 5), 1, -5.0, FAKE, None,
+        kw.get("flags", 0), None)
     assert dec(D=64) == 2
     assert dec(W=9) == 1
     assert dec(W=0) == 1
     assert dec(N=0) == 1
     assert dec(state=None) == 1
     assert dec(cq=None) == 1
+    assert dec(flags=8) == 1
 
 
 def test_binding_rejects_wrong_dtypes_on_cpu_tensors():

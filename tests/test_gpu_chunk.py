@@ -143,3 +143,32 @@ def test_planner_segmented_path(T, H, n_seqs):
     assert kda.chunk_fwd_plan_segments(T, H, n_seqs) >= 2
     inp = kda_synth.prefill_inputs(T, H, "bf16", seed=900 + T, z_std=1.0, init_std=0.05, n_init=n_seqs)
     check(*run_both(inp, n_seqs=n_seqs), "bf16")
+
+
+def raw_inputs(T, H, dtype, seed, n_seqs=1):
+    """Prefill inputs with unnormalised q, k (each row scaled by 0.5 .. 3) and beta logits."""
+    inp = kda_synth.prefill_inputs(T, H, dtype, seed=seed, z_std=1.0, init_std=0.05, n_init=n_seqs)
+    g = torch.Generator().manual_seed(seed)
+    t = inp["q"].dtype
+    inp["q"] = (inp["q"].float() * (0.5 + 2.5 * torch.rand((T, H, 1), generator=g))).to(t)
+    inp["k"] = (inp["k"].float() * (0.5 + 2.5 * torch.rand((T, H, 1), generator=g))).to(t)
+    inp["beta"] = torch.randn((T, H), generator=g)
+    return inp
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T,H,flags", [(333, 3, (True, True)), (333, 3, (True, False)), (333, 3, (False, True)),
+                                       (2048, 24, (True, True)), (8192, 1, (True, True))])
+def test_input_options(dtype, T, H, flags):
+    """KDA_FLAG_QK_L2NORM / KDA_FLAG_BETA_SIGMOID against the oracle on the
+    prepared inputs; the shapes take the fused launch (H=3), the three-kernel
+    path (H=24: 48 chains) and, in bf16, the automatic segments (H=1, T=8192)."""
+    l2, sig = flags
+    inp = raw_inputs(T, H, dtype, seed=300 + T + H)
+    d = to_dev(inp, DEV)
+    o, fin = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], init_state=d["init_state"],
+                           qk_l2norm=l2, beta_sigmoid=sig)
+    torch.cuda.synchronize()
+    qn, kn, bn = oracle.input_prep(inp["q"], inp["k"], inp["beta"], qk_l2norm=l2, beta_sigmoid=sig)
+    o_ref, f_ref = oracle.recurrent(qn, kn, inp["v"], inp["z"], inp["A"], bn, init_state=inp["init_state"])
+    check(o, fin, o_ref, f_ref, dtype)

@@ -76,3 +76,40 @@ def test_num_accepted_out_of_range_sets_error_and_skips():
     assert int(err.item()) & 2
     assert torch.equal(state[1], before[1]) and torch.equal(state[2], before[2])
     assert not torch.equal(state[0], before[0])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_input_options(dtype):
+    """KDA_FLAG_QK_L2NORM | KDA_FLAG_BETA_SIGMOID: unnormalised q, k and beta
+    logits in; the oracle runs on the prepared inputs (its input_prep), and the
+    cache keeps the drafts' inputs as given."""
+    N, H, W, seed = 6, 3, 5, 61
+    g = torch.Generator().manual_seed(seed)
+    state = kda_synth.decode_state(N, H, seed, std=0.05, device=DEV)
+    A = kda_synth.decode_A(H, seed, A_std=0.5, device=DEV)
+    cache = empty_cache(N, W, H, dtype)
+    ref_state = state.cpu()
+    raw_cache = tuple(c.cpu() for c in cache)
+    tol_o, tol_s = (1e-4, 1e-4) if dtype == "f32" else TOL["bf16"]
+    t = kda_synth.TORCH_DTYPE[dtype]
+    for step in range(3):
+        w = kda_synth.decode_window(N, W, H, step, seed, dtype, z_std=1.5)
+        qr = (w["q"].float() * (0.5 + 2.5 * torch.rand((N, W, H, 1), generator=g))).to(t)
+        kr = (w["k"].float() * (0.5 + 2.5 * torch.rand((N, W, H, 1), generator=g))).to(t)
+        br = torch.randn((N, W, H), generator=g)
+        nacc = None if step == 0 else w["num_accepted"]
+        dev = lambda x: x.to(DEV)
+        o = kda.decode_step(state, dev(qr), dev(kr), dev(w["v"]), dev(w["z"]), dev(br), A, cache,
+                            num_accepted=None if nacc is None else dev(nacc), qk_l2norm=True, beta_sigmoid=True)
+        torch.cuda.synchronize()
+        qn, kn, bn = oracle.input_prep(qr, kr, br, qk_l2norm=True, beta_sigmoid=True)
+        cqn, ckn, cbn = oracle.input_prep(raw_cache[0], raw_cache[1], raw_cache[4], qk_l2norm=True, beta_sigmoid=True)
+        o_ref, ref_state, _ = oracle.decode_step(ref_state, qn, kn, w["v"], w["z"], bn, A.cpu(), cqn, ckn,
+                                                 raw_cache[2], raw_cache[3], cbn, num_accepted=nacc)
+        assert rel_fro(o.cpu(), o_ref) <= tol_o, f"step {step}: o"
+        assert rel_fro(state.cpu(), ref_state) <= tol_s, f"step {step}: state"
+        # the new drafts' inputs, as given, become the cache
+        raw_cache = (qr[:, 1:].contiguous(), kr[:, 1:].contiguous(), w["v"][:, 1:].contiguous(),
+                     w["z"][:, 1:].contiguous(), br[:, 1:].contiguous())
+        for c, rc in zip(cache, raw_cache):
+            assert torch.equal(c.cpu(), rc.to(c.dtype)), f"step {step}: cache"

@@ -126,3 +126,23 @@ def test_segscan_1m_h8_full_size():
     # the last segment's exit state is the final state
     a, b = rng[-1]
     assert rel_fro(fin[0, 7], torch.from_numpy(S_next)) <= TOL["bf16"][1]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_segment_scan_input_options(dtype):
+    """The input options through kda_segment_scan (both phases prepare from the
+    same records): unnormalised q, k and beta logits in, oracle on the prepared inputs."""
+    inp = kda_synth.prefill_inputs(1500, 2, dtype, seed=77, z_std=1.5, A_std=0.5, init_std=0.05)
+    g = torch.Generator().manual_seed(77)
+    t = inp["q"].dtype
+    inp["q"] = (inp["q"].float() * (0.5 + 2.5 * torch.rand((1500, 2, 1), generator=g))).to(t)
+    inp["k"] = (inp["k"].float() * (0.5 + 2.5 * torch.rand((1500, 2, 1), generator=g))).to(t)
+    inp["beta"] = torch.randn((1500, 2), generator=g)
+    d = to_dev(inp, DEV)
+    o, fin = kda.segment_scan(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], 5,
+                              init_state=d["init_state"], qk_l2norm=True, beta_sigmoid=True)
+    torch.cuda.synchronize()
+    qn, kn, bn = oracle.input_prep(inp["q"], inp["k"], inp["beta"], qk_l2norm=True, beta_sigmoid=True)
+    o_ref, f_ref = oracle.recurrent(qn, kn, inp["v"], inp["z"], inp["A"], bn, init_state=inp["init_state"])
+    to, tf = TOL[dtype]
+    assert rel_fro(o, o_ref) <= to and rel_fro(fin, f_ref) <= tf

@@ -25,7 +25,7 @@ KDA_ERR_WORKSPACE = 5
 def noalloc_fn():
     lib = kda.load()
     fn = lib.kda_chunk_fwd_noalloc
-    fn.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, P, P, P]
+    fn.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, P, P, I, P]
     fn.restype = I
     return fn
 
@@ -42,7 +42,7 @@ def call_noalloc(fn, d, n_seqs):
     fin = torch.empty((n_seqs, H, Dm, Dm), device=q.device, dtype=torch.float32)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     rc = fn(_p(q), _p(d["k"]), _p(d["v"]), _p(d["z"]), _p(d["A"]), _p(d["beta"]), _p(d["cu_seqlens"]),
-            n_seqs, T, H, Dm, dt, -5.0, _p(d["init_state"]), _p(o), _p(fin), stream)
+            n_seqs, T, H, Dm, dt, -5.0, _p(d["init_state"]), _p(o), _p(fin), 0, stream)
     return rc, o, fin
 
 
@@ -51,7 +51,7 @@ def test_noalloc_rejects_calls_larger_than_its_array():
     # 8192 tokens x 16 heads needs ~170 MB of workspace, beyond the fixed array;
     # rejected on the host before anything is launched (no GPU touched)
     fake = ctypes.c_void_p(1 << 20)
-    rc = fn(fake, fake, fake, fake, fake, fake, None, 1, 8192, 16, 128, 0, -5.0, None, fake, None, None)
+    rc = fn(fake, fake, fake, fake, fake, fake, None, 1, 8192, 16, 128, 0, -5.0, None, fake, None, 0, None)
     assert rc == KDA_ERR_WORKSPACE
 
 
