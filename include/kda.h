@@ -120,6 +120,37 @@ int kda_version(void);
 size_t kda_chunk_fwd_workspace_size(int64_t T_total, int H, int n_seqs, int dtype);
 
 /* --------------------------------------------------------------------------
+ * kda_chunk_fwd_ckpt -- kda_chunk_fwd that also writes the state at
+ * interval-aligned positions of every document ("Kimi K3 模型结构（7）",
+ * section "混合架构的前缀缓存": a cached prefix is usable only where the KDA
+ * state was persisted, so after each forward the kernel saves the state at
+ * the last hash-aligned position, into a fresh slot).
+ * Same arguments, checks and results as kda_chunk_fwd, plus
+ *   ckpt_interval  tokens between checkpoints: a positive multiple of 64 (C)
+ *   ckpt_slot      (device) int32 [n_seqs, ckpt_per_seq]: ckpt_slot[n][j] is
+ *                  the page that receives the state of document n after its
+ *                  first (j + 1) * ckpt_interval tokens; -1 (or any value
+ *                  outside 0 .. n_slots - 1) skips it.  Positions past a
+ *                  document's end are never written, so a caller that wants
+ *                  only the last aligned state of each document marks only
+ *                  that entry.
+ *   ckpt_per_seq   columns of ckpt_slot (>= 1)
+ *   ckpt           (device) fp32 [n_slots, H, D, D], 16-byte aligned: pages
+ *   n_slots        pages in ckpt (>= 1)
+ * Invalid checkpoint arguments return KDA_ERR_INVALID_ARG before any launch.
+ * A call with checkpoints takes the three-kernel bf16 path (or the segmented
+ * one kda_chunk_fwd_plan_segments picks), not the single fused launch.
+ * ------------------------------------------------------------------------ */
+int kda_chunk_fwd_ckpt(const void *q, const void *k, const void *v,
+                       const float *z, const float *A, const float *beta,
+                       const int32_t *cu_seqlens, int n_seqs,
+                       int64_t T_total, int H, int D, int dtype, float g_min,
+                       const float *init_state, void *o, float *final_state,
+                       int ckpt_interval, const int32_t *ckpt_slot, int ckpt_per_seq,
+                       float *ckpt, int n_slots,
+                       void *workspace, size_t workspace_bytes, int flags, kda_stream_t stream);
+
+/* --------------------------------------------------------------------------
  * kda_chunk_fwd_plan_segments -- the segment count kda_chunk_fwd picks by
  * itself ("Kimi K3 模型结构（7）", section "KDA：三种执行形态" (SM-level CP):
  * when a few (document, head) chains over long documents would leave the

@@ -5,8 +5,8 @@ Three calls, each a hand-written CUDA kernel path behind the C ABI in
 (intra-device segment-parallel prefill) and ``decode_step`` (in-place decode
 with MTP draft replay).
 """
-from .kda import (KDAError, chunk_fwd, chunk_fwd_plan_segments, chunk_fwd_workspace_size, decode_step, load,
+from .kda import (KDAError, chunk_fwd, chunk_fwd_ckpt, chunk_fwd_plan_segments, chunk_fwd_workspace_size, decode_step, load,
                   library_path, read_device_error, segment_scan, segment_scan_workspace_size)
 
-__all__ = ["KDAError", "chunk_fwd", "chunk_fwd_plan_segments", "chunk_fwd_workspace_size", "decode_step", "load",
+__all__ = ["KDAError", "chunk_fwd", "chunk_fwd_ckpt", "chunk_fwd_plan_segments", "chunk_fwd_workspace_size", "decode_step", "load",
            "library_path", "read_device_error", "segment_scan", "segment_scan_workspace_size"]

@@ -60,6 +60,7 @@ int launch_fused_tc(const void *q, const void *k, const void *v, const float *z,
     const long long n_chain = (long long)sa.n_units * H * FUSED_SLICES;
     // the chains may take at most a quarter of the SMs, and there must be units to prepare
     if (sa.mode != SCAN_DOCS || n_chain < 1 || n_chain > n_sm / 4 || (long long)p.max_chunks * H < 1) return KDA_OK;
+    if (sa.ckpt) return KDA_OK;  // state checkpoints: the three-kernel path writes them
     int dev = 0, coop = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop)

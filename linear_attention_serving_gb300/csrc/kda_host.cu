@@ -149,7 +149,7 @@ int run_segment_scan(const void *q, const void *k, const void *v, const float *z
                      const float *beta, const int32_t *cu_seqlens, int n_seqs, int64_t T_total, int H,
                      int dtype, float g_min, const float *init_state, int n_segments, float *pairs_M,
                      float *pairs_S, void *o, float *final_state, void *workspace, const Workspace &w,
-                     int flags, cudaStream_t s) {
+                     int flags, cudaStream_t s, const ScanArgs *ckpt = nullptr) {
     int rc;
     Plan p;
     if ((rc = make_plan(cu_seqlens, n_seqs, T_total, workspace, w, s, p, flags))) return rc;
@@ -181,6 +181,13 @@ int run_segment_scan(const void *q, const void *k, const void *v, const float *z
     a.phase = 3;
     a.o = o;
     a.final_state = final_state;
+    if (ckpt) {
+        a.ckpt = ckpt->ckpt;
+        a.ckpt_slot = ckpt->ckpt_slot;
+        a.ckpt_per_seq = ckpt->ckpt_per_seq;
+        a.ckpt_n_slots = ckpt->ckpt_n_slots;
+        a.ckpt_ic = ckpt->ckpt_ic;
+    }
     if ((rc = launch_scan(a, dtype, s))) return rc;
     if ((rc = launch_empty_docs(p, H, init_state, final_state, s))) return rc;
     const size_t mat = sizeof(float) * (size_t)H * n_segments * D * D;
@@ -261,11 +268,16 @@ size_t kda_segment_scan_workspace_size(int64_t T_total, int H, int n_seqs, int n
     return workspace_layout(T_total, H, n_seqs, n_segments, dtype).total;
 }
 
-int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *z, const float *A,
-                  const float *beta, const int32_t *cu_seqlens, int n_seqs, int64_t T_total, int H,
-                  int Dm, int dtype, float g_min, const float *init_state, void *o,
-                  float *final_state, void *workspace, size_t workspace_bytes, int flags,
-                  kda_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// kda_chunk_fwd with an optional checkpoint description (ckpt fields of a ScanArgs).
+int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *z, const float *A,
+                   const float *beta, const int32_t *cu_seqlens, int n_seqs, int64_t T_total, int H,
+                   int Dm, int dtype, float g_min, const float *init_state, void *o,
+                   float *final_state, void *workspace, size_t workspace_bytes, int flags,
+                   kda_stream_t stream, const ScanArgs *ckpt) {
     int rc = check_prefill(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, Dm, dtype, g_min, o, flags);
     if (rc) return rc;
     const int n_seg = plan_segments(T_total, H, n_seqs, cu_seqlens != nullptr, dtype, device_sm_count());
@@ -275,7 +287,7 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *z, c
     note_begin(s);
     if (n_seg > 0)
         return run_segment_scan(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, dtype, g_min, init_state,
-                                n_seg, nullptr, nullptr, o, final_state, workspace, w, flags, s);
+                                n_seg, nullptr, nullptr, o, final_state, workspace, w, flags, s, ckpt);
     Plan p;
     // bf16: the header and the fused launch's ready flags, in one memset
     const size_t zero = dtype == KDA_BF16 ? w.off_ready + sizeof(int) * (size_t)w.max_chunks * H : 8;
@@ -293,6 +305,13 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *z, c
     a.init_state = init_state;
     a.o = o;
     a.final_state = final_state;
+    if (ckpt) {
+        a.ckpt = ckpt->ckpt;
+        a.ckpt_slot = ckpt->ckpt_slot;
+        a.ckpt_per_seq = ckpt->ckpt_per_seq;
+        a.ckpt_n_slots = ckpt->ckpt_n_slots;
+        a.ckpt_ic = ckpt->ckpt_ic;
+    }
     if (dtype == KDA_BF16) {
         // few (document, head) chains: prep, chains and outputs in one launch
         bool used = false;
@@ -303,6 +322,39 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *z, c
     }
     if ((rc = launch_prep(q, k, v, z, A, beta, H, dtype, g_min, p, records, s))) return rc;
     return launch_scan(a, dtype, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_chunk_fwd(const void *q, const void *k, const void *v, const float *z, const float *A,
+                  const float *beta, const int32_t *cu_seqlens, int n_seqs, int64_t T_total, int H,
+                  int Dm, int dtype, float g_min, const float *init_state, void *o,
+                  float *final_state, void *workspace, size_t workspace_bytes, int flags,
+                  kda_stream_t stream) {
+    return chunk_fwd_impl(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, Dm, dtype, g_min, init_state, o,
+                          final_state, workspace, workspace_bytes, flags, stream, nullptr);
+}
+
+int kda_chunk_fwd_ckpt(const void *q, const void *k, const void *v, const float *z, const float *A,
+                       const float *beta, const int32_t *cu_seqlens, int n_seqs, int64_t T_total, int H,
+                       int Dm, int dtype, float g_min, const float *init_state, void *o,
+                       float *final_state, int ckpt_interval, const int32_t *ckpt_slot, int ckpt_per_seq,
+                       float *ckpt, int n_slots, void *workspace, size_t workspace_bytes, int flags,
+                       kda_stream_t stream) {
+    if (ckpt_interval < C || ckpt_interval % C != 0 || ckpt_per_seq < 1 || n_slots < 1 || !ckpt_slot || !ckpt ||
+        !aligned16(ckpt))
+        return KDA_ERR_INVALID_ARG;
+    ScanArgs c;
+    memset(&c, 0, sizeof(c));
+    c.ckpt = ckpt;
+    c.ckpt_slot = ckpt_slot;
+    c.ckpt_per_seq = ckpt_per_seq;
+    c.ckpt_n_slots = n_slots;
+    c.ckpt_ic = ckpt_interval / C;
+    return chunk_fwd_impl(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, Dm, dtype, g_min, init_state, o,
+                          final_state, workspace, workspace_bytes, flags, stream, &c);
 }
 
 int kda_segment_scan(const void *q, const void *k, const void *v, const float *z, const float *A,

@@ -238,7 +238,30 @@ struct ScanArgs {
     float *pairs;              // [2][H][n_seg][D][D] (phase 1)
     void *o;                   // [T, H, D] dtype (null: no output)
     float *final_state;        // [n_seqs, H, D, D] or null
+    // state checkpoints (null ckpt: none): the state after every ckpt_ic chunks
+    // of a document goes to ckpt[slot], slot = ckpt_slot[doc * ckpt_per_seq + j]
+    float *ckpt;               // [n_slots, H, D, D]
+    const int32_t *ckpt_slot;  // [n_seqs, ckpt_per_seq], -1 = skip
+    int ckpt_per_seq;
+    int ckpt_n_slots;          // slots outside 0 .. n_slots - 1 are skipped
+    int ckpt_ic;               // checkpoint interval in chunks
 };
+
+// Index j of the checkpoint chunk c completes (the state after (j + 1) x
+// interval tokens of its document), or -1.  Only a full chunk ends on an
+// interval boundary: chunks are cut from each document's start.
+__device__ __forceinline__ int ckpt_index(const Plan &p, int c, const ChunkInfo &ci, int ic) {
+    if (ci.len != C) return -1;
+    const int first = p.uniform ? ci.doc * p.chunks_per_seq : p.doc_off[ci.doc];
+    const int k = c - first + 1;  // chunks of the document up to and including c
+    return k % ic == 0 ? k / ic - 1 : -1;
+}
+__device__ __forceinline__ float *ckpt_row(const ScanArgs &a, const ChunkInfo &ci, int c, int h, int row) {
+    const int j = ckpt_index(a.plan, c, ci, a.ckpt_ic);
+    if (j < 0 || j >= a.ckpt_per_seq) return nullptr;
+    const int slot = a.ckpt_slot[(size_t)ci.doc * a.ckpt_per_seq + j];
+    return (slot < 0 || slot >= a.ckpt_n_slots) ? nullptr : a.ckpt + (((size_t)slot * a.H + h) * D + row) * D;
+}
 constexpr int SCAN_DOCS = 0;
 constexpr int SCAN_SEGMENTS = 1;
 

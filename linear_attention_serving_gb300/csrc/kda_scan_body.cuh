@@ -376,6 +376,9 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
         __syncwarp();
         if (lane == 0) mbar_arrive(&sop_bar);
         const bool write_final = value_cols && a.final_state && a.phase != 1;
+        // checkpoints: not in output blocks (the fused launch leaves calls with
+        // checkpoints to the three-kernel path)
+        const bool write_ckpt = !EMIT_O && value_cols && a.ckpt && a.phase != 1;
         bool ok = true;
         int stage = 0;
         uint32_t ph = 0;
@@ -424,6 +427,17 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 float *f = a.final_state + (((size_t)doc * a.H + h) * D + t) * D + pc;
 #pragma unroll
                 for (int j = 0; j < NT; j += 4) *reinterpret_cast<float4 *>(f + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
+            }
+            if (!EMIT_O && write_ckpt) {
+                // the state after this chunk, when it ends on a checkpoint position
+                const ChunkInfo cik = plan_chunk(p, c0 + i);
+                float *f = ckpt_row(a, cik, c0 + i, h, t);
+                if (f) {
+                    f += pc;
+#pragma unroll
+                    for (int j = 0; j < NT; j += 4)
+                        *reinterpret_cast<float4 *>(f + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
+                }
             }
             if (next_first) {
                 // a document starts at the next chunk: the state restarts there

@@ -157,6 +157,14 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_simt_kernel(ScanArgs a) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) f[j] = nacc[j];
         }
+        if (value_cols && a.ckpt && a.phase != 1) {
+            // the state after this chunk, when it ends on a checkpoint position
+            float *f = ckpt_row(a, ci, c, h, row);
+            if (f) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) f[col0 + cc + j] = nacc[j];
+            }
+        }
     }
 
     if (a.mode == SCAN_SEGMENTS && a.phase == 1) {

@@ -55,6 +55,8 @@ def load(build_if_missing: bool = True):
     lib.kda_chunk_fwd_plan_segments.restype = I
     lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, P, P, P, S, I, P]
     lib.kda_chunk_fwd.restype = I
+    lib.kda_chunk_fwd_ckpt.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, P, P, I, P, I, P, I, P, S, I, P]
+    lib.kda_chunk_fwd_ckpt.restype = I
     lib.kda_segment_scan.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, I, P, P, P, P, P, S, I, P]
     lib.kda_segment_scan.restype = I
     lib.kda_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, I, P]
@@ -147,6 +149,35 @@ def chunk_fwd(q, k, v, z, A, beta, cu_seqlens=None, init_state=None, g_min=G_MIN
                            dt, float(g_min), _p(init_state), _p(o), _p(fin), _p(workspace),
                            workspace.numel(), _flags(qk_l2norm, beta_sigmoid), _stream(q.device))
     _check(rc, "kda_chunk_fwd")
+    return o, fin
+
+
+def chunk_fwd_ckpt(q, k, v, z, A, beta, ckpt_interval, ckpt_slot, ckpt, cu_seqlens=None, init_state=None,
+                   g_min=G_MIN, output_final_state=True, n_seqs=1, workspace=None, out=None, qk_l2norm=False,
+                   beta_sigmoid=False):
+    """kda_chunk_fwd_ckpt: chunk_fwd that also writes document states at
+    ckpt_interval-aligned positions.  ckpt_slot int32 [n, per_seq] (device) maps
+    (document, j) -> page of ckpt [n_slots, H, 128, 128] fp32 (device) for the
+    state after (j + 1) * ckpt_interval tokens; -1 skips."""
+    lib = load()
+    _contig(q, k, v, z, A, beta, cu_seqlens, init_state, ckpt_slot, ckpt)
+    T, H, Dm = q.shape
+    n = _n_seqs(cu_seqlens, n_seqs)
+    dt = _dtype_code(q)
+    if ckpt_slot.dtype != torch.int32 or ckpt_slot.dim() != 2 or ckpt_slot.shape[0] != n:
+        raise KDAError("ckpt_slot must be int32 [n_seqs, per_seq]")
+    if ckpt.dtype != torch.float32 or ckpt.dim() != 4 or tuple(ckpt.shape[1:]) != (H, Dm, Dm):
+        raise KDAError("ckpt must be fp32 [n_slots, H, 128, 128]")
+    o = out if out is not None else torch.empty_like(q)
+    fin = torch.empty((n, H, Dm, Dm), device=q.device, dtype=torch.float32) if output_final_state else None
+    need = lib.kda_chunk_fwd_workspace_size(T, H, n, dt)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    rc = lib.kda_chunk_fwd_ckpt(_p(q), _p(k), _p(v), _p(z), _p(A), _p(beta), _p(cu_seqlens), n, T, H, Dm,
+                                dt, float(g_min), _p(init_state), _p(o), _p(fin), int(ckpt_interval), _p(ckpt_slot),
+                                ckpt_slot.shape[1], _p(ckpt), ckpt.shape[0], _p(workspace), workspace.numel(),
+                                _flags(qk_l2norm, beta_sigmoid), _stream(q.device))
+    _check(rc, "kda_chunk_fwd_ckpt")
     return o, fin
 
 

@@ -125,3 +125,21 @@ def test_binding_rejects_wrong_dtypes_on_cpu_tensors():
     q = torch.zeros(4, 1, 128, dtype=torch.float16)
     with pytest.raises(kda.KDAError):
         kb._dtype_code(q)
+
+
+def test_chunk_fwd_ckpt_rejects_bad_checkpoint_arguments():
+    lib = kda.load()
+    f = lib.kda_chunk_fwd_ckpt
+
+    def call(interval=256, slot=FAKE, per_seq=4, ck=FAKE, n_slots=2):
+        return f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 128, 2, 128, 0, -5.0, None, FAKE, None,
+                 interval, slot, per_seq, ck, n_slots, None, 0, 0, None)
+
+    assert call(interval=0) == 1
+    assert call(interval=100) == 1        # not a multiple of the 64-token chunk
+    assert call(per_seq=0) == 1
+    assert call(n_slots=0) == 1
+    assert call(slot=None) == 1
+    assert call(ck=None) == 1
+    assert call(ck=ctypes.c_void_p((1 << 20) + 4)) == 1  # misaligned pages
+    assert call() == 5                    # valid checkpoints, but no workspace

@@ -172,3 +172,66 @@ def test_input_options(dtype, T, H, flags):
     qn, kn, bn = oracle.input_prep(inp["q"], inp["k"], inp["beta"], qk_l2norm=l2, beta_sigmoid=sig)
     o_ref, f_ref = oracle.recurrent(qn, kn, inp["v"], inp["z"], inp["A"], bn, init_state=inp["init_state"])
     check(o, fin, o_ref, f_ref, dtype)
+
+
+
+def ckpt_reference(inp, cu, positions):
+    """State of each document after its first p tokens: the oracle's final state
+    on that prefix (the checkpoints' plain definition)."""
+    out = {}
+    for n, ps in positions.items():
+        a = int(cu[n])
+        for p in ps:
+            sl = lambda x: x[a:a + p]
+            init = None if inp["init_state"] is None else inp["init_state"][n:n + 1]
+            _, f = oracle.recurrent(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["z"]), inp["A"],
+                                    sl(inp["beta"]), init_state=init)
+            out[(n, p)] = f[0]
+    return out
+
+
+@pytest.mark.parametrize("dtype,T,H,docs,interval", [
+    ("f32", 1000, 3, None, 256), ("bf16", 1000, 3, None, 256),
+    ("bf16", 1000, 2, [700, 300], 128), ("f32", 1000, 2, [700, 300], 128),
+    ("bf16", 8192, 1, None, 512)])
+def test_checkpoints(dtype, T, H, docs, interval):
+    """kda_chunk_fwd_ckpt: every marked (document, aligned position) page holds
+    the oracle's state after that prefix; skipped and out-of-document entries
+    leave their pages untouched; o and the final state are unchanged.  The
+    last case takes the automatic segments (the state comes from phase 3)."""
+    cu = torch.tensor([0] + list(np.cumsum(docs)), dtype=torch.int32) if docs else None
+    n = 1 if docs is None else len(docs)
+    inp = kda_synth.prefill_inputs(T, H, dtype, seed=500 + T + H, z_std=0.5, init_std=0.05,
+                                   cu_seqlens=cu, n_init=n)
+    lens = docs or [T]
+    per_seq = max(lens) // interval + 1  # includes one position past every document's end
+    slot = torch.full((n, per_seq), -1, dtype=torch.int32)
+    want, nxt = {}, 0
+    for d in range(n):
+        for j in range(per_seq):
+            if j % 3 == 1:
+                continue  # skipped on purpose
+            slot[d, j] = nxt
+            if (j + 1) * interval <= lens[d]:
+                want[(d, (j + 1) * interval)] = nxt
+            nxt += 1
+    ck = torch.full((nxt, H, 128, 128), float("nan"), device=DEV)
+    d_ = to_dev(inp, DEV)
+    o, fin = kda.chunk_fwd_ckpt(d_["q"], d_["k"], d_["v"], d_["z"], d_["A"], d_["beta"], interval, slot.to(DEV), ck,
+                                cu_seqlens=d_["cu_seqlens"], init_state=d_["init_state"], n_seqs=n)
+    torch.cuda.synchronize()
+    positions = {}
+    for (d, p) in want:
+        positions.setdefault(d, []).append(p)
+    ref = ckpt_reference(inp, [0] + list(np.cumsum(lens)), positions)
+    to, tf = TOL[dtype]
+    for key, s_idx in want.items():
+        e = rel_fro(ck[s_idx], ref[key])
+        assert e <= tf, f"checkpoint {key}: rel err {e:.3e}"
+    written = set(want.values())
+    for s_idx in range(nxt):
+        if s_idx not in written:
+            assert torch.isnan(ck[s_idx]).all(), f"page {s_idx} written"
+    o_ref, f_ref = oracle.recurrent(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"],
+                                    cu_seqlens=cu, init_state=inp["init_state"])
+    check(o, fin, o_ref, f_ref, dtype)
