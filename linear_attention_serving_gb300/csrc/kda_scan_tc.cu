@@ -6,20 +6,20 @@ namespace kda {
 
 namespace {
 
-template <int N, int STAGES, int TPR>
-__global__ void __launch_bounds__(ScanCfg<N, TPR>::THREADS, 1) scan_tc_kernel(ScanArgs a) {
+template <int N, int STAGES, int TPR, bool EMIT_O>
+__global__ void __launch_bounds__(ScanCfg<N, TPR, EMIT_O>::THREADS, 1) scan_tc_kernel(ScanArgs a) {
     extern __shared__ uint8_t smraw[];
-    scan_block<N, STAGES, TPR>(a, blockIdx.x, blockIdx.y, blockIdx.z * (N / 16), smraw, nullptr);
+    scan_block<N, STAGES, TPR, EMIT_O>(a, blockIdx.x, blockIdx.y, blockIdx.z * (N / 16), smraw, nullptr);
 }
 
-template <int N, int STAGES, int TPR>
+template <int N, int STAGES, int TPR, bool EMIT_O = false>
 int launch_n(const ScanArgs &a, cudaStream_t s) {
-    auto kern = scan_tc_kernel<N, STAGES, TPR>;
-    const size_t smem = scan_tc_smem_bytes<N, STAGES>();
+    auto kern = scan_tc_kernel<N, STAGES, TPR, EMIT_O>;
+    const size_t smem = scan_tc_smem_bytes<N, STAGES, EMIT_O>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return KDA_ERR_CUDA;
     dim3 grid(a.n_units, a.H, a.ncols / N);
-    kern<<<grid, ScanCfg<N, TPR>::THREADS, smem, s>>>(a);
+    kern<<<grid, ScanCfg<N, TPR, EMIT_O>::THREADS, smem, s>>>(a);
     note_launch("scan_tc", s);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -31,11 +31,17 @@ int launch_scan_tc(const ScanArgs &a, int n_sm, cudaStream_t s) {
     // Few independent column slices: narrow blocks spread the chains over more
     // SMs.  Many: wider blocks amortise the per-chunk latency.
     const long long slices16 = (long long)a.n_units * a.H * (a.ncols / 16);
-    int rc = slices16 <= 2LL * n_sm ? launch_n<16, 3, 1>(a, s) : launch_n<64, 2, 2>(a, s);
-    if (rc) return rc;
-    // the outputs of every chunk, from the entering states the scan stored
-    if (a.o && a.phase != 1) rc = launch_out_tc(a.plan, a.H, a.records, a.o, n_sm, s);
-    return rc;
+    if (slices16 <= 2LL * n_sm) {
+        const int rc = launch_n<16, 3, 1>(a, s);
+        // the outputs of every chunk, from the entering states the scan stored
+        return (rc || !a.o || a.phase == 1) ? rc : launch_out_tc(a.plan, a.H, a.records, a.o, n_sm, s);
+    }
+    // many chains: 64-column blocks that also form the outputs of their columns
+    // (no checkpoints in those blocks: a call with checkpoints stores the states
+    // and forms the outputs in a second pass)
+    if (a.o && a.phase != 1 && a.ncols == D && !a.ckpt) return launch_n<64, 3, 2, true>(a, s);
+    const int rc = launch_n<64, 2, 2>(a, s);
+    return (rc || !a.o || a.phase == 1) ? rc : launch_out_tc(a.plan, a.H, a.records, a.o, n_sm, s);
 }
 
 }  // namespace kda
