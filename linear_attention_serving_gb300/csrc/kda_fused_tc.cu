@@ -10,12 +10,12 @@
 // each finished record with a release flag, and a chain's producer waits for
 // the flag (acquire, bounded) before copying the record.  The chain blocks
 // start with one prep unit each, since their first records take a unit's
-// time to appear anyway.  The launch is
-// cooperative, so every block is resident and a waiting chain cannot starve
-// the prep it waits for; the prep never waits for a chain.  The chain blocks
-// also form the outputs O = O0 + Q' S of their columns (an M = 64 MMA issued
-// right after the chain's own, drained by four output warps): a chain keeps up
-// with the prep with time to spare, so the outputs cost no extra pass.
+// time to appear anyway.  The launch is cooperative, so every block is
+// resident and a waiting chain cannot starve the prep it waits for; the prep
+// never waits for a chain.  The chain blocks also form the outputs
+// O = O0 + Q' S of their columns (an M = 64 MMA issued right after the chain's
+// own, drained by four output warps): a chain keeps pace with the prep, so
+// the outputs cost no extra pass.
 #include "kda_prep_body.cuh"
 #include "kda_scan_body.cuh"
 

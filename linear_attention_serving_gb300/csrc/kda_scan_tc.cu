@@ -1,5 +1,8 @@
 // kda_scan_tc.cu -- the scan kernel for bf16 records (device code in
 // kda_scan_body.cuh): one block per (document or segment, head, column block).
+// Few chains: 16-column blocks that store each chunk's entering state for the
+// output kernel.  Many chains: 64-column blocks that form the outputs of their
+// columns themselves (as the fused launch's chain blocks do).
 #include "kda_scan_body.cuh"
 
 namespace kda {
