@@ -105,7 +105,11 @@ def test_segscan_1m_h8_full_size():
     inp = kda_synth.workload_inputs("segscan_1m_h8", device=DEV)
     o, fin, pm, ps = kda.segment_scan(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"],
                                       w.n_segments, return_pairs=True)
-    o_u, fin_u = kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"])
+    # the unsplit run: a one-document cu_seqlens keeps kda_chunk_fwd on its single
+    # chain per head (its planner segments only equal-length batches)
+    one_doc = torch.tensor([0, w.T], dtype=torch.int32, device=DEV)
+    assert kda.chunk_fwd_plan_segments(w.T, w.H, 1, varlen=True) == 0
+    o_u, fin_u = kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"], cu_seqlens=one_doc)
     torch.cuda.synchronize()
     assert rel_fro(o, o_u) <= 1e-3 and rel_fro(fin, fin_u) <= 1e-3
     T = w.T
