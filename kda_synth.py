@@ -12,7 +12,11 @@ Input recipe (all draws in fp32 from a seeded ``torch.Generator``, then cast):
   * z (gate logits) ~ N(0, z_std) per channel, fp32;  A_h ~ N(0, A_std) per head
     (A_std = 0 gives A_h = 0);
   * beta = sigmoid(N(0, 1)), fp32 (the method takes beta after its sigmoid);
-  * initial states ~ N(0, init_std) fp32, or none (zeros).
+  * initial states ~ N(0, init_std) fp32, or none (zeros);
+  * fused decode step: q, k, v ~ N(0, 1) before the short convolution (not
+    normalised), beta logits ~ N(0, 1), output-gate logits ~ N(0, 1), convolution
+    state ~ N(0, 1), convolution weights ~ U(-0.5, 0.5), output-norm weight
+    1 + N(0, 0.1).
 Standard deviations are the second argument of N(., .).
 """
 from __future__ import annotations
@@ -171,3 +175,40 @@ def segment_bounds(n_chunks: int, n_segments: int) -> list[tuple[int, int]]:
         out.append((c, c + n))
         c += n
     return out
+
+
+def decode_fused_params(H: int, seed: int, device="cpu") -> dict:
+    """Parameters of the fused decode step: short-convolution weights conv_w [3, H, D, 4]
+    (q, k, v; tap 3 multiplies the current token) ~ U(-0.5, 0.5), the range of the usual
+    fan-in initialisation of a width-4 depthwise convolution; output-norm weight
+    o_norm_w [D] = 1 + N(0, 0.1)."""
+    g = _gen(seed + 313, device)
+    conv_w = torch.rand((3, H, D, 4), generator=g, device=device, dtype=torch.float32).sub_(0.5)
+    o_norm_w = _randn((D,), g, device, std=0.1, mean=1.0)
+    return dict(conv_w=conv_w, o_norm_w=o_norm_w)
+
+
+def decode_conv_state(N: int, H: int, seed: int, device="cpu") -> torch.Tensor:
+    """Short-convolution state [N, H, 3, 3, D] fp32 (q, k, v; the last three projected
+    inputs, oldest first) ~ N(0, 1)."""
+    g = _gen(seed + 717, device)
+    return _randn((N, H, 3, 3, D), g, device)
+
+
+def decode_fused_window(N: int, W: int, H: int, step: int, seed: int, dtype: str = "f32",
+                        z_std: float = 1.0, device="cpu") -> dict:
+    """Projected inputs of one window of the fused decode step, before the short
+    convolution: q, k, v [N, W, H, D] ~ N(0, 1) (not normalised: the step normalises q
+    and k after the convolution), z [N, W, H, D] ~ N(0, z_std), beta logits [N, W, H]
+    ~ N(0, 1), output-gate logits o_gate [N, W, H, D] ~ N(0, 1) fp32, and
+    num_accepted [N] ~ U{0 .. W-1}."""
+    g = _gen(seed * 7919 + 17 * step + 5, device)
+    tdt = TORCH_DTYPE[dtype]
+    q = _randn((N, W, H, D), g, device).to(tdt)
+    k = _randn((N, W, H, D), g, device).to(tdt)
+    v = _randn((N, W, H, D), g, device).to(tdt)
+    z = _randn((N, W, H, D), g, device, std=z_std)
+    beta = _randn((N, W, H), g, device)
+    o_gate = _randn((N, W, H, D), g, device)
+    nacc = torch.randint(0, W, (N,), generator=g, device=device, dtype=torch.int32)
+    return dict(q=q, k=k, v=v, z=z, beta=beta, o_gate=o_gate, num_accepted=nacc)

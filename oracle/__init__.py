@@ -3,8 +3,10 @@
 TEST INFRASTRUCTURE ONLY.  The product library never imports, links or calls
 anything here; only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
 leg of ``bench.py`` may.  It shares no code with the CUDA path: the arithmetic
-lives in ``kda_oracle.c`` (plain C, double precision) and in the small numpy
-brute-force helpers below, each citing the passage it follows:
+lives in ``kda_oracle.c`` (plain C, double precision), in the small numpy
+brute-force helpers below, and in the numpy short convolution and gated output
+norm of the fused decode step (which runs the C recurrence in between), each
+citing the passage it follows:
 
   [K3-7] "Kimi K3 模型结构（7）：结构决定系统"
   [K3-2] "Kimi K3 模型结构（2）：序列维度（下），chunkwise 并行与下界衰减"
@@ -256,6 +258,114 @@ def decode_step(state, q, k, v, z, beta, A, cache_q, cache_k, cache_v, cache_z, 
     if rc < 0:
         raise ValueError("bad window")
     return o, st, (cq, ck, cv, cz, cb)
+
+
+# --------------------------------------------------------------------------
+# Fused decode step: short convolution, input options, recurrence, gated
+# output norm ([K3-7] "KDA：三种执行形态，三种内核", decode paragraph: one fused
+# kernel runs the replayed tokens, the bonus token and the next draft window
+# through short conv, input normalisation, gate, KDA recurrence and output
+# normalisation).
+# --------------------------------------------------------------------------
+
+CONV_WIDTH = 4  # [K3-7] "KDA 上下文并行", paragraph on backward / short conv: kernel width 4
+
+
+def short_conv(hist, x, w, silu=False):
+    """Causal depthwise short convolution over the token axis ([SA] "Kimi Linear": q, k
+    and v pass a short convolution after their projection, padded on the left so that it
+    stays causal; width 4 per [K3-7]).
+
+    hist [..., 3, C]: the three inputs before x, oldest first (the convolution state);
+    x [..., n, C]; w [..., C, 4] with tap 3 on the current token.
+    y_t = sum_j w[:, j] * s_{t+j} over the stream s = [hist, x]; with silu, y * sigmoid(y)
+    (the pages name no activation: silu is an option)."""
+    hist, x, w = _f64(hist), _f64(x), _f64(w)
+    s = np.concatenate([hist, x], axis=-2)
+    n = x.shape[-2]
+    y = np.zeros(x.shape)
+    for j in range(CONV_WIDTH):
+        y = y + w[..., None, :, j] * s[..., j:j + n, :]
+    if silu:
+        y = y / (1.0 + np.exp(-y))
+    return y
+
+
+def rms_norm_gated(o, gate, w, eps):
+    """Per-head output normalisation with the output forget gate ([SA] "Kimi Linear":
+    the KDA output is normalised per head and scaled by an output gate computed from a
+    linear projection): o / sqrt(mean(o^2) + eps) * w * sigmoid(gate), the mean over the
+    d_v channels of one (token, head).  o, gate [..., dv]; w [dv]."""
+    o, gate, w = _f64(o), _f64(gate), _f64(w)
+    r = 1.0 / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)
+    return o * r * w / (1.0 + np.exp(-gate))
+
+
+def decode_step_fused(state, q, k, v, z, beta, A, conv_w, conv_state, o_gate, o_norm_w, o_norm_eps,
+                      cache_q, cache_k, cache_v, cache_z, cache_beta, num_accepted=None, g_min=G_MIN,
+                      qk_l2norm=False, beta_sigmoid=False, conv_silu=False, return_prenorm=False):
+    """One fused decode step with MTP replay.
+
+    Per sequence b the committed token stream continues the convolution state:
+    [conv_state[b] (3 inputs), cached drafts 0 .. n_b - 1, t0]; the window's drafts
+    d1 .. d_{W-1} follow t0.  Steps, in the pages' order:
+      1. short convolution of the projected q, k, v over that stream (pre-convolution
+         values are what the cache and the convolution state hold);
+      2. input options on the convolved q, k (L2 norm) and beta (sigmoid);
+      3. the recurrence of ``decode_step``: replay, t0 committed, drafts speculative;
+      4. gated output norm of the window's outputs.
+    The new convolution state is the last three pre-convolution inputs of the committed
+    stream (ending at t0); the new cache holds the window's drafts as given.
+
+    state [N, H, dk, dv]; q, k, z [N, W, H, dk]; v [N, W, H, dv]; beta [N, W, H];
+    conv_w [3, H, dk, 4] (q, k, v; dk = dv); conv_state [N, H, 3, 3, dk]; o_gate [N, W, H, dv];
+    o_norm_w [dv]; cache_* [N, W-1, H, *].
+    Returns (o, new_state, new_cache, new_conv_state) [+ pre-norm o when return_prenorm]."""
+    st = _f64(state).copy()
+    q, k, v, z, beta, A, conv_w, o_gate, o_norm_w = map(
+        _f64, (q, k, v, z, beta, A, conv_w, o_gate, o_norm_w))
+    cs = _f64(conv_state).copy()
+    cq, ck, cv, cz, cb = (_f64(x).copy() for x in (cache_q, cache_k, cache_v, cache_z, cache_beta))
+    N, W, H, dk = q.shape
+    dv = v.shape[3]
+    if num_accepted is not None and hasattr(num_accepted, "detach"):
+        num_accepted = num_accepted.detach().cpu().numpy()
+    o = np.zeros((N, W, H, dv))
+    o_pre = np.zeros((N, W, H, dv))
+    for b in range(N):
+        n = 0 if num_accepted is None else int(num_accepted[b])
+        if not 0 <= n <= W - 1:
+            raise ValueError("bad window")
+        conv = []
+        for i, (x, cx) in enumerate(((q, cq), (k, ck), (v, cv))):
+            # [H, n + W, d]: replayed drafts, then the window
+            stream = np.concatenate([cx[b, :n], x[b]]).transpose(1, 0, 2)
+            y = short_conv(cs[b, :, i], stream, conv_w[i], conv_silu)
+            full = np.concatenate([cs[b, :, i], stream], axis=1)
+            cs[b, :, i] = full[:, n + 1:n + 4]  # the three inputs ending at t0
+            conv.append(y.transpose(1, 0, 2))    # [n + W, H, d]
+        yq, yk, yv = conv
+        zz = np.concatenate([cz[b, :n], z[b]])
+        bb = np.concatenate([cb[b, :n], beta[b]])
+        yq, yk, bb = input_prep(yq, yk, bb, qk_l2norm, beta_sigmoid)
+
+        def replay(x):
+            slots = np.zeros((1, W - 1) + x.shape[1:])
+            slots[0, :n] = x[:n]
+            return slots
+
+        ob, sb, _ = decode_step(st[b:b + 1], yq[None, n:], yk[None, n:], yv[None, n:], zz[None, n:],
+                                bb[None, n:], A, replay(yq), replay(yk), replay(yv), replay(zz),
+                                replay(bb), num_accepted=np.array([n]), g_min=g_min)
+        st[b] = sb[0]
+        o_pre[b] = ob[0]
+        o[b] = rms_norm_gated(ob[0], o_gate[b], o_norm_w, o_norm_eps)
+        # the new drafts' projected inputs, as given, replace this sequence's cache slots
+        for dst, src in ((cq, q), (ck, k), (cv, v), (cz, z), (cb, beta)):
+            dst[b] = src[b, 1:]
+    if return_prenorm:
+        return o, st, (cq, ck, cv, cz, cb), cs, o_pre
+    return o, st, (cq, ck, cv, cz, cb), cs
 
 
 # --------------------------------------------------------------------------

@@ -4,6 +4,7 @@ oracle's C source (on the CPU), rebuild it, and check that the pins catch each o
 import os
 import subprocess
 import tempfile
+import types
 
 import pytest
 
@@ -84,3 +85,60 @@ def test_unmutated_copy_passes_all_pins():
     with tempfile.TemporaryDirectory() as d:
         so = _build(open(SRC).read(), d, "clean")
         assert not _caught(so)
+
+
+# The fused decode step's convolution and output norm are numpy code in the
+# oracle's package: the same check, with the mistakes planted in a copy of that
+# module's source.
+PY_MUTANTS = [
+    ("conv_taps_reversed", "y = y + w[..., None, :, j] * s[..., j:j + n, :]",
+     "y = y + w[..., None, :, CONV_WIDTH - 1 - j] * s[..., j:j + n, :]"),
+    ("conv_without_history", "s = np.concatenate([hist, x], axis=-2)", "s = np.concatenate([0.0 * hist, x], axis=-2)"),
+    ("conv_silu_dropped", "y = y / (1.0 + np.exp(-y))", "y = y"),
+    ("conv_state_one_token_early", "cs[b, :, i] = full[:, n + 1:n + 4]", "cs[b, :, i] = full[:, n:n + 3]"),
+    ("replay_from_window_inputs", "stream = np.concatenate([cx[b, :n], x[b]])",
+     "stream = np.concatenate([x[b, 1:n + 1], x[b]])"),
+    ("norm_sum_not_mean", "np.mean(o * o, axis=-1, keepdims=True)", "np.sum(o * o, axis=-1, keepdims=True)"),
+    ("norm_over_heads", "np.mean(o * o, axis=-1, keepdims=True)", "np.mean(o * o, axis=-2, keepdims=True)"),
+    ("eps_outside_root", "np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps)",
+     "(np.sqrt(np.mean(o * o, axis=-1, keepdims=True)) + eps)"),
+    ("gate_without_sigmoid", "return o * r * w / (1.0 + np.exp(-gate))", "return o * r * w * gate"),
+    ("norm_without_weight", "return o * r * w / (1.0 + np.exp(-gate))", "return o * r / (1.0 + np.exp(-gate))"),
+    ("input_options_before_conv", "yq, yk, bb = input_prep(yq, yk, bb, qk_l2norm, beta_sigmoid)",
+     "_, _, bb = input_prep(yq, yk, bb, qk_l2norm, beta_sigmoid)"),
+]
+
+PY_PIN_TESTS = [
+    pins.test_short_conv_equals_numpy_convolve,
+    pins.test_short_conv_silu_closed_forms,
+    pins.test_gated_output_norm_invariants,
+    pins.test_fused_decode_with_unit_conv_is_plain_decode,
+    pins.test_fused_decode_equals_convolved_committed_stream,
+    pins.test_fused_decode_output_is_normalised_prenorm,
+]
+PY_FUNCS = ("short_conv", "rms_norm_gated", "decode_step_fused")
+
+
+def _py_caught(monkeypatch, src_text):
+    mod = types.ModuleType("oracle_mutant")
+    mod.__file__ = oracle.__file__
+    exec(compile(src_text, oracle.__file__, "exec"), mod.__dict__)
+    for f in PY_FUNCS:
+        monkeypatch.setattr(oracle, f, getattr(mod, f))
+    for t in PY_PIN_TESTS:
+        try:
+            t()
+        except (AssertionError, ValueError, FloatingPointError):
+            return True
+    return False
+
+
+@pytest.mark.parametrize("name,old,new", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_fused_pins_catch_planted_mistake(monkeypatch, name, old, new):
+    src = open(oracle.__file__).read()
+    assert old in src, f"mutation anchor for {name} not found"
+    assert _py_caught(monkeypatch, src.replace(old, new, 1)), f"no pin fails for planted mistake {name}"
+
+
+def test_unmutated_python_copy_passes_fused_pins(monkeypatch):
+    assert not _py_caught(monkeypatch, open(oracle.__file__).read())

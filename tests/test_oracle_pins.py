@@ -426,3 +426,162 @@ def test_input_prep_beta_sigmoid_closed_forms():
     assert np.allclose(b + oracle.input_prep(np.zeros((1, 1, 4)), np.zeros((1, 1, 4)), -x, beta_sigmoid=True)[2], 1.0)
     assert abs(b[0, 4] - 1 / (1 + math.exp(-3.0))) < 1e-15
     assert 0 < b[0, 0] < 1e-12 and 1 - b[0, 5] < 1e-12
+
+
+# ---------------------------------------------------------------- fused decode step
+
+def test_short_conv_equals_numpy_convolve():
+    """The depthwise causal convolution against numpy's discrete convolution per channel."""
+    r = np.random.default_rng(31)
+    C, n = 6, 9
+    hist, x, w = r.standard_normal((3, C)), r.standard_normal((n, C)), r.standard_normal((C, 4))
+    y = oracle.short_conv(hist, x, w)
+    s = np.concatenate([hist, x])
+    for c in range(C):
+        # numpy flips its second operand: reversed taps give tap 3 on the current token
+        assert np.allclose(y[:, c], np.convolve(s[:, c], w[c, ::-1], mode="valid"), rtol=0, atol=1e-13)
+    # causal: a later input leaves earlier outputs unchanged
+    x2 = x.copy()
+    x2[5] += 1.0
+    y2 = oracle.short_conv(hist, x2, w)
+    assert np.array_equal(y2[:5], y[:5]) and not np.allclose(y2[5], y[5])
+    # a unit impulse on the last tap copies the input; on the first, the input three tokens back
+    e = np.zeros((C, 4))
+    e[:, 3] = 1.0
+    assert np.array_equal(oracle.short_conv(hist, x, e), x)
+    e = np.zeros((C, 4))
+    e[:, 0] = 1.0
+    assert np.array_equal(oracle.short_conv(hist, x, e), s[:n])
+
+
+def test_short_conv_silu_closed_forms():
+    """SiLU option: silu(0) = 0, silu(y) - silu(-y) = y, silu(1) = 1 / (1 + 1/e)."""
+    C = 4
+    e = np.zeros((C, 4))
+    e[:, 3] = 1.0
+    x = np.array([[0.0, 1.0, -2.5, 7.0]])
+    hist = np.zeros((3, C))
+    yp = oracle.short_conv(hist, x, e, silu=True)
+    ym = oracle.short_conv(hist, -x, e, silu=True)
+    assert yp[0, 0] == 0.0
+    assert np.allclose(yp - ym, x, rtol=0, atol=1e-14)
+    assert abs(yp[0, 1] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-15
+    assert 0 < -ym[0, 3] < 7.0 * 1e-3  # large negative inputs are nearly cut off
+
+
+def test_gated_output_norm_invariants():
+    """o / rms(o) * w * sigmoid(gate) per (token, head): unit RMS with w = 1 and gate = 0 (up
+    to the factor 1/2), direction kept, scale invariance, gate odds e^g, eps under the root."""
+    r = np.random.default_rng(33)
+    o = r.standard_normal((5, 3, 32)) * 4.0
+    one = np.ones(32)
+    zero = np.zeros((5, 3, 32))
+    y = oracle.rms_norm_gated(o, zero, one, 0.0) * 2.0
+    assert np.allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, atol=1e-13)
+    ratio = y / o
+    assert np.allclose(ratio, ratio[..., :1], rtol=1e-12) and (ratio > 0).all()
+    assert np.allclose(oracle.rms_norm_gated(o * 17.0, zero, one, 0.0), y / 2.0, rtol=1e-13)
+    # per-row scaling: the norm is over the d_v channels of one (token, head) only
+    sc = r.uniform(0.1, 10.0, (5, 3, 1))
+    assert np.allclose(oracle.rms_norm_gated(o * sc, zero, one, 0.0), y / 2.0, rtol=1e-12)
+    w = r.uniform(0.5, 1.5, 32)
+    assert np.allclose(oracle.rms_norm_gated(o, zero, w, 0.0), y / 2.0 * w, rtol=1e-13)
+    g = r.standard_normal((5, 3, 32))
+    odds = oracle.rms_norm_gated(o, g, one, 0.0) / oracle.rms_norm_gated(o, -g, one, 0.0)
+    assert np.allclose(odds, np.exp(g), rtol=1e-12)
+    row = np.zeros((1, 1, 32))
+    row[0, 0, 3] = math.sqrt(32 * 1e-3)  # mean square 1e-3
+    t = oracle.rms_norm_gated(row, np.zeros((1, 1, 32)), one, 1e-3) * 2.0
+    assert abs(np.sqrt(np.mean(t * t)) - 1 / math.sqrt(2)) < 1e-12
+
+
+def _fused_setup(N, W, H, d, seed):
+    r = np.random.default_rng(seed)
+
+    def window():
+        return dict(q=r.standard_normal((N, W, H, d)), k=r.standard_normal((N, W, H, d)),
+                    v=r.standard_normal((N, W, H, d)), z=r.standard_normal((N, W, H, d)),
+                    beta=r.standard_normal((N, W, H)), o_gate=r.standard_normal((N, W, H, d)))
+
+    A = 0.3 * r.standard_normal(H)
+    S0 = 0.05 * r.standard_normal((N, H, d, d))
+    cs0 = r.standard_normal((N, H, 3, 3, d))
+    conv_w = r.uniform(-0.5, 0.5, (3, H, d, 4))
+    norm_w = 1.0 + 0.1 * r.standard_normal(d)
+    empty = (np.zeros((N, W - 1, H, d)),) * 4 + (np.zeros((N, W - 1, H)),)
+    return r, window, A, S0, cs0, conv_w, norm_w, empty
+
+
+def _fused(S, w, A, conv_w, cs, norm_w, cache, nacc, **opt):
+    return oracle.decode_step_fused(S, w["q"], w["k"], w["v"], w["z"], w["beta"], A, conv_w, cs,
+                                    w["o_gate"], norm_w, 1e-6, *cache, num_accepted=nacc,
+                                    return_prenorm=True, **opt)
+
+
+def test_fused_decode_with_unit_conv_is_plain_decode():
+    """With the convolution a unit impulse on the current token and no input options the
+    fused step's recurrence is the plain decode step, over two steps with replay."""
+    N, W, H, d = 4, 4, 2, 16
+    _, window, A, S0, cs0, _, norm_w, empty = _fused_setup(N, W, H, d, 35)
+    unit = np.zeros((3, H, d, 4))
+    unit[..., 3] = 1.0
+    w1, w2 = window(), window()
+    for w in (w1, w2):
+        w["beta"] = 1.0 / (1.0 + np.exp(-w["beta"]))
+    nacc = np.array([0, 3, 1, 2])
+    o1, S1, c1, cs1, p1 = _fused(S0, w1, A, unit, cs0, norm_w, empty, None)
+    o2, S2, c2, cs2, p2 = _fused(S1, w2, A, unit, cs1, norm_w, c1, nacc)
+    r1, T1, k1 = oracle.decode_step(S0, w1["q"], w1["k"], w1["v"], w1["z"], w1["beta"], A, *empty)
+    r2, T2, k2 = oracle.decode_step(T1, w2["q"], w2["k"], w2["v"], w2["z"], w2["beta"], A, *k1,
+                                    num_accepted=nacc)
+    assert rel(p1, r1) < 1e-13 and rel(S1, T1) < 1e-13
+    assert rel(p2, r2) < 1e-13 and rel(S2, T2) < 1e-13
+    for a, b in zip(c2, k2):
+        assert np.array_equal(a, b)
+
+
+def test_fused_decode_equals_convolved_committed_stream():
+    """Two fused steps equal numpy's convolution of the committed stream (convolution state,
+    t0, the accepted drafts, the next t0, then the new drafts) followed by the plain
+    recurrence; the convolution state then holds the last three committed inputs."""
+    N, W, H, d = 4, 5, 2, 16
+    _, window, A, S0, cs0, conv_w, norm_w, empty = _fused_setup(N, W, H, d, 37)
+    w1, w2 = window(), window()
+    nacc = np.array([0, 4, 2, 1])
+    opt = dict(qk_l2norm=True, beta_sigmoid=True, conv_silu=True)
+    _, S1, c1, cs1, _ = _fused(S0, w1, A, conv_w, cs0, norm_w, empty, None, **opt)
+    _, S2, _, cs2, p2 = _fused(S1, w2, A, conv_w, cs1, norm_w, c1, nacc, **opt)
+    for b in range(N):
+        n = nacc[b]
+        raw = {}
+        for i, name in enumerate(("q", "k", "v")):
+            s = np.concatenate([cs0[b, :, i].transpose(1, 0, 2), w1[name][b, :n + 1], w2[name][b]])
+            y = np.zeros((len(s) - 3, H, d))
+            for h in range(H):
+                for c in range(d):
+                    y[:, h, c] = np.convolve(s[:, h, c], conv_w[i, h, c, ::-1], mode="valid")
+            raw[name] = y * np.exp(y) / (1.0 + np.exp(y))  # SiLU as x / (1 + e^-x), rewritten
+            # the state after step 2 holds the inputs at t0(1) d1..dn, t0(2): the last three
+            assert np.array_equal(cs2[b, :, i], s[n + 2:n + 5].transpose(1, 0, 2))
+        z = np.concatenate([w1["z"][b, :n + 1], w2["z"][b]])
+        beta = np.concatenate([w1["beta"][b, :n + 1], w2["beta"][b]])
+        q, k, beta = oracle.input_prep(raw["q"], raw["k"], beta, qk_l2norm=True, beta_sigmoid=True)
+        o_ref, _ = oracle.recurrent(q, k, raw["v"], z, A, beta, init_state=S0[b:b + 1])
+        _, f_ref = oracle.recurrent(q[:n + 2], k[:n + 2], raw["v"][:n + 2], z[:n + 2], A, beta[:n + 2],
+                                    init_state=S0[b:b + 1])
+        assert rel(S2[b], f_ref[0]) < 1e-12
+        assert rel(p2[b], o_ref[n + 1:]) < 1e-12
+
+
+def test_fused_decode_output_is_normalised_prenorm():
+    """The fused outputs are the pre-norm outputs through the gated per-head norm; the new
+    cache holds the window's drafts as given (before the convolution)."""
+    N, W, H, d = 3, 3, 2, 16
+    _, window, A, S0, cs0, conv_w, norm_w, empty = _fused_setup(N, W, H, d, 39)
+    w1 = window()
+    w1["o_gate"][:] = 0.0
+    o, _, c, _, p = _fused(S0, w1, A, conv_w, cs0, np.ones(d), empty, None)
+    y = o * 2.0  # gate 0: sigmoid 1/2
+    assert np.allclose(y * np.sqrt(np.mean(p * p, axis=-1, keepdims=True) + 1e-6), p, rtol=1e-12)
+    for a, name in zip(c, ("q", "k", "v", "z", "beta")):
+        assert np.array_equal(a, w1[name][:, 1:])
