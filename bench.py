@@ -51,6 +51,7 @@ KERNEL_SOURCES = {
                                      "kda_tc.cuh", "kda_internal.cuh")],
     "out_tc": [_CSRC + f for f in ("kda_out_tc.cu", "kda_tc.cuh", "kda_internal.cuh")],
     "decode": [_CSRC + f for f in ("kda_decode.cu", "kda_tc.cuh", "kda_internal.cuh")],
+    "decode_fused": [_CSRC + f for f in ("kda_decode.cu", "kda_tc.cuh", "kda_internal.cuh")],
 }
 
 
@@ -283,7 +284,10 @@ def e2e_prefill(args, dev, kda, inputs):
 
 # ---------------------------------------------------------------- decode
 
-def bench_decode(args, dev, kda, steps=20, warmup=3):
+def bench_decode(args, dev, kda, steps=20, warmup=3, fused=False):
+    """The decode step over decode_mtp_b256_h96 (state 1.6 GB, larger than L2); with
+    fused, kda_decode_step_fused on the same shapes (short convolution, all input
+    options, gated output norm)."""
     w = kda_synth.WORKLOADS["decode_mtp_b256_h96"]
     N, H, W = w.N, w.H, w.W
     state = kda_synth.decode_state(N, H, w.seed, std=w.init_std, device=dev)
@@ -292,13 +296,26 @@ def bench_decode(args, dev, kda, steps=20, warmup=3):
     cache = (torch.zeros((N, W - 1, H, 128), dtype=t, device=dev), torch.zeros((N, W - 1, H, 128), dtype=t, device=dev),
              torch.zeros((N, W - 1, H, 128), dtype=t, device=dev), torch.zeros((N, W - 1, H, 128), device=dev),
              torch.zeros((N, W - 1, H), device=dev))
-    windows = [kda_synth.decode_window(N, W, H, s, w.seed, "f32", device=dev) for s in range(4)]
+    if fused:
+        prm = kda_synth.decode_fused_params(H, w.seed, device=dev)
+        cs = kda_synth.decode_conv_state(N, H, w.seed, device=dev)
+        windows = [kda_synth.decode_fused_window(N, W, H, s, w.seed, "f32", device=dev) for s in range(4)]
+
+        def step(wi, nacc):
+            kda.decode_step_fused(state, *(wi[n] for n in ("q", "k", "v", "z", "beta")), A, prm["conv_w"], cs,
+                                  wi["o_gate"], prm["o_norm_w"], cache, num_accepted=nacc, out=o,
+                                  qk_l2norm=True, beta_sigmoid=True, conv_silu=True)
+    else:
+        windows = [kda_synth.decode_window(N, W, H, s, w.seed, "f32", device=dev) for s in range(4)]
+
+        def step(wi, nacc):
+            kda.decode_step(state, *(wi[n] for n in ("q", "k", "v", "z", "beta")), A, cache,
+                            num_accepted=nacc, out=o)
     o = torch.empty_like(windows[0]["q"])
-    kda.decode_step(state, *(windows[0][n] for n in ("q", "k", "v", "z", "beta")), A, cache, out=o)
+    step(windows[0], None)
     for i in range(warmup):
         wi = windows[(i + 1) % 4]
-        kda.decode_step(state, *(wi[n] for n in ("q", "k", "v", "z", "beta")), A, cache,
-                        num_accepted=wi["num_accepted"], out=o)
+        step(wi, wi["num_accepted"])
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     committed = 0
@@ -308,8 +325,7 @@ def bench_decode(args, dev, kda, steps=20, warmup=3):
         wi = windows[(i + warmup + 1) % 4]
         torch.cuda._sleep(HOST_COVER_CYCLES)
         evs[i][0].record()
-        kda.decode_step(state, *(wi[n] for n in ("q", "k", "v", "z", "beta")), A, cache,
-                        num_accepted=wi["num_accepted"], out=o)
+        step(wi, wi["num_accepted"])
         evs[i][1].record()
     torch.cuda.synchronize()
     kda.profile_collect()
@@ -459,6 +475,18 @@ def main():
                          "achieved": step_bytes / (avg / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
                          "frac": step_bytes / (avg / 1e3) / 1e9 / hbm, "traffic": traffic_for("decode"),
                          "algorithmic_bytes_per_launch": step_bytes},
+        }
+        fc = bench_decode(args, dev, kda, fused=True)
+        fms = max_over_ranks(sum(fc["step_ms"]), ws, dev)
+        f_bytes = roofline.decode_fused_step_bytes(fc["N"], fc["H"], fc["W"], fc["accepted_total"] // fc["steps"])
+        favg = fms / fc["steps"]
+        line["decode_fused"] = {
+            "workload": "decode_mtp_b256_h96, short conv + L2 norm + beta sigmoid + gated output norm",
+            "value": fc["committed"] * ws / (fms / 1e3), "unit": "tokens/s", "ms_per_step": favg,
+            "roofline": {"kernel": "decode_fused", "bound": "hbm",
+                         "achieved": f_bytes / (favg / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": f_bytes / (favg / 1e3) / 1e9 / hbm, "traffic": traffic_for("decode_fused"),
+                         "algorithmic_bytes_per_launch": f_bytes},
         }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, used, sample = cpu_oracle_prefill(args.workload)

@@ -63,8 +63,10 @@ enum kda_dtype { KDA_BF16 = 0, KDA_F32 = 1 };
  *   KDA_FLAG_QK_L2NORM     q and k are divided by their L2 norm over the 128 key
  *                          channels, x / sqrt(sum(x^2) + 1e-6), per (token, head)
  *   KDA_FLAG_BETA_SIGMOID  beta holds logits; the kernels use 1 / (1 + exp(-beta))
+ *   KDA_FLAG_CONV_SILU     kda_decode_step_fused only: SiLU, y / (1 + exp(-y)), after
+ *                          the short convolution (the pages name no activation)
  * The decode cache keeps the projected inputs as given (unnormalised, logits). */
-enum kda_flags { KDA_FLAG_QK_L2NORM = 1, KDA_FLAG_BETA_SIGMOID = 2 };
+enum kda_flags { KDA_FLAG_QK_L2NORM = 1, KDA_FLAG_BETA_SIGMOID = 2, KDA_FLAG_CONV_SILU = 4 };
 
 /* Device error codes (bit flags) written into the workspace / error word. */
 enum kda_device_error {
@@ -282,6 +284,57 @@ int kda_decode_step(float *state,
                     const int32_t *num_accepted,
                     int N, int H, int D, int W, int dtype, float g_min,
                     void *o, int32_t *error_word, int flags, kda_stream_t stream);
+
+/* --------------------------------------------------------------------------
+ * kda_decode_step_fused -- the decode step with what the same paragraph puts
+ * in the fused kernel around the recurrence ("Kimi K3 模型结构（7）", section
+ * "KDA：三种执行形态，三种内核", decode: short convolution, input normalisation,
+ * gate, KDA recurrence and output normalisation in one loop over the replayed
+ * drafts, the bonus token and the next draft window).  The module around the
+ * recurrence is the one of "Kimi K3: the Manos, the Mythos ..." section "Kimi
+ * Linear": q, k, v pass a causal short convolution (left padding; width 4, as
+ * in "Kimi K3 模型结构（7）", section "KDA 上下文并行", short-conv note) after
+ * their projection; q and k are L2-normalised; the output is normalised per
+ * head and scaled by an output gate.
+ *
+ * Per sequence b the committed stream continues the convolution state:
+ * [conv_state (3 inputs), replayed drafts 0 .. n_b - 1, t0], and the window's
+ * drafts follow t0.  Per token, in order:
+ *   1. y_t = sum_{j<4} conv_w[., c, j] x_{t-3+j} per channel for each of q, k, v
+ *      (pre-convolution inputs x come from the window or the cache), then SiLU
+ *      with KDA_FLAG_CONV_SILU;
+ *   2. the input options (KDA_FLAG_QK_L2NORM on the convolved q, k;
+ *      KDA_FLAG_BETA_SIGMOID on beta);
+ *   3. the recurrence exactly as kda_decode_step (replay, t0 committed in place,
+ *      drafts speculative);
+ *   4. o = o_raw / sqrt(mean_c(o_raw^2) + o_norm_eps) * o_norm_w[c] * sigmoid(o_gate)
+ *      for the window's tokens, the mean over the 128 value channels of one
+ *      (token, head).
+ * The convolution state becomes the last three pre-convolution inputs of the
+ * committed stream (ending at t0); the cache takes the window's drafts as given.
+ *
+ * Arguments as kda_decode_step, plus
+ *   conv_w       (device) fp32 [3, H, D, 4]: taps of q, k, v per channel, tap 3
+ *                on the current token (16-byte aligned)
+ *   conv_state   (device) fp32 [N, H, 3, 3, D], read and written in place:
+ *                q, k, v x the three latest committed inputs, oldest first
+ *   o_gate       (device) fp32 [N, W, H, D]: output-gate logits
+ *   o_norm_w     (device) fp32 [D]: output-norm weight (one vector for all heads)
+ *   o_norm_eps   >= 0, added under the root
+ *   flags        0 or an OR of KDA_FLAG_QK_L2NORM, KDA_FLAG_BETA_SIGMOID,
+ *                KDA_FLAG_CONV_SILU
+ * A sequence with an out-of-range num_accepted keeps its convolution state too.
+ * ------------------------------------------------------------------------ */
+int kda_decode_step_fused(float *state,
+                          const void *q, const void *k, const void *v,
+                          const float *z, const float *beta, const float *A,
+                          const float *conv_w, float *conv_state,
+                          const float *o_gate, const float *o_norm_w, float o_norm_eps,
+                          void *cache_q, void *cache_k, void *cache_v,
+                          float *cache_z, float *cache_beta,
+                          const int32_t *num_accepted,
+                          int N, int H, int D, int W, int dtype, float g_min,
+                          void *o, int32_t *error_word, int flags, kda_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * kda_read_device_error -- synchronise `stream` and read the device error

@@ -3,10 +3,13 @@
 Three calls, each a hand-written CUDA kernel path behind the C ABI in
 ``include/kda.h``: ``chunk_fwd`` (chunkwise prefill), ``segment_scan``
 (intra-device segment-parallel prefill) and ``decode_step`` (in-place decode
-with MTP draft replay).
+with MTP draft replay), plus ``decode_step_fused`` (the decode step with the
+short convolution and the gated output norm around the recurrence).
 """
-from .kda import (KDAError, chunk_fwd, chunk_fwd_ckpt, chunk_fwd_plan_segments, chunk_fwd_workspace_size, decode_step, load,
+from .kda import (KDAError, chunk_fwd, chunk_fwd_ckpt, chunk_fwd_plan_segments, chunk_fwd_workspace_size, decode_step,
+                  decode_step_fused, load,
                   library_path, read_device_error, segment_scan, segment_scan_workspace_size)
 
-__all__ = ["KDAError", "chunk_fwd", "chunk_fwd_ckpt", "chunk_fwd_plan_segments", "chunk_fwd_workspace_size", "decode_step", "load",
+__all__ = ["KDAError", "chunk_fwd", "chunk_fwd_ckpt", "chunk_fwd_plan_segments", "chunk_fwd_workspace_size", "decode_step",
+           "decode_step_fused", "load",
            "library_path", "read_device_error", "segment_scan", "segment_scan_workspace_size"]

@@ -25,6 +25,16 @@
 // which removes the Diag(alpha) pass over the state for every token.  At most
 // 2W - 1 <= 15 tokens run per step, so s_t >= e^{5 * 15} = e^-75 stays a
 // normal fp32 number (bounded gate, "Kimi K3 模型结构（2）", "后果一").
+//
+// The fused instantiation (FUSE) adds what the same decode paragraph puts in
+// the kernel around the recurrence, with the module of "Kimi K3: the Manos,
+// the Mythos ..." section "Kimi Linear": a causal depthwise short convolution
+// (width 4) of the projected q, k and v over the committed stream (the cache
+// and the convolution state hold pre-convolution inputs, so a replay runs the
+// convolution again), and a per-head RMS norm of the outputs scaled by a
+// sigmoid output gate.  Per item it adds the convolution state to the rows'
+// bulk copy, reads the convolution weights of the head, and keeps the window's
+// raw outputs and gate factors in shared memory for a final pass.
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 
@@ -51,10 +61,14 @@ __device__ __forceinline__ void store_pair(__nv_bfloat16 *p, float a, float b) {
     *reinterpret_cast<__nv_bfloat162 *>(p) = __floats2bfloat162_rn(a, b);
 }
 
+constexpr int CONV_TAPS = 4;                  // short convolution width
+constexpr int CONV_HIST = CONV_TAPS - 1;      // inputs kept per channel between steps
+constexpr uint32_t CONV_STATE_BYTES = 3 * CONV_HIST * D * 4;  // q, k, v x 3 inputs x 128 channels
+
 struct DecSmem {
     int ntok_max;
-    size_t state, raw, kt, kh, qt, vt, total;
-    __host__ __device__ DecSmem(int W) {
+    size_t state, raw, kt, kh, qt, vt, cs, sg, ot, total;
+    __host__ __device__ DecSmem(int W, bool fuse) {
         ntok_max = 2 * W - 1;
         state = 0;                                        // [128][128] fp32
         raw = state + (size_t)D * D * 4;                  // [ntok][q | k | v | z]
@@ -62,34 +76,45 @@ struct DecSmem {
         kh = kt + (size_t)ntok_max * VPAD * 4;            // k / s_t    [ntok][VPAD]
         qt = kh + (size_t)ntok_max * VPAD * 4;            // s_t . q    [ntok][VPAD]
         vt = qt + (size_t)ntok_max * VPAD * 4;            // v          [ntok][D]
-        total = vt + (size_t)ntok_max * D * 4;
+        cs = vt + (size_t)ntok_max * D * 4;               // FUSE: convolution state [3][3][D]
+        sg = cs + (fuse ? CONV_STATE_BYTES : 0);          // FUSE: norm weight x sigmoid(gate) [W][D]
+        ot = sg + (fuse ? (size_t)W * D * 4 : 0);         // FUSE: the window's raw outputs [W][D]
+        total = ot + (fuse ? (size_t)W * D * 4 : 0);
     }
 };
+
 
 // One thread starts the bulk copies of item `item` (its state and token rows)
 // into shared memory; completion is counted on `bar`, in two parts so that the
 // state copy can start as soon as the state buffer is free and the rows copy
 // as soon as the row buffer is.  `nacc` was read ahead of time; when it is out
 // of range nothing is copied and the barrier completes without data.
+template <bool FUSE>
 __device__ __forceinline__ uint32_t item_bytes(int nacc, int W, uint32_t rowb) {
-    return (uint32_t)(D * D * 4) + (uint32_t)nacc * (2 * rowb + 512) + (uint32_t)W * (3 * rowb + 512);
+    // replayed rows carry no q unless the convolution needs it
+    const uint32_t replay_row = (FUSE ? 3 : 2) * rowb + 512;
+    return (uint32_t)(D * D * 4) + (uint32_t)nacc * replay_row + (uint32_t)W * (3 * rowb + 512) +
+           (FUSE ? CONV_STATE_BYTES : 0u);
 }
+template <bool FUSE>
 __device__ __forceinline__ void issue_state(int item, int nacc, int W, uint32_t rowb, const float *__restrict__ state,
                                             uint8_t *sm, const DecSmem &L, uint64_t *bar) {
     if (nacc < 0 || nacc > W - 1) {
         mbar_arrive(bar);
         return;
     }
-    mbar_expect_tx(bar, item_bytes(nacc, W, rowb));
+    mbar_expect_tx(bar, item_bytes<FUSE>(nacc, W, rowb));
     bulk_g2s(sm + L.state, state + (size_t)item * D * D, D * D * 4, bar);
 }
-template <typename InT>
+template <typename InT, bool FUSE>
 __device__ __forceinline__ void issue_rows(int item, int nacc, int H, int W, const InT *__restrict__ q,
                                            const InT *__restrict__ k, const InT *__restrict__ v,
-                                           const float *__restrict__ z, const InT *__restrict__ ck,
-                                           const InT *__restrict__ cv, const float *__restrict__ cz, uint8_t *sm,
-                                           const DecSmem &L, uint64_t *bar) {
+                                           const float *__restrict__ z, const InT *__restrict__ cq,
+                                           const InT *__restrict__ ck, const InT *__restrict__ cv,
+                                           const float *__restrict__ cz, const float *__restrict__ conv_state,
+                                           uint8_t *sm, const DecSmem &L, uint64_t *bar) {
     if (nacc < 0 || nacc > W - 1) return;
+    if (FUSE) bulk_g2s(sm + L.cs, conv_state + (size_t)item * (3 * CONV_HIST * D), CONV_STATE_BYTES, bar);
     const int b = item / H, h = item - b * H;
     const int ntok = nacc + W;
     const uint32_t rowb = (uint32_t)(D * sizeof(InT));
@@ -97,6 +122,7 @@ __device__ __forceinline__ void issue_rows(int item, int nacc, int H, int W, con
         uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
         if (t < nacc) {
             const size_t row = ((size_t)b * (W - 1) + t) * H + h;
+            if (FUSE) bulk_g2s(slot, cq + row * D, rowb, bar);
             bulk_g2s(slot + 512, ck + row * D, rowb, bar);
             bulk_g2s(slot + 1024, cv + row * D, rowb, bar);
             bulk_g2s(slot + 1536, cz + row * D, 512, bar);
@@ -120,30 +146,36 @@ __device__ __forceinline__ void load_betas(int item, int H, int W, int tid, cons
 }
 
 // OPTS compiles the input options (KDA_FLAG_*) in: a separate instantiation,
-// so that the default path keeps its registers.
-template <typename InT, bool OPTS>
+// so that the default path keeps its registers.  FUSE adds the short
+// convolution and the gated output norm (the fused step).
+template <typename InT, bool OPTS, bool FUSE>
 __global__ void __launch_bounds__(DEC_THREADS, 2)
 decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *__restrict__ k,
               const InT *__restrict__ v, const float *__restrict__ z, const float *__restrict__ beta,
               const float *__restrict__ A, InT *__restrict__ cq, InT *__restrict__ ck,
               InT *__restrict__ cv, float *__restrict__ cz, float *__restrict__ cb,
               const int32_t *__restrict__ nacc_p, int N, int H, int W, float g_min, InT *__restrict__ o,
-              int32_t *__restrict__ err, int flags) {
+              int32_t *__restrict__ err, int flags, DecFuse fz) {
     extern __shared__ __align__(128) uint8_t smdyn[];
     __shared__ uint64_t full_bar;
     __shared__ float sbeta[2][2 * MAX_W];
     __shared__ __align__(16) float scommit[VPAD];
     __shared__ float snorm[2 * MAX_W][4][2];  // KDA_FLAG_QK_L2NORM: squared norms per token and warp
+    __shared__ float sqo[MAX_W][DEC_THREADS / 32];  // FUSE: squared output sums per window token and warp
     const bool l2norm = OPTS && (flags & KDA_FLAG_QK_L2NORM) != 0;
     const bool bsig = OPTS && (flags & KDA_FLAG_BETA_SIGMOID) != 0;
+    const bool silu = FUSE && OPTS && (flags & KDA_FLAG_CONV_SILU) != 0;
 
-    const DecSmem L(W);
+    const DecSmem L(W, FUSE);
     uint8_t *sm = smdyn;
     float *sS = reinterpret_cast<float *>(sm + L.state);
     float(*kt)[VPAD] = reinterpret_cast<float(*)[VPAD]>(sm + L.kt);
     float(*kh)[VPAD] = reinterpret_cast<float(*)[VPAD]>(sm + L.kh);
     float(*qt)[VPAD] = reinterpret_cast<float(*)[VPAD]>(sm + L.qt);
     float(*vt)[D] = reinterpret_cast<float(*)[D]>(sm + L.vt);
+    const float(*cst)[CONV_HIST][D] = reinterpret_cast<const float(*)[CONV_HIST][D]>(sm + L.cs);
+    float(*sg)[D] = reinterpret_cast<float(*)[D]>(sm + L.sg);
+    float(*ot)[D] = reinterpret_cast<float(*)[D]>(sm + L.ot);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -171,8 +203,9 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
             load_betas(item + gridDim.x, H, W, tid, beta, cb, bc_nx, bw_nx);
         }
         if (tid == 0) {
-            issue_state(item, nacc_cur, W, rowb, state, sm, L, &full_bar);
-            issue_rows<InT>(item, nacc_cur, H, W, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
+            issue_state<FUSE>(item, nacc_cur, W, rowb, state, sm, L, &full_bar);
+            issue_rows<InT, FUSE>(item, nacc_cur, H, W, q, k, v, z, cq, ck, cv, cz, fz.conv_state, sm, L,
+                                  &full_bar);
         }
     }
     bool timed_out = false;
@@ -197,8 +230,9 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
             if (tid == 0) {
                 atomicOr(err, KDA_DEVERR_NUM_ACCEPTED);
                 if (next < n_items) {
-                    issue_state(next, nacc_next, W, rowb, state, sm, L, &full_bar);
-                    issue_rows<InT>(next, nacc_next, H, W, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
+                    issue_state<FUSE>(next, nacc_next, W, rowb, state, sm, L, &full_bar);
+                    issue_rows<InT, FUSE>(next, nacc_next, H, W, q, k, v, z, cq, ck, cv, cz, fz.conv_state, sm,
+                                          L, &full_bar);
                 }
             }
             nacc_cur = nacc_nx;
@@ -225,19 +259,56 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
             s1[i] = x.y;
         }
         __syncthreads();
-        if (tid == 0 && next < n_items) issue_state(next, nacc_next, W, rowb, state, sm, L, &full_bar);
+        if (tid == 0 && next < n_items) issue_state<FUSE>(next, nacc_next, W, rowb, state, sm, L, &full_bar);
         const float eA = expf(A[h]);
         if (tid < D) {
             // channel c of every token: inputs, the cumulative decay s_t over the
             // step's tokens, and the scaled vectors s_t k, k / s_t, s_t q
             const int c = tid, vc = vidx(c);
+            if (FUSE) {
+                // short convolution of q, k, v over [state, replayed drafts, window]:
+                // y_t = sum_j w_j x_{t-3+j}; the convolved q, k go to qt, kt (scaled in
+                // place below), v to vt.  At t0 the last three inputs become the state.
+                const float4 wq = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)0 * H + h) * D + c);
+                const float4 wk = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)1 * H + h) * D + c);
+                const float4 wv = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)2 * H + h) * D + c);
+                float xq0 = cst[0][0][c], xq1 = cst[0][1][c], xq2 = cst[0][2][c];
+                float xk0 = cst[1][0][c], xk1 = cst[1][1][c], xk2 = cst[1][2][c];
+                float xv0 = cst[2][0][c], xv1 = cst[2][1][c], xv2 = cst[2][2][c];
+                float *cs_out = fz.conv_state + (size_t)item * (3 * CONV_HIST * D) + c;
+                for (int t = 0; t < ntok; ++t) {
+                    const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
+                    const float xq = to_f32(reinterpret_cast<const InT *>(slot)[c]);
+                    const float xk = to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
+                    const float xv = to_f32(reinterpret_cast<const InT *>(slot + 1024)[c]);
+                    float yq = fmaf(wq.w, xq, fmaf(wq.z, xq2, fmaf(wq.y, xq1, wq.x * xq0)));
+                    float yk = fmaf(wk.w, xk, fmaf(wk.z, xk2, fmaf(wk.y, xk1, wk.x * xk0)));
+                    float yv = fmaf(wv.w, xv, fmaf(wv.z, xv2, fmaf(wv.y, xv1, wv.x * xv0)));
+                    xq0 = xq1; xq1 = xq2; xq2 = xq;
+                    xk0 = xk1; xk1 = xk2; xk2 = xk;
+                    xv0 = xv1; xv1 = xv2; xv2 = xv;
+                    if (t == nacc) {
+                        cs_out[0 * D] = xq0; cs_out[1 * D] = xq1; cs_out[2 * D] = xq2;
+                        cs_out[3 * D] = xk0; cs_out[4 * D] = xk1; cs_out[5 * D] = xk2;
+                        cs_out[6 * D] = xv0; cs_out[7 * D] = xv1; cs_out[8 * D] = xv2;
+                    }
+                    if (silu) {
+                        yq = yq / (1.f + expf(-yq));
+                        yk = yk / (1.f + expf(-yk));
+                        yv = yv / (1.f + expf(-yv));
+                    }
+                    qt[t][vc] = yq;
+                    kt[t][vc] = yk;
+                    vt[t][c] = yv;
+                }
+            }
             if (l2norm) {
                 // input option: squared norms of q and k over the 128 channels
                 // (replayed tokens carry no q)
                 for (int t = 0; t < ntok; ++t) {
                     const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
-                    const float qq = t < nacc ? 0.f : to_f32(reinterpret_cast<const InT *>(slot)[c]);
-                    const float kk = to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
+                    const float qq = t < nacc ? 0.f : FUSE ? qt[t][vc] : to_f32(reinterpret_cast<const InT *>(slot)[c]);
+                    const float kk = FUSE ? kt[t][vc] : to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
                     float pq = qq * qq, pk = kk * kk;
 #pragma unroll
                     for (int m = 16; m > 0; m >>= 1) {
@@ -254,8 +325,8 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
             float sc = 1.f;
             for (int t = 0; t < ntok; ++t) {
                 const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
-                float qq = t < nacc ? 0.f : to_f32(reinterpret_cast<const InT *>(slot)[c]);
-                float kk = to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
+                float qq = t < nacc ? 0.f : FUSE ? qt[t][vc] : to_f32(reinterpret_cast<const InT *>(slot)[c]);
+                float kk = FUSE ? kt[t][vc] : to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
                 if (l2norm) {
                     qq *= rsqrtf(snorm[t][0][0] + snorm[t][1][0] + snorm[t][2][0] + snorm[t][3][0] + L2NORM_EPS);
                     kk *= rsqrtf(snorm[t][0][1] + snorm[t][1][1] + snorm[t][2][1] + snorm[t][3][1] + L2NORM_EPS);
@@ -265,27 +336,39 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                 kt[t][vc] = kk * sc;
                 kh[t][vc] = __fdividef(kk, sc);
                 qt[t][vc] = qq * sc;
-                vt[t][c] = to_f32(reinterpret_cast<const InT *>(slot + 1024)[c]);
+                if (!FUSE) vt[t][c] = to_f32(reinterpret_cast<const InT *>(slot + 1024)[c]);
                 if (t == nacc) scommit[vc] = sc;
             }
-        } else if (tid == D) {
-            // the new drafts' projected inputs replace this sequence's cache slots
-            for (int t = nacc + 1; t < ntok; ++t) {
-                const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
-                const size_t row = ((size_t)b * (W - 1) + (t - nacc - 1)) * H + h;
-                bulk_s2g(cq + row * D, slot, rowb);
-                bulk_s2g(ck + row * D, slot + 512, rowb);
-                bulk_s2g(cv + row * D, slot + 1024, rowb);
-                bulk_s2g(cz + row * D, slot + 1536, 512);
+        } else {
+            if (tid == D) {
+                // the new drafts' projected inputs replace this sequence's cache slots
+                for (int t = nacc + 1; t < ntok; ++t) {
+                    const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
+                    const size_t row = ((size_t)b * (W - 1) + (t - nacc - 1)) * H + h;
+                    bulk_s2g(cq + row * D, slot, rowb);
+                    bulk_s2g(ck + row * D, slot + 512, rowb);
+                    bulk_s2g(cv + row * D, slot + 1024, rowb);
+                    bulk_s2g(cz + row * D, slot + 1536, 512);
+                }
+                bulk_commit();
             }
-            bulk_commit();
+            if (FUSE) {
+                // output gate: norm weight x sigmoid(gate logit) per window token and channel
+                const int c = tid - D;
+                const float wn = __ldg(fz.o_norm_w + c);
+                for (int j = 0; j < W; ++j) {
+                    const float gl = __ldg(fz.o_gate + (((size_t)b * W + j) * H + h) * D + c);
+                    sg[j][c] = wn / (1.f + expf(-gl));
+                }
+            }
         }
         if (tid < W - 1) cb[((size_t)b * (W - 1) + tid) * H + h] = sbt[nacc + 1 + tid];
         __syncthreads();
         // the row buffers are free once the cache copies have read them: the next item's token rows
         if (tid == D) bulk_wait_read_all();
         if (tid == D && next < n_items)
-            issue_rows<InT>(next, nacc_next, H, W, q, k, v, z, ck, cv, cz, sm, L, &full_bar);
+            issue_rows<InT, FUSE>(next, nacc_next, H, W, q, k, v, z, cq, ck, cv, cz, fz.conv_state, sm, L,
+                                  &full_bar);
 
         // the recurrence over replay + bonus + drafts
         const float *bt = sbt;
@@ -345,7 +428,18 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                     ao0 += __shfl_xor_sync(0xffffffffu, ao0, m);
                     ao1 += __shfl_xor_sync(0xffffffffu, ao1, m);
                 }
-                if (part == 0) store_pair(o + (((size_t)b * W + (t - nacc)) * H + h) * D + col, ao0, ao1);
+                if (FUSE) {
+                    // the window's raw outputs wait for their norm; squared sums per warp
+                    // (fixed order later: the result does not depend on warp timing)
+                    float pp = ao0 * ao0 + ao1 * ao1;
+                    pp += __shfl_xor_sync(0xffffffffu, pp, 1);
+                    pp += __shfl_xor_sync(0xffffffffu, pp, 2);
+                    pp += __shfl_xor_sync(0xffffffffu, pp, 4);
+                    if (part == 0) *reinterpret_cast<float2 *>(&ot[t - nacc][col]) = make_float2(ao0, ao1);
+                    if (lane == 0) sqo[t - nacc][warp] = pp;
+                } else if (part == 0) {
+                    store_pair(o + (((size_t)b * W + (t - nacc)) * H + h) * D + col, ao0, ao1);
+                }
             }
             if (t == nacc) {
                 // commit: S = Diag(s_t) S^, written back in place
@@ -367,44 +461,72 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
         bc_nx = bc_nn;
         bw_nx = bw_nn;
         __syncthreads();  // vectors are rewritten by the next item
+        if (FUSE) {
+            // gated RMS norm over the 128 value channels of each window token; the
+            // next item's shared-memory writes come after its first barrier
+            for (int i = tid; i < W * (D / 2); i += DEC_THREADS) {
+                const int j = i / (D / 2), cc = 2 * (i % (D / 2));
+                float ss = 0.f;
+#pragma unroll
+                for (int w8 = 0; w8 < DEC_THREADS / 32; ++w8) ss += sqo[j][w8];
+                const float r = rsqrtf(ss * (1.f / D) + fz.o_norm_eps);
+                const float2 ov = *reinterpret_cast<const float2 *>(&ot[j][cc]);
+                const float2 gv = *reinterpret_cast<const float2 *>(&sg[j][cc]);
+                store_pair(o + (((size_t)b * W + j) * H + h) * D + cc, ov.x * r * gv.x, ov.y * r * gv.y);
+            }
+        }
     }
     if (tid == D) bulk_wait_all();  // the cache copies have landed before the block exits
 }
 
 }  // namespace
 
+namespace {
+
+template <typename InT, bool FUSE>
+int launch_decode_t(float *state, const void *q, const void *k, const void *v, const float *z,
+                    const float *beta, const float *A, void *cq, void *ck, void *cv, float *cz, float *cb,
+                    const int32_t *nacc, int N, int H, int W, float g_min, void *o, int32_t *err, int flags,
+                    const DecFuse &fz, cudaStream_t s) {
+    const long long items = (long long)N * H;
+    const DecSmem L(W, FUSE);
+    const int smem = (int)L.total;
+    auto kern = flags ? decode_kernel<InT, true, FUSE> : decode_kernel<InT, false, FUSE>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    int per_sm = 1;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DEC_THREADS, smem);
+    const long long slots = (long long)device_sm_count() * (per_sm > 0 ? per_sm : 1);
+    const int grid = (int)(items < slots ? items : slots);
+    kern<<<grid, DEC_THREADS, smem, s>>>(state, (const InT *)q, (const InT *)k, (const InT *)v, z, beta, A,
+                                         (InT *)cq, (InT *)ck, (InT *)cv, cz, cb, nacc, N, H, W, g_min,
+                                         (InT *)o, err, flags, fz);
+    return KDA_OK;
+}
+
+}  // namespace
+
+// fz == nullptr: the plain step; otherwise the fused step with those operands.
 int launch_decode(float *state, const void *q, const void *k, const void *v, const float *z,
                   const float *beta, const float *A, void *cq, void *ck, void *cv, float *cz,
                   float *cb, const int32_t *nacc, int N, int H, int W, int dtype, float g_min,
-                  void *o, int32_t *err, int flags, cudaStream_t s) {
-    const long long items = (long long)N * H;
-    if (items <= 0) return KDA_OK;
+                  void *o, int32_t *err, int flags, const DecFuse *fz, cudaStream_t s) {
+    if ((long long)N * H <= 0) return KDA_OK;
     if (W > MAX_W) return KDA_ERR_UNSUPPORTED;
-    const DecSmem L(W);
-    const int smem = (int)L.total;
-    int per_sm = 1, n_sm = device_sm_count();
-    int grid;
-    if (dtype == KDA_BF16) {
-        auto kern = flags ? decode_kernel<__nv_bfloat16, true> : decode_kernel<__nv_bfloat16, false>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return KDA_ERR_CUDA;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DEC_THREADS, smem);
-        grid = (int)(items < (long long)n_sm * (per_sm > 0 ? per_sm : 1) ? items : (long long)n_sm * (per_sm > 0 ? per_sm : 1));
-        kern<<<grid, DEC_THREADS, smem, s>>>(
-            state, (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, z, beta, A,
-            (__nv_bfloat16 *)cq, (__nv_bfloat16 *)ck, (__nv_bfloat16 *)cv, cz, cb, nacc, N, H, W, g_min,
-            (__nv_bfloat16 *)o, err, flags);
-    } else {
-        auto kern = flags ? decode_kernel<float, true> : decode_kernel<float, false>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return KDA_ERR_CUDA;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DEC_THREADS, smem);
-        grid = (int)(items < (long long)n_sm * (per_sm > 0 ? per_sm : 1) ? items : (long long)n_sm * (per_sm > 0 ? per_sm : 1));
-        kern<<<grid, DEC_THREADS, smem, s>>>(state, (const float *)q, (const float *)k, (const float *)v, z,
-                                             beta, A, (float *)cq, (float *)ck, (float *)cv, cz, cb, nacc, N,
-                                             H, W, g_min, (float *)o, err, flags);
-    }
-    note_launch("decode", s);
+    const DecFuse none{};
+    int rc;
+    if (dtype == KDA_BF16)
+        rc = fz ? launch_decode_t<__nv_bfloat16, true>(state, q, k, v, z, beta, A, cq, ck, cv, cz, cb, nacc, N, H,
+                                                        W, g_min, o, err, flags, *fz, s)
+                : launch_decode_t<__nv_bfloat16, false>(state, q, k, v, z, beta, A, cq, ck, cv, cz, cb, nacc, N,
+                                                         H, W, g_min, o, err, flags, none, s);
+    else
+        rc = fz ? launch_decode_t<float, true>(state, q, k, v, z, beta, A, cq, ck, cv, cz, cb, nacc, N, H, W,
+                                                g_min, o, err, flags, *fz, s)
+                : launch_decode_t<float, false>(state, q, k, v, z, beta, A, cq, ck, cv, cz, cb, nacc, N, H, W,
+                                                 g_min, o, err, flags, none, s);
+    if (rc != KDA_OK) return rc;
+    note_launch(fz ? "decode_fused" : "decode", s);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

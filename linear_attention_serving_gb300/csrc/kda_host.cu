@@ -392,7 +392,35 @@ int kda_decode_step(float *state, const void *q, const void *k, const void *v, c
         return KDA_ERR_INVALID_ARG;
     note_begin((cudaStream_t)stream);
     return launch_decode(state, q, k, v, z, beta, A, cache_q, cache_k, cache_v, cache_z, cache_beta,
-                         num_accepted, N, H, W, dtype, g_min, o, error_word, flags, (cudaStream_t)stream);
+                         num_accepted, N, H, W, dtype, g_min, o, error_word, flags, nullptr,
+                         (cudaStream_t)stream);
+}
+
+int kda_decode_step_fused(float *state, const void *q, const void *k, const void *v, const float *z,
+                          const float *beta, const float *A, const float *conv_w, float *conv_state,
+                          const float *o_gate, const float *o_norm_w, float o_norm_eps, void *cache_q,
+                          void *cache_k, void *cache_v, float *cache_z, float *cache_beta,
+                          const int32_t *num_accepted, int N, int H, int Dm, int W, int dtype, float g_min,
+                          void *o, int32_t *error_word, int flags, kda_stream_t stream) {
+    if (Dm != D) return KDA_ERR_UNSUPPORTED;
+    if (flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BETA_SIGMOID | KDA_FLAG_CONV_SILU)) return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
+    if (N < 1 || H < 1 || W < 1 || W > 8) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)N * H >= (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
+    if (!(g_min >= -5.0f && g_min < 0.0f)) return KDA_ERR_INVALID_ARG;
+    if (!(o_norm_eps >= 0.0f) || o_norm_eps > 1e30f) return KDA_ERR_INVALID_ARG;
+    if (!state || !q || !k || !v || !z || !beta || !A || !o) return KDA_ERR_INVALID_ARG;
+    if (!conv_w || !conv_state || !o_gate || !o_norm_w) return KDA_ERR_INVALID_ARG;
+    if (W > 1 && (!cache_q || !cache_k || !cache_v || !cache_z || !cache_beta)) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(z) ||
+        !aligned16(o) || !aligned16(cache_q) || !aligned16(cache_k) || !aligned16(cache_v) ||
+        !aligned16(cache_z) || !aligned16(conv_w) || !aligned16(conv_state))
+        return KDA_ERR_INVALID_ARG;
+    note_begin((cudaStream_t)stream);
+    const DecFuse fz{conv_w, conv_state, o_gate, o_norm_w, o_norm_eps};
+    return launch_decode(state, q, k, v, z, beta, A, cache_q, cache_k, cache_v, cache_z, cache_beta,
+                         num_accepted, N, H, W, dtype, g_min, o, error_word, flags, &fz,
+                         (cudaStream_t)stream);
 }
 
 int kda_read_device_error(const void *workspace, int32_t *code, kda_stream_t stream) {

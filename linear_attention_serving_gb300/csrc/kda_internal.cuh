@@ -278,9 +278,18 @@ int launch_fused_tc(const void *q, const void *k, const void *v, const float *z,
 int device_sm_count();
 int launch_compose(const Plan &p, int H, int n_seg, const float *pairs, float *s_enter,
                    cudaStream_t s);
+// Extra operands of the fused decode step.
+struct DecFuse {
+    const float *conv_w;      // [3][H][D][4]: q, k, v taps, tap 3 on the current token
+    float *conv_state;        // [N][H][3][3][D]: q, k, v x the last three inputs, oldest first
+    const float *o_gate;      // [N][W][H][D] output-gate logits
+    const float *o_norm_w;    // [D]
+    float o_norm_eps;
+};
+// fz == nullptr runs the plain decode step.
 int launch_decode(float *state, const void *q, const void *k, const void *v, const float *z,
                   const float *beta, const float *A, void *cq, void *ck, void *cv, float *cz,
                   float *cb, const int32_t *nacc, int N, int H, int W, int dtype, float g_min,
-                  void *o, int32_t *err, int flags, cudaStream_t s);
+                  void *o, int32_t *err, int flags, const DecFuse *fz, cudaStream_t s);
 
 }  // namespace kda

@@ -61,6 +61,9 @@ def load(build_if_missing: bool = True):
     lib.kda_segment_scan.restype = I
     lib.kda_decode_step.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, I, P]
     lib.kda_decode_step.restype = I
+    lib.kda_decode_step_fused.argtypes = [P, P, P, P, P, P, P, P, P, P, P, F, P, P, P, P, P, P,
+                                          I, I, I, I, I, F, P, P, I, P]
+    lib.kda_decode_step_fused.restype = I
     lib.kda_read_device_error.argtypes = [P, P, P]
     lib.kda_read_device_error.restype = I
     _lib = lib
@@ -123,6 +126,7 @@ def _n_seqs(cu_seqlens, n_seqs):
 
 KDA_FLAG_QK_L2NORM = 1
 KDA_FLAG_BETA_SIGMOID = 2
+KDA_FLAG_CONV_SILU = 4
 
 
 def _flags(qk_l2norm: bool, beta_sigmoid: bool) -> int:
@@ -228,6 +232,40 @@ def decode_step(state, q, k, v, z, beta, A, cache, num_accepted=None, g_min=G_MI
                              float(g_min), _p(o), _p(error_word), _flags(qk_l2norm, beta_sigmoid),
                              _stream(q.device))
     _check(rc, "kda_decode_step")
+    return o
+
+
+def decode_step_fused(state, q, k, v, z, beta, A, conv_w, conv_state, o_gate, o_norm_w, cache,
+                      num_accepted=None, o_norm_eps=1e-6, g_min=G_MIN, error_word=None, out=None,
+                      qk_l2norm=False, beta_sigmoid=False, conv_silu=False):
+    """kda_decode_step_fused: the decode step with the short convolution of q, k, v in
+    front of the recurrence and the gated per-head output norm after it.
+    As decode_step, plus conv_w [3, H, 128, 4] fp32 (tap 3 on the current token),
+    conv_state [N, H, 3, 3, 128] fp32 (updated in place), o_gate [N, W, H, 128] fp32
+    (output-gate logits), o_norm_w [128] fp32.  q, k, v and the cache hold inputs before
+    the convolution.  Returns o [N, W, H, 128]."""
+    lib = load()
+    cq, ck, cv, cz, cb = cache if cache is not None else (None,) * 5
+    _contig(state, q, k, v, z, beta, A, conv_w, conv_state, o_gate, o_norm_w, cq, ck, cv, cz, cb,
+            num_accepted)
+    N, W, H, Dm = q.shape
+    if num_accepted is not None and num_accepted.dtype != torch.int32:
+        raise KDAError("num_accepted must be int32")
+    for t in (conv_w, conv_state, o_gate, o_norm_w):
+        if t.dtype != torch.float32:
+            raise KDAError("conv_w, conv_state, o_gate and o_norm_w must be float32")
+    if tuple(conv_w.shape) != (3, H, Dm, 4) or tuple(conv_state.shape) != (N, H, 3, 3, Dm):
+        raise KDAError("conv_w must be [3, H, D, 4] and conv_state [N, H, 3, 3, D]")
+    if tuple(o_gate.shape) != (N, W, H, Dm) or tuple(o_norm_w.shape) != (Dm,):
+        raise KDAError("o_gate must be [N, W, H, D] and o_norm_w [D]")
+    o = out if out is not None else torch.empty_like(q)
+    flags = _flags(qk_l2norm, beta_sigmoid) | (KDA_FLAG_CONV_SILU if conv_silu else 0)
+    rc = lib.kda_decode_step_fused(_p(state), _p(q), _p(k), _p(v), _p(z), _p(beta), _p(A), _p(conv_w),
+                                   _p(conv_state), _p(o_gate), _p(o_norm_w), float(o_norm_eps), _p(cq),
+                                   _p(ck), _p(cv), _p(cz), _p(cb), _p(num_accepted), N, H, Dm, W,
+                                   _dtype_code(q), float(g_min), _p(o), _p(error_word), flags,
+                                   _stream(q.device))
+    _check(rc, "kda_decode_step_fused")
     return o
 
 

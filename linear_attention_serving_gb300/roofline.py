@@ -63,12 +63,23 @@ def decode_step_bytes(N: int, H: int, W: int, accepted_total: int, in_bytes: int
                       D: int = D) -> int:
     """Bytes one decode step must move: the fp32 state once in and once out
     (8 D^2 per sequence and head), the window's projected inputs (q, k, v in
-    `in_bytes`, z fp32, beta fp32), the replayed cache entries, the new cache
-    entries and the outputs."""
+    `in_bytes`, z fp32, beta fp32), the replayed cache entries (a replayed token
+    needs no q), the new cache entries and the outputs."""
     per_tok = 3 * D * in_bytes + D * 4 + 4
     state = N * H * 8 * D * D
     window = N * W * H * per_tok
-    replay = accepted_total * H * per_tok
+    replay = accepted_total * H * (per_tok - D * in_bytes)
     cache_w = N * (W - 1) * H * per_tok
     out = N * W * H * D * in_bytes
     return state + window + replay + cache_w + out
+
+
+def decode_fused_step_bytes(N: int, H: int, W: int, accepted_total: int, in_bytes: int = 4,
+                            D: int = D) -> int:
+    """Bytes of one fused decode step: those of the plain step, plus the replayed
+    tokens' q (the convolution state of q needs it), the fp32 convolution state
+    once in and once out (3 x 3 x D per sequence and head), the output-gate logits
+    (fp32, per window token) and the convolution and norm weights once."""
+    extra = (accepted_total * H * D * in_bytes + N * H * 2 * 9 * D * 4 + N * W * H * D * 4
+             + 3 * H * D * 4 * 4 + D * 4)
+    return decode_step_bytes(N, H, W, accepted_total, in_bytes, D) + extra

@@ -118,6 +118,29 @@ def test_segment_scan_and_decode_reject_bad_arguments():
     assert dec(state=None) == 1
     assert dec(cq=None) == 1
     assert dec(flags=8) == 1
+    assert dec(flags=4) == 1  # the convolution option belongs to the fused step
+
+
+def test_decode_fused_rejects_bad_arguments():
+    lib = kda.load()
+    ALIGNED_BAD = 0x1008  # 8-byte aligned only
+
+    def dec(**kw):
+        return lib.kda_decode_step_fused(
+            FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, kw.get("conv_w", FAKE), kw.get("conv_state", FAKE),
+            kw.get("o_gate", FAKE), kw.get("o_norm_w", FAKE), kw.get("eps", 1e-6), kw.get("cq", FAKE), FAKE,
+            FAKE, FAKE, FAKE, None, kw.get("N", 4), 2, kw.get("D", 128), kw.get("W", 5), kw.get("dt", 1),
+            kw.get("g_min", -5.0), FAKE, None, kw.get("flags", 0), None)
+
+    assert dec(D=64) == 2
+    assert dec(W=9) == 1 and dec(W=0) == 1 and dec(N=0) == 1
+    assert dec(dt=7) == 1
+    assert dec(g_min=-6.0) == 1
+    assert dec(eps=-1.0) == 1 and dec(eps=float("nan")) == 1
+    for name in ("conv_w", "conv_state", "o_gate", "o_norm_w", "cq"):
+        assert dec(**{name: None}) == 1, name
+    assert dec(conv_w=ALIGNED_BAD) == 1 and dec(conv_state=ALIGNED_BAD) == 1
+    assert dec(flags=8) == 1
 
 
 def test_binding_rejects_wrong_dtypes_on_cpu_tensors():

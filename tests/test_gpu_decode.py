@@ -113,3 +113,103 @@ def test_decode_input_options(dtype):
                      w["z"][:, 1:].contiguous(), br[:, 1:].contiguous())
         for c, rc in zip(cache, raw_cache):
             assert torch.equal(c.cpu(), rc.to(c.dtype)), f"step {step}: cache"
+
+
+# ---------------------------------------------------------------- fused step
+
+FUSED_OPTS = dict(qk_l2norm=True, beta_sigmoid=True, conv_silu=True)
+
+
+def run_fused_steps(N, H, W, dtype, steps, seed, sample=None, opts=FUSED_OPTS, eps=1e-6, scale_qk=1.0):
+    """kda_decode_step_fused against oracle.decode_step_fused over several steps with
+    replay: outputs and states within the tolerance; the cache and the convolution
+    state (pre-convolution inputs) exact."""
+    state = kda_synth.decode_state(N, H, seed, std=0.05, device=DEV)
+    A = kda_synth.decode_A(H, seed, A_std=0.5, device=DEV)
+    prm = kda_synth.decode_fused_params(H, seed, device=DEV)
+    cs = kda_synth.decode_conv_state(N, H, seed, device=DEV)
+    cache = empty_cache(N, W, H, dtype)
+    idx = torch.arange(N) if sample is None else torch.tensor(sample)
+    ref_state, ref_cs = state.cpu()[idx], cs.cpu()[idx]
+    if scale_qk != 1.0:
+        ref_cs[:, :, :2] *= scale_qk
+        cs[:, :, :2] *= scale_qk
+    ref_cache = tuple(c.cpu()[idx] for c in cache)
+    tol_o, tol_s = (1e-4, 1e-4) if dtype == "f32" else TOL["bf16"]
+    t = kda_synth.TORCH_DTYPE[dtype]
+    for step in range(steps):
+        w = kda_synth.decode_fused_window(N, W, H, step, seed, dtype, z_std=1.5, device=DEV)
+        if scale_qk != 1.0:
+            w["q"] = (w["q"].float() * scale_qk).to(t)
+            w["k"] = (w["k"].float() * scale_qk).to(t)
+        if not opts.get("beta_sigmoid"):
+            w["beta"] = torch.sigmoid(w["beta"])
+        nacc = None if step == 0 else w["num_accepted"]
+        o = kda.decode_step_fused(state, w["q"], w["k"], w["v"], w["z"], w["beta"], A, prm["conv_w"], cs,
+                                  w["o_gate"], prm["o_norm_w"], cache, num_accepted=nacc, o_norm_eps=eps,
+                                  **opts)
+        torch.cuda.synchronize()
+        sel = lambda x: x.cpu()[idx]
+        o_ref, ref_state, ref_cache, ref_cs = oracle.decode_step_fused(
+            ref_state, sel(w["q"]), sel(w["k"]), sel(w["v"]), sel(w["z"]), sel(w["beta"]), A.cpu(),
+            prm["conv_w"].cpu(), ref_cs, sel(w["o_gate"]), prm["o_norm_w"].cpu(), eps, *ref_cache,
+            num_accepted=None if nacc is None else sel(nacc), **opts)
+        assert rel_fro(o.cpu()[idx], o_ref) <= tol_o, f"step {step}: o"
+        assert rel_fro(state.cpu()[idx], ref_state) <= tol_s, f"step {step}: state"
+        assert torch.equal(cs.cpu()[idx].double(), torch.from_numpy(ref_cs)), f"step {step}: conv state"
+        for c, rc in zip(cache, ref_cache):
+            assert torch.equal(c.cpu()[idx].double(), torch.from_numpy(rc)), f"step {step}: cache"
+    return o
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_fused_steps_small(dtype):
+    run_fused_steps(N=7, H=3, W=5, dtype=dtype, steps=4, seed=70)
+
+
+@pytest.mark.parametrize("W", [1, 2, 8])
+def test_decode_fused_window_sizes(W):
+    run_fused_steps(N=5, H=2, W=W, dtype="f32", steps=3, seed=71 + W)
+
+
+def test_decode_fused_without_options():
+    """No flags: plain convolution, beta as given, q and k not normalised (the inputs are
+    scaled down so that the convolved keys keep the delta rule contractive)."""
+    run_fused_steps(N=6, H=2, W=5, dtype="f32", steps=3, seed=75, opts={}, scale_qk=0.125)
+
+
+def test_decode_fused_l2norm_only():
+    run_fused_steps(N=6, H=2, W=5, dtype="f32", steps=3, seed=76, opts=dict(qk_l2norm=True, beta_sigmoid=True))
+
+
+def test_decode_fused_b256_h96_full_size():
+    """N=256, H=96, W=5, fp32, the full-size fused launch; sampled sequences against the oracle."""
+    run_fused_steps(N=256, H=96, W=5, dtype="f32", steps=2, seed=5, sample=[0, 1, 77, 128, 200, 255])
+
+
+def test_decode_fused_out_of_range_keeps_sequence():
+    N, H, W = 4, 2, 5
+    state = kda_synth.decode_state(N, H, 77, device=DEV)
+    prm = kda_synth.decode_fused_params(H, 77, device=DEV)
+    cs = kda_synth.decode_conv_state(N, H, 77, device=DEV)
+    before, cs_before = state.clone(), cs.clone()
+    A = torch.zeros(H, device=DEV)
+    cache = empty_cache(N, W, H, "f32")
+    w = kda_synth.decode_fused_window(N, W, H, 0, 77, "f32", device=DEV)
+    nacc = torch.tensor([0, 9, -1, 4], dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda.decode_step_fused(state, w["q"], w["k"], w["v"], w["z"], w["beta"], A, prm["conv_w"], cs, w["o_gate"],
+                          prm["o_norm_w"], cache, num_accepted=nacc, error_word=err, **FUSED_OPTS)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 2
+    for b in (1, 2):
+        assert torch.equal(state[b], before[b]) and torch.equal(cs[b], cs_before[b])
+    assert not torch.equal(state[0], before[0]) and not torch.equal(cs[3], cs_before[3])
+
+
+def test_decode_fused_deterministic():
+    outs = []
+    for _ in range(2):
+        N, H, W = 8, 4, 5
+        outs.append(run_fused_steps(N=N, H=H, W=W, dtype="f32", steps=2, seed=79).cpu())
+    assert torch.equal(outs[0], outs[1])
