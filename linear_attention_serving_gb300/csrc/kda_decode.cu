@@ -35,6 +35,15 @@
 // sigmoid output gate.  Per item it adds the convolution state to the rows'
 // bulk copy, reads the convolution weights of the head, and keeps the window's
 // raw outputs and gate factors in shared memory for a final pass.
+//
+// Token prep.  The plain step prepares the step's tokens in one pass over the
+// 128 channels.  With input options or the fusion it runs in two phases: all
+// 256 threads take a token half each (convolution sliding in registers, gate
+// factor, squared norms per warp), then the channel threads form the
+// cumulative decay and the scaled vectors while the others write the
+// convolution state and the output-gate factors.  Input options (beta's
+// sigmoid included) are applied once per item and token, never in the
+// recurrence loop.
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 
@@ -159,6 +168,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
     extern __shared__ __align__(128) uint8_t smdyn[];
     __shared__ uint64_t full_bar;
     __shared__ float sbeta[2][2 * MAX_W];
+    __shared__ float sbeff[OPTS ? 2 : 1][2 * MAX_W];  // OPTS: the betas the recurrence uses (after the sigmoid option)
     __shared__ __align__(16) float scommit[VPAD];
     __shared__ float snorm[2 * MAX_W][4][2];  // KDA_FLAG_QK_L2NORM: squared norms per token and warp
     __shared__ float sqo[MAX_W][DEC_THREADS / 32];  // FUSE: squared output sums per window token and warp
@@ -246,8 +256,14 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
         const int ntok = nacc + W;
         float *Sg = state + (size_t)item * D * D;
         float *sbt = sbeta[it & 1];
+        float *sbe = OPTS ? sbeff[it & 1] : sbt;
         if (tid < nacc) sbt[tid] = bc_cur;
         if (tid < W) sbt[nacc + tid] = bw_cur;
+        if (OPTS) {
+            // input option: beta logits through the sigmoid, once per item and token
+            if (tid < nacc) sbe[tid] = bsig ? 1.f / (1.f + expf(-bc_cur)) : bc_cur;
+            if (tid < W) sbe[nacc + tid] = bsig ? 1.f / (1.f + expf(-bw_cur)) : bw_cur;
+        }
 
         // state of this item: shared memory -> registers; then the state buffer
         // takes the next item's state while the token rows are still in use
@@ -261,105 +277,151 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
         __syncthreads();
         if (tid == 0 && next < n_items) issue_state<FUSE>(next, nacc_next, W, rowb, state, sm, L, &full_bar);
         const float eA = expf(A[h]);
-        if (tid < D) {
-            // channel c of every token: inputs, the cumulative decay s_t over the
-            // step's tokens, and the scaled vectors s_t k, k / s_t, s_t q
-            const int c = tid, vc = vidx(c);
-            if (FUSE) {
-                // short convolution of q, k, v over [state, replayed drafts, window]:
-                // y_t = sum_j w_j x_{t-3+j}; the convolved q, k go to qt, kt (scaled in
-                // place below), v to vt.  At t0 the last three inputs become the state.
-                const float4 wq = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)0 * H + h) * D + c);
-                const float4 wk = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)1 * H + h) * D + c);
-                const float4 wv = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)2 * H + h) * D + c);
-                float xq0 = cst[0][0][c], xq1 = cst[0][1][c], xq2 = cst[0][2][c];
-                float xk0 = cst[1][0][c], xk1 = cst[1][1][c], xk2 = cst[1][2][c];
-                float xv0 = cst[2][0][c], xv1 = cst[2][1][c], xv2 = cst[2][2][c];
-                float *cs_out = fz.conv_state + (size_t)item * (3 * CONV_HIST * D) + c;
-                for (int t = 0; t < ntok; ++t) {
-                    const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
-                    const float xq = to_f32(reinterpret_cast<const InT *>(slot)[c]);
-                    const float xk = to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
-                    const float xv = to_f32(reinterpret_cast<const InT *>(slot + 1024)[c]);
-                    float yq = fmaf(wq.w, xq, fmaf(wq.z, xq2, fmaf(wq.y, xq1, wq.x * xq0)));
-                    float yk = fmaf(wk.w, xk, fmaf(wk.z, xk2, fmaf(wk.y, xk1, wk.x * xk0)));
-                    float yv = fmaf(wv.w, xv, fmaf(wv.z, xv2, fmaf(wv.y, xv1, wv.x * xv0)));
-                    xq0 = xq1; xq1 = xq2; xq2 = xq;
-                    xk0 = xk1; xk1 = xk2; xk2 = xk;
-                    xv0 = xv1; xv1 = xv2; xv2 = xv;
-                    if (t == nacc) {
-                        cs_out[0 * D] = xq0; cs_out[1 * D] = xq1; cs_out[2 * D] = xq2;
-                        cs_out[3 * D] = xk0; cs_out[4 * D] = xk1; cs_out[5 * D] = xk2;
-                        cs_out[6 * D] = xv0; cs_out[7 * D] = xv1; cs_out[8 * D] = xv2;
-                    }
-                    if (silu) {
-                        yq = yq / (1.f + expf(-yq));
-                        yk = yk / (1.f + expf(-yk));
-                        yv = yv / (1.f + expf(-yv));
-                    }
-                    qt[t][vc] = yq;
-                    kt[t][vc] = yk;
-                    vt[t][c] = yv;
-                }
-            }
-            if (l2norm) {
-                // input option: squared norms of q and k over the 128 channels
-                // (replayed tokens carry no q)
-                for (int t = 0; t < ntok; ++t) {
-                    const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
-                    const float qq = t < nacc ? 0.f : FUSE ? qt[t][vc] : to_f32(reinterpret_cast<const InT *>(slot)[c]);
-                    const float kk = FUSE ? kt[t][vc] : to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
-                    float pq = qq * qq, pk = kk * kk;
-#pragma unroll
-                    for (int m = 16; m > 0; m >>= 1) {
-                        pq += __shfl_xor_sync(0xffffffffu, pq, m);
-                        pk += __shfl_xor_sync(0xffffffffu, pk, m);
-                    }
-                    if (lane == 0) {
-                        snorm[t][warp][0] = pq;
-                        snorm[t][warp][1] = pk;
-                    }
-                }
-                asm volatile("bar.sync 1, 128;" ::: "memory");  // the channel threads (warps 0-3) only
-            }
-            float sc = 1.f;
-            for (int t = 0; t < ntok; ++t) {
+        if (tid == D) {
+            // the new drafts' projected inputs replace this sequence's cache slots
+            // (the prep reads the raw rows but never writes them)
+            for (int t = nacc + 1; t < ntok; ++t) {
                 const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
-                float qq = t < nacc ? 0.f : FUSE ? qt[t][vc] : to_f32(reinterpret_cast<const InT *>(slot)[c]);
-                float kk = FUSE ? kt[t][vc] : to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
-                if (l2norm) {
-                    qq *= rsqrtf(snorm[t][0][0] + snorm[t][1][0] + snorm[t][2][0] + snorm[t][3][0] + L2NORM_EPS);
-                    kk *= rsqrtf(snorm[t][0][1] + snorm[t][1][1] + snorm[t][2][1] + snorm[t][3][1] + L2NORM_EPS);
+                const size_t row = ((size_t)b * (W - 1) + (t - nacc - 1)) * H + h;
+                bulk_s2g(cq + row * D, slot, rowb);
+                bulk_s2g(ck + row * D, slot + 512, rowb);
+                bulk_s2g(cv + row * D, slot + 1024, rowb);
+                bulk_s2g(cz + row * D, slot + 1536, 512);
+            }
+            bulk_commit();
+        }
+        // FUSE: the window's output-gate logits, loaded here and used after phase A
+        float gl[MAX_W];
+        if (FUSE && tid >= D) {
+#pragma unroll
+            for (int j = 0; j < MAX_W; ++j)
+                gl[j] = j < W ? __ldg(fz.o_gate + (((size_t)b * W + j) * H + h) * D + (tid - D)) : 0.f;
+        }
+        if (!FUSE && !OPTS) {
+            // plain step: channel c of every token in one pass (inputs, the
+            // cumulative decay s_t over the step's tokens, s_t k, k / s_t, s_t q)
+            if (tid < D) {
+                const int c = tid, vc = vidx(c);
+                float sc = 1.f;
+                for (int t = 0; t < ntok; ++t) {
+                    const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
+                    float qq = t < nacc ? 0.f : to_f32(reinterpret_cast<const InT *>(slot)[c]);
+                    float kk = to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
+                    const float zz = reinterpret_cast<const float *>(slot + 1536)[c];
+                    sc *= expf(kda_gate(g_min, eA, zz));
+                    kt[t][vc] = kk * sc;
+                    kh[t][vc] = __fdividef(kk, sc);
+                    qt[t][vc] = qq * sc;
+                    vt[t][c] = to_f32(reinterpret_cast<const InT *>(slot + 1024)[c]);
+                    if (t == nacc) scommit[vc] = sc;
                 }
-                const float zz = reinterpret_cast<const float *>(slot + 1536)[c];
-                sc *= expf(kda_gate(g_min, eA, zz));
-                kt[t][vc] = kk * sc;
-                kh[t][vc] = __fdividef(kk, sc);
-                qt[t][vc] = qq * sc;
-                if (!FUSE) vt[t][c] = to_f32(reinterpret_cast<const InT *>(slot + 1024)[c]);
-                if (t == nacc) scommit[vc] = sc;
             }
         } else {
-            if (tid == D) {
-                // the new drafts' projected inputs replace this sequence's cache slots
-                for (int t = nacc + 1; t < ntok; ++t) {
+            {
+                // phase A, token-parallel: warps 0-3 take the first half of the step's
+                // tokens and warps 4-7 the second, a warp = 32 channels of one token.
+                // The (convolved) inputs go to qt, kt, vt, the decay factor exp(g_t)
+                // to kh, and the squared norms of q and k to snorm.
+                const int c = tid & (D - 1), vc = vidx(c), quarter = warp & 3;
+                const int tmid = (ntok + 1) >> 1;
+                const int t_begin = tid < D ? 0 : tmid, t_end = tid < D ? tmid : ntok;
+                float4 wq, wk, wv;
+                float hq0, hq1, hq2, hk0, hk1, hk2, hv0, hv1, hv2;  // FUSE: x_{t-3}, x_{t-2}, x_{t-1}
+                if (FUSE) {
+                    wq = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)0 * H + h) * D + c);
+                    wk = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)1 * H + h) * D + c);
+                    wv = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)2 * H + h) * D + c);
+                    // the three inputs before t_begin: token rows, or the convolution state
+                    // for stream positions before the first token
+                    auto hist = [&](int x, int ps) {
+                        return ps >= 0 ? to_f32(reinterpret_cast<const InT *>(sm + L.raw + (size_t)ps * ROW_SLOT + x * 512)[c])
+                                       : cst[x][CONV_HIST + ps][c];
+                    };
+                    hq0 = hist(0, t_begin - 3), hq1 = hist(0, t_begin - 2), hq2 = hist(0, t_begin - 1);
+                    hk0 = hist(1, t_begin - 3), hk1 = hist(1, t_begin - 2), hk2 = hist(1, t_begin - 1);
+                    hv0 = hist(2, t_begin - 3), hv1 = hist(2, t_begin - 2), hv2 = hist(2, t_begin - 1);
+                }
+                for (int t = t_begin; t < t_end; ++t) {
                     const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
-                    const size_t row = ((size_t)b * (W - 1) + (t - nacc - 1)) * H + h;
-                    bulk_s2g(cq + row * D, slot, rowb);
-                    bulk_s2g(ck + row * D, slot + 512, rowb);
-                    bulk_s2g(cv + row * D, slot + 1024, rowb);
-                    bulk_s2g(cz + row * D, slot + 1536, 512);
+                    // replayed tokens of the plain step carry no q (never read below)
+                    float xq = to_f32(reinterpret_cast<const InT *>(slot)[c]);
+                    float xk = to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
+                    float xv = to_f32(reinterpret_cast<const InT *>(slot + 1024)[c]);
+                    if (FUSE) {
+                        // short convolution over [state, replayed drafts, window]:
+                        // y_t = sum_j w_j x_{t-3+j}, tap 3 on the current token
+                        float yq = fmaf(wq.w, xq, fmaf(wq.z, hq2, fmaf(wq.y, hq1, wq.x * hq0)));
+                        float yk = fmaf(wk.w, xk, fmaf(wk.z, hk2, fmaf(wk.y, hk1, wk.x * hk0)));
+                        float yv = fmaf(wv.w, xv, fmaf(wv.z, hv2, fmaf(wv.y, hv1, wv.x * hv0)));
+                        hq0 = hq1, hq1 = hq2, hq2 = xq;
+                        hk0 = hk1, hk1 = hk2, hk2 = xk;
+                        hv0 = hv1, hv1 = hv2, hv2 = xv;
+                        if (silu) {
+                            yq = __fdividef(yq, 1.f + __expf(-yq));
+                            yk = __fdividef(yk, 1.f + __expf(-yk));
+                            yv = __fdividef(yv, 1.f + __expf(-yv));
+                        }
+                        xq = yq;
+                        xk = yk;
+                        xv = yv;
+                    }
+                    qt[t][vc] = xq;
+                    kt[t][vc] = xk;
+                    vt[t][c] = xv;
+                    kh[t][vc] = expf(kda_gate(g_min, eA, reinterpret_cast<const float *>(slot + 1536)[c]));
+                    if (l2norm) {
+                        // input option: squared norms over the 128 channels (no q for replays)
+                        float pq = t < nacc ? 0.f : xq * xq, pk = xk * xk;
+#pragma unroll
+                        for (int m = 16; m > 0; m >>= 1) {
+                            pq += __shfl_xor_sync(0xffffffffu, pq, m);
+                            pk += __shfl_xor_sync(0xffffffffu, pk, m);
+                        }
+                        if (lane == 0) {
+                            snorm[t][quarter][0] = pq;
+                            snorm[t][quarter][1] = pk;
+                        }
+                    }
                 }
-                bulk_commit();
             }
-            if (FUSE) {
-                // output gate: norm weight x sigmoid(gate logit) per window token and channel
-                const int c = tid - D;
-                const float wn = __ldg(fz.o_norm_w + c);
-                for (int j = 0; j < W; ++j) {
-                    const float gl = __ldg(fz.o_gate + (((size_t)b * W + j) * H + h) * D + c);
-                    sg[j][c] = wn / (1.f + expf(-gl));
+            __syncthreads();
+            if (tid < D) {
+                // phase B, channel c: the cumulative decay s_t over the step's tokens
+                // and the scaled vectors s_t k, k / s_t, s_t q
+                const int c = tid, vc = vidx(c);
+                float sc = 1.f;
+                for (int t = 0; t < ntok; ++t) {
+                    sc *= kh[t][vc];
+                    float qq = t < nacc ? 0.f : qt[t][vc];
+                    float kk = kt[t][vc];
+                    if (l2norm) {
+                        qq *= rsqrtf(snorm[t][0][0] + snorm[t][1][0] + snorm[t][2][0] + snorm[t][3][0] + L2NORM_EPS);
+                        kk *= rsqrtf(snorm[t][0][1] + snorm[t][1][1] + snorm[t][2][1] + snorm[t][3][1] + L2NORM_EPS);
+                    }
+                    kt[t][vc] = kk * sc;
+                    kh[t][vc] = __fdividef(kk, sc);
+                    qt[t][vc] = qq * sc;
+                    if (t == nacc) scommit[vc] = sc;
                 }
+            } else if (FUSE) {
+                const int c = tid - D;
+                // the convolution state becomes the three inputs ending at t0 (stream
+                // positions nacc - 2 .. nacc; negative ones are still in the old state)
+                float *cs_out = fz.conv_state + (size_t)item * (3 * CONV_HIST * D) + c;
+#pragma unroll
+                for (int x = 0; x < 3; ++x)
+#pragma unroll
+                    for (int j = 0; j < CONV_HIST; ++j) {
+                        const int ps = nacc - (CONV_HIST - 1) + j;
+                        cs_out[(x * CONV_HIST + j) * D] =
+                            ps >= 0 ? to_f32(reinterpret_cast<const InT *>(sm + L.raw + (size_t)ps * ROW_SLOT + x * 512)[c])
+                                    : cst[x][CONV_HIST + ps][c];
+                    }
+                // output gate: norm weight x sigmoid(gate logit) per window token and channel
+                const float wn = __ldg(fz.o_norm_w + c);
+#pragma unroll
+                for (int j = 0; j < MAX_W; ++j)
+                    if (j < W) sg[j][c] = wn / (1.f + expf(-gl[j]));
             }
         }
         if (tid < W - 1) cb[((size_t)b * (W - 1) + tid) * H + h] = sbt[nacc + 1 + tid];
@@ -371,7 +433,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                                   &full_bar);
 
         // the recurrence over replay + bonus + drafts
-        const float *bt = sbt;
+        const float *bt = sbe;
         for (int t = 0; t < ntok; ++t) {
             // two partial sums per column keep the FMA chains short
             float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
@@ -394,7 +456,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                 acc1 += __shfl_xor_sync(0xffffffffu, acc1, m);
             }
             const float2 vv = *reinterpret_cast<const float2 *>(&vt[t][col]);
-            const float bb = bsig ? 1.f / (1.f + __expf(-bt[t])) : bt[t];  // input option: beta logit
+            const float bb = bt[t];
             const float u0 = bb * (vv.x - acc0), u1 = bb * (vv.y - acc1);
 #pragma unroll
             for (int i = 0; i < DEC_R; i += 4) {
