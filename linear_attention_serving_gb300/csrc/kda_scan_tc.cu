@@ -2,17 +2,47 @@
 // kda_scan_body.cuh): one block per (document or segment, head, column block).
 // Few chains: 16-column blocks that store each chunk's entering state for the
 // output kernel.  Many chains: 64-column blocks that form the outputs of their
-// columns themselves (as the fused launch's chain blocks do).
+// columns themselves (as the fused launch's chain blocks do).  Packed documents
+// of unequal length start longest first (the document is the grid's slowest
+// dimension, ranked by chunk count), so that the last blocks to start hold
+// the shortest chains.
 #include "kda_scan_body.cuh"
 
 namespace kda {
 
 namespace {
 
+constexpr int LPT_MAX_DOCS = 64;  // documents ranked by length (more keep the index order)
+
+// The document of rank r when the n documents are ordered by chunk count, the
+// longest first (ties by index).  Every thread of the block gets the answer.
+__device__ __forceinline__ int doc_of_rank(const Plan &p, int n, int r) {
+    __shared__ int s_nc[LPT_MAX_DOCS];
+    __shared__ int s_doc;
+    const int t = threadIdx.x;
+    if (t == 0) s_doc = r;
+    if (t < n) s_nc[t] = p.doc_off[t + 1] - p.doc_off[t];
+    __syncthreads();
+    if (t < n) {
+        const int mine = s_nc[t];
+        int rank = 0;
+        for (int e = 0; e < n; ++e) rank += (s_nc[e] > mine) || (s_nc[e] == mine && e < t);
+        if (rank == r) s_doc = t;
+    }
+    __syncthreads();
+    return s_doc;
+}
+
 template <int N, int STAGES, int TPR, bool EMIT_O>
-__global__ void __launch_bounds__(ScanCfg<N, TPR, EMIT_O>::THREADS, 1) scan_tc_kernel(ScanArgs a) {
+__global__ void __launch_bounds__(ScanCfg<N, TPR, EMIT_O>::THREADS, 1) scan_tc_kernel(ScanArgs a, int lpt) {
     extern __shared__ uint8_t smraw[];
-    scan_block<N, STAGES, TPR, EMIT_O>(a, blockIdx.x, blockIdx.y, blockIdx.z * (N / 16), smraw, nullptr);
+    int unit = blockIdx.x, h = blockIdx.y, cb = blockIdx.z;
+    if (lpt) {
+        unit = doc_of_rank(a.plan, a.n_units, blockIdx.z);
+        h = blockIdx.x;
+        cb = blockIdx.y;
+    }
+    scan_block<N, STAGES, TPR, EMIT_O>(a, unit, h, cb * (N / 16), smraw, nullptr);
 }
 
 template <int N, int STAGES, int TPR, bool EMIT_O = false>
@@ -21,8 +51,9 @@ int launch_n(const ScanArgs &a, cudaStream_t s) {
     const size_t smem = scan_tc_smem_bytes<N, STAGES, EMIT_O>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return KDA_ERR_CUDA;
-    dim3 grid(a.n_units, a.H, a.ncols / N);
-    kern<<<grid, ScanCfg<N, TPR, EMIT_O>::THREADS, smem, s>>>(a);
+    const int lpt = a.mode == SCAN_DOCS && !a.plan.uniform && a.n_units > 1 && a.n_units <= LPT_MAX_DOCS;
+    const dim3 grid = lpt ? dim3(a.H, a.ncols / N, a.n_units) : dim3(a.n_units, a.H, a.ncols / N);
+    kern<<<grid, ScanCfg<N, TPR, EMIT_O>::THREADS, smem, s>>>(a, lpt);
     note_launch("scan_tc", s);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
