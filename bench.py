@@ -220,6 +220,47 @@ def bench_prefill(args, dev, ws, kda):
                 launches=launches, clocks=clk, inputs=(q, k, v, z, A, beta, cu, init), workload=w)
 
 
+def bench_prefill_variants(dev, kda, inputs, steps=10, warmup=3):
+    """The same prefill workload through the optional paths: the in-kernel input
+    options (q, k L2 norm and beta sigmoid), and state checkpoints every 512 tokens
+    into 16 pages.  Device time per call with an L2 flush before each, as the main
+    step; kernel names from the library's launch marks."""
+    q, k, v, z, A, beta, cu, init = inputs
+    T, H = q.shape[0], q.shape[1]
+    n_seqs = 1 if cu is None else cu.numel() - 1
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    wsp = torch.empty(kda.chunk_fwd_workspace_size(T, H, n_seqs, q.dtype), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    per_seq = T // 512
+    slots = torch.arange(n_seqs * per_seq, dtype=torch.int32, device=dev).reshape(n_seqs, per_seq)
+    pages = torch.empty((n_seqs * per_seq, H, 128, 128), dtype=torch.float32, device=dev)
+    calls = {
+        "input_options": lambda: kda.chunk_fwd(q, k, v, z, A, beta, cu_seqlens=cu, init_state=init, workspace=wsp,
+                                               out=o, qk_l2norm=True, beta_sigmoid=True),
+        "checkpoints_every_512": lambda: kda.chunk_fwd_ckpt(q, k, v, z, A, beta, 512, slots, pages, cu_seqlens=cu,
+                                                            init_state=init, workspace=wsp, out=o),
+    }
+    out = {}
+    for name, fn in calls.items():
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        kda.profile_enable(True)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            torch.cuda._sleep(HOST_COVER_CYCLES)
+            evs[i][0].record()
+            fn()
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        marks = kda.profile_collect()
+        kda.profile_enable(False)
+        ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+        out[name] = {"ms_per_step": ms, "kernels": sorted(kernel_times(marks))}
+    return out
+
+
 def e2e_prefill(args, dev, kda, inputs):
     """Through the public API with inputs in pinned host memory: every step copies
     its inputs host -> device, runs kda_chunk_fwd, and reads o and the final state
@@ -459,6 +500,13 @@ def main():
         "clocks": pf["clocks"],
     }
     if rank == 0 and not args.no_e2e:
+        pv = bench_prefill_variants(dev, kda, pf["inputs"])
+        ckpt_bytes = (T // 512) * pf["n_seqs"] * H * 128 * 128 * 4
+        for name, r in pv.items():
+            b_ = path_bytes + (ckpt_bytes if name.startswith("checkpoints") else 0)
+            r["tokens_per_s"] = T / (r["ms_per_step"] / 1e3)
+            r["roofline_frac"] = b_ / (r["ms_per_step"] / 1e3) / 1e9 / hbm
+        line["prefill_variants"] = pv
         ms, h2d, d2h = e2e_prefill(args, dev, kda, pf["inputs"])
         line["e2e"] = {"value": T * ws / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": ms}

@@ -26,7 +26,9 @@ namespace {
 constexpr int FUSED_N = 64, FUSED_STAGES = 3, FUSED_TPR = 2;
 constexpr int FUSED_SLICES = D / FUSED_N;  // chain blocks per (document, head)
 
-template <bool OPTS>
+// OPTS: input options; CKPT: state checkpoints (separate instantiations, so
+// that the default launch keeps its registers).
+template <bool OPTS, bool CKPT>
 __global__ void __launch_bounds__(PT_THREADS, 1)
 fused_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z, const float *__restrict__ A,
@@ -46,7 +48,7 @@ fused_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
         const int per_doc = H * FUSED_SLICES;
         const int doc = blockIdx.x / per_doc, rem = blockIdx.x - doc * per_doc;
         const int h = rem / FUSED_SLICES, zc = rem - h * FUSED_SLICES;
-        scan_block<FUSED_N, FUSED_STAGES, FUSED_TPR, true>(sa, doc, h, zc * (FUSED_N / 16), smraw, ready);
+        scan_block<FUSED_N, FUSED_STAGES, FUSED_TPR, true, CKPT>(sa, doc, h, zc * (FUSED_N / 16), smraw, ready);
     }
 }
 
@@ -60,7 +62,6 @@ int launch_fused_tc(const void *q, const void *k, const void *v, const float *z,
     const long long n_chain = (long long)sa.n_units * H * FUSED_SLICES;
     // the chains may take at most a quarter of the SMs, and there must be units to prepare
     if (sa.mode != SCAN_DOCS || n_chain < 1 || n_chain > n_sm / 4 || (long long)p.max_chunks * H < 1) return KDA_OK;
-    if (sa.ckpt) return KDA_OK;  // state checkpoints: the three-kernel path writes them
     int dev = 0, coop = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop)
@@ -68,7 +69,8 @@ int launch_fused_tc(const void *q, const void *k, const void *v, const float *z,
     constexpr size_t chain_smem = scan_tc_smem_bytes<FUSED_N, FUSED_STAGES, true>();
     static_assert(ScanCfg<FUSED_N, FUSED_TPR, true>::THREADS <= PT_THREADS, "chain block fits the prep's block");
     const size_t smem = PREP_TC_SMEM > chain_smem ? PREP_TC_SMEM : chain_smem;
-    auto kern = p.flags ? fused_tc_kernel<true> : fused_tc_kernel<false>;
+    auto kern = p.flags ? (sa.ckpt ? fused_tc_kernel<true, true> : fused_tc_kernel<true, false>)
+                        : (sa.ckpt ? fused_tc_kernel<false, true> : fused_tc_kernel<false, false>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return KDA_ERR_CUDA;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, PT_THREADS, smem) != cudaSuccess ||

@@ -249,7 +249,7 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         // token's other 64 sit in the neighbouring warp)
         if (tid < 64) sbeta[tid] = b_next;
         if (l2norm) {
-#pragma unroll 1
+#pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const float2 qf = __bfloat1622float2(cin.q[r]), kf = __bfloat1622float2(cin.k[r]);
                 float pq = qf.x * qf.x + qf.y * qf.y, pk = kf.x * kf.x + kf.y * kf.y;

@@ -195,7 +195,9 @@ __device__ __forceinline__ void tmem_row(uint32_t taddr, float *out) {
 // `unit` (document or segment).  With `ready` non-null the producer waits,
 // before copying chunk c's record, until ready[c * H + h] is set (the record
 // is written by other blocks of the same launch).
-template <int N, int STAGES, int TPR, bool EMIT_O = false>
+// CKPT compiles the state checkpoints in (output blocks have them only in
+// their own instantiation, so that the default launch keeps its registers).
+template <int N, int STAGES, int TPR, bool EMIT_O = false, bool CKPT = !EMIT_O>
 __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, int zc16, uint8_t *smraw,
                                            const int *ready) {
     using ST = Stage<N, EMIT_O>;
@@ -376,9 +378,10 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
         __syncwarp();
         if (lane == 0) mbar_arrive(&sop_bar);
         const bool write_final = value_cols && a.final_state && a.phase != 1;
-        // checkpoints: not in output blocks (the fused launch leaves calls with
-        // checkpoints to the three-kernel path)
-        const bool write_ckpt = !EMIT_O && value_cols && a.ckpt && a.phase != 1;
+        const bool write_ckpt = CKPT && value_cols && a.ckpt && a.phase != 1;
+        // one document per chain (SCAN_DOCS): its checkpoints are counted down
+        // instead of derived from the chunk table at every chunk
+        int ck_left = a.ckpt_ic, ck_j = 0;
         bool ok = true;
         int stage = 0;
         uint32_t ph = 0;
@@ -428,10 +431,24 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
 #pragma unroll
                 for (int j = 0; j < NT; j += 4) *reinterpret_cast<float4 *>(f + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
             }
-            if (!EMIT_O && write_ckpt) {
+            if (CKPT && write_ckpt) {
                 // the state after this chunk, when it ends on a checkpoint position
-                const ChunkInfo cik = plan_chunk(p, c0 + i);
-                float *f = ckpt_row(a, cik, c0 + i, h, t);
+                // (only a full chunk does; a document's last chunk may be partial)
+                float *f = nullptr;
+                if (!segs) {
+                    if (--ck_left == 0) {
+                        ck_left = a.ckpt_ic;
+                        if (ck_j < a.ckpt_per_seq && (i + 1 < nchunks || plan_chunk(p, c0 + i).len == C)) {
+                            const int slot = a.ckpt_slot[(size_t)unit * a.ckpt_per_seq + ck_j];
+                            if (slot >= 0 && slot < a.ckpt_n_slots)
+                                f = a.ckpt + (((size_t)slot * a.H + h) * D + t) * D;
+                        }
+                        ++ck_j;
+                    }
+                } else {
+                    const ChunkInfo cik = plan_chunk(p, c0 + i);
+                    f = ckpt_row(a, cik, c0 + i, h, t);
+                }
                 if (f) {
                     f += pc;
 #pragma unroll

@@ -33,7 +33,7 @@ __device__ __forceinline__ int doc_of_rank(const Plan &p, int n, int r) {
     return s_doc;
 }
 
-template <int N, int STAGES, int TPR, bool EMIT_O>
+template <int N, int STAGES, int TPR, bool EMIT_O, bool CKPT>
 __global__ void __launch_bounds__(ScanCfg<N, TPR, EMIT_O>::THREADS, 1) scan_tc_kernel(ScanArgs a, int lpt) {
     extern __shared__ uint8_t smraw[];
     int unit = blockIdx.x, h = blockIdx.y, cb = blockIdx.z;
@@ -42,12 +42,12 @@ __global__ void __launch_bounds__(ScanCfg<N, TPR, EMIT_O>::THREADS, 1) scan_tc_k
         h = blockIdx.x;
         cb = blockIdx.y;
     }
-    scan_block<N, STAGES, TPR, EMIT_O>(a, unit, h, cb * (N / 16), smraw, nullptr);
+    scan_block<N, STAGES, TPR, EMIT_O, CKPT>(a, unit, h, cb * (N / 16), smraw, nullptr);
 }
 
-template <int N, int STAGES, int TPR, bool EMIT_O = false>
+template <int N, int STAGES, int TPR, bool EMIT_O = false, bool CKPT = !EMIT_O>
 int launch_n(const ScanArgs &a, cudaStream_t s) {
-    auto kern = scan_tc_kernel<N, STAGES, TPR, EMIT_O>;
+    auto kern = scan_tc_kernel<N, STAGES, TPR, EMIT_O, CKPT>;
     const size_t smem = scan_tc_smem_bytes<N, STAGES, EMIT_O>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return KDA_ERR_CUDA;
@@ -71,9 +71,9 @@ int launch_scan_tc(const ScanArgs &a, int n_sm, cudaStream_t s) {
         return (rc || !a.o || a.phase == 1) ? rc : launch_out_tc(a.plan, a.H, a.records, a.o, n_sm, s);
     }
     // many chains: 64-column blocks that also form the outputs of their columns
-    // (no checkpoints in those blocks: a call with checkpoints stores the states
-    // and forms the outputs in a second pass)
-    if (a.o && a.phase != 1 && a.ncols == D && !a.ckpt) return launch_n<64, 3, 2, true>(a, s);
+    // (checkpoints in an instantiation of their own)
+    if (a.o && a.phase != 1 && a.ncols == D)
+        return a.ckpt ? launch_n<64, 3, 2, true, true>(a, s) : launch_n<64, 3, 2, true, false>(a, s);
     const int rc = launch_n<64, 2, 2>(a, s);
     return (rc || !a.o || a.phase == 1) ? rc : launch_out_tc(a.plan, a.H, a.records, a.o, n_sm, s);
 }

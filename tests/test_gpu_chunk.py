@@ -193,12 +193,14 @@ def ckpt_reference(inp, cu, positions):
 @pytest.mark.parametrize("dtype,T,H,docs,interval", [
     ("f32", 1000, 3, None, 256), ("bf16", 1000, 3, None, 256),
     ("bf16", 1000, 2, [700, 300], 128), ("f32", 1000, 2, [700, 300], 128),
-    ("bf16", 8192, 1, None, 512)])
+    ("bf16", 8192, 1, None, 512), ("bf16", 6400, 16, [320] * 20, 128)])
 def test_checkpoints(dtype, T, H, docs, interval):
     """kda_chunk_fwd_ckpt: every marked (document, aligned position) page holds
     the oracle's state after that prefix; skipped and out-of-document entries
     leave their pages untouched; o and the final state are unchanged.  The
-    last case takes the automatic segments (the state comes from phase 3)."""
+    bf16 cases with few chains run the fused launch; 8192 x 1 takes the automatic
+    segments (the state comes from phase 3); 20 documents x 16 heads take the
+    scan blocks that form the outputs themselves."""
     cu = torch.tensor([0] + list(np.cumsum(docs)), dtype=torch.int32) if docs else None
     n = 1 if docs is None else len(docs)
     inp = kda_synth.prefill_inputs(T, H, dtype, seed=500 + T + H, z_std=0.5, init_std=0.05,
