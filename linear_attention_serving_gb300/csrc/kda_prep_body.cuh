@@ -249,19 +249,37 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         // token's other 64 sit in the neighbouring warp)
         if (tid < 64) sbeta[tid] = b_next;
         if (l2norm) {
+            // transpose reduction: eight token sums over the warp's 32 lanes in 9
+            // shuffles per tensor; lane l ends with token ((l >> 2) & 7)'s total
+            float pq[8], pk[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const float2 qf = __bfloat1622float2(cin.q[r]), kf = __bfloat1622float2(cin.k[r]);
-                float pq = qf.x * qf.x + qf.y * qf.y, pk = kf.x * kf.x + kf.y * kf.y;
+                pq[r] = qf.x * qf.x + qf.y * qf.y;
+                pk[r] = kf.x * kf.x + kf.y * kf.y;
+            }
+            const bool b4 = (lane & 16) != 0, b3 = (lane & 8) != 0, b2 = (lane & 4) != 0;
+            float q4[4], k4[4], q2[2], k2[2];
 #pragma unroll
-                for (int m = 16; m > 0; m >>= 1) {
-                    pq += __shfl_xor_sync(0xffffffffu, pq, m);
-                    pk += __shfl_xor_sync(0xffffffffu, pk, m);
-                }
-                if (lane == 0) {
-                    snorm[4 * (8 * rg + r) + (warp & 1)] = pq;
-                    snorm[4 * (8 * rg + r) + 2 + (warp & 1)] = pk;
-                }
+            for (int j = 0; j < 4; ++j) {  // keep tokens 4 b4 + j, send the other half
+                q4[j] = (b4 ? pq[j + 4] : pq[j]) + __shfl_xor_sync(0xffffffffu, b4 ? pq[j] : pq[j + 4], 16);
+                k4[j] = (b4 ? pk[j + 4] : pk[j]) + __shfl_xor_sync(0xffffffffu, b4 ? pk[j] : pk[j + 4], 16);
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {  // tokens 4 b4 + 2 b3 + j
+                q2[j] = (b3 ? q4[j + 2] : q4[j]) + __shfl_xor_sync(0xffffffffu, b3 ? q4[j] : q4[j + 2], 8);
+                k2[j] = (b3 ? k4[j + 2] : k4[j]) + __shfl_xor_sync(0xffffffffu, b3 ? k4[j] : k4[j + 2], 8);
+            }
+            float sq = (b2 ? q2[1] : q2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? q2[0] : q2[1], 4);
+            float sk = (b2 ? k2[1] : k2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? k2[0] : k2[1], 4);
+            sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+            sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+            sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+            sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+            if ((lane & 3) == 0) {
+                const int r = (lane >> 2) & 7;
+                snorm[4 * (8 * rg + r) + (warp & 1)] = sq;
+                snorm[4 * (8 * rg + r) + 2 + (warp & 1)] = sk;
             }
         }
         __syncthreads();
