@@ -125,8 +125,8 @@ int make_plan(const int32_t *cu, int n_seqs, int64_t T_total, void *ws, const Wo
 //                    the chains leave free (all SMs without the fused launch);
 //   segments         pay a second pass over the chain and the composition
 //                    (about 25 us per segment), so they win only when the
-//                    chain is over 1.5x the preparation; their count balances
-//                    chain length against composition, n = sqrt(chunks / 18).
+//                    chain is over 1.5x the preparation; their count is set
+//                    by the scan's waves (below).
 // Returns 0 for one chain per (document, head).
 int plan_segments(int64_t T_total, int H, int n_seqs, bool varlen, int dtype, int n_sm) {
     if (varlen || dtype != KDA_BF16 || T_total <= 0 || n_seqs < 1 || H < 1) return 0;
@@ -138,7 +138,16 @@ int plan_segments(int64_t T_total, int H, int n_seqs, bool varlen, int dtype, in
     const double prep_us = 10.3 * units / (double)(prep_sms > 0 ? prep_sms : 1);
     const double chain_us = 1.3 * (double)chunks;
     if (chain_us <= 1.5 * prep_us) return 0;
-    int64_t n = llround(sqrt((double)total / 18.0));
+    // Segment count, measured on GB300: the scan blocks run one per SM, so
+    // whole waves decide the time.  Take the most segments whose phase 3 (two
+    // 64-column blocks per (segment, head)) fits in one wave of the SMs, and
+    // phase 1 (four per pair) in two; more segments or an extra partial wave
+    // cost more than the shorter chains save.  At most sqrt(chunks / 6), where
+    // the composition (about 25 us per segment) outweighs the shorter chains
+    // (about 4 us per chunk over the three phases).
+    int64_t n = n_sm / (2LL * H);
+    const int64_t cap = llround(sqrt((double)total / 6.0));
+    if (n > cap) n = cap;
     if (n > 64) n = 64;
     if (n > total / 2) n = total / 2;
     return n >= 2 ? (int)n : 0;
