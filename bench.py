@@ -100,7 +100,8 @@ def traffic_for(kernel):
 
 
 class ClockSampler:
-    """nvidia-smi clocks sampled every 200 ms while the timed region runs."""
+    """nvidia-smi clocks sampled every 200 ms from the start of the timed region
+    until --clock-window seconds of the same load have run."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -198,6 +199,7 @@ def bench_prefill(args, dev, ws, kda):
     kda.profile_enable(True)
     launches0 = kda.launch_count()
     clocks.start()
+    t_clk = time.time()
     barrier(ws)
     torch.cuda.synchronize()
     for i in range(args.steps):
@@ -210,10 +212,17 @@ def bench_prefill(args, dev, ws, kda):
         evs[i][1].record()
     torch.cuda.synchronize()
     barrier(ws)
-    clk = clocks.stop()
     launches = kda.launch_count() - launches0
     marks = kda.profile_collect()
     kda.profile_enable(False)
+    # the timed steps last milliseconds, the clock samples come every 200 ms: the
+    # same step keeps running (untimed, after the marks are taken) until the
+    # samples cover --clock-window seconds of this load
+    while time.time() - t_clk < getattr(args, "clock_window", 0.0):
+        for _ in range(50):
+            step()
+        torch.cuda.synchronize()
+    clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     total_ms = max_over_ranks(sum(step_ms), ws, dev)
     return dict(T=T, H=H, n_seqs=n_seqs, total_ms=total_ms, step_ms=step_ms, marks=marks,
@@ -440,6 +449,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill_h16_t8k")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--clock-window", type=float, default=0.6,
+                    help="seconds of the prefill step the clock samples cover (0: the timed steps only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()

@@ -171,7 +171,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
     __shared__ float sbeff[OPTS ? 2 : 1][2 * MAX_W];  // OPTS: the betas the recurrence uses (after the sigmoid option)
     __shared__ __align__(16) float scommit[VPAD];
     __shared__ float snorm[2 * MAX_W][4][2];  // KDA_FLAG_QK_L2NORM: squared norms per token and warp
-    __shared__ float sqo[MAX_W][DEC_THREADS / 32];  // FUSE: squared output sums per window token and warp
+    __shared__ __align__(16) float sqo[MAX_W][DEC_THREADS / 32];  // FUSE: squared output sums per window token and warp
     const bool l2norm = OPTS && (flags & KDA_FLAG_QK_L2NORM) != 0;
     const bool bsig = OPTS && (flags & KDA_FLAG_BETA_SIGMOID) != 0;
     const bool silu = FUSE && OPTS && (flags & KDA_FLAG_CONV_SILU) != 0;
@@ -526,15 +526,17 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
         if (FUSE) {
             // gated RMS norm over the 128 value channels of each window token; the
             // next item's shared-memory writes come after its first barrier
-            for (int i = tid; i < W * (D / 2); i += DEC_THREADS) {
-                const int j = i / (D / 2), cc = 2 * (i % (D / 2));
-                float ss = 0.f;
-#pragma unroll
-                for (int w8 = 0; w8 < DEC_THREADS / 32; ++w8) ss += sqo[j][w8];
+            for (int i = tid; i < W * (D / 4); i += DEC_THREADS) {
+                const int j = i / (D / 4), cc = 4 * (i % (D / 4));
+                const float4 s0 = *reinterpret_cast<const float4 *>(&sqo[j][0]);
+                const float4 s1 = *reinterpret_cast<const float4 *>(&sqo[j][4]);
+                const float ss = ((s0.x + s0.y) + (s0.z + s0.w)) + ((s1.x + s1.y) + (s1.z + s1.w));
                 const float r = rsqrtf(ss * (1.f / D) + fz.o_norm_eps);
-                const float2 ov = *reinterpret_cast<const float2 *>(&ot[j][cc]);
-                const float2 gv = *reinterpret_cast<const float2 *>(&sg[j][cc]);
-                store_pair(o + (((size_t)b * W + j) * H + h) * D + cc, ov.x * r * gv.x, ov.y * r * gv.y);
+                const float4 ov = *reinterpret_cast<const float4 *>(&ot[j][cc]);
+                const float4 gv = *reinterpret_cast<const float4 *>(&sg[j][cc]);
+                InT *op = o + (((size_t)b * W + j) * H + h) * D + cc;
+                store_pair(op, ov.x * r * gv.x, ov.y * r * gv.y);
+                store_pair(op + 2, ov.z * r * gv.z, ov.w * r * gv.w);
             }
         }
     }
