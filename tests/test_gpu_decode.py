@@ -213,3 +213,35 @@ def test_decode_fused_deterministic():
         N, H, W = 8, 4, 5
         outs.append(run_fused_steps(N=N, H=H, W=W, dtype="f32", steps=2, seed=79).cpu())
     assert torch.equal(outs[0], outs[1])
+
+
+def test_decode_fused_unit_conv_matches_plain_step():
+    """Cross-path check: with the convolution a unit impulse on the current token and no
+    options, the fused step feeds the recurrence the same values as the plain step, so
+    the states and caches agree bit for bit, and its outputs are the plain outputs through
+    the gated per-head RMS norm."""
+    N, H, W, seed = 16, 4, 5, 81
+    state_a = kda_synth.decode_state(N, H, seed, device=DEV)
+    state_b = state_a.clone()
+    A = kda_synth.decode_A(H, seed, A_std=0.5, device=DEV)
+    cache_a, cache_b = empty_cache(N, W, H, "f32"), empty_cache(N, W, H, "f32")
+    conv_w = torch.zeros((3, H, 128, 4), device=DEV)
+    conv_w[..., 3] = 1.0
+    cs = torch.zeros((N, H, 3, 3, 128), device=DEV)
+    norm_w = kda_synth.decode_fused_params(H, seed, device=DEV)["o_norm_w"]
+    for step in range(3):
+        w = kda_synth.decode_window(N, W, H, step, seed, "f32", z_std=1.5, device=DEV)
+        gate = torch.randn((N, W, H, 128), generator=torch.Generator().manual_seed(step)).to(DEV)
+        nacc = None if step == 0 else w["num_accepted"]
+        args = [w[n] for n in ("q", "k", "v", "z", "beta")]
+        o_a = kda.decode_step(state_a, *args, A, cache_a, num_accepted=nacc)
+        o_b = kda.decode_step_fused(state_b, *args, A, conv_w, cs, gate, norm_w, cache_b, num_accepted=nacc,
+                                    o_norm_eps=1e-6)
+        torch.cuda.synchronize()
+        assert torch.equal(state_a, state_b), f"step {step}: state"
+        for ca, cb in zip(cache_a, cache_b):
+            assert torch.equal(ca, cb), f"step {step}: cache"
+        oa = o_a.double().cpu()
+        ref = oa / torch.sqrt(oa.pow(2).mean(-1, keepdim=True) + 1e-6) * norm_w.double().cpu() \
+            * torch.sigmoid(gate.double().cpu())
+        assert rel_fro(o_b.cpu(), ref) <= 1e-5, f"step {step}: o"
