@@ -7,7 +7,8 @@
 // folded into W, U0, Q', O0):
 //   U = U0 - W S,   O = O0 + Q' S,   S <- Diag(a_C) S + K_restore^T U.
 // The columns of S evolve independently (every update acts on the left), so a
-// block owns 32 state columns.  With 256 state columns the extra 128 columns
+// block owns 16 state columns (more blocks on the SMs, two per SM in shared
+// memory), a thread one row and 8 of them.  With 256 state columns the extra 128 columns
 // start from the identity and see V = 0: they carry the transition M of
 // "Kimi K3 模型结构（7）" eq. (17) (M I = M), giving the segment pair (M, S~).
 // Document starts reset the state ("文档边界").
@@ -20,7 +21,8 @@ namespace kda {
 namespace {
 
 constexpr int SCAN_THREADS = 256;
-constexpr int NC = 32;       // state columns per block
+constexpr int NC = 16;       // state columns per block
+constexpr int PER = NC / 2;  // state columns per thread (two threads per row)
 constexpr int LDA = 132;     // padded row stride of 128-wide fp32 tiles
 constexpr int LDS = NC + 1;  // padded row stride of NC-wide tiles
 
@@ -98,7 +100,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_simt_kernel(ScanArgs a) {
         return;
     }
 
-    const int row = tid >> 1, cc = (tid & 1) * 16;  // this thread's 16 outputs
+    const int row = tid >> 1, cc = (tid & 1) * PER;  // this thread's PER outputs
     for (int c = c0; c < c1; ++c) {
         const ChunkInfo ci = plan_chunk(p, c);
         const char *rec = (const char *)a.records +
@@ -114,17 +116,17 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_simt_kernel(ScanArgs a) {
         __syncthreads();
 
         // D1 = [W ; Q'] S   (row < 64: W S, row >= 64: Q' S)
-        float acc[16];
+        float acc[PER];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+        for (int j = 0; j < PER; ++j) acc[j] = 0.f;
         for (int kk = 0; kk < D; ++kk) {
             const float w = a1[row * LDA + kk];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[j] = fmaf(w, S[kk * LDS + cc + j], acc[j]);
+            for (int j = 0; j < PER; ++j) acc[j] = fmaf(w, S[kk * LDS + cc + j], acc[j]);
         }
         if (row < C) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < PER; ++j) {
                 const int g = col0 + cc + j;
                 const float u0 = (g < D) ? rec_u0(rec, row, g) : 0.f;
                 U[row * LDS + cc + j] = u0 - acc[j];
@@ -133,36 +135,36 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_simt_kernel(ScanArgs a) {
             const int r = row - C;
             float *orow = reinterpret_cast<float *>(a.o) + ((size_t)(ci.tok + r) * a.H + h) * D + col0 + cc;
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
+            for (int j = 0; j < PER; ++j)
                 orow[j] = rec_o0(rec, r, col0 + cc + j) + acc[j];
         }
         __syncthreads();
 
         // S <- Diag(a_C) S + K_restore^T U
-        float nacc[16];
+        float nacc[PER];
         const float dec = ac[row];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) nacc[j] = dec * S[row * LDS + cc + j];
+        for (int j = 0; j < PER; ++j) nacc[j] = dec * S[row * LDS + cc + j];
         for (int t = 0; t < C; ++t) {
             const float kv = kr[t * LDA + row];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) nacc[j] = fmaf(kv, U[t * LDS + cc + j], nacc[j]);
+            for (int j = 0; j < PER; ++j) nacc[j] = fmaf(kv, U[t * LDS + cc + j], nacc[j]);
         }
         __syncthreads();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) S[row * LDS + cc + j] = nacc[j];
+        for (int j = 0; j < PER; ++j) S[row * LDS + cc + j] = nacc[j];
 
         if (value_cols && a.final_state && a.phase != 1 && (ci.flags & CHUNK_LAST)) {
             float *f = a.final_state + (((size_t)ci.doc * a.H + h) * D + row) * D + col0 + cc;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) f[j] = nacc[j];
+            for (int j = 0; j < PER; ++j) f[j] = nacc[j];
         }
         if (value_cols && a.ckpt && a.phase != 1) {
             // the state after this chunk, when it ends on a checkpoint position
             float *f = ckpt_row(a, ci, c, h, row);
             if (f) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) f[col0 + cc + j] = nacc[j];
+                for (int j = 0; j < PER; ++j) f[col0 + cc + j] = nacc[j];
             }
         }
     }
