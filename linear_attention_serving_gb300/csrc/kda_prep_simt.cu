@@ -27,7 +27,11 @@ namespace {
 
 constexpr int LD = 132;         // padded row stride of [64][128] fp32 tiles
 constexpr int LDM = 65;         // padded row stride of [64][64] fp32 matrices
-constexpr int PREP_THREADS = 256;
+constexpr int PREP_THREADS = 512;
+constexpr int PT_ROWS = 4;                                  // rows of a thread's tile of the 64 x 128 products
+constexpr int PT_COLS = C * D / (PREP_THREADS * PT_ROWS);  // its columns (4 at 512 threads)
+constexpr int PT_CGROUPS = D / PT_COLS;                     // column groups across the threads
+static_assert(PT_COLS % 4 == 0 && C * D == PREP_THREADS * PT_ROWS * PT_COLS, "product tiling");
 
 struct PrepSmem {
     // float offsets
@@ -245,78 +249,86 @@ prep_simt_kernel(const float *__restrict__ q, const float *__restrict__ k, const
     }
     __syncthreads();
 
-    // thread tile of the 64 x 128 products: 4 rows x 8 columns
-    const int r0 = (tid >> 4) * 4, c0 = (tid & 15) * 8;
+    // thread tile of the 64 x 128 products: PT_ROWS rows x PT_COLS columns
+    const int r0 = (tid / PT_CGROUPS) * PT_ROWS, c0 = (tid % PT_CGROUPS) * PT_COLS;
 
     // 7. W = INV B1 -> xf
     {
-        float acc[4][8] = {};
-        for (int s = 0; s <= r0 + 3; ++s) {
-            const float4 b0 = *reinterpret_cast<const float4 *>(xk + s * LD + c0);
-            const float4 b1 = *reinterpret_cast<const float4 *>(xk + s * LD + c0 + 4);
-            const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        float acc[PT_ROWS][PT_COLS] = {};
+        for (int s = 0; s <= r0 + PT_ROWS - 1; ++s) {
+            float bb[PT_COLS];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int j4 = 0; j4 < PT_COLS; j4 += 4) {
+                const float4 b = *reinterpret_cast<const float4 *>(xk + s * LD + c0 + j4);
+                bb[j4] = b.x, bb[j4 + 1] = b.y, bb[j4 + 2] = b.z, bb[j4 + 3] = b.w;
+            }
+#pragma unroll
+            for (int i = 0; i < PT_ROWS; ++i) {
                 const float a = INV[(r0 + i) * LDM + s];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a, bb[j], acc[i][j]);
+                for (int j = 0; j < PT_COLS; ++j) acc[i][j] = fmaf(a, bb[j], acc[i][j]);
             }
         }
         __syncthreads();  // every read of xf as the key operand finished long ago; keep order simple
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < PT_ROWS; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) xf[(r0 + i) * LD + c0 + j] = acc[i][j];
+            for (int j = 0; j < PT_COLS; ++j) xf[(r0 + i) * LD + c0 + j] = acc[i][j];
     }
     __syncthreads();
     // 8. U0 = INV B2 -> xk (B1 no longer needed)
     {
-        float acc[4][8] = {};
-        for (int s = 0; s <= r0 + 3; ++s) {
-            const float4 b0 = *reinterpret_cast<const float4 *>(xv + s * LD + c0);
-            const float4 b1 = *reinterpret_cast<const float4 *>(xv + s * LD + c0 + 4);
-            const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        float acc[PT_ROWS][PT_COLS] = {};
+        for (int s = 0; s <= r0 + PT_ROWS - 1; ++s) {
+            float bb[PT_COLS];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int j4 = 0; j4 < PT_COLS; j4 += 4) {
+                const float4 b = *reinterpret_cast<const float4 *>(xv + s * LD + c0 + j4);
+                bb[j4] = b.x, bb[j4 + 1] = b.y, bb[j4 + 2] = b.z, bb[j4 + 3] = b.w;
+            }
+#pragma unroll
+            for (int i = 0; i < PT_ROWS; ++i) {
                 const float a = INV[(r0 + i) * LDM + s];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a, bb[j], acc[i][j]);
+                for (int j = 0; j < PT_COLS; ++j) acc[i][j] = fmaf(a, bb[j], acc[i][j]);
             }
         }
         __syncthreads();
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < PT_ROWS; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) xk[(r0 + i) * LD + c0 + j] = acc[i][j];
+            for (int j = 0; j < PT_COLS; ++j) xk[(r0 + i) * LD + c0 + j] = acc[i][j];
     }
     __syncthreads();
 
     // 9. Q' = Q_decay - M_qk W,  O0 = M_qk U0;  write W, Q', U0, O0
     {
-        float aw[4][8] = {}, au[4][8] = {};
-        for (int s = 0; s <= r0 + 3; ++s) {
-            const float4 w0 = *reinterpret_cast<const float4 *>(xf + s * LD + c0);
-            const float4 w1 = *reinterpret_cast<const float4 *>(xf + s * LD + c0 + 4);
-            const float4 u0 = *reinterpret_cast<const float4 *>(xk + s * LD + c0);
-            const float4 u1 = *reinterpret_cast<const float4 *>(xk + s * LD + c0 + 4);
-            const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        float aw[PT_ROWS][PT_COLS] = {}, au[PT_ROWS][PT_COLS] = {};
+        for (int s = 0; s <= r0 + PT_ROWS - 1; ++s) {
+            float ww[PT_COLS], uu[PT_COLS];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int j4 = 0; j4 < PT_COLS; j4 += 4) {
+                const float4 w = *reinterpret_cast<const float4 *>(xf + s * LD + c0 + j4);
+                const float4 u = *reinterpret_cast<const float4 *>(xk + s * LD + c0 + j4);
+                ww[j4] = w.x, ww[j4 + 1] = w.y, ww[j4 + 2] = w.z, ww[j4 + 3] = w.w;
+                uu[j4] = u.x, uu[j4 + 1] = u.y, uu[j4 + 2] = u.z, uu[j4 + 3] = u.w;
+            }
+#pragma unroll
+            for (int i = 0; i < PT_ROWS; ++i) {
                 const float a = Mqk[(r0 + i) * LDM + s];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < PT_COLS; ++j) {
                     aw[i][j] = fmaf(a, ww[j], aw[i][j]);
                     au[i][j] = fmaf(a, uu[j], au[i][j]);
                 }
             }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < PT_ROWS; ++i) {
             const int r = r0 + i;
-            float wv[8], qv[8], uv[8], ov[8];
+            float wv[PT_COLS], qv[PT_COLS], uv[PT_COLS], ov[PT_COLS];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < PT_COLS; ++j) {
                 wv[j] = xf[r * LD + c0 + j];
                 qv[j] = xq[r * LD + c0 + j] - aw[i][j];
                 uv[j] = xk[r * LD + c0 + j];
@@ -328,7 +340,7 @@ prep_simt_kernel(const float *__restrict__ q, const float *__restrict__ k, const
                 float *U = reinterpret_cast<float *>(rec + REC_F32_U0) + r * D + c0;
                 float *O = reinterpret_cast<float *>(rec + REC_F32_O0) + r * D + c0;
 #pragma unroll
-                for (int j = 0; j < 8; j += 4) {
+                for (int j = 0; j < PT_COLS; j += 4) {
                     *reinterpret_cast<float4 *>(W + j) = make_float4(wv[j], wv[j + 1], wv[j + 2], wv[j + 3]);
                     *reinterpret_cast<float4 *>(Q + j) = make_float4(qv[j], qv[j + 1], qv[j + 2], qv[j + 3]);
                     *reinterpret_cast<float4 *>(U + j) = make_float4(uv[j], uv[j + 1], uv[j + 2], uv[j + 3]);
