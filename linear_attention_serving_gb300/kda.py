@@ -92,9 +92,20 @@ def _stream(device) -> ctypes.c_void_p:
 
 
 def _contig(*ts):
+    """Every tensor the kernels touch: contiguous and on one CUDA device (a host
+    tensor would hand the kernels a host pointer)."""
+    dev = None
     for t in ts:
-        if t is not None and not t.is_contiguous():
+        if t is None:
+            continue
+        if not t.is_contiguous():
             raise KDAError("all tensors must be contiguous")
+        if t.device.type != "cuda":
+            raise KDAError("all tensors must be CUDA tensors")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise KDAError("all tensors must be on the same CUDA device")
 
 
 def chunk_fwd_workspace_size(T_total: int, H: int, n_seqs: int, dtype=torch.bfloat16) -> int:
@@ -140,7 +151,7 @@ def chunk_fwd(q, k, v, z, A, beta, cu_seqlens=None, init_state=None, g_min=G_MIN
     cu_seqlens int32 [n+1] (device) or None (n_seqs equal-length sequences).
     Returns (o [T, H, 128] in q's dtype, final_state [n, H, 128, 128] fp32 or None)."""
     lib = load()
-    _contig(q, k, v, z, A, beta, cu_seqlens, init_state)
+    _contig(q, k, v, z, A, beta, cu_seqlens, init_state, workspace, out)
     T, H, Dm = q.shape
     n = _n_seqs(cu_seqlens, n_seqs)
     dt = _dtype_code(q)
@@ -164,7 +175,7 @@ def chunk_fwd_ckpt(q, k, v, z, A, beta, ckpt_interval, ckpt_slot, ckpt, cu_seqle
     (document, j) -> page of ckpt [n_slots, H, 128, 128] fp32 (device) for the
     state after (j + 1) * ckpt_interval tokens; -1 skips."""
     lib = load()
-    _contig(q, k, v, z, A, beta, cu_seqlens, init_state, ckpt_slot, ckpt)
+    _contig(q, k, v, z, A, beta, cu_seqlens, init_state, ckpt_slot, ckpt, workspace, out)
     T, H, Dm = q.shape
     n = _n_seqs(cu_seqlens, n_seqs)
     dt = _dtype_code(q)
@@ -191,7 +202,7 @@ def segment_scan(q, k, v, z, A, beta, n_segments, cu_seqlens=None, init_state=No
     """kda_segment_scan: intra-device segment-parallel prefill.
     Returns (o, final_state) or (o, final_state, pairs_M, pairs_S) with pairs [H, n_seg, 128, 128]."""
     lib = load()
-    _contig(q, k, v, z, A, beta, cu_seqlens, init_state)
+    _contig(q, k, v, z, A, beta, cu_seqlens, init_state, workspace)
     T, H, Dm = q.shape
     n = _n_seqs(cu_seqlens, n_seqs)
     dt = _dtype_code(q)
@@ -222,7 +233,7 @@ def decode_step(state, q, k, v, z, beta, A, cache, num_accepted=None, g_min=G_MI
     num_accepted int32 [N] (device) or None.  Returns o [N, W, H, 128]."""
     lib = load()
     cq, ck, cv, cz, cb = cache if cache is not None else (None,) * 5
-    _contig(state, q, k, v, z, beta, A, cq, ck, cv, cz, cb, num_accepted)
+    _contig(state, q, k, v, z, beta, A, cq, ck, cv, cz, cb, num_accepted, error_word, out)
     N, W, H, Dm = q.shape
     if num_accepted is not None and num_accepted.dtype != torch.int32:
         raise KDAError("num_accepted must be int32")
@@ -247,7 +258,7 @@ def decode_step_fused(state, q, k, v, z, beta, A, conv_w, conv_state, o_gate, o_
     lib = load()
     cq, ck, cv, cz, cb = cache if cache is not None else (None,) * 5
     _contig(state, q, k, v, z, beta, A, conv_w, conv_state, o_gate, o_norm_w, cq, ck, cv, cz, cb,
-            num_accepted)
+            num_accepted, error_word, out)
     N, W, H, Dm = q.shape
     if num_accepted is not None and num_accepted.dtype != torch.int32:
         raise KDAError("num_accepted must be int32")
@@ -270,6 +281,7 @@ def decode_step_fused(state, q, k, v, z, beta, A, conv_w, conv_state, o_gate, o_
 
 
 def read_device_error(workspace: torch.Tensor) -> int:
+    _contig(workspace)
     code = ctypes.c_int32(0)
     rc = load().kda_read_device_error(_p(workspace), ctypes.byref(code), _stream(workspace.device))
     _check(rc, "kda_read_device_error")

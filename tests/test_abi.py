@@ -143,6 +143,30 @@ def test_decode_fused_rejects_bad_arguments():
     assert dec(flags=8) == 1
 
 
+def test_binding_rejects_host_tensors_before_any_launch():
+    """Host tensors would hand the kernels host pointers: every call refuses them
+    (and tensors spread over devices) before it reaches the library."""
+    import torch
+    bf = torch.bfloat16
+    q = torch.zeros(64, 2, 128, dtype=bf)
+    z = torch.zeros(64, 2, 128)
+    A, beta = torch.zeros(2), torch.zeros(64, 2)
+    with pytest.raises(kda.KDAError, match="CUDA"):
+        kda.chunk_fwd(q, q, q, z, A, beta)
+    with pytest.raises(kda.KDAError, match="CUDA"):
+        kda.segment_scan(q, q, q, z, A, beta, 2)
+    qd = torch.zeros(2, 5, 2, 128)
+    state = torch.zeros(2, 2, 128, 128)
+    cache = tuple(torch.zeros(2, 4, 2, 128) for _ in range(4)) + (torch.zeros(2, 4, 2),)
+    with pytest.raises(kda.KDAError, match="CUDA"):
+        kda.decode_step(state, qd, qd, qd, qd, torch.zeros(2, 5, 2), A, cache)
+    with pytest.raises(kda.KDAError, match="CUDA"):
+        kda.decode_step_fused(state, qd, qd, qd, qd, torch.zeros(2, 5, 2), A, torch.zeros(3, 2, 128, 4),
+                              torch.zeros(2, 2, 3, 3, 128), qd, torch.ones(128), cache)
+    with pytest.raises(kda.KDAError, match="CUDA"):
+        kda.read_device_error(torch.zeros(256, dtype=torch.uint8))
+
+
 def test_binding_rejects_wrong_dtypes_on_cpu_tensors():
     import torch
     q = torch.zeros(4, 1, 128, dtype=torch.float16)
