@@ -7,7 +7,8 @@ bit-identical values.
 
 Input recipe (all draws in fp32 from a seeded ``torch.Generator``, then cast):
   * q, k ~ N(0, 1), L2-normalised over d_k per (token, head) before the cast
-    (the method takes normalised q, k; normalising in the kernel is a later step);
+    (the method takes normalised q, k; the kernels' L2-norm option, tested on
+    unnormalised inputs of its own, can do it instead);
   * v ~ N(0, 1);
   * z (gate logits) ~ N(0, z_std) per channel, fp32;  A_h ~ N(0, A_std) per head
     (A_std = 0 gives A_h = 0);
