@@ -69,6 +69,12 @@ def test_segment_planner_host_logic():
     assert kda.chunk_fwd_workspace_size(1 << 20, 8, 1) >= kda.segment_scan_workspace_size(1 << 20, 8, 1, n)
     # more heads leave the chain less exposed: the planner never asks for more segments
     assert kda.chunk_fwd_plan_segments(1 << 20, 64, 1, bf16) <= n
+    # whole waves: phase 3 (two blocks per (segment, head)) fits one wave of the SMs
+    # and one more segment would not (the device count is 148 without a GPU, 152 on GB300)
+    for sms in (148, 152):
+        assert 2 * n * 8 <= sms < 2 * (n + 1) * 8
+    # short sequences: the composition cap keeps the count small
+    assert kda.chunk_fwd_plan_segments(32768, 4, 1, bf16) <= 10
 
 
 FAKE = ctypes.c_void_p(1 << 20)  # aligned dummy address; never dereferenced on these paths
