@@ -140,8 +140,9 @@ size_t kda_chunk_fwd_workspace_size(int64_t T_total, int H, int n_seqs, int dtyp
  *   ckpt           (device) fp32 [n_slots, H, D, D], 16-byte aligned: pages
  *   n_slots        pages in ckpt (>= 1)
  * Invalid checkpoint arguments return KDA_ERR_INVALID_ARG before any launch.
- * A call with checkpoints takes the three-kernel bf16 path (or the segmented
- * one kda_chunk_fwd_plan_segments picks), not the single fused launch.
+ * A call with checkpoints runs the same path as kda_chunk_fwd (fused launch,
+ * three kernels or segments), in instantiations that carry the checkpoint
+ * stores.
  * ------------------------------------------------------------------------ */
 int kda_chunk_fwd_ckpt(const void *q, const void *k, const void *v,
                        const float *z, const float *A, const float *beta,
