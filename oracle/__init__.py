@@ -124,17 +124,21 @@ def gate(z, A, g_min=G_MIN):
 L2NORM_EPS = 1e-6  # added to the sum of squares under the root; the pages give the flag, not the constant
 
 
-def input_prep(q, k, beta, qk_l2norm=False, beta_sigmoid=False, eps=L2NORM_EPS):
+def input_prep(q, k, beta, qk_l2norm=False, beta_sigmoid=False, eps=L2NORM_EPS, q_scale=False):
     """The kernel-side input options of the pages' chunk_kda / fused_recurrent_kda
     interface ([K3-2] "训练、prefill、decode 各用哪种形式": use_qk_l2norm_in_kernel,
     use_beta_sigmoid_in_kernel):
     q and k divided by their L2 norm over the key dimension, q / sqrt(sum(q^2) + eps),
     per (token, head); beta replaced by its logistic sigmoid 1 / (1 + exp(-beta)).
+    With q_scale, q is then multiplied by dk^-1/2 (the usual attention scale of that
+    interface; the pages name no scale, so the recurrence itself uses none).
     q, k [..., dk]; beta any shape.  Returns fp64 copies (unchanged when a flag is off)."""
     q, k, beta = _f64(q), _f64(k), _f64(beta)
     if qk_l2norm:
         q = q / np.sqrt(np.sum(q * q, axis=-1, keepdims=True) + eps)
         k = k / np.sqrt(np.sum(k * k, axis=-1, keepdims=True) + eps)
+    if q_scale:
+        q = q / np.sqrt(q.shape[-1])
     if beta_sigmoid:
         beta = 1.0 / (1.0 + np.exp(-beta))
     return q, k, beta
@@ -303,7 +307,8 @@ def rms_norm_gated(o, gate, w, eps):
 
 def decode_step_fused(state, q, k, v, z, beta, A, conv_w, conv_state, o_gate, o_norm_w, o_norm_eps,
                       cache_q, cache_k, cache_v, cache_z, cache_beta, num_accepted=None, g_min=G_MIN,
-                      qk_l2norm=False, beta_sigmoid=False, conv_silu=False, return_prenorm=False):
+                      qk_l2norm=False, beta_sigmoid=False, conv_silu=False, return_prenorm=False,
+                      q_scale=False):
     """One fused decode step with MTP replay.
 
     Per sequence b the committed token stream continues the convolution state:
@@ -311,7 +316,7 @@ def decode_step_fused(state, q, k, v, z, beta, A, conv_w, conv_state, o_gate, o_
     d1 .. d_{W-1} follow t0.  Steps, in the pages' order:
       1. short convolution of the projected q, k, v over that stream (pre-convolution
          values are what the cache and the convolution state hold);
-      2. input options on the convolved q, k (L2 norm) and beta (sigmoid);
+      2. input options on the convolved q, k (L2 norm, q scale) and beta (sigmoid);
       3. the recurrence of ``decode_step``: replay, t0 committed, drafts speculative;
       4. gated output norm of the window's outputs.
     The new convolution state is the last three pre-convolution inputs of the committed
@@ -347,7 +352,7 @@ def decode_step_fused(state, q, k, v, z, beta, A, conv_w, conv_state, o_gate, o_
         yq, yk, yv = conv
         zz = np.concatenate([cz[b, :n], z[b]])
         bb = np.concatenate([cb[b, :n], beta[b]])
-        yq, yk, bb = input_prep(yq, yk, bb, qk_l2norm, beta_sigmoid)
+        yq, yk, bb = input_prep(yq, yk, bb, qk_l2norm, beta_sigmoid, q_scale=q_scale)
 
         def replay(x):
             slots = np.zeros((1, W - 1) + x.shape[1:])

@@ -104,8 +104,19 @@ PY_MUTANTS = [
      "(np.sqrt(np.mean(o * o, axis=-1, keepdims=True)) + eps)"),
     ("gate_without_sigmoid", "return o * r * w / (1.0 + np.exp(-gate))", "return o * r * w * gate"),
     ("norm_without_weight", "return o * r * w / (1.0 + np.exp(-gate))", "return o * r / (1.0 + np.exp(-gate))"),
-    ("input_options_before_conv", "yq, yk, bb = input_prep(yq, yk, bb, qk_l2norm, beta_sigmoid)",
-     "_, _, bb = input_prep(yq, yk, bb, qk_l2norm, beta_sigmoid)"),
+    ("input_options_before_conv", "yq, yk, bb = input_prep(yq, yk, bb, qk_l2norm, beta_sigmoid, q_scale=q_scale)",
+     "_, _, bb = input_prep(yq, yk, bb, qk_l2norm, beta_sigmoid, q_scale=q_scale)"),
+    ("q_scale_inverted", "q = q / np.sqrt(q.shape[-1])", "q = q * np.sqrt(q.shape[-1])"),
+    ("q_scale_on_k", "q = q / np.sqrt(q.shape[-1])", "k = k / np.sqrt(k.shape[-1])"),
+    ("q_scale_before_norm", """    if qk_l2norm:
+        q = q / np.sqrt(np.sum(q * q, axis=-1, keepdims=True) + eps)
+        k = k / np.sqrt(np.sum(k * k, axis=-1, keepdims=True) + eps)
+    if q_scale:
+        q = q / np.sqrt(q.shape[-1])""", """    if q_scale:
+        q = q / np.sqrt(q.shape[-1])
+    if qk_l2norm:
+        q = q / np.sqrt(np.sum(q * q, axis=-1, keepdims=True) + eps)
+        k = k / np.sqrt(np.sum(k * k, axis=-1, keepdims=True) + eps)"""),
 ]
 
 PY_PIN_TESTS = [
@@ -115,8 +126,9 @@ PY_PIN_TESTS = [
     pins.test_fused_decode_with_unit_conv_is_plain_decode,
     pins.test_fused_decode_equals_convolved_committed_stream,
     pins.test_fused_decode_output_is_normalised_prenorm,
+    pins.test_input_prep_q_scale_closed_forms,
 ]
-PY_FUNCS = ("short_conv", "rms_norm_gated", "decode_step_fused")
+PY_FUNCS = ("short_conv", "rms_norm_gated", "decode_step_fused", "input_prep")
 
 
 def _py_caught(monkeypatch, src_text):

@@ -419,6 +419,29 @@ def test_input_prep_l2norm_closed_forms():
     assert np.array_equal(q2, q) and np.array_equal(k2, k) and np.array_equal(b2, np.ones((5, 3)))
 
 
+def test_input_prep_q_scale_closed_forms():
+    """q times dk^-1/2 = 1/sqrt(128) = 0.08838834764831845 (a closed value), after the
+    L2 norm (so a normalised q has norm 1/sqrt(128)); k and beta untouched; and, o
+    being linear in q, the recurrence's outputs scale by the same factor while the
+    state does not change."""
+    r = np.random.default_rng(12)
+    q = r.standard_normal((6, 2, 128)) * 2.0
+    k = r.standard_normal((6, 2, 128))
+    b = r.random((6, 2))
+    qs, ks, bs = oracle.input_prep(q, k, b, q_scale=True)
+    assert abs(1.0 / math.sqrt(128) - 0.08838834764831845) < 1e-16
+    assert np.allclose(qs, q * 0.08838834764831845, rtol=1e-15, atol=0)
+    assert np.array_equal(ks, k) and np.array_equal(bs, b)
+    qn, _, _ = oracle.input_prep(q, k, b, qk_l2norm=True, q_scale=True)
+    assert np.allclose(np.linalg.norm(qn, axis=-1), 0.08838834764831845, rtol=1e-6)
+    v, z = r.standard_normal((6, 2, 128)), r.standard_normal((6, 2, 128))
+    A = np.zeros(2)
+    o1, s1 = oracle.recurrent(q, k, v, z, A, b)
+    o2, s2 = oracle.recurrent(qs, k, v, z, A, b)
+    assert np.allclose(o2, o1 * 0.08838834764831845, rtol=1e-12, atol=1e-14)
+    assert np.array_equal(s1, s2)
+
+
 def test_input_prep_beta_sigmoid_closed_forms():
     x = np.array([[-30.0, -2.0, 0.0, 0.5, 3.0, 30.0]])
     _, _, b = oracle.input_prep(np.zeros((1, 1, 4)), np.zeros((1, 1, 4)), x, beta_sigmoid=True)
