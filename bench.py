@@ -332,6 +332,93 @@ def e2e_prefill(args, dev, kda, inputs):
     return ms, h2d, d2h
 
 
+# ---------------------------------------------------------------- the other prefill configurations
+
+def timed_calls(fn, kda, flush, steps, warmup):
+    """Device time of `fn` per call (CUDA events on the current stream, an L2
+    flush and a host-cover spin before each call, outside its events), and the
+    library's kernel marks of the timed calls."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    kda.profile_enable(True)
+    launches0 = kda.launch_count()
+    for i in range(steps):
+        flush.zero_()
+        torch.cuda._sleep(HOST_COVER_CYCLES)
+        evs[i][0].record()
+        fn()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    launches = kda.launch_count() - launches0
+    marks = kda.profile_collect()
+    kda.profile_enable(False)
+    ms = [a.elapsed_time(b) for a, b in evs]
+    kt = {n: sum(v) for n, v in kernel_times(marks).items()}
+    tot = sum(kt.values()) or 1.0
+    return {"ms_per_call": statistics.mean(ms), "ms_min": min(ms), "calls": steps,
+            "launches_per_call": launches / steps,
+            "kernel_ms_per_call": {n: v / steps for n, v in kt.items()},
+            "kernel_share": {n: v / tot for n, v in kt.items()}}
+
+
+def bench_other_configs(dev, kda, roofline, hbm, steps=6, warmup=3):
+    """The workloads other than the headline, each through the public calls with
+    device-resident inputs: tiny_fp32 (kda_chunk_fwd, exact fp32 path),
+    varlen_32k_h32 (kda_chunk_fwd over packed documents) and segscan_1m_h8
+    (kda_chunk_fwd, which picks its own segments, and kda_segment_scan with the
+    configuration's 148 segments).  Throughput is workload tokens per second;
+    roofline_frac divides the pages' kernel-level byte count (pro-rated by tokens,
+    per-document states included) by the call time and the HBM peak."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    clocks.start()
+    for name in ("tiny_fp32", "varlen_32k_h32", "segscan_1m_h8"):
+        w = kda_synth.WORKLOADS[name]
+        inp = kda_synth.workload_inputs(name, device=dev)
+        q, k, v, z, A, beta = (inp[n] for n in ("q", "k", "v", "z", "A", "beta"))
+        cu, init = inp["cu_seqlens"], inp["init_state"]
+        n_seqs = 1 if cu is None else cu.numel() - 1
+        if cu is not None:
+            cu = cu.to(dev)
+        T, H = w.T, w.H
+        bytes_call = roofline.prefill_kernel_bytes(T, H, n_seqs)
+
+        def entry(r, what):
+            r["path"] = what
+            r["tokens_per_s"] = T / (r["ms_per_call"] / 1e3)
+            r["algorithmic_bytes"] = bytes_call
+            r["roofline_frac"] = bytes_call / (r["ms_per_call"] / 1e3) / 1e9 / hbm
+            return r
+
+        res = {"T": T, "H": H, "n_seqs": n_seqs, "dtype": w.dtype}
+        wsp = torch.empty(kda.chunk_fwd_workspace_size(T, H, n_seqs, q.dtype), dtype=torch.uint8, device=dev)
+        o = torch.empty_like(q)
+        fn = lambda: kda.chunk_fwd(q, k, v, z, A, beta, cu_seqlens=cu, init_state=init, workspace=wsp, out=o)
+        nseg = kda.chunk_fwd_plan_segments(T, H, n_seqs, q.dtype, varlen=cu is not None)
+        res["chunk_fwd"] = entry(timed_calls(fn, kda, flush, steps, warmup),
+                                 f"kda_chunk_fwd ({nseg} automatic segments)" if nseg else "kda_chunk_fwd")
+        del wsp
+        if w.n_segments:
+            torch.cuda.empty_cache()
+            wsp = torch.empty(kda.segment_scan_workspace_size(T, H, n_seqs, w.n_segments, q.dtype),
+                              dtype=torch.uint8, device=dev)
+            fn = lambda: kda.segment_scan(q, k, v, z, A, beta, w.n_segments, cu_seqlens=cu, init_state=init,
+                                          workspace=wsp)
+            res["segment_scan"] = entry(timed_calls(fn, kda, flush, steps, warmup),
+                                        f"kda_segment_scan ({w.n_segments} segments)")
+            del wsp
+        if w.dtype == "f32":
+            res["note"] = "latency-bound: the byte count takes well under a microsecond at the HBM peak"
+        out[name] = res
+        del inp, q, k, v, z, A, beta, o
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    return out, clk
+
+
 # ---------------------------------------------------------------- decode
 
 def bench_decode(args, dev, kda, steps=20, warmup=3, fused=False):
@@ -410,13 +497,22 @@ def cpu_oracle_prefill(workload, heads=None, min_seconds=0.0):
     return tok_s, used, f"{workload}: {hs} of {w.H} heads x {w.T} tokens, {reps} pass(es), {dt:.2f} s each"
 
 
+def workload_config(workload, ws):
+    """The `config` object of both arms' JSON lines."""
+    w = kda_synth.WORKLOADS[workload]
+    return {"workload": workload, "B": 1, "H": w.H, "T": w.T, "d": 128, "C": 64,
+            "l2": "flushed before every step (256 MB write), outside the step's events",
+            "host_launch": "hidden: a device spin precedes each step's first event",
+            "parallelism": f"independent copy per GPU x{ws}"}
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return
     import oracle
     oracle.build()
     w = kda_synth.WORKLOADS[args.workload]
-    heads = max(1, w.H // 8)
+    heads = w.H  # every head: the oracle threads over (sequence, head), so all host cores work
     for _ in range(args.warmup if args.warmup < 2 else 1):
         cpu_oracle_prefill(args.workload, heads)
     vals = []
@@ -431,7 +527,7 @@ def run_reference(args, ws, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.workload, "B": 1, "H": w.H, "T": w.T, "d": 128},
+        "data": "synthetic", "config": workload_config(args.workload, args.gpus),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
                          "sample": f"each step: {sample}"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -449,6 +545,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill_h16_t8k")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the tiny, packed-varlen and 1M-token segment-scan configurations")
     ap.add_argument("--clock-window", type=float, default=0.6,
                     help="seconds of the prefill step the clock samples cover (0: the timed steps only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -500,10 +598,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "B": 1, "H": H, "T": T, "d": 128, "C": 64,
-                   "l2": "flushed before every step (256 MB write), outside the step's events",
-                   "host_launch": "hidden: a device spin precedes each step's first event",
-                   "parallelism": f"independent copy per GPU x{ws}"},
+        "config": workload_config(args.workload, ws),
         "roofline": roof,
         "path_roofline": {"bytes_per_step": path_bytes, "frac": path_frac, "peak": hbm,
                           "note": "pages' kernel-level count T/C(8C^2+22CD)+8D^2 per head"},
@@ -521,6 +616,10 @@ def main():
         ms, h2d, d2h = e2e_prefill(args, dev, kda, pf["inputs"])
         line["e2e"] = {"value": T * ws / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+    if rank == 0 and not args.no_configs:
+        cfgs, cclk = bench_other_configs(dev, kda, roofline, hbm)
+        line["other_configs"] = cfgs
+        line["other_configs_clocks"] = cclk
     if not args.no_decode:
         dc = bench_decode(args, dev, kda)
         dms = sum(dc["step_ms"])

@@ -65,8 +65,17 @@ enum kda_dtype { KDA_BF16 = 0, KDA_F32 = 1 };
  *   KDA_FLAG_BETA_SIGMOID  beta holds logits; the kernels use 1 / (1 + exp(-beta))
  *   KDA_FLAG_CONV_SILU     kda_decode_step_fused only: SiLU, y / (1 + exp(-y)), after
  *                          the short convolution (the pages name no activation)
+ *   KDA_FLAG_Q_SCALE       q is multiplied by d_k^-1/2 = 1 / sqrt(128) (after the L2
+ *                          norm when both are set), the usual attention scale of the
+ *                          chunk_kda interface; the pages give no scale, so it is off
+ *                          by default (o = S^T q)
  * The decode cache keeps the projected inputs as given (unnormalised, logits). */
-enum kda_flags { KDA_FLAG_QK_L2NORM = 1, KDA_FLAG_BETA_SIGMOID = 2, KDA_FLAG_CONV_SILU = 4 };
+enum kda_flags {
+    KDA_FLAG_QK_L2NORM = 1,
+    KDA_FLAG_BETA_SIGMOID = 2,
+    KDA_FLAG_CONV_SILU = 4,
+    KDA_FLAG_Q_SCALE = 8
+};
 
 /* Device error codes (bit flags) written into the workspace / error word. */
 enum kda_device_error {
@@ -184,20 +193,27 @@ int kda_chunk_fwd(const void *q, const void *k, const void *v,
  * device synchronisation a cudaMalloc may imply).
  *
  * Same arguments, checks and results as kda_chunk_fwd, without workspace and
- * workspace_bytes (and without the automatic segmentation).  The workspace is a fixed array of
- * KDA_NOALLOC_SCRATCH_BYTES bytes in device global memory owned by the library
- * (every GPU that loads the library holds it until exit); the call allocates
- * nothing and calls no allocating routine.
- *   - A call whose kda_chunk_fwd_workspace_size(T_total, H, n_seqs, dtype)
- *     exceeds KDA_NOALLOC_SCRATCH_BYTES returns KDA_ERR_WORKSPACE before any
- *     launch (about 500 (chunk, head) pairs in bf16, 400 in fp32).
+ * workspace_bytes.  It always runs the preparation and scan kernels one after
+ * the other (never the single fused launch or the automatic segments), so its
+ * results equal kda_chunk_fwd's up to rounding.  The workspace is a fixed array
+ * of KDA_NOALLOC_SCRATCH_BYTES bytes in device global memory owned by the
+ * library (every GPU that loads the library holds it until exit); the call
+ * allocates nothing and calls no allocating routine.
+ *   - The call needs the workspace of that sequential path: a header, the
+ *     chunk table and one record per (chunk, head), with chunks =
+ *     T_total / 64 + n_seqs (132,096 bytes per record in bf16, 164,352 in
+ *     fp32).  A call needing more than KDA_NOALLOC_SCRATCH_BYTES returns
+ *     KDA_ERR_WORKSPACE before any launch (about 500 (chunk, head) records in
+ *     bf16, 400 in fp32).
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     that device current) and caches it with the device's CUDA context; a
+ *     call under a new context (after a device reset) looks it up again.
+ *     Make the first call on each device before any stream capture.
  *   - Every call uses the same array: calls whose executions overlap on the
  *     GPU race.  Order them, e.g. by issuing them on one stream.
- *   - Device-side errors (bad cu_seqlens) are recorded in the array's first
- *     word, which the next call clears.
+ *   - Device-side errors (bad cu_seqlens, a timed-out wait) are recorded in
+ *     the array's first word, which the next call clears;
+ *     kda_noalloc_read_device_error() reads it.
  * ------------------------------------------------------------------------ */
 #define KDA_NOALLOC_SCRATCH_BYTES (64ull << 20)
 
@@ -207,6 +223,13 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                           int64_t T_total, int H, int D, int dtype, float g_min,
                           const float *init_state, void *o, float *final_state,
                           int flags, kda_stream_t stream);
+
+/* kda_noalloc_read_device_error -- synchronise `stream` and read the device
+ * error code (bit flags of kda_device_error) that the last
+ * kda_chunk_fwd_noalloc on the current device recorded in the library's
+ * array.  Allocates nothing.  Returns KDA_OK, KDA_ERR_INVALID_ARG (code NULL)
+ * or KDA_ERR_CUDA. */
+int kda_noalloc_read_device_error(int32_t *code, kda_stream_t stream);
 
 /* --------------------------------------------------------------------------
  * kda_segment_scan -- intra-device context parallelism over one long packed
@@ -227,13 +250,24 @@ int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
  * Results equal kda_chunk_fwd on the same inputs up to rounding.
  *
  * Arguments as kda_chunk_fwd, plus
- *   n_segments   >= 1 (more segments than chunks leaves some empty)
- *   pairs_M      (device) fp32 [H, n_segments, D, D] or NULL: M of each segment
- *   pairs_S      (device) fp32 [H, n_segments, D, D] or NULL: S~ of each segment
- *   workspace    at least kda_segment_scan_workspace_size() bytes.
+ *   n_segments   >= 1 (more segments than chunks leaves some empty), or 0 for
+ *                the automatic count kda_segment_scan_auto_segments() returns
+ *   pairs_M      (device) fp32 [H, n, D, D] or NULL: M of each segment
+ *   pairs_S      (device) fp32 [H, n, D, D] or NULL: S~ of each segment
+ *                (n = n_segments, or the automatic count)
+ *   workspace    at least kda_segment_scan_workspace_size() bytes (same
+ *                n_segments, 0 included).
  * ------------------------------------------------------------------------ */
 size_t kda_segment_scan_workspace_size(int64_t T_total, int H, int n_seqs, int n_segments,
                                        int dtype);
+
+/* The segment count kda_segment_scan takes for n_segments = 0: the most
+ * segments whose rerun (two blocks per (segment, head)) fits in one wave of
+ * the current device's SMs, at most sqrt(chunks / 6) (beyond it the
+ * sequential composition costs more than the shorter chains save), at most 64
+ * and half the chunks, at least 1; chunks = T_total / 64 + n_seqs.  No device
+ * work; 0 for invalid shapes. */
+int kda_segment_scan_auto_segments(int64_t T_total, int H, int n_seqs);
 
 int kda_segment_scan(const void *q, const void *k, const void *v,
                      const float *z, const float *A, const float *beta,
@@ -360,6 +394,18 @@ int kda_read_device_error(const void *workspace, int32_t *code, kda_stream_t str
 int kda_profile_enable(int on);
 int kda_profile_collect(const char **names, float *ms, int max);
 long long kda_launch_count(void);
+
+/* kda_set_wait_budget -- the clock-cycle limit of the library's waits on
+ * flags that other blocks of the same launch raise (the fused prefill's
+ * record-ready flags) and of the decode's waits on its own copies, for every
+ * call made afterwards in this process (not thread-safe against calls in
+ * flight on other host threads).  A wait that runs out records
+ * KDA_DEVERR_TIMEOUT (workspace error word, decode error word), its block
+ * stops, lets its own copies and tensor-core work finish and frees its TMEM,
+ * and the call's outputs are then undefined.  cycles <= 0 restores the
+ * default (2e9 cycles, about one second).  Returns the previous limit.  Meant
+ * for tests of the timeout path; the other waits keep the default. */
+long long kda_set_wait_budget(long long cycles);
 
 #ifdef __cplusplus
 }

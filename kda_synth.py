@@ -144,7 +144,7 @@ def decode_state(N: int, H: int, seed: int, std: float = 0.05, device="cpu") -> 
 
 
 def decode_window(N: int, W: int, H: int, step: int, seed: int, dtype: str = "f32",
-                  z_std: float = 1.0, A_std: float = 0.0, device="cpu") -> dict:
+                  z_std: float = 1.0, A_std: float = 0.0, device="cpu", z_mean: float = 0.0) -> dict:
     """Projected inputs of one decode window [t0, d1 .. d_{W-1}]: q, k, v, z [N, W, H, D],
     beta [N, W, H], and num_accepted [N] ~ U{0 .. W-1} for this step."""
     g = _gen(seed * 7919 + 17 * step + 1, device)
@@ -152,7 +152,7 @@ def decode_window(N: int, W: int, H: int, step: int, seed: int, dtype: str = "f3
     q = _unit_rows(_randn((N, W, H, D), g, device)).to(tdt)
     k = _unit_rows(_randn((N, W, H, D), g, device)).to(tdt)
     v = _randn((N, W, H, D), g, device).to(tdt)
-    z = _randn((N, W, H, D), g, device, std=z_std)
+    z = _randn((N, W, H, D), g, device, std=z_std, mean=z_mean)
     beta = torch.sigmoid(_randn((N, W, H), g, device))
     nacc = torch.randint(0, W, (N,), generator=g, device=device, dtype=torch.int32)
     return dict(q=q, k=k, v=v, z=z, beta=beta, num_accepted=nacc)

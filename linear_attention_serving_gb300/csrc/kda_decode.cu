@@ -164,7 +164,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
               const float *__restrict__ A, InT *__restrict__ cq, InT *__restrict__ ck,
               InT *__restrict__ cv, float *__restrict__ cz, float *__restrict__ cb,
               const int32_t *__restrict__ nacc_p, int N, int H, int W, float g_min, InT *__restrict__ o,
-              int32_t *__restrict__ err, int flags, DecFuse fz) {
+              int32_t *__restrict__ err, int flags, DecFuse fz, long long wait_budget) {
     extern __shared__ __align__(128) uint8_t smdyn[];
     __shared__ uint64_t full_bar;
     __shared__ float sbeta[2][2 * MAX_W];
@@ -174,6 +174,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
     __shared__ __align__(16) float sqo[MAX_W][DEC_THREADS / 32];  // FUSE: squared output sums per window token and warp
     const bool l2norm = OPTS && (flags & KDA_FLAG_QK_L2NORM) != 0;
     const bool bsig = OPTS && (flags & KDA_FLAG_BETA_SIGMOID) != 0;
+    const bool qscale = OPTS && (flags & KDA_FLAG_Q_SCALE) != 0;
     const bool silu = FUSE && OPTS && (flags & KDA_FLAG_CONV_SILU) != 0;
 
     const DecSmem L(W, FUSE);
@@ -230,15 +231,20 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
             load_betas(next2, H, W, tid, beta, cb, bc_nn, bw_nn);
         }
         const int nacc = nacc_cur;
-        if (!mbar_wait(&full_bar, (uint32_t)(it & 1))) timed_out = true;
+        if (!mbar_wait_for(&full_bar, (uint32_t)(it & 1), wait_budget)) timed_out = true;
         if (__syncthreads_or(timed_out)) {
-            if (tid == 0) atomicOr(err, KDA_DEVERR_TIMEOUT);
+            if (tid == 0) {
+                if (err) atomicOr(err, KDA_DEVERR_TIMEOUT);
+                // the item's copies are still landing in shared memory: let them
+                // finish (fixed budget) before the block leaves
+                mbar_wait(&full_bar, (uint32_t)(it & 1));
+            }
             break;
         }
         if (nacc < 0 || nacc > W - 1) {
             // out-of-range accepted count: this sequence is left untouched
             if (tid == 0) {
-                atomicOr(err, KDA_DEVERR_NUM_ACCEPTED);
+                if (err) atomicOr(err, KDA_DEVERR_NUM_ACCEPTED);
                 if (next < n_items) {
                     issue_state<FUSE>(next, nacc_next, W, rowb, state, sm, L, &full_bar);
                     issue_rows<InT, FUSE>(next, nacc_next, H, W, q, k, v, z, cq, ck, cv, cz, fz.conv_state, sm,
@@ -398,6 +404,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                         qq *= rsqrtf(snorm[t][0][0] + snorm[t][1][0] + snorm[t][2][0] + snorm[t][3][0] + L2NORM_EPS);
                         kk *= rsqrtf(snorm[t][0][1] + snorm[t][1][1] + snorm[t][2][1] + snorm[t][3][1] + L2NORM_EPS);
                     }
+                    if (qscale) qq *= Q_SCALE;  // input option: q d_k^-1/2, after the norm
                     kt[t][vc] = kk * sc;
                     kh[t][vc] = __fdividef(kk, sc);
                     qt[t][vc] = qq * sc;
@@ -564,7 +571,7 @@ int launch_decode_t(float *state, const void *q, const void *k, const void *v, c
     const int grid = (int)(items < slots ? items : slots);
     kern<<<grid, DEC_THREADS, smem, s>>>(state, (const InT *)q, (const InT *)k, (const InT *)v, z, beta, A,
                                          (InT *)cq, (InT *)ck, (InT *)cv, cz, cb, nacc, N, H, W, g_min,
-                                         (InT *)o, err, flags, fz);
+                                         (InT *)o, err, flags, fz, wait_budget());
     return KDA_OK;
 }
 

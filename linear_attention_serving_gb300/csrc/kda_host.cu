@@ -38,6 +38,12 @@ int device_sm_count() {
     return cached[dev];
 }
 
+namespace {
+constexpr long long DEFAULT_WAIT_BUDGET = 2000000000ll;  // about one second at GB300 clocks
+long long g_wait_budget = DEFAULT_WAIT_BUDGET;
+}  // namespace
+long long wait_budget() { return __atomic_load_n(&g_wait_budget, __ATOMIC_RELAXED); }
+
 void note_launch(const char *name, cudaStream_t s) {
     __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);
     prof_mark(name, s);
@@ -51,12 +57,14 @@ bool aligned16(const void *p) { return p == nullptr || ((uintptr_t)p & 15u) == 0
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
-// Validation shared by kda_chunk_fwd and kda_segment_scan.
-int check_prefill(const void *q, const void *k, const void *v, const float *z, const float *A,
+}  // namespace
+
+// Validation shared by kda_chunk_fwd, its variants and kda_segment_scan.
+int kda::check_prefill(const void *q, const void *k, const void *v, const float *z, const float *A,
                   const float *beta, const int32_t *cu, int n_seqs, int64_t T_total, int H, int Dm,
                   int dtype, float g_min, const void *o, int flags) {
     if (Dm != D) return KDA_ERR_UNSUPPORTED;
-    if (flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BETA_SIGMOID)) return KDA_ERR_INVALID_ARG;
+    if (flags & ~PREFILL_FLAGS) return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
     if (H < 1 || n_seqs < 1 || T_total < 0 || T_total >= (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
     if (!(g_min >= -5.0f && g_min < 0.0f)) return KDA_ERR_INVALID_ARG;
@@ -70,6 +78,8 @@ int check_prefill(const void *q, const void *k, const void *v, const float *z, c
     if ((int64_t)(T_total / C + n_seqs) >= (int64_t)INT32_MAX / 2) return KDA_ERR_INVALID_ARG;
     return KDA_OK;
 }
+
+namespace {
 
 // Prep launch by input type: tcgen05 tensor cores for bf16 inputs, exact fp32
 // CUDA cores for fp32 inputs.
@@ -100,6 +110,7 @@ int make_plan(const int32_t *cu, int n_seqs, int64_t T_total, void *ws, const Wo
     p.table = (const ChunkInfo *)(base + w.off_table);
     p.doc_off = (const int32_t *)(base + w.off_doc);
     p.n_chunks = (const int32_t *)(base + 4);
+    p.wait_budget = wait_budget();
     int rc = cuda_status(cudaMemsetAsync(base, 0, zero_bytes, s));
     if (rc) return rc;
     if (!cu) {
@@ -127,6 +138,22 @@ int make_plan(const int32_t *cu, int n_seqs, int64_t T_total, void *ws, const Wo
 //                    (about 25 us per segment), so they win only when the
 //                    chain is over 1.5x the preparation; their count is set
 //                    by the scan's waves (below).
+// Segment count, measured on GB300: the scan blocks run one per SM, so whole
+// waves decide the time.  Take the most segments whose phase 3 (two 64-column
+// blocks per (segment, head)) fits in one wave of the SMs, and phase 1 (four
+// per pair) in two; more segments or an extra partial wave cost more than the
+// shorter chains save.  At most sqrt(chunks / 6), where the composition (about
+// 25 us per segment) outweighs the shorter chains (about 4 us per chunk over
+// the three phases); at most 64 and half the chunks; at least 1.
+int wave_segments(int64_t total_chunks, int H, int n_sm) {
+    int64_t n = n_sm / (2LL * H);
+    const int64_t cap = llround(sqrt((double)total_chunks / 6.0));
+    if (n > cap) n = cap;
+    if (n > 64) n = 64;
+    if (n > total_chunks / 2) n = total_chunks / 2;
+    return n >= 1 ? (int)n : 1;
+}
+
 // Returns 0 for one chain per (document, head).
 int plan_segments(int64_t T_total, int H, int n_seqs, bool varlen, int dtype, int n_sm) {
     if (varlen || dtype != KDA_BF16 || T_total <= 0 || n_seqs < 1 || H < 1) return 0;
@@ -138,19 +165,15 @@ int plan_segments(int64_t T_total, int H, int n_seqs, bool varlen, int dtype, in
     const double prep_us = 10.3 * units / (double)(prep_sms > 0 ? prep_sms : 1);
     const double chain_us = 1.3 * (double)chunks;
     if (chain_us <= 1.5 * prep_us) return 0;
-    // Segment count, measured on GB300: the scan blocks run one per SM, so
-    // whole waves decide the time.  Take the most segments whose phase 3 (two
-    // 64-column blocks per (segment, head)) fits in one wave of the SMs, and
-    // phase 1 (four per pair) in two; more segments or an extra partial wave
-    // cost more than the shorter chains save.  At most sqrt(chunks / 6), where
-    // the composition (about 25 us per segment) outweighs the shorter chains
-    // (about 4 us per chunk over the three phases).
-    int64_t n = n_sm / (2LL * H);
-    const int64_t cap = llround(sqrt((double)total / 6.0));
-    if (n > cap) n = cap;
-    if (n > 64) n = 64;
-    if (n > total / 2) n = total / 2;
-    return n >= 2 ? (int)n : 0;
+    const int n = wave_segments(total, H, n_sm);
+    return n >= 2 ? n : 0;
+}
+
+// kda_segment_scan's n_segments, with 0 meaning the wave rule's count.
+int resolve_segments(int n_segments, int64_t T_total, int H, int n_seqs) {
+    if (n_segments != 0) return n_segments;
+    if (T_total < 0 || H < 1 || n_seqs < 1) return 0;
+    return wave_segments(T_total / C + n_seqs, H, device_sm_count());
 }
 
 // The three phases of the segment scan over a workspace laid out for n_segments.
@@ -259,6 +282,11 @@ int kda_profile_collect(const char **names, float *ms, int max) {
 
 long long kda_launch_count(void) { return (long long)__atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
 
+long long kda_set_wait_budget(long long cycles) {
+    const long long v = cycles > 0 ? cycles : DEFAULT_WAIT_BUDGET;
+    return __atomic_exchange_n(&g_wait_budget, v, __ATOMIC_RELAXED);
+}
+
 size_t kda_chunk_fwd_workspace_size(int64_t T_total, int H, int n_seqs, int dtype) {
     if (T_total < 0 || H < 1 || n_seqs < 1) return 0;
     // room for the segmented path whenever an equal-length batch of this shape takes it
@@ -273,8 +301,13 @@ int kda_chunk_fwd_plan_segments(int64_t T_total, int H, int n_seqs, int dtype, i
 
 size_t kda_segment_scan_workspace_size(int64_t T_total, int H, int n_seqs, int n_segments,
                                        int dtype) {
+    n_segments = resolve_segments(n_segments, T_total, H, n_seqs);
     if (T_total < 0 || H < 1 || n_seqs < 1 || n_segments < 1) return 0;
     return workspace_layout(T_total, H, n_seqs, n_segments, dtype).total;
+}
+
+int kda_segment_scan_auto_segments(int64_t T_total, int H, int n_seqs) {
+    return resolve_segments(0, T_total, H, n_seqs);
 }
 
 }  // extern "C"
@@ -373,6 +406,7 @@ int kda_segment_scan(const void *q, const void *k, const void *v, const float *z
                      size_t workspace_bytes, int flags, kda_stream_t stream) {
     int rc = check_prefill(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, Dm, dtype, g_min, o, flags);
     if (rc) return rc;
+    n_segments = resolve_segments(n_segments, T_total, H, n_seqs);
     if (n_segments < 1 || n_segments > (1 << 20)) return KDA_ERR_INVALID_ARG;
     const Workspace w = workspace_layout(T_total, H, n_seqs, n_segments, dtype);
     if (!workspace || workspace_bytes < w.total || ((uintptr_t)workspace & 255u)) return KDA_ERR_WORKSPACE;
@@ -388,7 +422,7 @@ int kda_decode_step(float *state, const void *q, const void *k, const void *v, c
                     int Dm, int W, int dtype, float g_min, void *o, int32_t *error_word, int flags,
                     kda_stream_t stream) {
     if (Dm != D) return KDA_ERR_UNSUPPORTED;
-    if (flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BETA_SIGMOID)) return KDA_ERR_INVALID_ARG;
+    if (flags & ~PREFILL_FLAGS) return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
     if (N < 1 || H < 1 || W < 1 || W > 8) return KDA_ERR_INVALID_ARG;
     if ((int64_t)N * H >= (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
@@ -412,7 +446,7 @@ int kda_decode_step_fused(float *state, const void *q, const void *k, const void
                           const int32_t *num_accepted, int N, int H, int Dm, int W, int dtype, float g_min,
                           void *o, int32_t *error_word, int flags, kda_stream_t stream) {
     if (Dm != D) return KDA_ERR_UNSUPPORTED;
-    if (flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BETA_SIGMOID | KDA_FLAG_CONV_SILU)) return KDA_ERR_INVALID_ARG;
+    if (flags & ~(PREFILL_FLAGS | KDA_FLAG_CONV_SILU)) return KDA_ERR_INVALID_ARG;
     if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
     if (N < 1 || H < 1 || W < 1 || W > 8) return KDA_ERR_INVALID_ARG;
     if ((int64_t)N * H >= (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;

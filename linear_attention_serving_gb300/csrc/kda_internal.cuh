@@ -58,9 +58,13 @@ struct Plan {
     const int32_t *n_chunks; // table mode: device count
     int32_t *err;            // device error word (bit flags kda_device_error)
     int flags;               // input options (KDA_FLAG_*) for the preparation kernels
+    long long wait_budget;   // clock cycles a wait on another block's flag may take
 };
 
 constexpr float L2NORM_EPS = 1e-6f;  // KDA_FLAG_QK_L2NORM: x / sqrt(sum(x^2) + eps)
+constexpr float Q_SCALE = 0.08838834764831845f;  // KDA_FLAG_Q_SCALE: d_k^-1/2 = 1 / sqrt(128)
+// every input option of the prefill and the plain decode step
+constexpr int PREFILL_FLAGS = KDA_FLAG_QK_L2NORM | KDA_FLAG_BETA_SIGMOID | KDA_FLAG_Q_SCALE;
 
 __device__ __forceinline__ int plan_n_chunks(const Plan &p) {
     return p.uniform ? p.n_seqs * p.chunks_per_seq : *p.n_chunks;
@@ -208,6 +212,16 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 __device__ __forceinline__ float kda_gate(float g_min, float eA, float z) {
     return g_min / (1.0f + expf(-eA * z));
 }
+
+// Clock-cycle budget of the waits on flags that other blocks raise and of the
+// decode's waits on its own copies (kda_set_wait_budget; about one second by
+// default).
+long long wait_budget();
+
+// Argument checks of kda_chunk_fwd, shared by its variants (kda_host.cu).
+int check_prefill(const void *q, const void *k, const void *v, const float *z, const float *A,
+                  const float *beta, const int32_t *cu, int n_seqs, int64_t T_total, int H, int Dm,
+                  int dtype, float g_min, const void *o, int flags);
 
 // Per-launch bookkeeping (kda_host.cu): counts every launch and, when
 // profiling is enabled, records an event after it on stream `s`.

@@ -11,10 +11,15 @@
 //
 // Nothing here allocates: the device address of the array is looked up once
 // per device (the first call on that device, with that device current) and
-// cached; every later call only launches kernels and issues one
-// cudaMemsetAsync of the workspace header.  All calls share the one array, so
-// calls whose executions overlap on the GPU race on it; the caller must order
-// them (for example by issuing them on one stream).
+// cached together with the CUDA context it belongs to; a call under another
+// context (after a device reset, say) looks it up again.  Every other call
+// only launches kernels and issues one cudaMemsetAsync of the workspace
+// header.  All calls share the one array, so calls whose executions overlap on
+// the GPU race on it; the caller must order them (for example by issuing them
+// on one stream).  The array's first word is the device error word of the
+// last call (kda_noalloc_read_device_error reads it).
+#include <cuda.h>  // CUcontext / CUresult types only: the driver function comes through the runtime
+
 #include <cstring>
 #include <mutex>
 
@@ -30,23 +35,46 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCR
 
 constexpr int MAX_DEVICES = 64;
 void *g_scratch_addr[MAX_DEVICES] = {nullptr};
+CUcontext g_scratch_ctx[MAX_DEVICES] = {nullptr};
 std::mutex g_scratch_mu;
 
-// Device address of the scratch array on the current device, looked up once.
+// cuCtxGetCurrent, fetched through the runtime so that the library keeps no
+// link-time dependency on the driver library.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return (CtxGetCurrentFn)f;
+    }();
+    return fn;
+}
+
+// Device address of the scratch array on the current device, looked up on the
+// first call under the current context of that device.
 int scratch_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return KDA_ERR_CUDA;
+    CtxGetCurrentFn get_ctx = ctx_get_current();
+    if (!get_ctx) return KDA_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) != CUDA_SUCCESS) return KDA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || !ctx || g_scratch_ctx[dev] != ctx) {
+        // the lookup also makes the device's primary context current when no
+        // runtime call has done so yet
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KDA_ERR_CUDA;
+        if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return KDA_ERR_CUDA;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_addr[dev];
     return KDA_OK;
 }
-
-bool aligned16(const void *p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
 
 }  // namespace
 
@@ -56,23 +84,16 @@ extern "C" int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v
                                      const float *init_state, void *o, float *final_state,
                                      int flags, kda_stream_t stream) {
     // the same argument checks as kda_chunk_fwd
-    if (Dm != D) return KDA_ERR_UNSUPPORTED;
-    if (flags & ~(KDA_FLAG_QK_L2NORM | KDA_FLAG_BETA_SIGMOID)) return KDA_ERR_INVALID_ARG;
-    if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
-    if (H < 1 || n_seqs < 1 || T_total < 0 || T_total >= (int64_t)INT32_MAX) return KDA_ERR_INVALID_ARG;
-    if (!(g_min >= -5.0f && g_min < 0.0f)) return KDA_ERR_INVALID_ARG;
-    if (T_total > 0 && (!q || !k || !v || !z || !beta || !o)) return KDA_ERR_INVALID_ARG;
-    if (!A) return KDA_ERR_INVALID_ARG;
-    if (!cu_seqlens && (T_total % n_seqs) != 0) return KDA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(z) || !aligned16(o))
-        return KDA_ERR_INVALID_ARG;
-    if ((int64_t)(T_total / C + n_seqs) >= (int64_t)INT32_MAX / 2) return KDA_ERR_INVALID_ARG;
-    // the call must fit the fixed scratch array
+    int rc = check_prefill(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, Dm, dtype, g_min, o, flags);
+    if (rc) return rc;
+    // the call must fit the fixed scratch array: this path runs the prep and
+    // scan kernels one after the other (no fused launch, no segments), whose
+    // workspace is the layout without segment buffers
     const Workspace w = workspace_layout(T_total, H, n_seqs, 0, dtype);
     if (w.total > (size_t)KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
 
     void *ws = nullptr;
-    int rc = scratch_address(&ws);
+    rc = scratch_address(&ws);
     if (rc) return rc;
     cudaStream_t s = (cudaStream_t)stream;
     note_begin(s);
@@ -88,6 +109,7 @@ extern "C" int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v
     p.doc_off = (const int32_t *)(base + w.off_doc);
     p.n_chunks = (const int32_t *)(base + 4);
     p.flags = flags;
+    p.wait_budget = wait_budget();
     if (cudaMemsetAsync(base, 0, 8, s) != cudaSuccess) return KDA_ERR_CUDA;
     if (!cu_seqlens) {
         p.uniform = 1;
@@ -118,4 +140,18 @@ extern "C" int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v
     a.o = o;
     a.final_state = final_state;
     return dtype == KDA_BF16 ? launch_scan_tc(a, device_sm_count(), s) : launch_scan_simt(a, dtype, s);
+}
+
+extern "C" int kda_noalloc_read_device_error(int32_t *code, kda_stream_t stream) {
+    if (!code) return KDA_ERR_INVALID_ARG;
+    void *ws = nullptr;
+    const int rc = scratch_address(&ws);
+    if (rc) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    *code = h;
+    return KDA_OK;
 }

@@ -190,6 +190,7 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
     float *snorm = sHalf + 8 * 128;  // [64 tokens][q half 0, q half 1, k half 0, k half 1]
     const bool l2norm = OPTS && (plan.flags & KDA_FLAG_QK_L2NORM) != 0;
     const bool bsig = OPTS && (plan.flags & KDA_FLAG_BETA_SIGMOID) != 0;
+    const bool qscale = OPTS && (plan.flags & KDA_FLAG_Q_SCALE) != 0;
     const float gm2 = g_min * LOG2E;
 
     if (tid == 0) {
@@ -325,7 +326,8 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int i = 8 * rg + r;
-                const float2 qf = __bfloat1622float2(cin.q[r]);
+                float2 qf = __bfloat1622float2(cin.q[r]);
+                if (qscale) qf = mul2(qf, make_float2(Q_SCALE, Q_SCALE));  // input option: q d_k^-1/2
                 const float2 kf = __bfloat1622float2(cin.k[r]);
                 const float2 vf = __bfloat1622float2(cin.v[r]);
                 const float2 c2 = add2(carry, rl[r]);

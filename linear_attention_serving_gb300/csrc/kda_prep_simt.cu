@@ -103,12 +103,18 @@ prep_simt_kernel(const float *__restrict__ q, const float *__restrict__ k, const
                 pq += __shfl_xor_sync(0xffffffffu, pq, m);
                 pk += __shfl_xor_sync(0xffffffffu, pk, m);
             }
-            const float iq = 1.f / sqrtf(pq + L2NORM_EPS), ik = 1.f / sqrtf(pk + L2NORM_EPS);
+            float iq = 1.f / sqrtf(pq + L2NORM_EPS);
+            const float ik = 1.f / sqrtf(pk + L2NORM_EPS);
+            if (plan.flags & KDA_FLAG_Q_SCALE) iq *= Q_SCALE;  // input option: q d_k^-1/2 after the norm
             for (int col = lane; col < D; col += 32) {
                 xq[r * LD + col] *= iq;
                 xk[r * LD + col] *= ik;
             }
         }
+        __syncthreads();
+    } else if (plan.flags & KDA_FLAG_Q_SCALE) {
+        // input option: q d_k^-1/2
+        for (int idx = tid; idx < C * D; idx += PREP_THREADS) xq[(idx / D) * LD + idx % D] *= Q_SCALE;
         __syncthreads();
     }
 

@@ -168,16 +168,17 @@ __device__ __forceinline__ void load_slices(const uint8_t *base, int r, int rows
     }
 }
 
-// Bounded wait until *flag is set by another block of the same launch; the
-// acquire and the proxy fence order the bulk copies that follow after the
-// writes the flag publishes.
-__device__ __forceinline__ bool wait_flag(const int *flag) {
+// Wait until *flag is set by another block of the same launch, giving up
+// after `budget` clock cycles (the launch's budget for waits on other blocks)
+// or as soon as the block's abort flag rises; the acquire and the proxy fence
+// order the bulk copies that follow after the writes the flag publishes.
+__device__ __forceinline__ bool wait_flag(const int *flag, long long budget, const volatile int *abort) {
     const long long t0 = clock64();
     while (true) {
         int v;
         asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
         if (v != 0) break;
-        if (clock64() - t0 > WAIT_BUDGET_CYCLES) return false;
+        if (*abort || clock64() - t0 > budget) return false;
         __nanosleep(64);
     }
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -203,7 +204,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
     using ST = Stage<N, EMIT_O>;
     using CF = ScanCfg<N, TPR, EMIT_O>;
     constexpr int NT = CF::NT;
-    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], g_bar, sop_bar, o_bar[2], oempty_bar[2];
+    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], g_bar, sop_bar, o_bar[2], oempty_bar[2], drain_bar;
     __shared__ uint64_t qfull_bar[ST::QSTAGES], qfree_bar[ST::QSTAGES];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -237,6 +238,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
             mbar_init(&empty_bar[s], CF::CHAIN_WARPS);  // released by the chain warps once they read it
         }
         mbar_init(&g_bar, 1);
+        mbar_init(&drain_bar, 1);
         mbar_init(&sop_bar, CF::CHAIN_WARPS);  // the chain warps' parts of the next S operand
         for (int b = 0; b < 2; ++b) {
             mbar_init(&o_bar[b], 1);                // output accumulator b written
@@ -254,6 +256,8 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_g = tmem_slot;
+    const volatile int *abort = &abort_flag;
+    const long long flag_budget = p.wait_budget;
 
     if (warp == CF::PRODUCER_WARP) {
         // ------------------------------------------------------------ producer
@@ -265,9 +269,9 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
             uint32_t ph = 0;
             for (int i = 0; i < nchunks; ++i) {
                 // the record first: its flag is read while the stage drains
-                if (ready && !wait_flag(ready + (size_t)(c0 + i) * a.H + h)) { timed_out = true; break; }
-                if (!mbar_wait(&empty_bar[stage], ph ^ 1u)) { timed_out = true; break; }
-                if (*(volatile int *)&abort_flag) break;
+                if (ready && !wait_flag(ready + (size_t)(c0 + i) * a.H + h, flag_budget, abort)) { timed_out = true; break; }
+                if (!mbar_wait_ab(&empty_bar[stage], ph ^ 1u, abort)) { timed_out = true; break; }
+                if (*abort) break;
                 const char *rec = records + (size_t)(c0 + i) * rec_stride + (size_t)h * REC_BF16_BYTES;
                 uint8_t *st = sm + stage * ST::BYTES;
                 mbar_expect_tx(&full_bar[stage], bytes);
@@ -278,7 +282,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 issued = i + 1;
                 if (EMIT_O) {
                     const int qs = i % ST::QSTAGES;
-                    if (!mbar_wait(&qfree_bar[qs], (uint32_t)(((i / ST::QSTAGES) & 1) ^ 1))) { timed_out = true; break; }
+                    if (!mbar_wait_ab(&qfree_bar[qs], (uint32_t)(((i / ST::QSTAGES) & 1) ^ 1), abort)) { timed_out = true; break; }
                     mbar_expect_tx(&qfull_bar[qs], (uint32_t)ST::QBYTES);
                     bulk_g2s(qring + qs * ST::QBYTES, rec + REC_BF16_QP, (uint32_t)ST::QBYTES, &qfull_bar[qs]);
                     q_issued = i + 1;
@@ -288,7 +292,8 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                     ph ^= 1u;
                 }
             }
-            if (timed_out || *(volatile int *)&abort_flag) {
+            if (timed_out) abort_flag = 1;  // the other warps stop at their next wait
+            if (timed_out || *abort) {
                 // let the copies this thread started land before the block exits
                 for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
                     mbar_wait(&full_bar[i % STAGES], (uint32_t)((i / STAGES) & 1));
@@ -308,8 +313,8 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
             for (int i = 0; i < nchunks; ++i) {
                 const int b = i & 1;
                 // chunk i's S operand is complete (and the accumulator of chunk i - 1 read)
-                if (!mbar_wait(&sop_bar, (uint32_t)(i & 1)) || !mbar_wait(&full_bar[stage], ph) ||
-                    *(volatile int *)&abort_flag) {
+                if (!mbar_wait_ab(&sop_bar, (uint32_t)(i & 1), abort) || !mbar_wait_ab(&full_bar[stage], ph, abort) ||
+                    *abort) {
                     abort_flag = 1;
                     break;
                 }
@@ -325,8 +330,8 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                     // O = Q' S_enter of this chunk into output accumulator b, once the
                     // output warps have read what chunk i - 2 left there
                     const int qs = i % ST::QSTAGES;
-                    if ((i >= 2 && !mbar_wait(&oempty_bar[b], (uint32_t)(((i - 2) >> 1) & 1))) ||
-                        !mbar_wait(&qfull_bar[qs], (uint32_t)((i / ST::QSTAGES) & 1))) {
+                    if ((i >= 2 && !mbar_wait_ab(&oempty_bar[b], (uint32_t)(((i - 2) >> 1) & 1), abort)) ||
+                        !mbar_wait_ab(&qfull_bar[qs], (uint32_t)((i / ST::QSTAGES) & 1), abort)) {
                         abort_flag = 1;
                         break;
                     }
@@ -345,6 +350,10 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                     ph ^= 1u;
                 }
             }
+            // every MMA this thread issued has completed before TMEM is freed, also
+            // when the block stopped early
+            mma_commit(&drain_bar);
+            mbar_wait(&drain_bar, 0);
         }
     } else if (warp < CF::CHAIN_WARPS) {
         // ------------------------------------------------------------ chain warps
@@ -399,7 +408,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 doc = ci.doc;
                 last = (ci.flags & CHUNK_LAST) != 0;
             }
-            ok = mbar_wait(&full_bar[stage], ph);
+            ok = mbar_wait_ab(&full_bar[stage], ph, abort);
             // the entering state of this chunk, for the output kernel
             if (emit_s) store_s<NT>(records + (size_t)(c0 + i) * rec_stride + (size_t)h * REC_BF16_BYTES, pc / 16, t, pk);
             // ---- S <- Diag(a_C) S + H - G S; a_C and H are read while the MMA runs
@@ -410,7 +419,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
             else
 #pragma unroll
                 for (int j = 0; j < NT; ++j) hv[j] = 0.f;
-            ok = ok && mbar_wait(&g_bar, (uint32_t)(i & 1));
+            ok = ok && mbar_wait_ab(&g_bar, (uint32_t)(i & 1), abort);
             // a warp stops as a whole; the others then run out of their bounded waits
             if (!__all_sync(0xffffffffu, ok) || *(volatile int *)&abort_flag) {
                 ok = false;
@@ -464,7 +473,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
             pack_row<NT>(s, pk);
             if (EMIT_O && i >= 1 && i + 1 < nchunks) {
                 // operand buffer b ^ 1 was also read by chunk i - 1's output MMA
-                const bool okk = mbar_wait(&o_bar[b ^ 1], (uint32_t)(((i - 1) >> 1) & 1));
+                const bool okk = mbar_wait_ab(&o_bar[b ^ 1], (uint32_t)(((i - 1) >> 1) & 1), abort);
                 if (!__all_sync(0xffffffffu, okk)) {
                     ok = false;
                     break;
@@ -512,7 +521,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
             // O0 of this thread's token and the block's columns, read straight from
             // the record (ST::NS 16-column slices of 64 tokens x 32 bytes), after
             // the record's ready flag when another part of the launch writes it
-            bool okw = !ready || wait_flag(ready + (size_t)c * a.H + h);
+            bool okw = !ready || wait_flag(ready + (size_t)c * a.H + h, flag_budget, abort);
             uint4 o0v[2 * ST::NS];
             if (okw && mine) {
                 const char *o0 = records + (size_t)c * rec_stride + (size_t)h * REC_BF16_BYTES + REC_BF16_O0 +
@@ -523,9 +532,12 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                     o0v[2 * sl + 1] = *reinterpret_cast<const uint4 *>(o0 + sl * REC_BF16_OSLICE + 16);
                 }
             }
-            okw = okw && mbar_wait(&o_bar[b], (uint32_t)((i >> 1) & 1));
+            okw = okw && mbar_wait_ab(&o_bar[b], (uint32_t)((i >> 1) & 1), abort);
             if (!__all_sync(0xffffffffu, okw) || *(volatile int *)&abort_flag) {
-                if (lane == 0) abort_flag = 1;
+                if (lane == 0) {
+                    abort_flag = 1;
+                    atomicOr(p.err, KDA_DEVERR_TIMEOUT);
+                }
                 break;
             }
             tc_fence_after();

@@ -3,7 +3,10 @@
 //
 // Every wait is bounded by a clock budget; a wait that runs out returns false
 // and the caller records KDA_DEVERR_TIMEOUT and leaves its loop, so no kernel
-// of this library can spin forever.
+// of this library can spin forever.  Waits on data that the block itself
+// brings in or computes use the fixed budget below; waits on flags that other
+// blocks raise, and the decode's waits on its copies, take the budget of the
+// launch (kda_set_wait_budget, the same fixed value by default).
 #pragma once
 
 #include <stdint.h>
@@ -41,12 +44,41 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking probe of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase with the given parity to complete, giving up after
+// `budget` clock cycles.  The clock is read before every suspending try_wait
+// (which can sleep in hardware until the phase completes), so that a short
+// budget, not the hardware's suspend window, bounds the wait.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, long long budget) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (clock64() - t0 > budget) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+    }
+}
 // Bounded wait for the phase with the given parity to complete.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, WAIT_BUDGET_CYCLES);
+}
+// Bounded wait that also gives up as soon as *abort (a block-local flag in
+// shared memory, raised by the part of the block that timed out) is nonzero.
+__device__ __forceinline__ bool mbar_wait_ab(uint64_t *bar, uint32_t parity, const volatile int *abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
         if (clock64() - t0 > WAIT_BUDGET_CYCLES) return false;
+    }
     return true;
 }
 

@@ -66,6 +66,14 @@ def load(build_if_missing: bool = True):
     lib.kda_decode_step_fused.restype = I
     lib.kda_read_device_error.argtypes = [P, P, P]
     lib.kda_read_device_error.restype = I
+    lib.kda_segment_scan_auto_segments.argtypes = [L, I, I]
+    lib.kda_segment_scan_auto_segments.restype = I
+    lib.kda_set_wait_budget.argtypes = [ctypes.c_longlong]
+    lib.kda_set_wait_budget.restype = ctypes.c_longlong
+    lib.kda_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, P, P, I, P]
+    lib.kda_chunk_fwd_noalloc.restype = I
+    lib.kda_noalloc_read_device_error.argtypes = [P, P]
+    lib.kda_noalloc_read_device_error.restype = I
     _lib = lib
     return lib
 
@@ -138,15 +146,17 @@ def _n_seqs(cu_seqlens, n_seqs):
 KDA_FLAG_QK_L2NORM = 1
 KDA_FLAG_BETA_SIGMOID = 2
 KDA_FLAG_CONV_SILU = 4
+KDA_FLAG_Q_SCALE = 8
 
 
-def _flags(qk_l2norm: bool, beta_sigmoid: bool) -> int:
-    return (KDA_FLAG_QK_L2NORM if qk_l2norm else 0) | (KDA_FLAG_BETA_SIGMOID if beta_sigmoid else 0)
+def _flags(qk_l2norm: bool, beta_sigmoid: bool, q_scale: bool = False) -> int:
+    return ((KDA_FLAG_QK_L2NORM if qk_l2norm else 0) | (KDA_FLAG_BETA_SIGMOID if beta_sigmoid else 0)
+            | (KDA_FLAG_Q_SCALE if q_scale else 0))
 
 
 def chunk_fwd(q, k, v, z, A, beta, cu_seqlens=None, init_state=None, g_min=G_MIN,
               output_final_state=True, n_seqs=1, workspace=None, out=None, qk_l2norm=False,
-              beta_sigmoid=False):
+              beta_sigmoid=False, q_scale=False):
     """kda_chunk_fwd: chunkwise prefill.  q, k, v, z [T, H, 128]; A [H]; beta [T, H];
     cu_seqlens int32 [n+1] (device) or None (n_seqs equal-length sequences).
     Returns (o [T, H, 128] in q's dtype, final_state [n, H, 128, 128] fp32 or None)."""
@@ -162,14 +172,14 @@ def chunk_fwd(q, k, v, z, A, beta, cu_seqlens=None, init_state=None, g_min=G_MIN
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     rc = lib.kda_chunk_fwd(_p(q), _p(k), _p(v), _p(z), _p(A), _p(beta), _p(cu_seqlens), n, T, H, Dm,
                            dt, float(g_min), _p(init_state), _p(o), _p(fin), _p(workspace),
-                           workspace.numel(), _flags(qk_l2norm, beta_sigmoid), _stream(q.device))
+                           workspace.numel(), _flags(qk_l2norm, beta_sigmoid, q_scale), _stream(q.device))
     _check(rc, "kda_chunk_fwd")
     return o, fin
 
 
 def chunk_fwd_ckpt(q, k, v, z, A, beta, ckpt_interval, ckpt_slot, ckpt, cu_seqlens=None, init_state=None,
                    g_min=G_MIN, output_final_state=True, n_seqs=1, workspace=None, out=None, qk_l2norm=False,
-                   beta_sigmoid=False):
+                   beta_sigmoid=False, q_scale=False):
     """kda_chunk_fwd_ckpt: chunk_fwd that also writes document states at
     ckpt_interval-aligned positions.  ckpt_slot int32 [n, per_seq] (device) maps
     (document, j) -> page of ckpt [n_slots, H, 128, 128] fp32 (device) for the
@@ -191,20 +201,23 @@ def chunk_fwd_ckpt(q, k, v, z, A, beta, ckpt_interval, ckpt_slot, ckpt, cu_seqle
     rc = lib.kda_chunk_fwd_ckpt(_p(q), _p(k), _p(v), _p(z), _p(A), _p(beta), _p(cu_seqlens), n, T, H, Dm,
                                 dt, float(g_min), _p(init_state), _p(o), _p(fin), int(ckpt_interval), _p(ckpt_slot),
                                 ckpt_slot.shape[1], _p(ckpt), ckpt.shape[0], _p(workspace), workspace.numel(),
-                                _flags(qk_l2norm, beta_sigmoid), _stream(q.device))
+                                _flags(qk_l2norm, beta_sigmoid, q_scale), _stream(q.device))
     _check(rc, "kda_chunk_fwd_ckpt")
     return o, fin
 
 
 def segment_scan(q, k, v, z, A, beta, n_segments, cu_seqlens=None, init_state=None, g_min=G_MIN,
                  output_final_state=True, return_pairs=False, n_seqs=1, workspace=None, qk_l2norm=False,
-                 beta_sigmoid=False):
-    """kda_segment_scan: intra-device segment-parallel prefill.
+                 beta_sigmoid=False, q_scale=False):
+    """kda_segment_scan: intra-device segment-parallel prefill; n_segments = 0 takes
+    the automatic count (segment_scan_auto_segments).
     Returns (o, final_state) or (o, final_state, pairs_M, pairs_S) with pairs [H, n_seg, 128, 128]."""
     lib = load()
     _contig(q, k, v, z, A, beta, cu_seqlens, init_state, workspace)
     T, H, Dm = q.shape
     n = _n_seqs(cu_seqlens, n_seqs)
+    if n_segments == 0:
+        n_segments = segment_scan_auto_segments(T, H, n)
     dt = _dtype_code(q)
     o = torch.empty_like(q)
     fin = torch.empty((n, H, Dm, Dm), device=q.device, dtype=torch.float32) if output_final_state else None
@@ -217,8 +230,8 @@ def segment_scan(q, k, v, z, A, beta, n_segments, cu_seqlens=None, init_state=No
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     rc = lib.kda_segment_scan(_p(q), _p(k), _p(v), _p(z), _p(A), _p(beta), _p(cu_seqlens), n, T, H, Dm,
                               dt, float(g_min), _p(init_state), int(n_segments), _p(pm), _p(ps),
-                              _p(o), _p(fin), _p(workspace), workspace.numel(), _flags(qk_l2norm, beta_sigmoid),
-                              _stream(q.device))
+                              _p(o), _p(fin), _p(workspace), workspace.numel(),
+                              _flags(qk_l2norm, beta_sigmoid, q_scale), _stream(q.device))
     _check(rc, "kda_segment_scan")
     if return_pairs:
         return o, fin, pm, ps
@@ -226,7 +239,7 @@ def segment_scan(q, k, v, z, A, beta, n_segments, cu_seqlens=None, init_state=No
 
 
 def decode_step(state, q, k, v, z, beta, A, cache, num_accepted=None, g_min=G_MIN,
-                error_word=None, out=None, qk_l2norm=False, beta_sigmoid=False):
+                error_word=None, out=None, qk_l2norm=False, beta_sigmoid=False, q_scale=False):
     """kda_decode_step: in-place state update with MTP replay.
     state [N, H, 128, 128] fp32 (updated in place); q, k, v, z [N, W, H, 128]; beta [N, W, H];
     cache = (cache_q, cache_k, cache_v, cache_z, cache_beta) with W-1 slots (updated in place);
@@ -240,7 +253,7 @@ def decode_step(state, q, k, v, z, beta, A, cache, num_accepted=None, g_min=G_MI
     o = out if out is not None else torch.empty_like(q)
     rc = lib.kda_decode_step(_p(state), _p(q), _p(k), _p(v), _p(z), _p(beta), _p(A), _p(cq), _p(ck),
                              _p(cv), _p(cz), _p(cb), _p(num_accepted), N, H, Dm, W, _dtype_code(q),
-                             float(g_min), _p(o), _p(error_word), _flags(qk_l2norm, beta_sigmoid),
+                             float(g_min), _p(o), _p(error_word), _flags(qk_l2norm, beta_sigmoid, q_scale),
                              _stream(q.device))
     _check(rc, "kda_decode_step")
     return o
@@ -248,7 +261,7 @@ def decode_step(state, q, k, v, z, beta, A, cache, num_accepted=None, g_min=G_MI
 
 def decode_step_fused(state, q, k, v, z, beta, A, conv_w, conv_state, o_gate, o_norm_w, cache,
                       num_accepted=None, o_norm_eps=1e-6, g_min=G_MIN, error_word=None, out=None,
-                      qk_l2norm=False, beta_sigmoid=False, conv_silu=False):
+                      qk_l2norm=False, beta_sigmoid=False, conv_silu=False, q_scale=False):
     """kda_decode_step_fused: the decode step with the short convolution of q, k, v in
     front of the recurrence and the gated per-head output norm after it.
     As decode_step, plus conv_w [3, H, 128, 4] fp32 (tap 3 on the current token),
@@ -270,7 +283,7 @@ def decode_step_fused(state, q, k, v, z, beta, A, conv_w, conv_state, o_gate, o_
     if tuple(o_gate.shape) != (N, W, H, Dm) or tuple(o_norm_w.shape) != (Dm,):
         raise KDAError("o_gate must be [N, W, H, D] and o_norm_w [D]")
     o = out if out is not None else torch.empty_like(q)
-    flags = _flags(qk_l2norm, beta_sigmoid) | (KDA_FLAG_CONV_SILU if conv_silu else 0)
+    flags = _flags(qk_l2norm, beta_sigmoid, q_scale) | (KDA_FLAG_CONV_SILU if conv_silu else 0)
     rc = lib.kda_decode_step_fused(_p(state), _p(q), _p(k), _p(v), _p(z), _p(beta), _p(A), _p(conv_w),
                                    _p(conv_state), _p(o_gate), _p(o_norm_w), float(o_norm_eps), _p(cq),
                                    _p(ck), _p(cv), _p(cz), _p(cb), _p(num_accepted), N, H, Dm, W,
@@ -285,6 +298,47 @@ def read_device_error(workspace: torch.Tensor) -> int:
     code = ctypes.c_int32(0)
     rc = load().kda_read_device_error(_p(workspace), ctypes.byref(code), _stream(workspace.device))
     _check(rc, "kda_read_device_error")
+    return int(code.value)
+
+
+def segment_scan_auto_segments(T_total: int, H: int, n_seqs: int = 1) -> int:
+    """kda_segment_scan_auto_segments: the count kda_segment_scan takes for n_segments = 0."""
+    return int(load().kda_segment_scan_auto_segments(T_total, H, n_seqs))
+
+
+def set_wait_budget(cycles: int) -> int:
+    """kda_set_wait_budget: clock-cycle limit of the waits on other blocks' flags and of
+    the decode's copy waits for the calls that follow (<= 0: the default, about one
+    second).  Returns the previous limit."""
+    return int(load().kda_set_wait_budget(int(cycles)))
+
+
+def chunk_fwd_noalloc(q, k, v, z, A, beta, cu_seqlens=None, init_state=None, g_min=G_MIN,
+                      output_final_state=True, n_seqs=1, out=None, qk_l2norm=False, beta_sigmoid=False,
+                      q_scale=False):
+    """kda_chunk_fwd_noalloc: chunk_fwd with the library's fixed device array as its
+    workspace (the library allocates nothing; this binding still allocates o and the
+    final state with torch unless `out` is given and output_final_state is False)."""
+    lib = load()
+    _contig(q, k, v, z, A, beta, cu_seqlens, init_state, out)
+    T, H, Dm = q.shape
+    n = _n_seqs(cu_seqlens, n_seqs)
+    o = out if out is not None else torch.empty_like(q)
+    fin = torch.empty((n, H, Dm, Dm), device=q.device, dtype=torch.float32) if output_final_state else None
+    rc = lib.kda_chunk_fwd_noalloc(_p(q), _p(k), _p(v), _p(z), _p(A), _p(beta), _p(cu_seqlens), n, T, H, Dm,
+                                   _dtype_code(q), float(g_min), _p(init_state), _p(o), _p(fin),
+                                   _flags(qk_l2norm, beta_sigmoid, q_scale), _stream(q.device))
+    _check(rc, "kda_chunk_fwd_noalloc")
+    return o, fin
+
+
+def noalloc_read_device_error(device=None) -> int:
+    """kda_noalloc_read_device_error: the device error word of the last
+    kda_chunk_fwd_noalloc on the current device."""
+    code = ctypes.c_int32(0)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    rc = load().kda_noalloc_read_device_error(ctypes.byref(code), _stream(dev))
+    _check(rc, "kda_noalloc_read_device_error")
     return int(code.value)
 
 

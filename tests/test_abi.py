@@ -50,7 +50,7 @@ def test_workspace_sizes_grow_with_work():
     assert kda.segment_scan_workspace_size(8192, 16, 1, 4) > s1
     lib = kda.load()
     assert lib.kda_chunk_fwd_workspace_size(-1, 16, 1, 0) == 0
-    assert lib.kda_segment_scan_workspace_size(64, 1, 1, 0, 0) == 0
+    assert lib.kda_segment_scan_workspace_size(64, 1, 1, -1, 0) == 0
 
 
 def test_segment_planner_host_logic():
@@ -107,9 +107,12 @@ def test_chunk_fwd_rejects_bad_arguments_before_launch():
 
 def test_segment_scan_and_decode_reject_bad_arguments():
     lib = kda.load()
+    r = lib.kda_segment_scan(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 128, 2, 128, 0, -5.0, None, -1,
+                             None, None, FAKE, None, None, 0, 0, None)
+    assert r == 1  # a negative segment count
     r = lib.kda_segment_scan(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 128, 2, 128, 0, -5.0, None, 0,
                              None, None, FAKE, None, None, 0, 0, None)
-    assert r == 1  # zero segments
+    assert r == 5  # zero is the automatic count: accepted, then the missing workspace is reported
     r = lib.kda_segment_scan(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 128, 2, 96, 0, -5.0, None, 4,
                              None, None, FAKE, None, None, 0, 0, None)
     assert r == 2
@@ -123,7 +126,7 @@ def test_segment_scan_and_decode_reject_bad_arguments():
     assert dec(N=0) == 1
     assert dec(state=None) == 1
     assert dec(cq=None) == 1
-    assert dec(flags=8) == 1
+    assert dec(flags=16) == 1
     assert dec(flags=4) == 1  # the convolution option belongs to the fused step
 
 
@@ -146,7 +149,7 @@ def test_decode_fused_rejects_bad_arguments():
     for name in ("conv_w", "conv_state", "o_gate", "o_norm_w", "cq"):
         assert dec(**{name: None}) == 1, name
     assert dec(conv_w=ALIGNED_BAD) == 1 and dec(conv_state=ALIGNED_BAD) == 1
-    assert dec(flags=8) == 1
+    assert dec(flags=16) == 1
 
 
 def test_binding_rejects_host_tensors_before_any_launch():
@@ -196,3 +199,41 @@ def test_chunk_fwd_ckpt_rejects_bad_checkpoint_arguments():
     assert call(ck=None) == 1
     assert call(ck=ctypes.c_void_p((1 << 20) + 4)) == 1  # misaligned pages
     assert call() == 5                    # valid checkpoints, but no workspace
+
+
+def test_wait_budget_setter_returns_previous_and_restores_default():
+    lib = kda.load()
+    default = kda.set_wait_budget(12345)
+    assert default == 2_000_000_000
+    assert kda.set_wait_budget(0) == 12345   # <= 0 restores the default
+    assert kda.set_wait_budget(-7) == default
+    assert kda.set_wait_budget(default) == default
+
+
+def test_segment_scan_auto_count_host_logic():
+    """n_segments = 0: the wave rule's count (two rerun blocks per (segment, head)
+    in one wave of the SMs, at most sqrt(chunks / 6), 64 and half the chunks, at
+    least 1); the workspace size follows the resolved count."""
+    lib = kda.load()
+    n = kda.segment_scan_auto_segments(1 << 20, 8, 1)
+    assert 2 <= n <= 64
+    assert kda.segment_scan_auto_segments(64, 1, 1) == 1
+    assert kda.segment_scan_auto_segments(-1, 8, 1) == 0
+    assert lib.kda_segment_scan_workspace_size(1 << 20, 8, 1, 0, 0) == \
+        lib.kda_segment_scan_workspace_size(1 << 20, 8, 1, n, 0)
+
+
+def test_q_scale_flag_accepted_unknown_flags_rejected():
+    """KDA_FLAG_Q_SCALE is a valid input option of every compute call; an unknown
+    bit is rejected before any launch (no GPU touched)."""
+    lib = kda.load()
+    fake = ctypes.c_void_p(1 << 20)
+    args = (fake, fake, fake, fake, fake, fake, None, 1, 64, 1, 128, 0, -5.0, None, fake, None)
+    # a workspace of zero bytes: a valid flag gets as far as the workspace check
+    assert lib.kda_chunk_fwd(*args, fake, 0, 8, None) == 5
+    assert lib.kda_chunk_fwd(*args, fake, 0, 16, None) == 1
+
+
+def test_noalloc_error_reader_rejects_null():
+    lib = kda.load()
+    assert lib.kda_noalloc_read_device_error(None, None) == 1

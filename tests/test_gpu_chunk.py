@@ -6,13 +6,15 @@ import torch
 import kda_synth
 import linear_attention_serving_gb300 as kda
 import oracle
-from kda_testutil import TOL, rel_fro, to_dev
+from kda_testutil import TOL, err_report, rel_fro, to_dev
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
 def run_both(inp, n_seqs=1):
+    """kda_chunk_fwd on the GPU and the oracle on the same inputs; returns
+    (o, final state, oracle o, oracle final state, cu_seqlens used)."""
     d = to_dev(inp, DEV)
     o, fin = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"],
                            cu_seqlens=d["cu_seqlens"], init_state=d["init_state"], n_seqs=n_seqs)
@@ -23,29 +25,37 @@ def run_both(inp, n_seqs=1):
         cu = torch.arange(0, T + 1, T // n_seqs, dtype=torch.int32)
     o_ref, f_ref = oracle.recurrent(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"],
                                     cu_seqlens=cu, init_state=inp["init_state"])
-    return o, fin, o_ref, f_ref
+    return o, fin, o_ref, f_ref, cu
 
 
-def check(o, fin, o_ref, f_ref, dtype):
+def check(o, fin, o_ref, f_ref, dtype, cu=None):
+    """Whole-tensor tolerance on o and the final state; the messages also name
+    the worst (sequence, head) block."""
     to, tf = TOL[dtype]
-    eo, ef = rel_fro(o, o_ref), rel_fro(fin, f_ref)
+    eo, mo = err_report(o, o_ref, "tokens", cu)
+    ef, mf = err_report(fin, f_ref, "state")
     assert np.isfinite(eo) and np.isfinite(ef)
-    assert eo <= to, f"o rel err {eo:.3e} > {to}"
-    assert ef <= tf, f"final_state rel err {ef:.3e} > {tf}"
-    return eo, ef
+    assert eo <= to, f"o: {mo} > {to}"
+    assert ef <= tf, f"final_state: {mf} > {tf}"
+    return eo, ef, mo, mf
+
+
+def check_run(res, dtype):
+    o, fin, o_ref, f_ref, cu = res
+    return check(o, fin, o_ref, f_ref, dtype, cu)
 
 
 def test_tiny_fp32_workload():
     """B=1, H=2, T=256, fp32, z~N(0,1), A=0, zero init, seed 0."""
     inp = kda_synth.workload_inputs("tiny_fp32")
-    check(*run_both(inp), "f32")
+    check_run(run_both(inp), "f32")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 200, 333])
 def test_ragged_lengths(dtype, T):
     inp = kda_synth.prefill_inputs(T, 3, dtype, seed=100 + T, z_std=1.5, A_std=0.5, init_std=0.05)
-    check(*run_both(inp), dtype)
+    check_run(run_both(inp), dtype)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -53,7 +63,7 @@ def test_slow_decay_carries_state_across_chunks(dtype):
     """z ~ N(-10, 1): g ~ -2e-4 per token, small beta: the state entering a chunk
     dominates its outputs, so the inter-chunk path is exercised (not washed out)."""
     inp = kda_synth.prefill_inputs(700, 2, dtype, seed=7, z_mean=-10.0, beta_mean=-4.0, init_std=0.5)
-    check(*run_both(inp), dtype)
+    check_run(run_both(inp), dtype)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -61,7 +71,7 @@ def test_gate_at_lower_bound(dtype):
     """z ~ N(8, 1): g close to g_min = -5 everywhere; the 16-token sub-tile factors
     reach e^{+-80} and must stay finite."""
     inp = kda_synth.prefill_inputs(256, 2, dtype, seed=8, z_mean=8.0, init_std=0.05)
-    check(*run_both(inp), dtype)
+    check_run(run_both(inp), dtype)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -69,25 +79,25 @@ def test_packed_documents_with_empty_and_short_docs(dtype):
     lens = [100, 0, 1, 64, 130, 0, 77]
     cu = kda_synth.cu_from_lengths(lens)
     inp = kda_synth.prefill_inputs(sum(lens), 2, dtype, seed=9, cu_seqlens=cu, init_std=0.05)
-    check(*run_both(inp), dtype)
+    check_run(run_both(inp), dtype)
 
 
 def test_equal_length_batch_without_cu_seqlens():
     inp = kda_synth.prefill_inputs(4 * 96, 2, "bf16", seed=10, init_std=0.05, n_init=4)
-    check(*run_both(inp, n_seqs=4), "bf16")
+    check_run(run_both(inp, n_seqs=4), "bf16")
 
 
 def test_prefill_h16_t8k_full_size():
     """Full size prefill: B=1, H=16, T=8192, bf16, z~N(0,1.5), A~N(0,0.5)."""
     inp = kda_synth.workload_inputs("prefill_h16_t8k")
-    eo, ef = check(*run_both(inp), "bf16")
-    print(f"prefill_h16_t8k: o {eo:.3e}, final_state {ef:.3e}")
+    eo, ef, mo, mf = check_run(run_both(inp), "bf16")
+    print(f"prefill_h16_t8k: o {mo}; final_state {mf}")
 
 
 def test_varlen_32k_h32_full_size():
     inp = kda_synth.workload_inputs("varlen_32k_h32")
-    eo, ef = check(*run_both(inp), "bf16")
-    print(f"varlen_32k_h32: o {eo:.3e}, final_state {ef:.3e}")
+    eo, ef, mo, mf = check_run(run_both(inp), "bf16")
+    print(f"varlen_32k_h32: o {mo}; final_state {mf}")
 
 
 def test_bitwise_deterministic():
@@ -142,7 +152,7 @@ def test_planner_segmented_path(T, H, n_seqs):
     oracle, across the document boundary of the two-document batch too."""
     assert kda.chunk_fwd_plan_segments(T, H, n_seqs) >= 2
     inp = kda_synth.prefill_inputs(T, H, "bf16", seed=900 + T, z_std=1.0, init_std=0.05, n_init=n_seqs)
-    check(*run_both(inp, n_seqs=n_seqs), "bf16")
+    check_run(run_both(inp, n_seqs=n_seqs), "bf16")
 
 
 def raw_inputs(T, H, dtype, seed, n_seqs=1):
@@ -157,19 +167,22 @@ def raw_inputs(T, H, dtype, seed, n_seqs=1):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("T,H,flags", [(333, 3, (True, True)), (333, 3, (True, False)), (333, 3, (False, True)),
-                                       (2048, 24, (True, True)), (8192, 1, (True, True))])
+@pytest.mark.parametrize("T,H,flags", [(333, 3, (True, True, False)), (333, 3, (True, False, False)),
+                                       (333, 3, (False, True, False)), (333, 3, (False, False, True)),
+                                       (333, 3, (True, True, True)), (2048, 24, (True, True, True)),
+                                       (8192, 1, (True, True, True))])
 def test_input_options(dtype, T, H, flags):
-    """KDA_FLAG_QK_L2NORM / KDA_FLAG_BETA_SIGMOID against the oracle on the
-    prepared inputs; the shapes take the fused launch (H=3), the three-kernel
-    path (H=24: 48 chains) and, in bf16, the automatic segments (H=1, T=8192)."""
-    l2, sig = flags
+    """KDA_FLAG_QK_L2NORM / KDA_FLAG_BETA_SIGMOID / KDA_FLAG_Q_SCALE against the
+    oracle on the prepared inputs; the shapes take the fused launch (H=3), the
+    three-kernel path (H=24: 48 chains) and, in bf16, the automatic segments
+    (H=1, T=8192)."""
+    l2, sig, qs = flags
     inp = raw_inputs(T, H, dtype, seed=300 + T + H)
     d = to_dev(inp, DEV)
     o, fin = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], init_state=d["init_state"],
-                           qk_l2norm=l2, beta_sigmoid=sig)
+                           qk_l2norm=l2, beta_sigmoid=sig, q_scale=qs)
     torch.cuda.synchronize()
-    qn, kn, bn = oracle.input_prep(inp["q"], inp["k"], inp["beta"], qk_l2norm=l2, beta_sigmoid=sig)
+    qn, kn, bn = oracle.input_prep(inp["q"], inp["k"], inp["beta"], qk_l2norm=l2, beta_sigmoid=sig, q_scale=qs)
     o_ref, f_ref = oracle.recurrent(qn, kn, inp["v"], inp["z"], inp["A"], bn, init_state=inp["init_state"])
     check(o, fin, o_ref, f_ref, dtype)
 
@@ -236,4 +249,4 @@ def test_checkpoints(dtype, T, H, docs, interval):
             assert torch.isnan(ck[s_idx]).all(), f"page {s_idx} written"
     o_ref, f_ref = oracle.recurrent(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"],
                                     cu_seqlens=cu, init_state=inp["init_state"])
-    check(o, fin, o_ref, f_ref, dtype)
+    check(o, fin, o_ref, f_ref, dtype, cu)

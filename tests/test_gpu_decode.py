@@ -5,7 +5,7 @@ import torch
 import kda_synth
 import linear_attention_serving_gb300 as kda
 import oracle
-from kda_testutil import TOL, rel_fro
+from kda_testutil import TOL, err_report, rel_fro
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -18,7 +18,11 @@ def empty_cache(N, W, H, dtype):
             torch.zeros((N, W - 1, H), device=DEV))
 
 
-def run_steps(N, H, W, dtype, steps, seed, sample=None, A_std=0.5):
+def run_steps(N, H, W, dtype, steps, seed, sample=None, A_std=0.5, z_mean=0.0, nacc_fill=None):
+    """Decode steps on the GPU against the oracle's step over the same windows
+    (all sequences unless `sample` names some); o and the state after every step
+    at the stated tolerances, the cache exactly.  nacc_fill replaces every
+    accepted count after the first step."""
     state = kda_synth.decode_state(N, H, seed, std=0.05, device=DEV)
     A = kda_synth.decode_A(H, seed, A_std=A_std, device=DEV)
     cache = empty_cache(N, W, H, dtype)
@@ -29,16 +33,20 @@ def run_steps(N, H, W, dtype, steps, seed, sample=None, A_std=0.5):
     ref_cache = tuple(c[idx] for c in ref_cache)
     tol_o, tol_s = (1e-4, 1e-4) if dtype == "f32" else TOL["bf16"]
     for step in range(steps):
-        w = kda_synth.decode_window(N, W, H, step, seed, dtype, z_std=1.5, device=DEV)
+        w = kda_synth.decode_window(N, W, H, step, seed, dtype, z_std=1.5, z_mean=z_mean, device=DEV)
         nacc = None if step == 0 else w["num_accepted"]
+        if nacc is not None and nacc_fill is not None:
+            nacc = torch.full_like(nacc, nacc_fill)
         o = kda.decode_step(state, w["q"], w["k"], w["v"], w["z"], w["beta"], A, cache, num_accepted=nacc)
         torch.cuda.synchronize()
         sel = lambda x: x.cpu()[idx]
         o_ref, ref_state, ref_cache = oracle.decode_step(
             ref_state, sel(w["q"]), sel(w["k"]), sel(w["v"]), sel(w["z"]), sel(w["beta"]), A.cpu(),
             *ref_cache, num_accepted=None if nacc is None else sel(nacc))
-        assert rel_fro(o.cpu()[idx], o_ref) <= tol_o, f"step {step}: o"
-        assert rel_fro(state.cpu()[idx], ref_state) <= tol_s, f"step {step}: state"
+        eo, mo = err_report(o.cpu()[idx], o_ref, "decode")
+        es, ms = err_report(state.cpu()[idx], ref_state, "state")
+        assert eo <= tol_o, f"step {step}: o {mo}"
+        assert es <= tol_s, f"step {step}: state {ms}"
         for c, rc in zip(cache, ref_cache):
             assert torch.equal(c.cpu()[idx].double(), torch.from_numpy(rc)), f"step {step}: cache"
     return state
@@ -55,10 +63,18 @@ def test_decode_window_sizes(W):
 
 
 def test_decode_mtp_b256_h96_full_size():
-    """N=256, H=96, W=5 (1 + 4 drafts), fp32: full-size launch, sampled sequences
-    checked against the oracle over several steps."""
-    run_steps(N=256, H=96, W=5, dtype="f32", steps=3, seed=5, sample=[0, 1, 77, 128, 200, 255],
-              A_std=0.0)
+    """N=256, H=96, W=5 (1 + 4 drafts), fp32: full-size launch, every sequence
+    and head checked against the oracle over three steps."""
+    run_steps(N=256, H=96, W=5, dtype="f32", steps=3, seed=5, A_std=0.0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_gate_at_bound_longest_window(dtype):
+    """The numeric extreme of the lazy per-row decay: the gate at its lower
+    bound (z ~ N(8, 1), g close to -5 on every channel), the largest window
+    (W = 8) and every draft accepted (num_accepted = 7), so one step runs 15
+    tokens and the row scale falls to about e^-75 while k / s_t grows to e^75."""
+    run_steps(N=6, H=3, W=8, dtype=dtype, steps=3, seed=46, z_mean=8.0, nacc_fill=7)
 
 
 def test_num_accepted_out_of_range_sets_error_and_skips():
@@ -79,10 +95,11 @@ def test_num_accepted_out_of_range_sets_error_and_skips():
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_decode_input_options(dtype):
-    """KDA_FLAG_QK_L2NORM | KDA_FLAG_BETA_SIGMOID: unnormalised q, k and beta
-    logits in; the oracle runs on the prepared inputs (its input_prep), and the
-    cache keeps the drafts' inputs as given."""
+@pytest.mark.parametrize("q_scale", [False, True])
+def test_decode_input_options(dtype, q_scale):
+    """KDA_FLAG_QK_L2NORM | KDA_FLAG_BETA_SIGMOID (and KDA_FLAG_Q_SCALE):
+    unnormalised q, k and beta logits in; the oracle runs on the prepared inputs
+    (its input_prep), and the cache keeps the drafts' inputs as given."""
     N, H, W, seed = 6, 3, 5, 61
     g = torch.Generator().manual_seed(seed)
     state = kda_synth.decode_state(N, H, seed, std=0.05, device=DEV)
@@ -100,14 +117,18 @@ def test_decode_input_options(dtype):
         nacc = None if step == 0 else w["num_accepted"]
         dev = lambda x: x.to(DEV)
         o = kda.decode_step(state, dev(qr), dev(kr), dev(w["v"]), dev(w["z"]), dev(br), A, cache,
-                            num_accepted=None if nacc is None else dev(nacc), qk_l2norm=True, beta_sigmoid=True)
+                            num_accepted=None if nacc is None else dev(nacc), qk_l2norm=True, beta_sigmoid=True,
+                            q_scale=q_scale)
         torch.cuda.synchronize()
-        qn, kn, bn = oracle.input_prep(qr, kr, br, qk_l2norm=True, beta_sigmoid=True)
-        cqn, ckn, cbn = oracle.input_prep(raw_cache[0], raw_cache[1], raw_cache[4], qk_l2norm=True, beta_sigmoid=True)
+        qn, kn, bn = oracle.input_prep(qr, kr, br, qk_l2norm=True, beta_sigmoid=True, q_scale=q_scale)
+        cqn, ckn, cbn = oracle.input_prep(raw_cache[0], raw_cache[1], raw_cache[4], qk_l2norm=True, beta_sigmoid=True,
+                                          q_scale=q_scale)
         o_ref, ref_state, _ = oracle.decode_step(ref_state, qn, kn, w["v"], w["z"], bn, A.cpu(), cqn, ckn,
                                                  raw_cache[2], raw_cache[3], cbn, num_accepted=nacc)
-        assert rel_fro(o.cpu(), o_ref) <= tol_o, f"step {step}: o"
-        assert rel_fro(state.cpu(), ref_state) <= tol_s, f"step {step}: state"
+        eo, mo = err_report(o.cpu(), o_ref, "decode")
+        es, ms = err_report(state.cpu(), ref_state, "state")
+        assert eo <= tol_o, f"step {step}: o {mo}"
+        assert es <= tol_s, f"step {step}: state {ms}"
         # the new drafts' inputs, as given, become the cache
         raw_cache = (qr[:, 1:].contiguous(), kr[:, 1:].contiguous(), w["v"][:, 1:].contiguous(),
                      w["z"][:, 1:].contiguous(), br[:, 1:].contiguous())
@@ -154,8 +175,10 @@ def run_fused_steps(N, H, W, dtype, steps, seed, sample=None, opts=FUSED_OPTS, e
             ref_state, sel(w["q"]), sel(w["k"]), sel(w["v"]), sel(w["z"]), sel(w["beta"]), A.cpu(),
             prm["conv_w"].cpu(), ref_cs, sel(w["o_gate"]), prm["o_norm_w"].cpu(), eps, *ref_cache,
             num_accepted=None if nacc is None else sel(nacc), **opts)
-        assert rel_fro(o.cpu()[idx], o_ref) <= tol_o, f"step {step}: o"
-        assert rel_fro(state.cpu()[idx], ref_state) <= tol_s, f"step {step}: state"
+        eo, mo = err_report(o.cpu()[idx], o_ref, "decode")
+        es, ms = err_report(state.cpu()[idx], ref_state, "state")
+        assert eo <= tol_o, f"step {step}: o {mo}"
+        assert es <= tol_s, f"step {step}: state {ms}"
         assert torch.equal(cs.cpu()[idx].double(), torch.from_numpy(ref_cs)), f"step {step}: conv state"
         for c, rc in zip(cache, ref_cache):
             assert torch.equal(c.cpu()[idx].double(), torch.from_numpy(rc)), f"step {step}: cache"
@@ -182,9 +205,14 @@ def test_decode_fused_l2norm_only():
     run_fused_steps(N=6, H=2, W=5, dtype="f32", steps=3, seed=76, opts=dict(qk_l2norm=True, beta_sigmoid=True))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_fused_with_q_scale(dtype):
+    run_fused_steps(N=6, H=2, W=5, dtype=dtype, steps=3, seed=78, opts=dict(FUSED_OPTS, q_scale=True))
+
+
 def test_decode_fused_b256_h96_full_size():
-    """N=256, H=96, W=5, fp32, the full-size fused launch; sampled sequences against the oracle."""
-    run_fused_steps(N=256, H=96, W=5, dtype="f32", steps=2, seed=5, sample=[0, 1, 77, 128, 200, 255])
+    """N=256, H=96, W=5, fp32, the full-size fused launch; every sequence and head against the oracle."""
+    run_fused_steps(N=256, H=96, W=5, dtype="f32", steps=2, seed=5)
 
 
 def test_decode_fused_out_of_range_keeps_sequence():

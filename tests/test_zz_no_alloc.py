@@ -4,10 +4,12 @@ device for its own pool, or a latency-critical path where a cudaMalloc and the
 device synchronisation it may bring are not acceptable).  It takes its
 workspace from a fixed array owned by the library instead of from the caller.
 
-Called through the C ABI with ctypes and checked against kda_chunk_fwd on two
-calls in a row with different inputs, so that anything the first call leaves in
-the shared array cannot hide a fault in the second.  This file is collected
-last so that a run stopping at the first failure has run every other test.
+Called through the C ABI with ctypes and checked against kda_chunk_fwd and
+against the fp64 oracle on two calls in a row with different inputs, so that
+anything the first call leaves in the shared array cannot hide a fault in the
+second; and a bad cu_seqlens must show up in the array's error word, which
+kda_noalloc_read_device_error reads.  This file is collected last so that a run
+stopping at the first failure has run every other test.
 """
 import ctypes
 
@@ -16,7 +18,8 @@ import torch
 
 import kda_synth
 import linear_attention_serving_gb300 as kda
-from kda_testutil import TOL, rel_fro, to_dev
+import oracle
+from kda_testutil import TOL, err_report, rel_fro, to_dev
 
 P, I, L, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
 KDA_ERR_WORKSPACE = 5
@@ -72,6 +75,33 @@ def test_noalloc_matches_chunk_fwd_on_two_calls(dtype):
         rc, o, fin = call_noalloc(fn, d, n)
         torch.cuda.synchronize()
         assert rc == 0, f"call {call}: status {rc}"
+        assert kda.noalloc_read_device_error() == 0
         to, tf = TOL[dtype]
         assert rel_fro(o, o_ref) <= to, f"call {call}: o"
         assert rel_fro(fin, f_ref) <= tf, f"call {call}: final state"
+        # and against the oracle on the same inputs
+        oo, of = oracle.recurrent(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"],
+                                  cu_seqlens=cu, init_state=inp["init_state"])
+        eo, mo = err_report(o, oo, "tokens", cu, n)
+        ef, mf = err_report(fin, of, "state")
+        assert eo <= to, f"call {call}: o vs oracle {mo}"
+        assert ef <= tf, f"call {call}: final state vs oracle {mf}"
+
+
+@pytest.mark.gpu
+def test_noalloc_reports_bad_cu_seqlens():
+    """Decreasing document offsets, built on the host: the call returns KDA_OK (the
+    check needs device data), writes nothing, and its error word holds
+    KDA_DEVERR_CU_SEQLENS; the next good call clears it."""
+    fn = noalloc_fn()
+    inp = kda_synth.prefill_inputs(256, 1, "bf16", seed=79)
+    d = to_dev(inp, "cuda")
+    d["cu_seqlens"] = torch.tensor([0, 200, 100, 256], dtype=torch.int32, device="cuda")
+    d["init_state"] = None
+    rc, o, _ = call_noalloc(fn, d, 3)
+    assert rc == 0
+    assert kda.noalloc_read_device_error() & 1
+    d["cu_seqlens"] = torch.tensor([0, 100, 200, 256], dtype=torch.int32, device="cuda")
+    rc, o, fin = call_noalloc(fn, d, 3)
+    assert rc == 0
+    assert kda.noalloc_read_device_error() == 0
