@@ -30,18 +30,16 @@ constexpr int FUSED_SLICES = D / FUSED_N;  // chain blocks per (document, head)
 // that the default launch keeps its registers).
 template <bool OPTS, bool CKPT>
 __global__ void __launch_bounds__(PT_THREADS, 1)
-fused_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z, const float *__restrict__ A,
-                const float *__restrict__ beta, int H, float g_min, Plan plan, char *__restrict__ records,
-                ScanArgs sa, int n_chain, int *ready) {
+fused_tc_kernel(const __grid_constant__ InputMaps maps, const float *__restrict__ A, const float *__restrict__ beta,
+                int H, float g_min, Plan plan, char *__restrict__ records, ScanArgs sa, int n_chain, int *ready) {
     extern __shared__ uint8_t smraw[];
     // A chain would only wait for its first records at the start, so each chain
     // block first prepares one unit (units 0 .. n_chain - 1); prep block j takes
     // units n_chain + j, n_chain + j + n_prep, ...  (One call site: the prep
     // code is inlined once.)
     const bool chain = (int)blockIdx.x < n_chain;
-    prep_blocks<OPTS>(q, k, v, z, A, beta, H, g_min, plan, records, smraw, blockIdx.x,
-                chain ? (1 << 30) : (int)gridDim.x - n_chain, ready);
+    prep_blocks<OPTS>(&maps, A, beta, H, g_min, plan, records, smraw, blockIdx.x,
+                      chain ? (1 << 30) : (int)gridDim.x - n_chain, ready);
     if (chain) {
         fence_async_smem();
         __syncthreads();
@@ -55,7 +53,7 @@ fused_tc_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__rest
 }  // namespace
 
 int launch_fused_tc(const void *q, const void *k, const void *v, const float *z, const float *A,
-                    const float *beta, int H, float g_min, const ScanArgs &sa, int *ready, int n_sm,
+                    const float *beta, int64_t T_total, int H, float g_min, const ScanArgs &sa, int *ready, int n_sm,
                     cudaStream_t s, bool *used) {
     *used = false;
     const Plan &p = sa.plan;
@@ -76,12 +74,14 @@ int launch_fused_tc(const void *q, const void *k, const void *v, const float *z,
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, PT_THREADS, smem) != cudaSuccess ||
         per_sm < 1)
         return KDA_OK;
-    const __nv_bfloat16 *qb = (const __nv_bfloat16 *)q, *kb = (const __nv_bfloat16 *)k, *vb = (const __nv_bfloat16 *)v;
+    InputMaps maps;
+    const int rc = make_input_maps(q, k, v, z, T_total, H, &maps);
+    if (rc) return rc;
     char *records = (char *)sa.records;
     Plan plan = p;
     ScanArgs a = sa;
     int nc = (int)n_chain;
-    void *args[] = {&qb, &kb, &vb, &z, &A, &beta, &H, &g_min, &plan, &records, &a, &nc, &ready};
+    void *args[] = {&maps, &A, &beta, &H, &g_min, &plan, &records, &a, &nc, &ready};
     const cudaError_t e = cudaLaunchCooperativeKernel((const void *)kern, dim3(n_sm), dim3(PT_THREADS),
                                                       args, smem, s);
     if (e != cudaSuccess) {

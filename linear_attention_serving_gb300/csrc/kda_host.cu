@@ -84,9 +84,10 @@ namespace {
 // Prep launch by input type: tcgen05 tensor cores for bf16 inputs, exact fp32
 // CUDA cores for fp32 inputs.
 int launch_prep(const void *q, const void *k, const void *v, const float *z, const float *A,
-                const float *beta, int H, int dtype, float g_min, const Plan &p, void *records,
+                const float *beta, int64_t T_total, int H, int dtype, float g_min, const Plan &p, void *records,
                 cudaStream_t s) {
-    if (dtype == KDA_BF16) return launch_prep_tc(q, k, v, z, A, beta, H, g_min, p, records, device_sm_count(), s);
+    if (dtype == KDA_BF16)
+        return launch_prep_tc(q, k, v, z, A, beta, T_total, H, g_min, p, records, device_sm_count(), s);
     return launch_prep_simt(q, k, v, z, A, beta, H, dtype, g_min, p, records, s);
 }
 
@@ -189,7 +190,7 @@ int run_segment_scan(const void *q, const void *k, const void *v, const float *z
     void *records = base + w.off_rec;
     float *pairs = (float *)(base + w.off_pairs);
     float *s_enter = (float *)(base + w.off_enter);
-    if ((rc = launch_prep(q, k, v, z, A, beta, H, dtype, g_min, p, records, s))) return rc;
+    if ((rc = launch_prep(q, k, v, z, A, beta, T_total, H, dtype, g_min, p, records, s))) return rc;
 
     ScanArgs a;
     memset(&a, 0, sizeof(a));
@@ -357,12 +358,12 @@ int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *z, 
     if (dtype == KDA_BF16) {
         // few (document, head) chains: prep, chains and outputs in one launch
         bool used = false;
-        if ((rc = launch_fused_tc(q, k, v, z, A, beta, H, g_min, a, (int *)((char *)workspace + w.off_ready),
-                                  device_sm_count(), s, &used)))
+        if ((rc = launch_fused_tc(q, k, v, z, A, beta, T_total, H, g_min, a,
+                                  (int *)((char *)workspace + w.off_ready), device_sm_count(), s, &used)))
             return rc;
         if (used) return KDA_OK;
     }
-    if ((rc = launch_prep(q, k, v, z, A, beta, H, dtype, g_min, p, records, s))) return rc;
+    if ((rc = launch_prep(q, k, v, z, A, beta, T_total, H, dtype, g_min, p, records, s))) return rc;
     return launch_scan(a, dtype, s);
 }
 

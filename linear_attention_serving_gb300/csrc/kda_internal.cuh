@@ -21,6 +21,7 @@
 // as the pages, with the state-independent products moved off the chain.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (a type only; the driver functions come through the runtime)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -279,15 +280,22 @@ __device__ __forceinline__ float *ckpt_row(const ScanArgs &a, const ChunkInfo &c
 constexpr int SCAN_DOCS = 0;
 constexpr int SCAN_SEGMENTS = 1;
 
+// Tensor maps of the bf16 prep's input tiles (kda_tma.cu): q, k, v, z as 3-D
+// tensors {D, H, T}, box {D, 1, C} (one head over one 64-token chunk).
+struct InputMaps {
+    CUtensorMap q, k, v, z;
+};
+int make_input_maps(const void *q, const void *k, const void *v, const float *z, int64_t T, int H, InputMaps *out);
+
 int launch_prep_tc(const void *q, const void *k, const void *v, const float *z, const float *A,
-                   const float *beta, int H, float g_min, const Plan &p, void *records, int n_sm,
+                   const float *beta, int64_t T_total, int H, float g_min, const Plan &p, void *records, int n_sm,
                    cudaStream_t s);
 int launch_scan_simt(const ScanArgs &a, int dtype, cudaStream_t s);
 int launch_scan_tc(const ScanArgs &a, int n_sm, cudaStream_t s);
 int launch_out_tc(const Plan &p, int H, const void *records, void *o, int n_sm, cudaStream_t s);
 // `ready` holds plan max_chunks x H flags that the caller has zeroed on stream s.
 int launch_fused_tc(const void *q, const void *k, const void *v, const float *z, const float *A,
-                    const float *beta, int H, float g_min, const ScanArgs &sa, int *ready, int n_sm,
+                    const float *beta, int64_t T_total, int H, float g_min, const ScanArgs &sa, int *ready, int n_sm,
                     cudaStream_t s, bool *used);
 int device_sm_count();
 int launch_compose(const Plan &p, int H, int n_seg, const float *pairs, float *s_enter,

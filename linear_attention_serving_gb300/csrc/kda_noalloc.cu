@@ -123,7 +123,7 @@ extern "C" int kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v
 
     void *records = base + w.off_rec;
     if (dtype == KDA_BF16)
-        rc = launch_prep_tc(q, k, v, z, A, beta, H, g_min, p, records, device_sm_count(), s);
+        rc = launch_prep_tc(q, k, v, z, A, beta, T_total, H, g_min, p, records, device_sm_count(), s);
     else
         rc = launch_prep_simt(q, k, v, z, A, beta, H, dtype, g_min, p, records, s);
     if (rc) return rc;

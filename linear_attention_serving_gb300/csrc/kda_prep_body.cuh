@@ -15,8 +15,9 @@
 //
 // One block per SM walks (chunk, head) units with 512 threads:
 //  1. operand build, thread = (2 channels, 8 tokens): q, k, v, z of its
-//     channels and tokens (the next unit's are prefetched while the current one
-//     computes); gate of "Kimi K3 模型结构（2）" eq. (5) in base-2 log space;
+//     channels and tokens, read from the unit's input tiles, which the tensor
+//     memory accelerator (TMA) loaded into shared memory while the previous
+//     unit computed; gate of "Kimi K3 模型结构（2）" eq. (5) in base-2 log space;
 //     cumulative log decay inside each 16-token sub-tile ("数值问题：1/Γ 会溢出");
 //     e_i = exp(G_i - G_{tile start}) in (e^-80, 1]; and every MMA operand of
 //     the chunk, in bf16 with the 128-byte swizzle: for key tile q the
@@ -33,11 +34,12 @@
 //  5. [W | U0] becomes the MN-major operand of the MMAs issued together:
 //     K_restore^T [W | U0] = [G | H] (M = 128) and, with M = 64,
 //     Q' = I Q_decay + (-M_qk) W and O0 = M_qk U0; G, H, Q', O0 go to the record.
-// The record is staged in shared memory and written with bulk copies that
-// overlap the next unit.  Where chain blocks consume the records as they
-// appear, the thread that issued the copies waits for them to complete while
-// the next unit's inverse runs on the other threads, then raises the unit's
-// ready flag.  Every wait is bounded; a timeout records
+// The record is staged in shared memory, in the operand areas the last
+// products have finished reading, and written with bulk copies that overlap
+// the next unit's first phases.  Where chain blocks consume the records as
+// they appear, the thread that issued the copies waits for them to complete
+// while the next unit's inverse runs on the other threads, then raises the
+// unit's ready flag.  Every wait is bounded; a timeout records
 // KDA_DEVERR_TIMEOUT and ends the block.
 #pragma once
 
@@ -57,10 +59,11 @@ constexpr int PT_STORE_TID = 256;  // issues the bulk stores of a record and pub
 constexpr float LOG2E = 1.4426950408889634f;
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr int SM_AREG = 0;           // A_q images (2 k-blocks x 320 rows x 128 B); after their MMA,
-                                     // fp32 L | INV | scratch, then the record staging.  A read of
-                                     // an image past its valid rows runs into the following bytes;
-                                     // those rows are ignored.
+constexpr int SM_AREG = 0;           // the unit's input tiles (TMA), read into registers at its
+                                     // start; then the A_q images (2 k-blocks x 320 rows x 128 B);
+                                     // after their MMA, fp32 L | INV | scratch; then free for the
+                                     // next unit's input tiles.  A read of an image past its valid
+                                     // rows runs into the following bytes; those rows are ignored.
 constexpr int SM_AREG_KB = 40960;    // offset of the second k-block of the A_q images
 constexpr int SM_BQ = 81920;         // key-side images, 2 k-blocks x (4 tiles x 16 rows x 128 B)
 constexpr int SM_B2 = 98304;         // [Diag(beta) K_decay | Diag(beta) V]^T (256 rows x 64 tokens);
@@ -75,19 +78,27 @@ constexpr int SM_MISC = 196608;      // beta [64] | partial log2-decay sums [8][
 constexpr int SM_BYTES = SM_MISC + 256 + 4096 + 1024;
 constexpr size_t PREP_TC_SMEM = SM_BYTES + 1024;
 
-// staging of the output record: written after the last MMA has read its
-// operands, read by the bulk stores while the next unit builds B2, KRT, BQ, QD
-constexpr int ST_G = SM_AREG;          // 32 KB
-constexpr int ST_H = SM_AREG + 32768;  // 32 KB
-constexpr int ST_QP = SM_AREG + 65536; // 16 KB
-constexpr int ST_O0 = SM_A2;           // 16 KB
+// staging of the output record, in operand areas that the unit's last products
+// have read: written by the last epilogue, read by the bulk stores until the
+// next unit's operand build (which waits for that before writing B2, KRT,
+// BQ, QD; A2 is rewritten only after the next inverse)
+constexpr int ST_G = SM_B2;   // 32 KB
+constexpr int ST_H = SM_KRT;  // 32 KB (KRT and QD)
+constexpr int ST_QP = SM_BQ;  // 16 KB
+constexpr int ST_O0 = SM_A2;  // 16 KB
+static_assert(SM_QD == SM_KRT + 16384 && SM_MQ == SM_QD + 16384, "H staging spans KRT and QD");
 
-// fp32 matrices inside SM_AREG (row stride TRI_LD floats), below ST_QP
+// the unit's input tiles inside SM_AREG: [64 tokens][128 channels] each
+constexpr int IN_Q = 0, IN_K = 16384, IN_V = 32768, IN_Z = 49152;  // q, k, v bf16; z fp32
+constexpr uint32_t IN_BYTES = 81920;
+static_assert(IN_BYTES <= SM_BQ - SM_AREG, "input tiles fit the image area");
+
+// fp32 matrices inside SM_AREG (row stride TRI_LD floats)
 constexpr int MAT_BYTES = 64 * TRI_LD * 4;
 constexpr int SM_L = 0;
 constexpr int SM_INV = MAT_BYTES;
 constexpr int SM_TMP = 2 * MAT_BYTES;
-static_assert(3 * MAT_BYTES <= 65536, "fp32 work matrices overlap the Q' staging");
+static_assert(3 * MAT_BYTES <= SM_BQ - SM_AREG, "fp32 work matrices fit the image area");
 
 __device__ __forceinline__ int arow_base(int q) { return q == 0 ? 0 : (q == 1 ? 128 : (q == 2 ? 224 : 288)); }
 
@@ -105,24 +116,28 @@ struct BuildIn {
     __nv_bfloat162 q[8], k[8], v[8];
     float2 z[8];
 };
-// The next unit's inputs are fetched in three parts, each issued right after an
-// MMA so that the loads overlap the tensor-core work instead of the build.
-template <int PART>
-__device__ __forceinline__ void load_part(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                                          const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z, int H,
-                                          int h, int t0, int len, int rg, int cp, BuildIn &in) {
+// This thread's inputs from the unit's tiles in shared memory; rows at or past
+// the chunk's length (another document, or zeros past the tensor) read as 0.
+__device__ __forceinline__ void read_inputs(const uint8_t *tiles, int len, int rg, int cp, BuildIn &in) {
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
         const int i = 8 * rg + r;
-        const size_t a = ((size_t)(t0 + i) * H + h) * D + 2 * cp;
         const bool ok = i < len;
-        if (PART == 0) in.z[r] = ok ? *reinterpret_cast<const float2 *>(z + a) : make_float2(0.f, 0.f);
-        if (PART == 1) {
-            in.q[r] = ok ? *reinterpret_cast<const __nv_bfloat162 *>(q + a) : __float2bfloat162_rn(0.f);
-            in.k[r] = ok ? *reinterpret_cast<const __nv_bfloat162 *>(k + a) : __float2bfloat162_rn(0.f);
-        }
-        if (PART == 2) in.v[r] = ok ? *reinterpret_cast<const __nv_bfloat162 *>(v + a) : __float2bfloat162_rn(0.f);
+        const int e = i * D + 2 * cp;
+        in.z[r] = ok ? *reinterpret_cast<const float2 *>(tiles + IN_Z + 4 * e) : make_float2(0.f, 0.f);
+        in.q[r] = ok ? *reinterpret_cast<const __nv_bfloat162 *>(tiles + IN_Q + 2 * e) : __float2bfloat162_rn(0.f);
+        in.k[r] = ok ? *reinterpret_cast<const __nv_bfloat162 *>(tiles + IN_K + 2 * e) : __float2bfloat162_rn(0.f);
+        in.v[r] = ok ? *reinterpret_cast<const __nv_bfloat162 *>(tiles + IN_V + 2 * e) : __float2bfloat162_rn(0.f);
     }
+}
+// One thread: the TMA loads of a unit's four input tiles (head h, the chunk
+// starting at token t0) into the tile area, counted on `bar`.
+__device__ __forceinline__ void load_tiles(const InputMaps *maps, uint8_t *tiles, int h, int t0, uint64_t *bar) {
+    mbar_expect_tx(bar, IN_BYTES);
+    tma_load_3d(tiles + IN_Q, &maps->q, 0, h, t0, bar);
+    tma_load_3d(tiles + IN_K, &maps->k, 0, h, t0, bar);
+    tma_load_3d(tiles + IN_V, &maps->v, 0, h, t0, bar);
+    tma_load_3d(tiles + IN_Z, &maps->z, 0, h, t0, bar);
 }
 
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
@@ -171,12 +186,11 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
 // registers.  With `ready` non-null, ready[u] is set (release, after
 // the record's bulk stores have completed) once unit u's record is in memory.
 template <bool OPTS>
-__device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                                            const __nv_bfloat16 *__restrict__ v, const float *__restrict__ z,
-                                            const float *__restrict__ A, const float *__restrict__ beta, int H,
-                                            float g_min, const Plan &plan, char *__restrict__ records,
-                                            uint8_t *smraw, int first, int stride, int *ready) {
-    __shared__ uint64_t mbar_p, mbar_w, mbar_g;
+__device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *__restrict__ A,
+                                            const float *__restrict__ beta, int H, float g_min, const Plan &plan,
+                                            char *__restrict__ records, uint8_t *smraw, int first, int stride,
+                                            int *ready) {
+    __shared__ uint64_t mbar_p, mbar_w, mbar_g, mbar_in, mbar_dr;
     __shared__ uint32_t tmem_slot;
 
     if (plan_failed(plan)) return;
@@ -197,6 +211,8 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         mbar_init(&mbar_p, 1);
         mbar_init(&mbar_w, 1);
         mbar_init(&mbar_g, 1);
+        mbar_init(&mbar_in, 1);
+        mbar_init(&mbar_dr, 1);
         mbar_fence_init();
     }
     // a block that publishes its records may run a chain afterwards, which
@@ -224,13 +240,13 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
     BuildIn cin;
     float b_next = 0.f, a_next = 0.f;
     int u = first;
-    int u_prev = -1;  // unit whose record is being written by the bulk stores
+    int u_prev = -1;  // unit whose record was written last (its flag is raised during the next inverse)
+    int tiles_issued = 0, tiles_landed = 0;  // TMA tile loads into the tile area (one per unit)
     ChunkInfo ci;
     if (u < n_units) {
         ci = plan_chunk(plan, u / H);
-        load_part<0>(q, k, v, z, H, u % H, ci.tok, ci.len, rg, cp, cin);
-        load_part<1>(q, k, v, z, H, u % H, ci.tok, ci.len, rg, cp, cin);
-        load_part<2>(q, k, v, z, H, u % H, ci.tok, ci.len, rg, cp, cin);
+        if (tid == 0) load_tiles(maps, sm + SM_AREG, u % H, ci.tok, &mbar_in);
+        tiles_issued = 1;
         if (tid < 64 && tid < ci.len) {
             b_next = beta[(size_t)(ci.tok + tid) * H + u % H];
             if (bsig) b_next = 1.f / (1.f + __expf(-b_next));  // input option: beta logit
@@ -241,6 +257,11 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
     for (int it = 0; u < n_units && !timed_out; u += stride, ++it) {
         const int cidx = u / H, h = u - cidx * H;
         char *rec = records + ((size_t)cidx * H + h) * REC_BF16_BYTES;
+
+        // ---- 0. the unit's input tiles have landed: this thread's part into registers
+        if (!__syncthreads_and(mbar_wait(&mbar_in, (uint32_t)(it & 1)))) { timed_out = true; break; }
+        tiles_landed = it + 1;
+        read_inputs(sm + SM_AREG, ci.len, rg, cp, cin);
 
         // ---- 1. gate, partial log2-decay sums of each 8-token group, and beta
         float2 rl[8];
@@ -283,6 +304,8 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
                 snorm[4 * (8 * rg + r) + 2 + (warp & 1)] = sk;
             }
         }
+        // the previous unit's record has left the staging areas the build rewrites
+        if (tid == PT_STORE_TID) bulk_wait_read_all();
         __syncthreads();
 
         // tile sums Delta_t (log2), exp(Delta_t), and this thread's carry into its tile
@@ -374,8 +397,6 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
                 *reinterpret_cast<uint4 *>(sm + SM_KRT + c * 128 + sw) = make_uint4(bkr[j][0], bkr[j][1], bkr[j][2], bkr[j][3]);
             }
         }
-        // the previous unit's record has left the staging area
-        if (tid == PT_STORE_TID) bulk_wait_read_all();
         __syncthreads();
 
         // ---- 1c. query-side rows of the A_q images
@@ -423,13 +444,12 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
             }
             mma_commit(&mbar_p);
         }
-        // next unit: its gate inputs now, q and k after the next MMA, v after the last
+        // next unit: its betas now, its input tiles once the image area is free
         const int u_next = u + stride;
         const bool has_next = u_next < n_units;
         ChunkInfo ci_next = ci;
         if (has_next) {
             ci_next = plan_chunk(plan, u_next / H);
-            load_part<0>(q, k, v, z, H, u_next % H, ci_next.tok, ci_next.len, rg, cp, cin);
             if (tid < 64) {
                 b_next = tid < ci_next.len ? beta[(size_t)(ci_next.tok + tid) * H + u_next % H] : 0.f;
                 if (bsig && tid < ci_next.len) b_next = 1.f / (1.f + __expf(-b_next));
@@ -512,6 +532,11 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
 
         // ---- 4. INV [Diag(beta) K_decay | Diag(beta) V] = [W | U0]  (M = 64, N = 256, K = 64)
         if (tid == 0) {
+            if (has_next) {
+                // the image area is free until the next unit's build: its input tiles
+                fence_async_smem();
+                load_tiles(maps, sm + SM_AREG, u_next % H, ci_next.tok, &mbar_in);
+            }
             tc_fence_after();
             constexpr uint32_t IDW = idesc_bf16_f32(64, 256);
 #pragma unroll
@@ -522,7 +547,7 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
             }
             mma_commit(&mbar_w);
         }
-        if (has_next) load_part<1>(q, k, v, z, H, u_next % H, ci_next.tok, ci_next.len, rg, cp, cin);
+        if (has_next) ++tiles_issued;
         ok = mbar_wait(&mbar_w, (uint32_t)(it & 1));
         __syncwarp();
         tc_fence_after();
@@ -569,7 +594,6 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
                          sdesc_mn(smem_u32(sm + SM_QD + s * 2048), 8192, 1024, SWZ_128B), IDM, true);
             mma_commit(&mbar_g);
         }
-        if (has_next) load_part<2>(q, k, v, z, H, u_next % H, ci_next.tok, ci_next.len, rg, cp, cin);
         ok = mbar_wait(&mbar_g, (uint32_t)(it & 1));
         __syncwarp();
         tc_fence_after();
@@ -634,7 +658,14 @@ __device__ __forceinline__ void prep_blocks(const __nv_bfloat16 *__restrict__ q,
         bulk_wait_all();
         if (ready && u_prev >= 0 && !timed_out) publish(ready + u_prev);
     }
-    if (tid == 0 && timed_out) atomicOr(plan.err, KDA_DEVERR_TIMEOUT);
+    if (tid == 0) {
+        if (timed_out) atomicOr(plan.err, KDA_DEVERR_TIMEOUT);
+        // tile loads and tensor-core work this block started have finished
+        // before the block leaves or frees its TMEM (no-ops after a full run)
+        if (tiles_issued > tiles_landed) mbar_wait(&mbar_in, (uint32_t)((tiles_issued - 1) & 1));
+        mma_commit(&mbar_dr);
+        mbar_wait(&mbar_dr, 0);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
