@@ -330,7 +330,8 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
         if (rg == 0)
             *reinterpret_cast<float2 *>(rec + REC_BF16_AC + 8 * cp) = mul2(mul2(eD[0], eD[1]), mul2(eD[2], eD[3]));
 
-        // ---- 1b. per-token operands that do not touch the staging area
+        // ---- 1b. per-token factors, the key sides and the query-side rows of the
+        // A_q images (what the first products read)
         if (l2norm) {
             // input option: this thread's q and k divided by their tokens' norms
             // (rounded back to bf16, as the operands they feed are)
@@ -342,64 +343,22 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
                 cin.k[r] = __float22bfloat162_rn(mul2(__bfloat1622float2(cin.k[r]), make_float2(ik, ik)));
             }
         }
-        float2 qe[8], ke[8];
-        {
-            // token-contiguous images, two tokens per packed word: [channel][token pair]
-            uint32_t bkd[2][4], bv[2][4], bkr[2][4];
+        float2 qe[8], ke[8], kx[8];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int i = 8 * rg + r;
-                float2 qf = __bfloat1622float2(cin.q[r]);
-                if (qscale) qf = mul2(qf, make_float2(Q_SCALE, Q_SCALE));  // input option: q d_k^-1/2
-                const float2 kf = __bfloat1622float2(cin.k[r]);
-                const float2 vf = __bfloat1622float2(cin.v[r]);
-                const float2 c2 = add2(carry, rl[r]);
-                const float2 e = ex2x2(c2);
-                const float2 x = ex2x2(add2(Dl, make_float2(-c2.x, -c2.y)));  // exp(Delta_p) / e_i
-                const float b = sbeta[i];
-                qe[r] = mul2(qf, e);
-                ke[r] = mul2(kf, e);
-                const float2 kx = mul2(kf, x);
-                const float2 vbkd = mul2(mul2(ePfx, make_float2(b, b)), ke[r]);  // Diag(beta) K_decay
-                const float2 vbv = mul2(vf, make_float2(b, b));                  // Diag(beta) V
-                const float2 vbkr = mul2(eSfx, kx);                              // K_restore = exp(G_last - G_i) k_i
-                {
-                    // channel j of this token -> low (even token) or high (odd token) half of a word
-                    const uint32_t w0 = bf2(make_float2(vbkd.x, vbkd.y)), w1 = bf2(make_float2(vbv.x, vbv.y)),
-                                   w2 = bf2(make_float2(vbkr.x, vbkr.y));
-                    const int pr = r >> 1;
-                    if ((r & 1) == 0) {
-                        bkd[0][pr] = w0 & 0xFFFFu;
-                        bkd[1][pr] = w0 >> 16;
-                        bv[0][pr] = w1 & 0xFFFFu;
-                        bv[1][pr] = w1 >> 16;
-                        bkr[0][pr] = w2 & 0xFFFFu;
-                        bkr[1][pr] = w2 >> 16;
-                    } else {
-                        bkd[0][pr] |= w0 << 16;
-                        bkd[1][pr] |= w0 & 0xFFFF0000u;
-                        bv[0][pr] |= w1 << 16;
-                        bv[1][pr] |= w1 & 0xFFFF0000u;
-                        bkr[0][pr] |= w2 << 16;
-                        bkr[1][pr] |= w2 & 0xFFFF0000u;
-                    }
-                }
-                // key side of key tile p, and Q_decay
-                *reinterpret_cast<uint32_t *>(sm + SM_BQ + kb * 8192 + tile * 2048 + swz(i - 16 * tile, cc)) = bf2(kx);
-                *reinterpret_cast<uint32_t *>(sm + SM_QD + kb * 8192 + swz(i, cc)) = bf2(mul2(ePfx, qe[r]));
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int c = 2 * cp + j;
-                const uint32_t sw = (uint32_t)(((rg ^ (c & 7)) & 7) << 4);
-                *reinterpret_cast<uint4 *>(sm + SM_B2 + c * 128 + sw) = make_uint4(bkd[j][0], bkd[j][1], bkd[j][2], bkd[j][3]);
-                *reinterpret_cast<uint4 *>(sm + SM_B2 + (128 + c) * 128 + sw) = make_uint4(bv[j][0], bv[j][1], bv[j][2], bv[j][3]);
-                *reinterpret_cast<uint4 *>(sm + SM_KRT + c * 128 + sw) = make_uint4(bkr[j][0], bkr[j][1], bkr[j][2], bkr[j][3]);
-            }
+        for (int r = 0; r < 8; ++r) {
+            const int i = 8 * rg + r;
+            float2 qf = __bfloat1622float2(cin.q[r]);
+            if (qscale) qf = mul2(qf, make_float2(Q_SCALE, Q_SCALE));  // input option: q d_k^-1/2
+            const float2 kf = __bfloat1622float2(cin.k[r]);
+            const float2 c2 = add2(carry, rl[r]);
+            const float2 e = ex2x2(c2);
+            const float2 x = ex2x2(add2(Dl, make_float2(-c2.x, -c2.y)));  // exp(Delta_p) / e_i
+            qe[r] = mul2(qf, e);
+            ke[r] = mul2(kf, e);
+            kx[r] = mul2(kf, x);
+            // key side of key tile p
+            *reinterpret_cast<uint32_t *>(sm + SM_BQ + kb * 8192 + tile * 2048 + swz(i - 16 * tile, cc)) = bf2(kx[r]);
         }
-        __syncthreads();
-
-        // ---- 1c. query-side rows of the A_q images
         {
             uint8_t *abase = sm + SM_AREG + kb * SM_AREG_KB;
 #pragma unroll
@@ -444,6 +403,51 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
             }
             mma_commit(&mbar_p);
         }
+
+        // ---- 1c. while those products run: the token-contiguous operands of the
+        // later products, Diag(beta) K_decay, Diag(beta) V, K_restore^T, and Q_decay
+        {
+            // two tokens per packed word: [channel][token pair]
+            uint32_t bkd[2][4], bv[2][4], bkr[2][4];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int i = 8 * rg + r;
+                const float2 vf = __bfloat1622float2(cin.v[r]);
+                const float b = sbeta[i];
+                const float2 vbkd = mul2(mul2(ePfx, make_float2(b, b)), ke[r]);  // Diag(beta) K_decay
+                const float2 vbv = mul2(vf, make_float2(b, b));                  // Diag(beta) V
+                const float2 vbkr = mul2(eSfx, kx[r]);                           // K_restore = exp(G_last - G_i) k_i
+                // channel j of this token -> low (even token) or high (odd token) half of a word
+                const uint32_t w0 = bf2(make_float2(vbkd.x, vbkd.y)), w1 = bf2(make_float2(vbv.x, vbv.y)),
+                               w2 = bf2(make_float2(vbkr.x, vbkr.y));
+                const int pr = r >> 1;
+                if ((r & 1) == 0) {
+                    bkd[0][pr] = w0 & 0xFFFFu;
+                    bkd[1][pr] = w0 >> 16;
+                    bv[0][pr] = w1 & 0xFFFFu;
+                    bv[1][pr] = w1 >> 16;
+                    bkr[0][pr] = w2 & 0xFFFFu;
+                    bkr[1][pr] = w2 >> 16;
+                } else {
+                    bkd[0][pr] |= w0 << 16;
+                    bkd[1][pr] |= w0 & 0xFFFF0000u;
+                    bv[0][pr] |= w1 << 16;
+                    bv[1][pr] |= w1 & 0xFFFF0000u;
+                    bkr[0][pr] |= w2 << 16;
+                    bkr[1][pr] |= w2 & 0xFFFF0000u;
+                }
+                *reinterpret_cast<uint32_t *>(sm + SM_QD + kb * 8192 + swz(i, cc)) = bf2(mul2(ePfx, qe[r]));
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int c = 2 * cp + j;
+                const uint32_t sw = (uint32_t)(((rg ^ (c & 7)) & 7) << 4);
+                *reinterpret_cast<uint4 *>(sm + SM_B2 + c * 128 + sw) = make_uint4(bkd[j][0], bkd[j][1], bkd[j][2], bkd[j][3]);
+                *reinterpret_cast<uint4 *>(sm + SM_B2 + (128 + c) * 128 + sw) = make_uint4(bv[j][0], bv[j][1], bv[j][2], bv[j][3]);
+                *reinterpret_cast<uint4 *>(sm + SM_KRT + c * 128 + sw) = make_uint4(bkr[j][0], bkr[j][1], bkr[j][2], bkr[j][3]);
+            }
+        }
+        fence_async_smem();  // read by the later products, issued after the next barriers
         // next unit: its betas now, its input tiles once the image area is free
         const int u_next = u + stride;
         const bool has_next = u_next < n_units;

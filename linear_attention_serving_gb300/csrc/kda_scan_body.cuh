@@ -19,16 +19,21 @@
 // Chain warps (4 per TPR): thread t of a row group owns state row t (TMEM lane
 //   t) and N / TPR of its columns; the fp32 state master lives in registers,
 //   its bf16 copy (double buffered) in shared memory is the B operand
-//   (MN-major) of the next chunk's MMA.  Each warp publishes its rows of that
-//   operand on an mbarrier, so the warps never wait for one another; a_C and H
-//   are read while the MMA runs.
-// MMA warp: waits for the chain warps' rows and the chunk's stage, issues the
-//   chunk's MMA and commits it; with EMIT_O it then issues the chunk's output
-//   MMA O = Q' S_enter (M = 64) into one of two TMEM accumulators.
+//   (MN-major) of the next chunk's MMA; a_C and H are read while the MMA runs.
+//   After writing their rows of that operand the chain warps arrive at a named
+//   barrier and go on.
+// MMA warp: waits at that barrier (a hardware barrier wakes it at once),
+//   checks the chunk's stage and issues the chain's MMA.
+// Output-MMA warp (EMIT_O): once a chunk's chain MMA is issued, issues its
+//   output MMA O = Q' S_enter (M = 64) into one of two TMEM accumulators, so
+//   that the chain never waits for the output path.
 // Producer warp: waits for a chunk's record (its ready flag, when another part
 //   of the launch writes it), then streams G, a_C and the block's H slices
-//   through a bulk-copy pipeline, and (EMIT_O) Q' through a ring of its own.
-// Output warps (EMIT_O): load O0 from the record, read an output accumulator,
+//   through a bulk-copy pipeline.
+// Q' producer warp (EMIT_O): the same for Q' and the block's O0 slices, through
+//   a ring of their own, so that the chain's stages never wait for the output
+//   path.
+// Output warps (EMIT_O): read O0 from that ring, read an output accumulator,
 //   add, store bf16 o.
 // Every wait is bounded; on a timeout the block records KDA_DEVERR_TIMEOUT,
 // leaves its loops, and frees its TMEM.
@@ -46,41 +51,60 @@ using namespace tc;
 // Block layout for N state columns with TPR threads per state row: warps
 // 0 .. 4 TPR - 1 run the chain (warp w: rows 32 (w % 4) .., columns
 // (w / 4) N / TPR ..), then the MMA warp, the producer warp and, when the
-// block forms the outputs itself (EMIT_O), four output warps.
+// block forms the outputs itself (EMIT_O), the output-MMA warp, the Q'
+// producer warp and four output warps.
 template <int N, int TPR, bool EMIT_O = false>
 struct ScanCfg {
     static constexpr int NT = N / TPR;  // state columns per chain thread
     static constexpr int CHAIN_WARPS = 4 * TPR;
     static constexpr int MMA_WARP = CHAIN_WARPS;
     static constexpr int PRODUCER_WARP = CHAIN_WARPS + 1;
-    static constexpr int OUT_WARP0 = CHAIN_WARPS + 2;
+    static constexpr int OMMA_WARP = CHAIN_WARPS + 2;
+    static constexpr int QPROD_WARP = CHAIN_WARPS + 3;
+    static constexpr int OUT_WARP0 = CHAIN_WARPS + 4;
     static constexpr int OUT_WARPS = EMIT_O ? 4 : 0;
-    static constexpr int THREADS = 32 * (CHAIN_WARPS + 2 + OUT_WARPS);
+    static constexpr int THREADS = 32 * (CHAIN_WARPS + 2 + (EMIT_O ? 2 + OUT_WARPS : 0));
+    static constexpr int OPERAND_BAR_THREADS = 32 * (CHAIN_WARPS + 1);  // chain warps + MMA warp
     static_assert(NT % 16 == 0, "a chain thread owns whole 16-column blocks");
 };
+// Named barrier at which the chain warps hand the next S operand to the MMA
+// warp: they arrive without waiting, the MMA warp waits.
+constexpr int OPERAND_BAR = 1;
+__device__ __forceinline__ void bar_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
-// pipeline stage: G (32 KB) | a_C | H slices, as laid out in the record.  With
-// EMIT_O, Q' (the output MMA's A operand) rides a ring of its own, freed by
-// that MMA's commit, and the output warps read O0 straight from the record, so
-// that the stages the chain waits on stay small enough for a deep pipeline.
+// A pipeline stage holds one chunk's G (32 KB, the MMA operand) and its a_C
+// and the block's H slices.  With EMIT_O, Q' (the output MMA's A operand) and
+// the block's O0 slices ride a ring of their own, freed once that MMA and the
+// output warps have read them, so that the stages the chain waits on stay
+// small.  Shared memory, from a 1024-byte-aligned base:
+//   [G of every stage | Q' + O0 ring slots | 2 S operands | a_C + H of every stage]
+// (the operands 1024-byte aligned; the a_C + H areas need 16 bytes).
 template <int N, bool EMIT_O = false>
 struct Stage {
     static constexpr int NS = N / 16;
-    static constexpr int G = 0;
-    static constexpr int AC = (int)REC_BF16_AC;
-    static constexpr int H = (int)REC_BF16_SHARED;
-    static constexpr int BYTES = ((H + NS * (int)REC_BF16_HSLICE) + 1023) / 1024 * 1024;
-    static constexpr int QBYTES = EMIT_O ? 16384 : 0;  // one Q' ring slot (1024-aligned)
+    static constexpr int G_BYTES = 32768;                                        // G of one stage
+    static constexpr int AC = 0;                                                 // in a stage's a_C + H area
+    static constexpr int H = (int)(REC_BF16_SHARED - REC_BF16_AC);               // H slices after a_C
+    static constexpr int AH_BYTES = H + NS * (int)REC_BF16_HSLICE;               // a_C + H of one stage
+    static constexpr int QO0 = 16384;                                            // O0 slices after Q' in a slot
+    static constexpr int QUSED = EMIT_O ? QO0 + NS * (int)REC_BF16_OSLICE : 0;   // bytes copied per slot
+    static constexpr int QBYTES = (QUSED + 1023) / 1024 * 1024;                  // one ring slot (1024-aligned)
     static constexpr int QSTAGES = 2;
     static constexpr int SOP = 2 * N * 128;  // one bf16 S operand: 128 rows x N columns
     static constexpr int OCOL = N;           // TMEM: output accumulators at N and 2 N
     static constexpr int NCOLS = EMIT_O ? 256 : (N < 32 ? 32 : N);
+    static_assert(H % 16 == 0 && AH_BYTES % 16 == 0, "stage areas keep bulk-copy alignment");
 };
 
 template <int N, int STAGES, bool EMIT_O = false>
 constexpr size_t scan_tc_smem_bytes() {
     using ST = Stage<N, EMIT_O>;
-    return (size_t)STAGES * ST::BYTES + (size_t)ST::QSTAGES * ST::QBYTES + 2 * ST::SOP + 1024;
+    return (size_t)STAGES * (ST::G_BYTES + ST::AH_BYTES) + (size_t)ST::QSTAGES * ST::QBYTES + 2 * ST::SOP + 1024;
 }
 
 __device__ __forceinline__ float state_init(const ScanArgs &a, int unit, int h, int r, int g) {
@@ -204,7 +228,8 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
     using ST = Stage<N, EMIT_O>;
     using CF = ScanCfg<N, TPR, EMIT_O>;
     constexpr int NT = CF::NT;
-    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], g_bar, sop_bar, o_bar[2], oempty_bar[2], drain_bar;
+    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], g_bar, sop_bar[2], o_bar[2], oempty_bar[2], drain_bar,
+        odrain_bar;
     __shared__ uint64_t qfull_bar[ST::QSTAGES], qfree_bar[ST::QSTAGES];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -227,8 +252,9 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
     const int nchunks = c1 - c0;
 
     uint8_t *sm = smraw + ((1024 - (smem_u32(smraw) & 1023)) & 1023);
-    uint8_t *qring = sm + STAGES * ST::BYTES;
+    uint8_t *qring = sm + STAGES * ST::G_BYTES;
     uint8_t *sop0 = qring + ST::QSTAGES * ST::QBYTES;
+    uint8_t *aharea = sop0 + 2 * ST::SOP;  // a_C + H of every stage
     char *records = (char *)a.records;
     const size_t rec_stride = (size_t)a.H * REC_BF16_BYTES;
 
@@ -239,14 +265,19 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
         }
         mbar_init(&g_bar, 1);
         mbar_init(&drain_bar, 1);
-        mbar_init(&sop_bar, CF::CHAIN_WARPS);  // the chain warps' parts of the next S operand
+        mbar_init(&odrain_bar, 1);
+        // chunk i's chain MMA issued, so its S operand is complete (for the output
+        // MMA); two of them alternate, so that a waiter one chunk behind never
+        // mistakes a later phase for the one it waits for
+        mbar_init(&sop_bar[0], 1);
+        mbar_init(&sop_bar[1], 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&o_bar[b], 1);                // output accumulator b written
             mbar_init(&oempty_bar[b], CF::OUT_WARPS > 0 ? CF::OUT_WARPS : 1);  // and read back
         }
         for (int s = 0; s < ST::QSTAGES; ++s) {
             mbar_init(&qfull_bar[s], 1);
-            mbar_init(&qfree_bar[s], 1);  // the output MMA's commit
+            mbar_init(&qfree_bar[s], 1 + CF::OUT_WARPS);  // the output MMA's commit and the output warps
         }
         abort_flag = 0;
         mbar_fence_init();
@@ -262,7 +293,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
     if (warp == CF::PRODUCER_WARP) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int issued = 0, q_issued = 0;
+            int issued = 0;
             bool timed_out = false;
             const uint32_t bytes = (uint32_t)REC_BF16_SHARED + (value_cols ? (uint32_t)(ST::NS * REC_BF16_HSLICE) : 0u);
             int stage = 0;
@@ -273,20 +304,14 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 if (!mbar_wait_ab(&empty_bar[stage], ph ^ 1u, abort)) { timed_out = true; break; }
                 if (*abort) break;
                 const char *rec = records + (size_t)(c0 + i) * rec_stride + (size_t)h * REC_BF16_BYTES;
-                uint8_t *st = sm + stage * ST::BYTES;
+                uint8_t *ah = aharea + stage * ST::AH_BYTES;
                 mbar_expect_tx(&full_bar[stage], bytes);
-                bulk_g2s(st, rec, (uint32_t)REC_BF16_SHARED, &full_bar[stage]);
+                bulk_g2s(sm + stage * ST::G_BYTES, rec + REC_BF16_G, (uint32_t)ST::G_BYTES, &full_bar[stage]);
+                bulk_g2s(ah + ST::AC, rec + REC_BF16_AC, (uint32_t)ST::H, &full_bar[stage]);
                 if (value_cols)
-                    bulk_g2s(st + ST::H, rec + REC_BF16_H + (size_t)(col0 / 16) * REC_BF16_HSLICE,
+                    bulk_g2s(ah + ST::H, rec + REC_BF16_H + (size_t)(col0 / 16) * REC_BF16_HSLICE,
                              (uint32_t)(ST::NS * REC_BF16_HSLICE), &full_bar[stage]);
                 issued = i + 1;
-                if (EMIT_O) {
-                    const int qs = i % ST::QSTAGES;
-                    if (!mbar_wait_ab(&qfree_bar[qs], (uint32_t)(((i / ST::QSTAGES) & 1) ^ 1), abort)) { timed_out = true; break; }
-                    mbar_expect_tx(&qfull_bar[qs], (uint32_t)ST::QBYTES);
-                    bulk_g2s(qring + qs * ST::QBYTES, rec + REC_BF16_QP, (uint32_t)ST::QBYTES, &qfull_bar[qs]);
-                    q_issued = i + 1;
-                }
                 if (++stage == STAGES) {
                     stage = 0;
                     ph ^= 1u;
@@ -297,63 +322,113 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 // let the copies this thread started land before the block exits
                 for (int i = (issued > STAGES ? issued - STAGES : 0); i < issued; ++i)
                     mbar_wait(&full_bar[i % STAGES], (uint32_t)((i / STAGES) & 1));
+                if (timed_out) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
+            }
+        }
+    } else if (EMIT_O && warp == CF::QPROD_WARP) {
+        // ------------------------------------------------------------ Q' producer
+        if (lane == 0) {
+            int q_issued = 0;
+            bool timed_out = false;
+            for (int i = 0; i < nchunks; ++i) {
+                if (ready && !wait_flag(ready + (size_t)(c0 + i) * a.H + h, flag_budget, abort)) { timed_out = true; break; }
+                const int qs = i % ST::QSTAGES;
+                if (!mbar_wait_ab(&qfree_bar[qs], (uint32_t)(((i / ST::QSTAGES) & 1) ^ 1), abort)) { timed_out = true; break; }
+                if (*abort) break;
+                const char *rec = records + (size_t)(c0 + i) * rec_stride + (size_t)h * REC_BF16_BYTES;
+                mbar_expect_tx(&qfull_bar[qs], (uint32_t)ST::QUSED);
+                bulk_g2s(qring + qs * ST::QBYTES, rec + REC_BF16_QP, 16384u, &qfull_bar[qs]);
+                bulk_g2s(qring + qs * ST::QBYTES + ST::QO0, rec + REC_BF16_O0 + (size_t)(col0 / 16) * REC_BF16_OSLICE,
+                         (uint32_t)(ST::NS * REC_BF16_OSLICE), &qfull_bar[qs]);
+                q_issued = i + 1;
+            }
+            if (timed_out) abort_flag = 1;
+            if (timed_out || *abort) {
                 for (int i = (q_issued > ST::QSTAGES ? q_issued - ST::QSTAGES : 0); i < q_issued; ++i)
                     mbar_wait(&qfull_bar[i % ST::QSTAGES], (uint32_t)((i / ST::QSTAGES) & 1));
                 if (timed_out) atomicOr(p.err, KDA_DEVERR_TIMEOUT);
             }
         }
     } else if (warp == CF::MMA_WARP) {
-        // ------------------------------------------------------------ MMA issue
+        // ------------------------------------------------------------ chain MMAs
+        // Chunk i: wait for the chunk's stage (G), then at the operand barrier
+        // until every chain warp has written its rows of S_i (or given up), then
+        // issue S_i -> G S_i.  The stage wait comes first so that it overlaps the
+        // chain's update of the previous chunk.  The chain warps arrive once per
+        // chunk, also when they stop, so this warp never waits at a barrier
+        // nobody reaches.
+        const uint64_t gd0 = sdesc_sw128(smem_u32(sm));
+        const uint64_t sd0 = sop_desc<N>(sop0);
+        int stage = 0;
+        uint32_t ph = 0;
+        bool issued_any = false;
+        for (int i = 0; i < nchunks; ++i) {
+            bool go = true;
+            if (lane == 0 && !mbar_wait_ab(&full_bar[stage], ph, abort)) {
+                abort_flag = 1;
+                go = false;
+            }
+            bar_sync(OPERAND_BAR, CF::OPERAND_BAR_THREADS);
+            if (*abort || !__shfl_sync(0xffffffffu, (int)go, 0)) break;
+            if (lane == 0) {
+                {
+                    tc_fence_after();
+                    constexpr uint32_t IDESC = idesc_bf16_f32_bmn(128, N);
+                    const uint64_t gd = gd0 + (uint64_t)((stage * ST::G_BYTES) >> 4);
+                    const uint64_t sd = sd0 + (uint64_t)(((i & 1) * ST::SOP) >> 4);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mma_bf16(tmem_g, gd + (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                                 sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDESC, k > 0);
+                    mma_commit(&g_bar);
+                    if (EMIT_O) mbar_arrive(&sop_bar[i & 1]);
+                    issued_any = true;
+                }
+            }
+            __syncwarp();
+            if (++stage == STAGES) {
+                stage = 0;
+                ph ^= 1u;
+            }
+        }
+        if (lane == 0 && issued_any) {
+            // every chain MMA has completed before TMEM is freed, also when the
+            // block stopped early
+            mma_commit(&drain_bar);
+            mbar_wait(&drain_bar, 0);
+        }
+    } else if (EMIT_O && warp == CF::OMMA_WARP) {
+        // ------------------------------------------------------------ output MMAs
         if (lane == 0) {
-            constexpr uint32_t IDESC = idesc_bf16_f32_bmn(128, N);
-            const uint64_t gd0 = sdesc_sw128(smem_u32(sm + ST::G));
             const uint64_t sd0 = sop_desc<N>(sop0);
-            int stage = 0;
-            uint32_t ph = 0;
             for (int i = 0; i < nchunks; ++i) {
-                const int b = i & 1;
-                // chunk i's S operand is complete (and the accumulator of chunk i - 1 read)
-                if (!mbar_wait_ab(&sop_bar, (uint32_t)(i & 1), abort) || !mbar_wait_ab(&full_bar[stage], ph, abort) ||
-                    *abort) {
+                const int b = i & 1, qs = i % ST::QSTAGES;
+                // chunk i's chain MMA is issued (so its S operand is complete), the
+                // output warps have read what chunk i - 2 left in accumulator b, and
+                // chunk i's Q' has landed
+                if (!mbar_wait_ab(&sop_bar[b], (uint32_t)((i >> 1) & 1), abort) ||
+                    (i >= 2 && !mbar_wait_ab(&oempty_bar[b], (uint32_t)(((i - 2) >> 1) & 1), abort)) ||
+                    !mbar_wait_ab(&qfull_bar[qs], (uint32_t)((i / ST::QSTAGES) & 1), abort)) {
                     abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t gd = gd0 + (uint64_t)((stage * ST::BYTES) >> 4);
+                constexpr uint32_t IDO = idesc_bf16_f32_bmn(64, N);
+                const uint64_t qd = sdesc_sw128(smem_u32(qring + qs * ST::QBYTES));
                 const uint64_t sd = sd0 + (uint64_t)((b * ST::SOP) >> 4);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_bf16(tmem_g, gd + (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
-                             sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDESC, k > 0);
-                mma_commit(&g_bar);
-                if (EMIT_O) {
-                    // O = Q' S_enter of this chunk into output accumulator b, once the
-                    // output warps have read what chunk i - 2 left there
-                    const int qs = i % ST::QSTAGES;
-                    if ((i >= 2 && !mbar_wait_ab(&oempty_bar[b], (uint32_t)(((i - 2) >> 1) & 1), abort)) ||
-                        !mbar_wait_ab(&qfull_bar[qs], (uint32_t)((i / ST::QSTAGES) & 1), abort)) {
-                        abort_flag = 1;
-                        break;
-                    }
-                    tc_fence_after();
-                    constexpr uint32_t IDO = idesc_bf16_f32_bmn(64, N);
-                    const uint64_t qd = sdesc_sw128(smem_u32(qring + qs * ST::QBYTES));
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        mma_bf16(tmem_g + ST::OCOL + b * N, qd + (uint64_t)(((k >> 2) * 8192 + (k & 3) * 32) >> 4),
-                                 sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDO, k > 0);
-                    mma_commit(&o_bar[b]);
-                    mma_commit(&qfree_bar[qs]);  // Q' read
-                }
-                if (++stage == STAGES) {
-                    stage = 0;
-                    ph ^= 1u;
-                }
+                    mma_bf16(tmem_g + ST::OCOL + b * N, qd + (uint64_t)(((k >> 2) * 8192 + (k & 3) * 32) >> 4),
+                             sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDO, k > 0);
+                mma_commit(&o_bar[b]);
+                mma_commit(&qfree_bar[qs]);  // Q' read
             }
-            // every MMA this thread issued has completed before TMEM is freed, also
-            // when the block stopped early
-            mma_commit(&drain_bar);
-            mbar_wait(&drain_bar, 0);
+            // every output MMA has completed before TMEM is freed, also when the
+            // block stopped early
+            if (nchunks > 0) {
+                mma_commit(&odrain_bar);
+                mbar_wait(&odrain_bar, 0);
+            }
         }
     } else if (warp < CF::CHAIN_WARPS) {
         // ------------------------------------------------------------ chain warps
@@ -384,8 +459,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
         write_sop<N, NT>(sop0, t, part * NT / 16, pk);
         fence_async_smem();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sop_bar);
+        if (nchunks > 0) bar_arrive(OPERAND_BAR, CF::OPERAND_BAR_THREADS);  // S_0 is written
         const bool write_final = value_cols && a.final_state && a.phase != 1;
         const bool write_ckpt = CKPT && value_cols && a.ckpt && a.phase != 1;
         // one document per chain (SCAN_DOCS): its checkpoints are counted down
@@ -410,85 +484,86 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
             }
             ok = mbar_wait_ab(&full_bar[stage], ph, abort);
             // the entering state of this chunk, for the output kernel
-            if (emit_s) store_s<NT>(records + (size_t)(c0 + i) * rec_stride + (size_t)h * REC_BF16_BYTES, pc / 16, t, pk);
+            if (emit_s && ok) store_s<NT>(records + (size_t)(c0 + i) * rec_stride + (size_t)h * REC_BF16_BYTES, pc / 16, t, pk);
             // ---- S <- Diag(a_C) S + H - G S; a_C and H are read while the MMA runs
-            const uint8_t *stg = sm + stage * ST::BYTES;
-            const float ac = reinterpret_cast<const float *>(stg + ST::AC)[t];
-            float hv[NT];
-            if (value_cols) load_slices<NT>(stg + ST::H + slice_offset(0, part * NT, 128), t, 128, hv);
-            else
+            const uint8_t *stg = aharea + stage * ST::AH_BYTES;
+            float ac = 0.f, hv[NT];
 #pragma unroll
-                for (int j = 0; j < NT; ++j) hv[j] = 0.f;
+            for (int j = 0; j < NT; ++j) hv[j] = 0.f;
+            if (ok) {
+                ac = reinterpret_cast<const float *>(stg + ST::AC)[t];
+                if (value_cols) load_slices<NT>(stg + ST::H + slice_offset(0, part * NT, 128), t, 128, hv);
+            }
             ok = ok && mbar_wait_ab(&g_bar, (uint32_t)(i & 1), abort);
-            // a warp stops as a whole; the others then run out of their bounded waits
-            if (!__all_sync(0xffffffffu, ok) || *(volatile int *)&abort_flag) {
+            // a warp that gave up skips the update, raises the abort flag, and still
+            // arrives at the operand barrier before it stops
+            bool good = __all_sync(0xffffffffu, ok) && !*abort;
+            if (good) {
+                tc_fence_after();
+                float d[NT];
+                tmem_row<NT>(tmem_g + lane_off + part * NT, d);
+#pragma unroll
+                for (int j = 0; j < NT; j += 2) {
+                    const float2 r2 = __ffma2_rn(make_float2(ac, ac), make_float2(s[j], s[j + 1]),
+                                                 make_float2(hv[j] - d[j], hv[j + 1] - d[j + 1]));
+                    s[j] = r2.x;
+                    s[j + 1] = r2.y;
+                }
+                if (write_final && last) {
+                    float *f = a.final_state + (((size_t)doc * a.H + h) * D + t) * D + pc;
+#pragma unroll
+                    for (int j = 0; j < NT; j += 4) *reinterpret_cast<float4 *>(f + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
+                }
+                if (CKPT && write_ckpt) {
+                    // the state after this chunk, when it ends on a checkpoint position
+                    // (only a full chunk does; a document's last chunk may be partial)
+                    float *f = nullptr;
+                    if (!segs) {
+                        if (--ck_left == 0) {
+                            ck_left = a.ckpt_ic;
+                            if (ck_j < a.ckpt_per_seq && (i + 1 < nchunks || plan_chunk(p, c0 + i).len == C)) {
+                                const int slot = a.ckpt_slot[(size_t)unit * a.ckpt_per_seq + ck_j];
+                                if (slot >= 0 && slot < a.ckpt_n_slots)
+                                    f = a.ckpt + (((size_t)slot * a.H + h) * D + t) * D;
+                            }
+                            ++ck_j;
+                        }
+                    } else {
+                        const ChunkInfo cik = plan_chunk(p, c0 + i);
+                        f = ckpt_row(a, cik, c0 + i, h, t);
+                    }
+                    if (f) {
+                        f += pc;
+#pragma unroll
+                        for (int j = 0; j < NT; j += 4)
+                            *reinterpret_cast<float4 *>(f + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
+                    }
+                }
+                if (next_first) {
+                    // a document starts at the next chunk: the state restarts there
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) s[j] = state_reset(a, ci_next.doc, h, t, pc + j);
+                }
+                pack_row<NT>(s, pk);
+                if (EMIT_O && i >= 1 && i + 1 < nchunks) {
+                    // operand buffer b ^ 1 was also read by chunk i - 1's output MMA
+                    good = __all_sync(0xffffffffu, mbar_wait_ab(&o_bar[b ^ 1], (uint32_t)(((i - 1) >> 1) & 1), abort));
+                }
+                if (good && i + 1 < nchunks) {
+                    write_sop<N, NT>(sop0 + (b ^ 1) * ST::SOP, t, part * NT / 16, pk);
+                    fence_async_smem();
+                }
+            }
+            tc_fence_before();
+            if (!good && lane == 0) abort_flag = 1;
+            __syncwarp();
+            if (i + 1 < nchunks) bar_arrive(OPERAND_BAR, CF::OPERAND_BAR_THREADS);  // S_{i+1} (or the stop)
+            if (!good) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
-            float d[NT];
-            tmem_row<NT>(tmem_g + lane_off + part * NT, d);
-#pragma unroll
-            for (int j = 0; j < NT; j += 2) {
-                const float2 r2 = __ffma2_rn(make_float2(ac, ac), make_float2(s[j], s[j + 1]),
-                                             make_float2(hv[j] - d[j], hv[j + 1] - d[j + 1]));
-                s[j] = r2.x;
-                s[j + 1] = r2.y;
-            }
-            if (write_final && last) {
-                float *f = a.final_state + (((size_t)doc * a.H + h) * D + t) * D + pc;
-#pragma unroll
-                for (int j = 0; j < NT; j += 4) *reinterpret_cast<float4 *>(f + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
-            }
-            if (CKPT && write_ckpt) {
-                // the state after this chunk, when it ends on a checkpoint position
-                // (only a full chunk does; a document's last chunk may be partial)
-                float *f = nullptr;
-                if (!segs) {
-                    if (--ck_left == 0) {
-                        ck_left = a.ckpt_ic;
-                        if (ck_j < a.ckpt_per_seq && (i + 1 < nchunks || plan_chunk(p, c0 + i).len == C)) {
-                            const int slot = a.ckpt_slot[(size_t)unit * a.ckpt_per_seq + ck_j];
-                            if (slot >= 0 && slot < a.ckpt_n_slots)
-                                f = a.ckpt + (((size_t)slot * a.H + h) * D + t) * D;
-                        }
-                        ++ck_j;
-                    }
-                } else {
-                    const ChunkInfo cik = plan_chunk(p, c0 + i);
-                    f = ckpt_row(a, cik, c0 + i, h, t);
-                }
-                if (f) {
-                    f += pc;
-#pragma unroll
-                    for (int j = 0; j < NT; j += 4)
-                        *reinterpret_cast<float4 *>(f + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
-                }
-            }
-            if (next_first) {
-                // a document starts at the next chunk: the state restarts there
-#pragma unroll
-                for (int j = 0; j < NT; ++j) s[j] = state_reset(a, ci_next.doc, h, t, pc + j);
-            }
-            pack_row<NT>(s, pk);
-            if (EMIT_O && i >= 1 && i + 1 < nchunks) {
-                // operand buffer b ^ 1 was also read by chunk i - 1's output MMA
-                const bool okk = mbar_wait_ab(&o_bar[b ^ 1], (uint32_t)(((i - 1) >> 1) & 1), abort);
-                if (!__all_sync(0xffffffffu, okk)) {
-                    ok = false;
-                    break;
-                }
-            }
-            if (i + 1 < nchunks) {
-                write_sop<N, NT>(sop0 + (b ^ 1) * ST::SOP, t, part * NT / 16, pk);
-                fence_async_smem();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (i + 1 < nchunks) mbar_arrive(&sop_bar);
-                mbar_arrive(&empty_bar[stage]);
-            }
+            // stage i is read (a_C, H here, G by chunk i's MMA, which has completed)
+            if (lane == 0) mbar_arrive(&empty_bar[stage]);
             if (++stage == STAGES) {
                 stage = 0;
                 ph ^= 1u;
@@ -518,20 +593,23 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
             const int c = c0 + i;
             const ChunkInfo ci = plan_chunk(p, c);
             const bool mine = a.o && lane < 16 && r < ci.len;
-            // O0 of this thread's token and the block's columns, read straight from
-            // the record (ST::NS 16-column slices of 64 tokens x 32 bytes), after
-            // the record's ready flag when another part of the launch writes it
-            bool okw = !ready || wait_flag(ready + (size_t)c * a.H + h, flag_budget, abort);
+            // O0 of this thread's token and the block's columns, from the ring slot
+            // the producer filled with the chunk's Q' and O0 slices (ST::NS slices of
+            // 64 tokens x 32 bytes); the slot is released once every output warp has
+            // its rows
+            const int qs = i % ST::QSTAGES;
+            bool okw = mbar_wait_ab(&qfull_bar[qs], (uint32_t)((i / ST::QSTAGES) & 1), abort);
             uint4 o0v[2 * ST::NS];
             if (okw && mine) {
-                const char *o0 = records + (size_t)c * rec_stride + (size_t)h * REC_BF16_BYTES + REC_BF16_O0 +
-                                 (size_t)(col0 / 16) * REC_BF16_OSLICE + (size_t)r * 32;
+                const uint8_t *o0 = qring + qs * ST::QBYTES + ST::QO0 + r * 32;
 #pragma unroll
                 for (int sl = 0; sl < ST::NS; ++sl) {
                     o0v[2 * sl] = *reinterpret_cast<const uint4 *>(o0 + sl * REC_BF16_OSLICE);
                     o0v[2 * sl + 1] = *reinterpret_cast<const uint4 *>(o0 + sl * REC_BF16_OSLICE + 16);
                 }
             }
+            __syncwarp();
+            if (okw && lane == 0) mbar_arrive(&qfree_bar[qs]);
             okw = okw && mbar_wait_ab(&o_bar[b], (uint32_t)((i >> 1) & 1), abort);
             if (!__all_sync(0xffffffffu, okw) || *(volatile int *)&abort_flag) {
                 if (lane == 0) {
