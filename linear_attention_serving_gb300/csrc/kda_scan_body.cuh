@@ -485,15 +485,28 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
             ok = mbar_wait_ab(&full_bar[stage], ph, abort);
             // the entering state of this chunk, for the output kernel
             if (emit_s && ok) store_s<NT>(records + (size_t)(c0 + i) * rec_stride + (size_t)h * REC_BF16_BYTES, pc / 16, t, pk);
-            // ---- S <- Diag(a_C) S + H - G S; a_C and H are read while the MMA runs
+            // ---- S <- Diag(a_C) S + H - G S: Diag(a_C) S + H is formed while the
+            // chunk's MMA runs (it does not depend on G S)
             const uint8_t *stg = aharea + stage * ST::AH_BYTES;
-            float ac = 0.f, hv[NT];
+            float hv[NT];
 #pragma unroll
             for (int j = 0; j < NT; ++j) hv[j] = 0.f;
             if (ok) {
-                ac = reinterpret_cast<const float *>(stg + ST::AC)[t];
+                const float ac = reinterpret_cast<const float *>(stg + ST::AC)[t];
                 if (value_cols) load_slices<NT>(stg + ST::H + slice_offset(0, part * NT, 128), t, 128, hv);
+#pragma unroll
+                for (int j = 0; j < NT; j += 2) {
+                    const float2 r2 = __ffma2_rn(make_float2(ac, ac), make_float2(s[j], s[j + 1]),
+                                                 make_float2(hv[j], hv[j + 1]));
+                    hv[j] = r2.x;
+                    hv[j + 1] = r2.y;
+                }
             }
+            // operand buffer b ^ 1 (rewritten below) was also read by chunk i - 1's
+            // output MMA, which the tensor pipe ran before this chunk's MMA: checked
+            // here, while this chunk's MMA runs
+            if (EMIT_O && ok && i >= 1 && i + 1 < nchunks)
+                ok = mbar_wait_ab(&o_bar[b ^ 1], (uint32_t)(((i - 1) >> 1) & 1), abort);
             ok = ok && mbar_wait_ab(&g_bar, (uint32_t)(i & 1), abort);
             // a warp that gave up skips the update, raises the abort flag, and still
             // arrives at the operand barrier before it stops
@@ -503,12 +516,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 float d[NT];
                 tmem_row<NT>(tmem_g + lane_off + part * NT, d);
 #pragma unroll
-                for (int j = 0; j < NT; j += 2) {
-                    const float2 r2 = __ffma2_rn(make_float2(ac, ac), make_float2(s[j], s[j + 1]),
-                                                 make_float2(hv[j] - d[j], hv[j + 1] - d[j + 1]));
-                    s[j] = r2.x;
-                    s[j + 1] = r2.y;
-                }
+                for (int j = 0; j < NT; ++j) s[j] = hv[j] - d[j];
                 if (write_final && last) {
                     float *f = a.final_state + (((size_t)doc * a.H + h) * D + t) * D + pc;
 #pragma unroll
@@ -545,11 +553,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                     for (int j = 0; j < NT; ++j) s[j] = state_reset(a, ci_next.doc, h, t, pc + j);
                 }
                 pack_row<NT>(s, pk);
-                if (EMIT_O && i >= 1 && i + 1 < nchunks) {
-                    // operand buffer b ^ 1 was also read by chunk i - 1's output MMA
-                    good = __all_sync(0xffffffffu, mbar_wait_ab(&o_bar[b ^ 1], (uint32_t)(((i - 1) >> 1) & 1), abort));
-                }
-                if (good && i + 1 < nchunks) {
+                if (i + 1 < nchunks) {
                     write_sop<N, NT>(sop0 + (b ^ 1) * ST::SOP, t, part * NT / 16, pk);
                     fence_async_smem();
                 }
