@@ -190,7 +190,7 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
                                             const float *__restrict__ beta, int H, float g_min, const Plan &plan,
                                             char *__restrict__ records, uint8_t *smraw, int first, int stride,
                                             int *ready) {
-    __shared__ uint64_t mbar_p, mbar_w, mbar_g, mbar_in, mbar_dr;
+    __shared__ uint64_t mbar_p, mbar_w, mbar_g, mbar_q, mbar_in, mbar_dr;
     __shared__ uint32_t tmem_slot;
 
     if (plan_failed(plan)) return;
@@ -211,6 +211,7 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
         mbar_init(&mbar_p, 1);
         mbar_init(&mbar_w, 1);
         mbar_init(&mbar_g, 1);
+        mbar_init(&mbar_q, 1);
         mbar_init(&mbar_in, 1);
         mbar_init(&mbar_dr, 1);
         mbar_fence_init();
@@ -579,50 +580,38 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
         // ---- 5. K_restore^T [W | U0] = [G | H] (M = 128), and with M = 64
         //         (-M_qk) [W | U0] = [-M_qk W | -O0] (one N = 256 product), to which
         //         I Q_decay is added on the left half: Q' = Q_decay - M_qk W.  The
-        //         epilogue flips the sign of the right half back to O0.
+        //         epilogue flips the sign of the right half back to O0.  The M = 64
+        //         group goes first, with a commit of its own: its epilogue stages Q'
+        //         and O0 in areas the [G | H] products do not read, while they run.
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t IDG = idesc_bf16_f32_bmn(128, 256), IDM = idesc_bf16_f32_bmn(64, 128);
             constexpr uint32_t IDW = idesc_bf16_f32_bmn(64, 256);
             constexpr uint32_t NEG_A = 1u << 13;
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint32_t b0 = smem_u32(sm + SM_B2 + s * 2048);
-                const uint64_t am = sdesc_sw128(smem_u32(sm + SM_MQ + s * 32));
-                mma_bf16(tmem, sdesc_sw128(smem_u32(sm + SM_KRT + s * 32)), sdesc_mn(b0, 8192, 1024, SWZ_128B), IDG, s > 0);
-                mma_bf16(tmem + 256, am, sdesc_mn(b0, 8192, 1024, SWZ_128B), IDW | NEG_A, s > 0);
-            }
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem + 256, sdesc_sw128(smem_u32(sm + SM_MQ + s * 32)),
+                         sdesc_mn(smem_u32(sm + SM_B2 + s * 2048), 8192, 1024, SWZ_128B), IDW | NEG_A, s > 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tmem + 256, sdesc_sw128(smem_u32(sm + SM_ID + s * 32)),
                          sdesc_mn(smem_u32(sm + SM_QD + s * 2048), 8192, 1024, SWZ_128B), IDM, true);
+            mma_commit(&mbar_q);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem, sdesc_sw128(smem_u32(sm + SM_KRT + s * 32)),
+                         sdesc_mn(smem_u32(sm + SM_B2 + s * 2048), 8192, 1024, SWZ_128B), IDG, s > 0);
             mma_commit(&mbar_g);
         }
-        ok = mbar_wait(&mbar_g, (uint32_t)(it & 1));
+        ok = mbar_wait(&mbar_q, (uint32_t)(it & 1));
         __syncwarp();
         tc_fence_after();
         {
-            const int c = lg * 32 + lane;  // state row (channel) of [G | H]
             const int m = 16 * lg + lane;  // token of [M_qk W | O0] (lanes < 16)
 #pragma unroll
             for (int cb = 0; cb < 4; cb += 2) {
                 const int col = 64 * qt + 16 * cb;
                 float d[32];
-                tmem_ld16(tmem + lane_off + col, d);
-                tmem_ld16(tmem + lane_off + col + 16, d + 16);
-                tmem_ld_wait();
-                if (qt < 2) {
-#pragma unroll
-                    for (int h8 = 0; h8 < 4; ++h8)
-                        *reinterpret_cast<uint4 *>(sm + ST_G + sw128_offset(c, col + 8 * h8, 128)) = pack8(d + 8 * h8);
-                } else {
-#pragma unroll
-                    for (int h16 = 0; h16 < 2; ++h16) {
-                        uint8_t *dst = sm + ST_H + slice_offset(c, col + 16 * h16 - 128, 128);
-                        *reinterpret_cast<uint4 *>(dst) = pack8(d + 16 * h16);
-                        *reinterpret_cast<uint4 *>(dst + 16) = pack8(d + 16 * h16 + 8);
-                    }
-                }
                 tmem_ld16(tmem + lane_off + 256 + col, d);
                 tmem_ld16(tmem + lane_off + 256 + col + 16, d + 16);
                 tmem_ld_wait();
@@ -640,6 +629,32 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
                             *reinterpret_cast<uint4 *>(dst) = pack8(d + 16 * h16);
                             *reinterpret_cast<uint4 *>(dst + 16) = pack8(d + 16 * h16 + 8);
                         }
+                    }
+                }
+            }
+        }
+        ok = mbar_wait(&mbar_g, (uint32_t)(it & 1)) && ok;
+        __syncwarp();
+        tc_fence_after();
+        {
+            const int c = lg * 32 + lane;  // state row (channel) of [G | H]
+#pragma unroll
+            for (int cb = 0; cb < 4; cb += 2) {
+                const int col = 64 * qt + 16 * cb;
+                float d[32];
+                tmem_ld16(tmem + lane_off + col, d);
+                tmem_ld16(tmem + lane_off + col + 16, d + 16);
+                tmem_ld_wait();
+                if (qt < 2) {
+#pragma unroll
+                    for (int h8 = 0; h8 < 4; ++h8)
+                        *reinterpret_cast<uint4 *>(sm + ST_G + sw128_offset(c, col + 8 * h8, 128)) = pack8(d + 8 * h8);
+                } else {
+#pragma unroll
+                    for (int h16 = 0; h16 < 2; ++h16) {
+                        uint8_t *dst = sm + ST_H + slice_offset(c, col + 16 * h16 - 128, 128);
+                        *reinterpret_cast<uint4 *>(dst) = pack8(d + 16 * h16);
+                        *reinterpret_cast<uint4 *>(dst + 16) = pack8(d + 16 * h16 + 8);
                     }
                 }
             }
