@@ -55,9 +55,9 @@ KERNEL_SOURCES = {
 }
 
 
-# About 50 us of device spin ahead of each timed step's first event, while the
+# About 200 us of device spin ahead of each timed step's first event, while the
 # host enqueues the step: the events then time the device's work only.
-HOST_COVER_CYCLES = 100_000
+HOST_COVER_CYCLES = 400_000
 
 
 # ---------------------------------------------------------------- environment

@@ -563,10 +563,8 @@ int launch_decode_t(float *state, const void *q, const void *k, const void *v, c
     const DecSmem L(W, FUSE);
     const int smem = (int)L.total;
     auto kern = flags ? decode_kernel<InT, true, FUSE> : decode_kernel<InT, false, FUSE>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return KDA_ERR_CUDA;
     int per_sm = 1;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DEC_THREADS, smem);
+    if (prepare_kernel((const void *)kern, smem, DEC_THREADS, &per_sm) != KDA_OK) return KDA_ERR_CUDA;
     const long long slots = (long long)device_sm_count() * (per_sm > 0 ? per_sm : 1);
     const int grid = (int)(items < slots ? items : slots);
     kern<<<grid, DEC_THREADS, smem, s>>>(state, (const InT *)q, (const InT *)k, (const InT *)v, z, beta, A,

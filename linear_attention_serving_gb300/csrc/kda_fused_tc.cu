@@ -69,11 +69,8 @@ int launch_fused_tc(const void *q, const void *k, const void *v, const float *z,
     const size_t smem = PREP_TC_SMEM > chain_smem ? PREP_TC_SMEM : chain_smem;
     auto kern = p.flags ? (sa.ckpt ? fused_tc_kernel<true, true> : fused_tc_kernel<true, false>)
                         : (sa.ckpt ? fused_tc_kernel<false, true> : fused_tc_kernel<false, false>);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return KDA_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, PT_THREADS, smem) != cudaSuccess ||
-        per_sm < 1)
-        return KDA_OK;
+    if (prepare_kernel((const void *)kern, (int)smem, PT_THREADS, &per_sm) != KDA_OK) return KDA_ERR_CUDA;
+    if (per_sm < 1) return KDA_OK;
     InputMaps maps;
     const int rc = make_input_maps(q, k, v, z, T_total, H, &maps);
     if (rc) return rc;

@@ -3,6 +3,7 @@
 #include <cstdint>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "kda_internal.cuh"
 
@@ -43,6 +44,38 @@ constexpr long long DEFAULT_WAIT_BUDGET = 2000000000ll;  // about one second at 
 long long g_wait_budget = DEFAULT_WAIT_BUDGET;
 }  // namespace
 long long wait_budget() { return __atomic_load_n(&g_wait_budget, __ATOMIC_RELAXED); }
+
+namespace {
+struct KernelSetup {
+    const void *func;
+    int smem, threads, dev, per_sm;
+};
+constexpr int SETUP_MAX = 128;
+KernelSetup g_setup[SETUP_MAX];
+int g_nsetup = 0;
+std::mutex g_setup_mu;
+}  // namespace
+
+int prepare_kernel(const void *func, int smem_bytes, int threads, int *blocks_per_sm) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    for (int i = 0; i < g_nsetup; ++i) {
+        const KernelSetup &k = g_setup[i];
+        if (k.func == func && k.smem == smem_bytes && k.threads == threads && k.dev == dev) {
+            if (blocks_per_sm) *blocks_per_sm = k.per_sm;
+            return KDA_OK;
+        }
+    }
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, threads, (size_t)smem_bytes) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (g_nsetup < SETUP_MAX) g_setup[g_nsetup++] = KernelSetup{func, smem_bytes, threads, dev, per_sm};
+    if (blocks_per_sm) *blocks_per_sm = per_sm;
+    return KDA_OK;
+}
 
 void note_launch(const char *name, cudaStream_t s) {
     __atomic_add_fetch(&g_launches, 1ull, __ATOMIC_RELAXED);

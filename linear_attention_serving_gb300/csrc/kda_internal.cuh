@@ -224,6 +224,12 @@ int check_prefill(const void *q, const void *k, const void *v, const float *z, c
                   const float *beta, const int32_t *cu, int n_seqs, int64_t T_total, int H, int Dm,
                   int dtype, float g_min, const void *o, int flags);
 
+// Sets a kernel's dynamic shared-memory limit to smem_bytes and returns (in
+// *blocks_per_sm, when non-null) how many blocks of `threads` threads fit on an
+// SM; the driver is asked once per (kernel, size, device) and the answer is
+// cached, so repeated calls cost no driver round trips (kda_host.cu).
+int prepare_kernel(const void *func, int smem_bytes, int threads, int *blocks_per_sm);
+
 // Per-launch bookkeeping (kda_host.cu): counts every launch and, when
 // profiling is enabled, records an event after it on stream `s`.
 void note_launch(const char *name, cudaStream_t s);

@@ -26,8 +26,7 @@ int launch_prep_tc(const void *q, const void *k, const void *v, const float *z, 
     int rc = make_input_maps(q, k, v, z, T_total, H, &maps);
     if (rc) return rc;
     auto kern = p.flags ? prep_tc_kernel<true> : prep_tc_kernel<false>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PREP_TC_SMEM) != cudaSuccess)
-        return KDA_ERR_CUDA;
+    if (prepare_kernel((const void *)kern, (int)PREP_TC_SMEM, PT_THREADS, nullptr) != KDA_OK) return KDA_ERR_CUDA;
     const int grid = (int)(units < n_sm ? units : n_sm);
     kern<<<grid, PT_THREADS, PREP_TC_SMEM, s>>>(maps, A, beta, H, g_min, p, (char *)records);
     note_launch("prep_tc", s);

@@ -49,7 +49,7 @@ template <int N, int STAGES, int TPR, bool EMIT_O = false, bool CKPT = !EMIT_O>
 int launch_n(const ScanArgs &a, cudaStream_t s) {
     auto kern = scan_tc_kernel<N, STAGES, TPR, EMIT_O, CKPT>;
     const size_t smem = scan_tc_smem_bytes<N, STAGES, EMIT_O>();
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (prepare_kernel((const void *)kern, (int)smem, ScanCfg<N, TPR, EMIT_O>::THREADS, nullptr) != KDA_OK)
         return KDA_ERR_CUDA;
     const int lpt = a.mode == SCAN_DOCS && !a.plan.uniform && a.n_units > 1 && a.n_units <= LPT_MAX_DOCS;
     const dim3 grid = lpt ? dim3(a.H, a.ncols / N, a.n_units) : dim3(a.n_units, a.H, a.ncols / N);
