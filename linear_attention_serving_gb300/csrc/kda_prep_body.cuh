@@ -28,7 +28,7 @@
 //  2. four block-column MMAs (M = 128 for key tiles 0 and 1, M = 64 for tiles 2
 //     and 3, whose images have at most 64 rows) give M_qk and A_kk, from which
 //     L = StrictTril(Diag(beta) A_kk) (fp32) and the bf16 operand M_qk;
-//  3. INV = (I + L)^-1 in fp32 CUDA cores ("UT 变换"), stored as a bf16 operand;
+//  3. INV = (I + L)^-1 in fp32 CUDA cores ("UT 变换"), written as a bf16 operand;
 //  4. one M = 64, N = 256, K = 64 MMA: INV [Diag(beta) K_decay | Diag(beta) V]
 //     = [W | U0];
 //  5. [W | U0] becomes the MN-major operand of the MMAs issued together:
@@ -55,7 +55,7 @@ using namespace tc;
 
 constexpr int PT_THREADS = 512;
 constexpr int PT_TMEM_COLS = 512;
-constexpr int PT_STORE_TID = 256;  // issues the bulk stores of a record and publishes it
+constexpr int PT_STORE_TID = 384;  // issues the bulk stores of a record and publishes it
 constexpr float LOG2E = 1.4426950408889634f;
 
 // shared-memory map (bytes from a 1024-aligned base)
@@ -510,30 +510,16 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
         ok = !__syncthreads_or(!ok);
         if (!ok) { timed_out = true; break; }
 
-        // ---- 3. INV = (I + L)^-1, then its bf16 image (row i, k = s)
-        // the storing thread idles during the inverse's block products: it
+        // ---- 3. INV = (I + L)^-1, written as its bf16 image (row i, k = s).
+        // The storing thread idles during the inverse's block products: it
         // waits there for the previous unit's record to be complete in memory
         // and publishes it
-        tri_inverse<PT_THREADS>(Lm, INV, tmp, tid, [&] {
+        tri_inverse<PT_THREADS>(Lm, INV, tmp, sm + SM_A2, tid, [&] {
             if (tid == PT_STORE_TID && ready && u_prev >= 0) {
                 bulk_wait_all();
                 publish(ready + u_prev);
             }
         });
-        {
-            const int i = tid >> 3, g8 = tid & 7;
-            const float4 a = *reinterpret_cast<const float4 *>(INV + i * TRI_LD + 8 * g8);
-            const float4 b = *reinterpret_cast<const float4 *>(INV + i * TRI_LD + 8 * g8 + 4);
-            uint4 w;
-            w.x = bf2(make_float2(a.x, a.y));
-            w.y = bf2(make_float2(a.z, a.w));
-            w.z = bf2(make_float2(b.x, b.y));
-            w.w = bf2(make_float2(b.z, b.w));
-            *reinterpret_cast<uint4 *>(sm + SM_A2 + swz_chunk(i, g8)) = w;
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
 
         // ---- 4. INV [Diag(beta) K_decay | Diag(beta) V] = [W | U0]  (M = 64, N = 256, K = 64)
         if (tid == 0) {
