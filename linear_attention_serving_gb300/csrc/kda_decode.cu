@@ -273,13 +273,10 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
 
         // state of this item: shared memory -> registers; then the state buffer
         // takes the next item's state while the token rows are still in use
-        float s0[DEC_R], s1[DEC_R];
+        // (row r: columns col, col + 1 as one pair, updated by paired fp32 FMAs)
+        float2 sp[DEC_R];
 #pragma unroll
-        for (int i = 0; i < DEC_R; ++i) {
-            const float2 x = *reinterpret_cast<const float2 *>(&sS[(rbase + i) * D + col]);
-            s0[i] = x.x;
-            s1[i] = x.y;
-        }
+        for (int i = 0; i < DEC_R; ++i) sp[i] = *reinterpret_cast<const float2 *>(&sS[(rbase + i) * D + col]);
         __syncthreads();
         if (tid == 0 && next < n_items) issue_state<FUSE>(next, nacc_next, W, rowb, state, sm, L, &full_bar);
         const float eA = expf(A[h]);
@@ -442,21 +439,18 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
         // the recurrence over replay + bonus + drafts
         const float *bt = sbe;
         for (int t = 0; t < ntok; ++t) {
-            // two partial sums per column keep the FMA chains short
-            float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
+            // two partial sums per column keep the FMA chains short: pa (rows i, i + 2)
+            // and pb (rows i + 1, i + 3), each holding both columns
+            float2 pa = make_float2(0.f, 0.f), pb = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < DEC_R; i += 4) {
                 const float4 kv = *reinterpret_cast<const float4 *>(&kt[t][vidx(rbase + i)]);
-                a0 = fmaf(s0[i], kv.x, a0);
-                a1 = fmaf(s0[i + 1], kv.y, a1);
-                a0 = fmaf(s0[i + 2], kv.z, a0);
-                a1 = fmaf(s0[i + 3], kv.w, a1);
-                c0 = fmaf(s1[i], kv.x, c0);
-                c1 = fmaf(s1[i + 1], kv.y, c1);
-                c0 = fmaf(s1[i + 2], kv.z, c0);
-                c1 = fmaf(s1[i + 3], kv.w, c1);
+                pa = __ffma2_rn(sp[i], make_float2(kv.x, kv.x), pa);
+                pb = __ffma2_rn(sp[i + 1], make_float2(kv.y, kv.y), pb);
+                pa = __ffma2_rn(sp[i + 2], make_float2(kv.z, kv.z), pa);
+                pb = __ffma2_rn(sp[i + 3], make_float2(kv.w, kv.w), pb);
             }
-            float acc0 = a0 + a1, acc1 = c0 + c1;
+            float acc0 = pa.x + pb.x, acc1 = pa.y + pb.y;
 #pragma unroll
             for (int m = 8; m < 32; m <<= 1) {  // the four row parts
                 acc0 += __shfl_xor_sync(0xffffffffu, acc0, m);
@@ -464,34 +458,26 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
             }
             const float2 vv = *reinterpret_cast<const float2 *>(&vt[t][col]);
             const float bb = bt[t];
-            const float u0 = bb * (vv.x - acc0), u1 = bb * (vv.y - acc1);
+            const float2 uu = make_float2(bb * (vv.x - acc0), bb * (vv.y - acc1));
 #pragma unroll
             for (int i = 0; i < DEC_R; i += 4) {
                 const float4 kv = *reinterpret_cast<const float4 *>(&kh[t][vidx(rbase + i)]);
-                s0[i] = fmaf(kv.x, u0, s0[i]);
-                s0[i + 1] = fmaf(kv.y, u0, s0[i + 1]);
-                s0[i + 2] = fmaf(kv.z, u0, s0[i + 2]);
-                s0[i + 3] = fmaf(kv.w, u0, s0[i + 3]);
-                s1[i] = fmaf(kv.x, u1, s1[i]);
-                s1[i + 1] = fmaf(kv.y, u1, s1[i + 1]);
-                s1[i + 2] = fmaf(kv.z, u1, s1[i + 2]);
-                s1[i + 3] = fmaf(kv.w, u1, s1[i + 3]);
+                sp[i] = __ffma2_rn(make_float2(kv.x, kv.x), uu, sp[i]);
+                sp[i + 1] = __ffma2_rn(make_float2(kv.y, kv.y), uu, sp[i + 1]);
+                sp[i + 2] = __ffma2_rn(make_float2(kv.z, kv.z), uu, sp[i + 2]);
+                sp[i + 3] = __ffma2_rn(make_float2(kv.w, kv.w), uu, sp[i + 3]);
             }
             if (t >= nacc) {
-                float b0 = 0.f, b1 = 0.f, d0 = 0.f, d1 = 0.f;
+                float2 qa = make_float2(0.f, 0.f), qb = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int i = 0; i < DEC_R; i += 4) {
                     const float4 qv = *reinterpret_cast<const float4 *>(&qt[t][vidx(rbase + i)]);
-                    b0 = fmaf(s0[i], qv.x, b0);
-                    b1 = fmaf(s0[i + 1], qv.y, b1);
-                    b0 = fmaf(s0[i + 2], qv.z, b0);
-                    b1 = fmaf(s0[i + 3], qv.w, b1);
-                    d0 = fmaf(s1[i], qv.x, d0);
-                    d1 = fmaf(s1[i + 1], qv.y, d1);
-                    d0 = fmaf(s1[i + 2], qv.z, d0);
-                    d1 = fmaf(s1[i + 3], qv.w, d1);
+                    qa = __ffma2_rn(sp[i], make_float2(qv.x, qv.x), qa);
+                    qb = __ffma2_rn(sp[i + 1], make_float2(qv.y, qv.y), qb);
+                    qa = __ffma2_rn(sp[i + 2], make_float2(qv.z, qv.z), qa);
+                    qb = __ffma2_rn(sp[i + 3], make_float2(qv.w, qv.w), qb);
                 }
-                float ao0 = b0 + b1, ao1 = d0 + d1;
+                float ao0 = qa.x + qb.x, ao1 = qa.y + qb.y;
 #pragma unroll
                 for (int m = 8; m < 32; m <<= 1) {  // the four row parts
                     ao0 += __shfl_xor_sync(0xffffffffu, ao0, m);
@@ -515,10 +501,10 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
 #pragma unroll
                 for (int i = 0; i < DEC_R; i += 4) {
                     const float4 sc4 = *reinterpret_cast<const float4 *>(&scommit[vidx(rbase + i)]);
-                    __stcs(reinterpret_cast<float2 *>(&Sg[(size_t)(rbase + i) * D + col]), make_float2(s0[i] * sc4.x, s1[i] * sc4.x));
-                    __stcs(reinterpret_cast<float2 *>(&Sg[(size_t)(rbase + i + 1) * D + col]), make_float2(s0[i + 1] * sc4.y, s1[i + 1] * sc4.y));
-                    __stcs(reinterpret_cast<float2 *>(&Sg[(size_t)(rbase + i + 2) * D + col]), make_float2(s0[i + 2] * sc4.z, s1[i + 2] * sc4.z));
-                    __stcs(reinterpret_cast<float2 *>(&Sg[(size_t)(rbase + i + 3) * D + col]), make_float2(s0[i + 3] * sc4.w, s1[i + 3] * sc4.w));
+                    __stcs(reinterpret_cast<float2 *>(&Sg[(size_t)(rbase + i) * D + col]), __fmul2_rn(sp[i], make_float2(sc4.x, sc4.x)));
+                    __stcs(reinterpret_cast<float2 *>(&Sg[(size_t)(rbase + i + 1) * D + col]), __fmul2_rn(sp[i + 1], make_float2(sc4.y, sc4.y)));
+                    __stcs(reinterpret_cast<float2 *>(&Sg[(size_t)(rbase + i + 2) * D + col]), __fmul2_rn(sp[i + 2], make_float2(sc4.z, sc4.z)));
+                    __stcs(reinterpret_cast<float2 *>(&Sg[(size_t)(rbase + i + 3) * D + col]), __fmul2_rn(sp[i + 3], make_float2(sc4.w, sc4.w)));
                 }
             }
         }
