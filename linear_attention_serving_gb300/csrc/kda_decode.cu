@@ -145,6 +145,14 @@ __device__ __forceinline__ void issue_rows(int item, int nacc, int H, int W, con
     }
 }
 
+// Decay factor exp(g) of one channel, g = g_min sigmoid(e^{A_h} z) (the gate of
+// "Kimi K3 模型结构（2）" eq. (5)), with the hardware base-2 exponential and a
+// fast reciprocal; relative error a few fp32 ulp.
+__device__ __forceinline__ float dec_decay(float g_min, float eA, float z) {
+    const float e = ex2(-eA * z * 1.4426950408889634f);
+    return ex2(__fdividef(g_min, 1.f + e) * 1.4426950408889634f);
+}
+
 // beta of token slot t of item `item` for either accepted count: thread t < W-1
 // holds the cached draft's beta in `bc`, thread t < W the window's in `bw`.
 __device__ __forceinline__ void load_betas(int item, int H, int W, int tid, const float *__restrict__ beta,
@@ -222,6 +230,15 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
     bool timed_out = false;
     for (int it = 0; item < n_items; item += gridDim.x, ++it) {
         const int b = item / H, h = item - b * H;
+        // FUSE: the head's convolution taps of this thread's channel, loaded before
+        // the wait for the item's copies so that their latency hides behind it
+        float4 wq, wk, wv;
+        if (FUSE) {
+            const int c = tid & (D - 1);
+            wq = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)0 * H + h) * D + c);
+            wk = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)1 * H + h) * D + c);
+            wv = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)2 * H + h) * D + c);
+        }
         const int next = item + gridDim.x, next2 = next + gridDim.x;
         const int nacc_next = nacc_nx;
         int nacc_nn = 0;
@@ -311,7 +328,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                     float qq = t < nacc ? 0.f : to_f32(reinterpret_cast<const InT *>(slot)[c]);
                     float kk = to_f32(reinterpret_cast<const InT *>(slot + 512)[c]);
                     const float zz = reinterpret_cast<const float *>(slot + 1536)[c];
-                    sc *= expf(kda_gate(g_min, eA, zz));
+                    sc *= dec_decay(g_min, eA, zz);
                     kt[t][vc] = kk * sc;
                     kh[t][vc] = __fdividef(kk, sc);
                     qt[t][vc] = qq * sc;
@@ -328,12 +345,8 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                 const int c = tid & (D - 1), vc = vidx(c), quarter = warp & 3;
                 const int tmid = (ntok + 1) >> 1;
                 const int t_begin = tid < D ? 0 : tmid, t_end = tid < D ? tmid : ntok;
-                float4 wq, wk, wv;
                 float hq0, hq1, hq2, hk0, hk1, hk2, hv0, hv1, hv2;  // FUSE: x_{t-3}, x_{t-2}, x_{t-1}
                 if (FUSE) {
-                    wq = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)0 * H + h) * D + c);
-                    wk = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)1 * H + h) * D + c);
-                    wv = __ldg(reinterpret_cast<const float4 *>(fz.conv_w) + ((size_t)2 * H + h) * D + c);
                     // the three inputs before t_begin: token rows, or the convolution state
                     // for stream positions before the first token
                     auto hist = [&](int x, int ps) {
@@ -371,7 +384,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                     qt[t][vc] = xq;
                     kt[t][vc] = xk;
                     vt[t][c] = xv;
-                    kh[t][vc] = expf(kda_gate(g_min, eA, reinterpret_cast<const float *>(slot + 1536)[c]));
+                    kh[t][vc] = dec_decay(g_min, eA, reinterpret_cast<const float *>(slot + 1536)[c]);
                     if (l2norm) {
                         // input option: squared norms over the 128 channels (no q for replays)
                         float pq = t < nacc ? 0.f : xq * xq, pk = xk * xk;
@@ -425,7 +438,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                 const float wn = __ldg(fz.o_norm_w + c);
 #pragma unroll
                 for (int j = 0; j < MAX_W; ++j)
-                    if (j < W) sg[j][c] = wn / (1.f + expf(-gl[j]));
+                    if (j < W) sg[j][c] = __fdividef(wn, 1.f + __expf(-gl[j]));
             }
         }
         if (tid < W - 1) cb[((size_t)b * (W - 1) + tid) * H + h] = sbt[nacc + 1 + tid];
