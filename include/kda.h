@@ -169,14 +169,26 @@ int kda_chunk_fwd_ckpt(const void *q, const void *k, const void *v,
  * chain, not the parallel preparation, setting the time, kda_chunk_fwd runs
  * the kda_segment_scan decomposition with this many segments instead; its
  * results equal the single-chain run up to rounding).
- *   varlen  nonzero when the call passes cu_seqlens: such calls (document
- *           lengths only on the device) always take the single-chain path
+ *   varlen  nonzero when the call passes cu_seqlens: the count for the
+ *           longest document such a batch can hold (one of T_total tokens).
+ *           The call itself plans from its actual longest document: when
+ *           this bound is nonzero it reads cu_seqlens back to the host (it
+ *           waits once for the stream; not while the stream is captured into
+ *           a graph, which keeps the single-chain path).
  * Returns 0 for the single-chain path, else the segment count (2 .. 64).  The
  * choice depends on the shape, the dtype (bf16 only) and the current device's
- * SM count; kda_chunk_fwd_workspace_size already includes the room it needs.
+ * SM count; kda_chunk_fwd_workspace_size already includes the room it needs
+ * (a call given less keeps the single-chain path, with the same results).
  * No device work; never fails (invalid shapes return 0).
  * ------------------------------------------------------------------------ */
 int kda_chunk_fwd_plan_segments(int64_t T_total, int H, int n_seqs, int dtype, int varlen);
+
+/* The timing model behind that choice, measured on GB300: microseconds per
+ * (chunk, head) preparation unit on one SM, and per chunk of one chain.  A
+ * chain over L chunks is split when 1.3 us x L exceeds 1.5 times the
+ * preparation time of the batch on the SMs the chains leave free.  NULL
+ * arguments are skipped. */
+void kda_planner_model(double *prep_us_per_unit, double *chain_us_per_chunk);
 
 int kda_chunk_fwd(const void *q, const void *k, const void *v,
                   const float *z, const float *A, const float *beta,

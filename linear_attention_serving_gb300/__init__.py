@@ -8,10 +8,10 @@ short convolution and the gated output norm around the recurrence).
 """
 from .kda import (KDAError, chunk_fwd, chunk_fwd_ckpt, chunk_fwd_noalloc, chunk_fwd_plan_segments,
                   chunk_fwd_workspace_size, decode_step, decode_step_fused, launch_count, library_path, load,
-                  noalloc_read_device_error, profile_collect, profile_enable, read_device_error, segment_scan,
-                  segment_scan_auto_segments, segment_scan_workspace_size, set_wait_budget)
+                  noalloc_read_device_error, planner_model, profile_collect, profile_enable, read_device_error,
+                  segment_scan, segment_scan_auto_segments, segment_scan_workspace_size, set_wait_budget)
 
 __all__ = ["KDAError", "chunk_fwd", "chunk_fwd_ckpt", "chunk_fwd_noalloc", "chunk_fwd_plan_segments",
            "chunk_fwd_workspace_size", "decode_step", "decode_step_fused", "launch_count", "library_path", "load",
-           "noalloc_read_device_error", "profile_collect", "profile_enable", "read_device_error", "segment_scan",
-           "segment_scan_auto_segments", "segment_scan_workspace_size", "set_wait_budget"]
+           "noalloc_read_device_error", "planner_model", "profile_collect", "profile_enable", "read_device_error",
+           "segment_scan", "segment_scan_auto_segments", "segment_scan_workspace_size", "set_wait_budget"]

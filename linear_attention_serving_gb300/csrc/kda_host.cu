@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "kda_internal.cuh"
 
@@ -163,10 +164,12 @@ int make_plan(const int32_t *cu, int n_seqs, int64_t T_total, void *ws, const Wo
 // "KDA：三种执行形态" (SM-level CP): with few (document, head) chains over a
 // long document the sequential chain, not the parallel preparation, sets the
 // time; cutting the chunk list into segments that run side by side and are
-// then composed shortens it).  Only for equal-length bf16 batches, whose
-// document length is known on the host.  The model, measured on GB300:
+// then composed shortens it).  bf16 only.  Equal-length batches plan from
+// their length; packed batches from their longest document.  The model,
+// measured on GB300 (kda_planner_model returns it; a GPU test checks it
+// against the kernels):
 //   one chain        about 1.3 us per chunk (64 state columns per block);
-//   preparation      about 10.3 us per (chunk, head) unit on one SM, on the SMs
+//   preparation      about 8.6 us per (chunk, head) unit on one SM, on the SMs
 //                    the chains leave free (all SMs without the fused launch);
 //   segments         pay a second pass over the chain and the composition
 //                    (about 25 us per segment), so they win only when the
@@ -188,19 +191,59 @@ int wave_segments(int64_t total_chunks, int H, int n_sm) {
     return n >= 1 ? (int)n : 1;
 }
 
-// Returns 0 for one chain per (document, head).
-int plan_segments(int64_t T_total, int H, int n_seqs, bool varlen, int dtype, int n_sm) {
-    if (varlen || dtype != KDA_BF16 || T_total <= 0 || n_seqs < 1 || H < 1) return 0;
-    const int64_t chunks = (T_total / n_seqs + C - 1) / C;  // per document
-    const int64_t total = chunks * n_seqs;
+constexpr double PLAN_PREP_US_PER_UNIT = 8.6;
+constexpr double PLAN_CHAIN_US_PER_CHUNK = 1.3;
+
+// Segment count for a batch of n_seqs documents with `total` chunks in all,
+// the longest `longest` chunks; 0 for one chain per (document, head).
+int plan_from_chunks(int64_t longest, int64_t total, int H, int n_seqs, int dtype, int n_sm) {
+    if (dtype != KDA_BF16 || longest <= 0 || total <= 0 || n_seqs < 1 || H < 1) return 0;
     const double units = (double)total * H;
     const int64_t chains = 2LL * n_seqs * H;
     const int prep_sms = chains <= n_sm / 4 ? n_sm - (int)chains : n_sm;
-    const double prep_us = 10.3 * units / (double)(prep_sms > 0 ? prep_sms : 1);
-    const double chain_us = 1.3 * (double)chunks;
+    const double prep_us = PLAN_PREP_US_PER_UNIT * units / (double)(prep_sms > 0 ? prep_sms : 1);
+    const double chain_us = PLAN_CHAIN_US_PER_CHUNK * (double)longest;
     if (chain_us <= 1.5 * prep_us) return 0;
     const int n = wave_segments(total, H, n_sm);
     return n >= 2 ? n : 0;
+}
+
+// Equal-length batches (varlen = false) plan from their length.  Packed
+// batches (varlen) get the count for the longest document they can hold (one
+// of T_total tokens): an upper bound, since a call plans again from its actual
+// longest document.
+int plan_segments(int64_t T_total, int H, int n_seqs, bool varlen, int dtype, int n_sm) {
+    if (T_total <= 0 || n_seqs < 1 || H < 1) return 0;
+    if (varlen) {
+        const int64_t longest = (T_total + C - 1) / C;
+        return plan_from_chunks(longest, T_total / C + n_seqs, H, n_seqs, dtype, n_sm);
+    }
+    const int64_t chunks = (T_total / n_seqs + C - 1) / C;  // per document
+    return plan_from_chunks(chunks, chunks * n_seqs, H, n_seqs, dtype, n_sm);
+}
+
+// A packed call's own count: its longest document, read from cu_seqlens (the
+// call waits for the stream once).  Only asked when the bound above says
+// segments could pay, never while the stream is being captured into a graph.
+int plan_packed(const int32_t *cu_seqlens, int64_t T_total, int H, int n_seqs, int dtype, int n_sm,
+                cudaStream_t s) {
+    if (plan_segments(T_total, H, n_seqs, true, dtype, n_sm) == 0) return 0;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return 0;
+    std::vector<int32_t> cu((size_t)n_seqs + 1);
+    if (cudaMemcpyAsync(cu.data(), cu_seqlens, cu.size() * sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return 0;
+    int64_t longest = 0, total = 0;
+    for (int n = 0; n < n_seqs; ++n) {
+        const int64_t len = (int64_t)cu[n + 1] - cu[n];
+        if (len < 0) return 0;  // the plan kernel reports the bad offsets
+        const int64_t ch = (len + C - 1) / C;
+        longest = ch > longest ? ch : longest;
+        total += ch;
+    }
+    return plan_from_chunks(longest, total, H, n_seqs, dtype, n_sm);
 }
 
 // kda_segment_scan's n_segments, with 0 meaning the wave rule's count.
@@ -323,14 +366,24 @@ long long kda_set_wait_budget(long long cycles) {
 
 size_t kda_chunk_fwd_workspace_size(int64_t T_total, int H, int n_seqs, int dtype) {
     if (T_total < 0 || H < 1 || n_seqs < 1) return 0;
-    // room for the segmented path whenever an equal-length batch of this shape takes it
-    const int n_seg = plan_segments(T_total, H, n_seqs, false, dtype, device_sm_count());
-    return workspace_layout(T_total, H, n_seqs, n_seg, dtype).total;
+    // room for the segmented path whenever a batch of this shape can take it:
+    // equal lengths, or packed with a long document
+    const int n_sm = device_sm_count();
+    const int a = plan_segments(T_total, H, n_seqs, false, dtype, n_sm);
+    const int b = plan_segments(T_total, H, n_seqs, true, dtype, n_sm);
+    const size_t wa = workspace_layout(T_total, H, n_seqs, a, dtype).total;
+    const size_t wb = workspace_layout(T_total, H, n_seqs, b, dtype).total;
+    return wa > wb ? wa : wb;
 }
 
 int kda_chunk_fwd_plan_segments(int64_t T_total, int H, int n_seqs, int dtype, int varlen) {
     if (T_total < 0 || H < 1 || n_seqs < 1) return 0;
     return plan_segments(T_total, H, n_seqs, varlen != 0, dtype, device_sm_count());
+}
+
+void kda_planner_model(double *prep_us_per_unit, double *chain_us_per_chunk) {
+    if (prep_us_per_unit) *prep_us_per_unit = PLAN_PREP_US_PER_UNIT;
+    if (chain_us_per_chunk) *chain_us_per_chunk = PLAN_CHAIN_US_PER_CHUNK;
 }
 
 size_t kda_segment_scan_workspace_size(int64_t T_total, int H, int n_seqs, int n_segments,
@@ -356,10 +409,13 @@ int chunk_fwd_impl(const void *q, const void *k, const void *v, const float *z, 
                    kda_stream_t stream, const ScanArgs *ckpt) {
     int rc = check_prefill(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, Dm, dtype, g_min, o, flags);
     if (rc) return rc;
-    const int n_seg = plan_segments(T_total, H, n_seqs, cu_seqlens != nullptr, dtype, device_sm_count());
+    cudaStream_t s = (cudaStream_t)stream;
+    int n_seg = cu_seqlens ? plan_packed(cu_seqlens, T_total, H, n_seqs, dtype, device_sm_count(), s)
+                           : plan_segments(T_total, H, n_seqs, false, dtype, device_sm_count());
+    // a workspace sized for the single-chain path keeps that path (same results)
+    if (n_seg > 0 && workspace_bytes < workspace_layout(T_total, H, n_seqs, n_seg, dtype).total) n_seg = 0;
     const Workspace w = workspace_layout(T_total, H, n_seqs, n_seg, dtype);
     if (!workspace || workspace_bytes < w.total || ((uintptr_t)workspace & 255u)) return KDA_ERR_WORKSPACE;
-    cudaStream_t s = (cudaStream_t)stream;
     note_begin(s);
     if (n_seg > 0)
         return run_segment_scan(q, k, v, z, A, beta, cu_seqlens, n_seqs, T_total, H, dtype, g_min, init_state,

@@ -53,6 +53,8 @@ def load(build_if_missing: bool = True):
     lib.kda_segment_scan_workspace_size.restype = S
     lib.kda_chunk_fwd_plan_segments.argtypes = [L, I, I, I, I]
     lib.kda_chunk_fwd_plan_segments.restype = I
+    lib.kda_planner_model.argtypes = [P, P]
+    lib.kda_planner_model.restype = None
     lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, P, P, P, S, I, P]
     lib.kda_chunk_fwd.restype = I
     lib.kda_chunk_fwd_ckpt.argtypes = [P, P, P, P, P, P, P, I, L, I, I, I, F, P, P, P, I, P, I, P, I, P, S, I, P]
@@ -127,6 +129,14 @@ def chunk_fwd_plan_segments(T_total: int, H: int, n_seqs: int = 1, dtype=torch.b
     shape on the current device (0 = one chain per (document, head))."""
     code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
     return int(load().kda_chunk_fwd_plan_segments(T_total, H, n_seqs, code, int(varlen)))
+
+
+def planner_model() -> tuple:
+    """kda_planner_model: (microseconds per prep unit on one SM, microseconds per
+    chain chunk) behind kda_chunk_fwd's segment choice."""
+    a, b = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    load().kda_planner_model(ctypes.byref(a), ctypes.byref(b))
+    return a.value, b.value
 
 
 def segment_scan_workspace_size(T_total: int, H: int, n_seqs: int, n_segments: int,

@@ -56,14 +56,21 @@ def test_workspace_sizes_grow_with_work():
 def test_segment_planner_host_logic():
     """kda_chunk_fwd's own segment count: none for the bench's H=16, T=8192
     (the chains keep pace with the preparation) or for short documents; a few
-    dozen at most for a long document over few heads; never for varlen (document
-    lengths are on the device) or fp32; and the workspace size has room for it."""
+    dozen at most for a long document over few heads; for a packed batch, the
+    count for the longest document it can hold (the call plans again from its
+    actual lengths); never for fp32; and the workspace size has room for it."""
     bf16 = torch.bfloat16
     assert kda.chunk_fwd_plan_segments(8192, 16, 1, bf16) == 0
     assert kda.chunk_fwd_plan_segments(333, 3, 1, bf16) == 0
     n = kda.chunk_fwd_plan_segments(1 << 20, 8, 1, bf16)
     assert 2 <= n <= 64
-    assert kda.chunk_fwd_plan_segments(1 << 20, 8, 1, bf16, varlen=True) == 0
+    assert kda.chunk_fwd_plan_segments(1 << 20, 8, 1, bf16, varlen=True) == n
+    # 128 equal documents of 8192 tokens keep one chain each; packed, the same
+    # total could be one long document
+    assert kda.chunk_fwd_plan_segments(1 << 20, 8, 128, bf16) == 0
+    nv = kda.chunk_fwd_plan_segments(1 << 20, 8, 128, bf16, varlen=True)
+    assert 2 <= nv <= 64
+    assert kda.chunk_fwd_workspace_size(1 << 20, 8, 128) >= kda.segment_scan_workspace_size(1 << 20, 8, 128, nv)
     assert kda.chunk_fwd_plan_segments(1 << 20, 8, 1, torch.float32) == 0
     assert kda.chunk_fwd_plan_segments(-1, 8, 1, bf16) == 0 and kda.chunk_fwd_plan_segments(64, 0, 1, bf16) == 0
     assert kda.chunk_fwd_workspace_size(1 << 20, 8, 1) >= kda.segment_scan_workspace_size(1 << 20, 8, 1, n)

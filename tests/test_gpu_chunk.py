@@ -155,6 +155,36 @@ def test_planner_segmented_path(T, H, n_seqs):
     check_run(run_both(inp, n_seqs=n_seqs), "bf16")
 
 
+@pytest.mark.parametrize("lens,H", [([128, 12000, 352], 2), ([8192, 64, 1, 4096], 1)])
+def test_planner_segments_packed_long_document(lens, H):
+    """A packed batch whose longest document would leave one chain setting the
+    time: kda_chunk_fwd reads the document lengths, takes the segmented path
+    (the composition kernel runs) and matches the oracle, state resets at every
+    boundary included; a batch of the same total in short documents keeps one
+    chain per (document, head)."""
+    T = sum(lens)
+    assert kda.chunk_fwd_plan_segments(T, H, len(lens), varlen=True) >= 2
+    inp = kda_synth.prefill_inputs(T, H, "bf16", seed=950 + T, z_std=1.0, A_std=0.5, init_std=0.05,
+                                   cu_seqlens=kda_synth.cu_from_lengths(lens))
+    kda.profile_enable(True)
+    kda.profile_collect()
+    res = run_both(inp, n_seqs=len(lens))
+    names = [n for n, _ in kda.profile_collect()]
+    kda.profile_enable(False)
+    assert "compose" in names, names
+    check_run(res, "bf16")
+    # the same total in documents of at most 512 tokens: no segments
+    short = [512] * (T // 512) + ([T % 512] if T % 512 else [])
+    d = to_dev(kda_synth.prefill_inputs(T, H, "bf16", seed=951, cu_seqlens=kda_synth.cu_from_lengths(short)), DEV)
+    kda.profile_enable(True)
+    kda.profile_collect()
+    kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    names = [n for n, _ in kda.profile_collect()]
+    kda.profile_enable(False)
+    assert "compose" not in names, names
+
+
 def raw_inputs(T, H, dtype, seed, n_seqs=1):
     """Prefill inputs with unnormalised q, k (each row scaled by 0.5 .. 3) and beta logits."""
     inp = kda_synth.prefill_inputs(T, H, dtype, seed=seed, z_std=1.0, init_std=0.05, n_init=n_seqs)
