@@ -177,9 +177,10 @@ def chunk_fwd(q, k, v, z, A, beta, cu_seqlens=None, init_state=None, g_min=G_MIN
     dt = _dtype_code(q)
     o = out if out is not None else torch.empty_like(q)
     fin = torch.empty((n, H, Dm, Dm), device=q.device, dtype=torch.float32) if output_final_state else None
-    need = lib.kda_chunk_fwd_workspace_size(T, H, n, dt)
-    if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    if workspace is None:
+        # (a caller's own workspace is passed as given: one with room for the
+        # single-chain path only keeps that path, a smaller one is refused)
+        workspace = torch.empty(lib.kda_chunk_fwd_workspace_size(T, H, n, dt), device=q.device, dtype=torch.uint8)
     rc = lib.kda_chunk_fwd(_p(q), _p(k), _p(v), _p(z), _p(A), _p(beta), _p(cu_seqlens), n, T, H, Dm,
                            dt, float(g_min), _p(init_state), _p(o), _p(fin), _p(workspace),
                            workspace.numel(), _flags(qk_l2norm, beta_sigmoid, q_scale), _stream(q.device))
@@ -205,9 +206,10 @@ def chunk_fwd_ckpt(q, k, v, z, A, beta, ckpt_interval, ckpt_slot, ckpt, cu_seqle
         raise KDAError("ckpt must be fp32 [n_slots, H, 128, 128]")
     o = out if out is not None else torch.empty_like(q)
     fin = torch.empty((n, H, Dm, Dm), device=q.device, dtype=torch.float32) if output_final_state else None
-    need = lib.kda_chunk_fwd_workspace_size(T, H, n, dt)
-    if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    if workspace is None:
+        # (a caller's own workspace is passed as given: one with room for the
+        # single-chain path only keeps that path, a smaller one is refused)
+        workspace = torch.empty(lib.kda_chunk_fwd_workspace_size(T, H, n, dt), device=q.device, dtype=torch.uint8)
     rc = lib.kda_chunk_fwd_ckpt(_p(q), _p(k), _p(v), _p(z), _p(A), _p(beta), _p(cu_seqlens), n, T, H, Dm,
                                 dt, float(g_min), _p(init_state), _p(o), _p(fin), int(ckpt_interval), _p(ckpt_slot),
                                 ckpt_slot.shape[1], _p(ckpt), ckpt.shape[0], _p(workspace), workspace.numel(),

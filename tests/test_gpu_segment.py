@@ -156,13 +156,20 @@ def test_segscan_1m_h8_full_size():
                                     0, b - a, h, reset_at_begin=(a == 0))
         e_m, e_s = rel_fro(pm[h, i], M_ref), rel_fro(ps[h, i], St_ref)
         assert e_m <= 1e-2 and e_s <= 1e-2, f"pair ({h}, {i}): M {e_m:.3e}, S~ {e_s:.3e}"
-    # the unsplit run: a one-document cu_seqlens keeps kda_chunk_fwd on its single
-    # chain per head (its planner segments only equal-length batches)
+    # the unsplit run: kda_chunk_fwd given a workspace with room for one segment
+    # only keeps its single chain per head (its planner would take segments)
     del pm, ps
     one_doc = torch.tensor([0, w.T], dtype=torch.int32, device=DEV)
-    assert kda.chunk_fwd_plan_segments(w.T, w.H, 1, varlen=True) == 0
-    o_u, fin_u = kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"], cu_seqlens=one_doc)
+    assert kda.chunk_fwd_plan_segments(w.T, w.H, 1, varlen=True) >= 2
+    ws = torch.empty(kda.segment_scan_workspace_size(w.T, w.H, 1, 1), dtype=torch.uint8, device=DEV)
+    kda.profile_enable(True)
+    kda.profile_collect()
+    o_u, fin_u = kda.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["z"], inp["A"], inp["beta"], cu_seqlens=one_doc,
+                               workspace=ws)
     torch.cuda.synchronize()
+    names = [n for n, _ in kda.profile_collect()]
+    kda.profile_enable(False)
+    assert "compose" not in names, names
     assert rel_fro(o, o_u) <= 1e-3 and rel_fro(fin, fin_u) <= 1e-3
 
 
