@@ -130,13 +130,15 @@ __device__ __forceinline__ uint4 pack8f(const float *f) {
 }
 
 // The bf16 S operand is MN-major (k = state row, the block's N columns
-// contiguous): 16 columns with the 32-byte swizzle, 64 with the 128-byte one.
+// contiguous): 16 columns with the 32-byte swizzle, 64 with the 128-byte one,
+// 128 as two 64-column blocks BLOCK bytes apart.
 template <int N>
 struct SOp {
-    static_assert(N == 16 || N == 64, "S operand layouts exist for 16 and 64 columns");
-    static constexpr uint32_t ROW = 2 * N;       // bytes per state row
-    static constexpr uint32_t SBO = 8 * ROW;     // 8-row group
-    static constexpr uint32_t KSTEP = 16 * ROW;  // one K = 16 MMA step
+    static_assert(N == 16 || N == 64 || N == 128, "S operand layouts exist for 16, 64 and 128 columns");
+    static constexpr uint32_t ROW = N == 16 ? 32 : 128;  // bytes per state row of one block
+    static constexpr uint32_t SBO = 8 * ROW;              // 8-row group
+    static constexpr uint32_t KSTEP = 16 * ROW;           // one K = 16 MMA step
+    static constexpr uint32_t BLOCK = 128 * ROW;          // one block of columns (128 state rows)
     static constexpr uint32_t MODE = N == 16 ? SWZ_32B : SWZ_128B;
 };
 
@@ -150,12 +152,12 @@ __device__ __forceinline__ void pack_row(const float *s, uint4 *pk) {
 // NT packed columns [c16 * 16, c16 * 16 + NT) of row t into the S operand
 template <int N, int NT>
 __device__ __forceinline__ void write_sop(uint8_t *sop, int t, int c16, const uint4 *pk) {
-    uint8_t *row = sop + t * SOp<N>::ROW;
 #pragma unroll
     for (int c = 0; c < NT / 8; ++c) {
-        const int cg = 2 * c16 + c;  // 16-byte chunk of the row
-        const int sc = N == 16 ? (cg ^ ((t >> 2) & 1)) : (cg ^ (t & 7));
-        *reinterpret_cast<uint4 *>(row + sc * 16) = pk[c];
+        const int cg = 2 * c16 + c;  // 16-byte chunk of the state row, over all N columns
+        const int blk = N == 128 ? (cg >> 3) : 0, cb = N == 128 ? (cg & 7) : cg;
+        const int sc = N == 16 ? (cb ^ ((t >> 2) & 1)) : (cb ^ (t & 7));
+        *reinterpret_cast<uint4 *>(sop + blk * SOp<N>::BLOCK + t * SOp<N>::ROW + sc * 16) = pk[c];
     }
 }
 
@@ -173,7 +175,7 @@ __device__ __forceinline__ void store_s(char *rec, int blk0, int t, const uint4 
 
 template <int N>
 __device__ __forceinline__ uint64_t sop_desc(const uint8_t *sop) {
-    return sdesc_mn(smem_u32(sop), SOp<N>::SBO, SOp<N>::SBO, SOp<N>::MODE);
+    return sdesc_mn(smem_u32(sop), N == 128 ? SOp<N>::BLOCK : SOp<N>::SBO, SOp<N>::SBO, SOp<N>::MODE);
 }
 
 // N bf16 values of row r from consecutive 16-column slices of `rows` rows each

@@ -2,7 +2,8 @@
 // kda_scan_body.cuh): one block per (document or segment, head, column block).
 // Few chains: 16-column blocks that store each chunk's entering state for the
 // output kernel.  Many chains: 64-column blocks that form the outputs of their
-// columns themselves (as the fused launch's chain blocks do).  Packed documents
+// columns themselves (as the fused launch's chain blocks do), and 128-column
+// blocks for the segment pairs.  Packed documents
 // of unequal length start longest first (the document is the grid's slowest
 // dimension, ranked by chunk count), so that the last blocks to start hold
 // the shortest chains.
@@ -74,6 +75,9 @@ int launch_scan_tc(const ScanArgs &a, int n_sm, cudaStream_t s) {
     // (checkpoints in an instantiation of their own)
     if (a.o && a.phase != 1 && a.ncols == D)
         return a.ckpt ? launch_n<64, 3, 2, true, true>(a, s) : launch_n<64, 3, 2, true, false>(a, s);
+    // the segment pairs (256 columns: values and transition): 128-column blocks,
+    // so that each chunk's G is read twice per (segment, head), not four times
+    if (a.phase == 1 && a.ncols == 2 * D) return launch_n<128, 2, 4>(a, s);
     const int rc = launch_n<64, 2, 2>(a, s);
     return (rc || !a.o || a.phase == 1) ? rc : launch_out_tc(a.plan, a.H, a.records, a.o, n_sm, s);
 }
