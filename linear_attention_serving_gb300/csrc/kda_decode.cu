@@ -288,14 +288,6 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
             if (tid < W) sbe[nacc + tid] = bsig ? 1.f / (1.f + expf(-bw_cur)) : bw_cur;
         }
 
-        // state of this item: shared memory -> registers; then the state buffer
-        // takes the next item's state while the token rows are still in use
-        // (row r: columns col, col + 1 as one pair, updated by paired fp32 FMAs)
-        float2 sp[DEC_R];
-#pragma unroll
-        for (int i = 0; i < DEC_R; ++i) sp[i] = *reinterpret_cast<const float2 *>(&sS[(rbase + i) * D + col]);
-        __syncthreads();
-        if (tid == 0 && next < n_items) issue_state<FUSE>(next, nacc_next, W, rowb, state, sm, L, &full_bar);
         const float eA = expf(A[h]);
         if (tid == D) {
             // the new drafts' projected inputs replace this sequence's cache slots
@@ -442,7 +434,15 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
             }
         }
         if (tid < W - 1) cb[((size_t)b * (W - 1) + tid) * H + h] = sbt[nacc + 1 + tid];
+        // state of this item: shared memory -> registers, after the token prep (which
+        // so runs with the registers the state takes); past the barrier the state
+        // buffer takes the next item's state
+        // (row r: columns col, col + 1 as one pair, updated by paired fp32 FMAs)
+        float2 sp[DEC_R];
+#pragma unroll
+        for (int i = 0; i < DEC_R; ++i) sp[i] = *reinterpret_cast<const float2 *>(&sS[(rbase + i) * D + col]);
         __syncthreads();
+        if (tid == 0 && next < n_items) issue_state<FUSE>(next, nacc_next, W, rowb, state, sm, L, &full_bar);
         // the row buffers are free once the cache copies have read them: the next item's token rows
         if (tid == D) bulk_wait_read_all();
         if (tid == D && next < n_items)
