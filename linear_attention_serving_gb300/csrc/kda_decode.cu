@@ -315,6 +315,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
             if (tid < D) {
                 const int c = tid, vc = vidx(c);
                 float sc = 1.f;
+#pragma unroll 2
                 for (int t = 0; t < ntok; ++t) {
                     const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
                     float qq = t < nacc ? 0.f : to_f32(reinterpret_cast<const InT *>(slot)[c]);
@@ -349,6 +350,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                     hk0 = hist(1, t_begin - 3), hk1 = hist(1, t_begin - 2), hk2 = hist(1, t_begin - 1);
                     hv0 = hist(2, t_begin - 3), hv1 = hist(2, t_begin - 2), hv2 = hist(2, t_begin - 1);
                 }
+#pragma unroll 2
                 for (int t = t_begin; t < t_end; ++t) {
                     const uint8_t *slot = sm + L.raw + (size_t)t * ROW_SLOT;
                     // replayed tokens of the plain step carry no q (never read below)
@@ -398,6 +400,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
                 // and the scaled vectors s_t k, k / s_t, s_t q
                 const int c = tid, vc = vidx(c);
                 float sc = 1.f;
+#pragma unroll 2
                 for (int t = 0; t < ntok; ++t) {
                     sc *= kh[t][vc];
                     float qq = t < nacc ? 0.f : qt[t][vc];
