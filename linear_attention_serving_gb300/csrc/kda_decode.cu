@@ -230,6 +230,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
     bool timed_out = false;
     for (int it = 0; item < n_items; item += gridDim.x, ++it) {
         const int b = item / H, h = item - b * H;
+        const float A_h = __ldg(A + h);  // loaded before the wait for the item's copies
         // FUSE: the head's convolution taps of this thread's channel, loaded before
         // the wait for the item's copies so that their latency hides behind it
         float4 wq, wk, wv;
@@ -288,7 +289,7 @@ decode_kernel(float *__restrict__ state, const InT *__restrict__ q, const InT *_
             if (tid < W) sbe[nacc + tid] = bsig ? 1.f / (1.f + expf(-bw_cur)) : bw_cur;
         }
 
-        const float eA = expf(A[h]);
+        const float eA = expf(A_h);
         if (tid == D) {
             // the new drafts' projected inputs replace this sequence's cache slots
             // (the prep reads the raw rows but never writes them)
