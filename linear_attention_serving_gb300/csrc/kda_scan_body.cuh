@@ -8,13 +8,15 @@
 // K2 (U = INV Diag(beta)(V - K_decay S), S = Diag(a[-1]) S + K_restore^T U)
 // with its products regrouped so that only one tensor-core round trip sits on
 // the sequential path.  The output O = O0 + Q' S of every chunk is off the
-// path: this kernel stores each chunk's entering state S (bf16) into the
-// record, and the output kernel (kda_out_tc.cu) forms all outputs in parallel
-// afterwards.
+// path: either this kernel stores each chunk's entering state S (bf16) into
+// the record and the output kernel (kda_out_tc.cu) forms all outputs in
+// parallel afterwards, or (EMIT_O) the block forms its columns' outputs itself
+// on warps of their own.
 //
-// A block owns N state columns (columns evolve independently).  With 256
-// state columns the extra 128 start from the identity with H = 0: they carry
-// the transition M of "Kimi K3 模型结构（7）" eq. (17) for the segment pairs.
+// A block owns N = 16, 64 or 128 state columns (columns evolve independently).
+// With 256 state columns the extra 128 start from the identity with H = 0:
+// they carry the transition M of "Kimi K3 模型结构（7）" eq. (17) for the
+// segment pairs.
 //
 // Chain warps (4 per TPR): thread t of a row group owns state row t (TMEM lane
 //   t) and N / TPR of its columns; the fp32 state master lives in registers,
