@@ -29,9 +29,9 @@
 //     and 3, whose images have at most 64 rows) give M_qk and A_kk, from which
 //     L = StrictTril(Diag(beta) A_kk) (fp32) and the bf16 operand M_qk;
 //  3. INV = (I + L)^-1 in fp32 CUDA cores ("UT 变换"), written as a bf16 operand;
-//  4. one M = 64, N = 256, K = 64 MMA: INV [Diag(beta) K_decay | Diag(beta) V]
-//     = [W | U0];
-//  5. [W | U0] becomes the MN-major operand of the MMAs issued together:
+//  4. two M = 128, N = 64, K = 64 MMAs: [Diag(beta) K_decay | Diag(beta) V]^T
+//     INV^T = [W | U0]^T (a channel per TMEM lane);
+//  5. [W | U0]^T becomes the K-major B operand of the MMAs issued together:
 //     K_restore^T [W | U0] = [G | H] (M = 128) and, with M = 64,
 //     Q' = I Q_decay + (-M_qk) W and O0 = M_qk U0; G, H, Q', O0 go to the record.
 // The record is staged in shared memory, in the operand areas the last
@@ -67,7 +67,7 @@ constexpr int SM_AREG = 0;           // the unit's input tiles (TMA), read into 
 constexpr int SM_AREG_KB = 40960;    // offset of the second k-block of the A_q images
 constexpr int SM_BQ = 81920;         // key-side images, 2 k-blocks x (4 tiles x 16 rows x 128 B)
 constexpr int SM_B2 = 98304;         // [Diag(beta) K_decay | Diag(beta) V]^T (256 rows x 64 tokens);
-                                     // later [W | U0] MN-major (4 blocks of 64 columns x 64 tokens)
+                                     // later [W | U0]^T in the same K-major layout
 constexpr int SM_A2 = 131072;        // INV (64 rows x 64), then O0 staging
 constexpr int SM_KRT = 147456;       // K_restore^T: 128 channels x 64 tokens
 constexpr int SM_QD = 163840;        // Q_decay, MN-major (2 blocks of 64 channels x 64 tokens)
@@ -521,7 +521,10 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
             }
         });
 
-        // ---- 4. INV [Diag(beta) K_decay | Diag(beta) V] = [W | U0]  (M = 64, N = 256, K = 64)
+        // ---- 4. [W | U0]^T = [Diag(beta) K_decay | Diag(beta) V]^T INV^T: two M = 128,
+        //         N = 64, K = 64 products (the channels of K_decay, then of V, against
+        //         the INV image as a K-major B operand); every TMEM lane holds a
+        //         channel, so the epilogue below keeps all 128 lanes busy
         if (tid == 0) {
             if (has_next) {
                 // the image area is free until the next unit's build: its input tiles
@@ -529,12 +532,15 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
                 load_tiles(maps, sm + SM_AREG, u_next % H, ci_next.tok, &mbar_in);
             }
             tc_fence_after();
-            constexpr uint32_t IDW = idesc_bf16_f32(64, 256);
+            constexpr uint32_t IDT = idesc_bf16_f32(128, 64);
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t ad = sdesc_sw128(smem_u32(sm + SM_A2 + s * 32));
-                const uint64_t bd = sdesc_sw128(smem_u32(sm + SM_B2 + s * 32));
-                mma_bf16(tmem, ad, bd, IDW, s > 0);
+            for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ad = sdesc_sw128(smem_u32(sm + SM_B2 + hf * 16384 + s * 32));
+                    const uint64_t bd = sdesc_sw128(smem_u32(sm + SM_A2 + s * 32));
+                    mma_bf16(tmem + 64 * hf, ad, bd, IDT, s > 0);
+                }
             }
             mma_commit(&mbar_w);
         }
@@ -543,20 +549,17 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
         __syncwarp();
         tc_fence_after();
         {
-            // token m = 16 lg + lane (lanes < 16) -> [W | U0] MN-major, 64-column block qt
-            const int m = 16 * lg + lane;
+            // channel c = TMEM lane, tokens 32 qt .. 32 qt + 31 of the 128 columns
+            // [W^T | U0^T] -> row n of [W | U0]^T (K-major, the B2 layout): n = c for
+            // W, 128 + c for U0
+            const int c = lg * 32 + lane, n = (qt < 2 ? 0 : 128) + c, g0 = 4 * (qt & 1);
+            float d[32];
+            tmem_ld16(tmem + lane_off + 32 * qt, d);
+            tmem_ld16(tmem + lane_off + 32 * qt + 16, d + 16);
+            tmem_ld_wait();
 #pragma unroll
-            for (int cb = 0; cb < 4; cb += 2) {
-                float d[32];
-                tmem_ld16(tmem + lane_off + 64 * qt + 16 * cb, d);
-                tmem_ld16(tmem + lane_off + 64 * qt + 16 * cb + 16, d + 16);
-                tmem_ld_wait();
-                if (lane < 16) {
-#pragma unroll
-                    for (int h8 = 0; h8 < 4; ++h8)
-                        *reinterpret_cast<uint4 *>(sm + SM_B2 + qt * 8192 + swz_chunk(m, 2 * cb + h8)) = pack8(d + 8 * h8);
-                }
-            }
+            for (int h8 = 0; h8 < 4; ++h8)
+                *reinterpret_cast<uint4 *>(sm + SM_B2 + swz_chunk(n, g0 + h8)) = pack8(d + 8 * h8);
         }
         fence_async_smem();
         tc_fence_before();
@@ -571,13 +574,13 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
         //         and O0 in areas the [G | H] products do not read, while they run.
         if (tid == 0) {
             tc_fence_after();
-            constexpr uint32_t IDG = idesc_bf16_f32_bmn(128, 256), IDM = idesc_bf16_f32_bmn(64, 128);
-            constexpr uint32_t IDW = idesc_bf16_f32_bmn(64, 256);
+            constexpr uint32_t IDG = idesc_bf16_f32(128, 256), IDM = idesc_bf16_f32_bmn(64, 128);
+            constexpr uint32_t IDW = idesc_bf16_f32(64, 256);
             constexpr uint32_t NEG_A = 1u << 13;
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tmem + 256, sdesc_sw128(smem_u32(sm + SM_MQ + s * 32)),
-                         sdesc_mn(smem_u32(sm + SM_B2 + s * 2048), 8192, 1024, SWZ_128B), IDW | NEG_A, s > 0);
+                         sdesc_sw128(smem_u32(sm + SM_B2 + s * 32)), IDW | NEG_A, s > 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tmem + 256, sdesc_sw128(smem_u32(sm + SM_ID + s * 32)),
@@ -586,7 +589,7 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
 #pragma unroll
             for (int s = 0; s < 4; ++s)
                 mma_bf16(tmem, sdesc_sw128(smem_u32(sm + SM_KRT + s * 32)),
-                         sdesc_mn(smem_u32(sm + SM_B2 + s * 2048), 8192, 1024, SWZ_128B), IDG, s > 0);
+                         sdesc_sw128(smem_u32(sm + SM_B2 + s * 32)), IDG, s > 0);
             mma_commit(&mbar_g);
         }
         ok = mbar_wait(&mbar_q, (uint32_t)(it & 1));
