@@ -53,6 +53,25 @@ def test_workspace_sizes_grow_with_work():
     assert lib.kda_segment_scan_workspace_size(64, 1, 1, -1, 0) == 0
 
 
+def test_planner_model_constants():
+    """The timing model behind the planner's choice (kda_planner_model): positive,
+    the preparation of a (chunk, head) unit slower on one SM than a chain's step
+    (what makes long chains over few heads worth splitting), and the rule's
+    boundary where the bound says: a single chain just over 1.5x the preparation
+    of its batch on the SMs the chain leaves free gets segments."""
+    prep_us, chain_us = kda.planner_model()
+    assert prep_us > chain_us > 0
+    bf16 = torch.bfloat16
+    # one document, one head: chains = 2, so the preparation spreads over SMs - 2
+    sms = 148 if not torch.cuda.is_available() else torch.cuda.get_device_properties(0).multi_processor_count
+    for chunks in (64, 256, 4096):
+        units = chunks
+        prep = prep_us * units / (sms - 2)
+        expect_split = chain_us * chunks > 1.5 * prep
+        got = kda.chunk_fwd_plan_segments(chunks * 64, 1, 1, bf16)
+        assert (got >= 2) == expect_split, (chunks, got, chain_us * chunks, prep)
+
+
 def test_segment_planner_host_logic():
     """kda_chunk_fwd's own segment count: none for the bench's H=16, T=8192
     (the chains keep pace with the preparation) or for short documents; a few
