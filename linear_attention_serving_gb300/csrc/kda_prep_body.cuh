@@ -389,7 +389,7 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
         // 32 rows) are adjacent, so one M = 128, N = 32 MMA over both key tiles
         // serves them: the blocks it forms across the two (tile 2's rows against
         // tile 3's keys and the reverse) are never read.
-        if (tid == 0) {
+        if (warp == 0) {  // the whole warp: one elected lane issues
             tc_fence_after();
             constexpr uint32_t ID16 = idesc_bf16_f32(128, 16), ID32 = idesc_bf16_f32(128, 32);
 #pragma unroll
@@ -399,10 +399,10 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
                     const int kbs = s >> 2, w = s & 3;
                     const uint64_t ad = sdesc_sw128(smem_u32(sm + SM_AREG + kbs * SM_AREG_KB + arow_base(qq) * 128 + w * 32));
                     const uint64_t bd = sdesc_sw128(smem_u32(sm + SM_BQ + kbs * 8192 + qq * 2048 + w * 32));
-                    mma_bf16(tmem + 16 * qq, ad, bd, qq < 2 ? ID16 : ID32, s > 0);
+                    mma_bf16_w(tmem + 16 * qq, ad, bd, qq < 2 ? ID16 : ID32, s > 0);
                 }
             }
-            mma_commit(&mbar_p);
+            mma_commit_w(&mbar_p);
         }
 
         // ---- 1c. while those products run: the token-contiguous operands of the
@@ -525,12 +525,13 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
         //         N = 64, K = 64 products (the channels of K_decay, then of V, against
         //         the INV image as a K-major B operand); every TMEM lane holds a
         //         channel, so the epilogue below keeps all 128 lanes busy
-        if (tid == 0) {
-            if (has_next) {
+        if (warp == 0) {
+            if (lane == 0 && has_next) {
                 // the image area is free until the next unit's build: its input tiles
                 fence_async_smem();
                 load_tiles(maps, sm + SM_AREG, u_next % H, ci_next.tok, &mbar_in);
             }
+            __syncwarp();
             tc_fence_after();
             constexpr uint32_t IDT = idesc_bf16_f32(128, 64);
 #pragma unroll
@@ -539,10 +540,10 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
                 for (int s = 0; s < 4; ++s) {
                     const uint64_t ad = sdesc_sw128(smem_u32(sm + SM_B2 + hf * 16384 + s * 32));
                     const uint64_t bd = sdesc_sw128(smem_u32(sm + SM_A2 + s * 32));
-                    mma_bf16(tmem + 64 * hf, ad, bd, IDT, s > 0);
+                    mma_bf16_w(tmem + 64 * hf, ad, bd, IDT, s > 0);
                 }
             }
-            mma_commit(&mbar_w);
+            mma_commit_w(&mbar_w);
         }
         if (has_next) ++tiles_issued;
         ok = mbar_wait(&mbar_w, (uint32_t)(it & 1));
@@ -572,25 +573,25 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
         //         epilogue flips the sign of the right half back to O0.  The M = 64
         //         group goes first, with a commit of its own: its epilogue stages Q'
         //         and O0 in areas the [G | H] products do not read, while they run.
-        if (tid == 0) {
+        if (warp == 0) {
             tc_fence_after();
             constexpr uint32_t IDG = idesc_bf16_f32(128, 256), IDM = idesc_bf16_f32_bmn(64, 128);
             constexpr uint32_t IDW = idesc_bf16_f32(64, 256);
             constexpr uint32_t NEG_A = 1u << 13;
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tmem + 256, sdesc_sw128(smem_u32(sm + SM_MQ + s * 32)),
-                         sdesc_sw128(smem_u32(sm + SM_B2 + s * 32)), IDW | NEG_A, s > 0);
+                mma_bf16_w(tmem + 256, sdesc_sw128(smem_u32(sm + SM_MQ + s * 32)),
+                           sdesc_sw128(smem_u32(sm + SM_B2 + s * 32)), IDW | NEG_A, s > 0);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tmem + 256, sdesc_sw128(smem_u32(sm + SM_ID + s * 32)),
-                         sdesc_mn(smem_u32(sm + SM_QD + s * 2048), 8192, 1024, SWZ_128B), IDM, true);
-            mma_commit(&mbar_q);
+                mma_bf16_w(tmem + 256, sdesc_sw128(smem_u32(sm + SM_ID + s * 32)),
+                           sdesc_mn(smem_u32(sm + SM_QD + s * 2048), 8192, 1024, SWZ_128B), IDM, true);
+            mma_commit_w(&mbar_q);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tmem, sdesc_sw128(smem_u32(sm + SM_KRT + s * 32)),
-                         sdesc_sw128(smem_u32(sm + SM_B2 + s * 32)), IDG, s > 0);
-            mma_commit(&mbar_g);
+                mma_bf16_w(tmem, sdesc_sw128(smem_u32(sm + SM_KRT + s * 32)),
+                           sdesc_sw128(smem_u32(sm + SM_B2 + s * 32)), IDG, s > 0);
+            mma_commit_w(&mbar_g);
         }
         ok = mbar_wait(&mbar_q, (uint32_t)(it & 1));
         __syncwarp();
@@ -666,12 +667,15 @@ __device__ __forceinline__ void prep_blocks(const InputMaps *maps, const float *
         bulk_wait_all();
         if (ready && u_prev >= 0 && !timed_out) publish(ready + u_prev);
     }
-    if (tid == 0) {
-        if (timed_out) atomicOr(plan.err, KDA_DEVERR_TIMEOUT);
-        // tile loads and tensor-core work this block started have finished
-        // before the block leaves or frees its TMEM (no-ops after a full run)
-        if (tiles_issued > tiles_landed) mbar_wait(&mbar_in, (uint32_t)((tiles_issued - 1) & 1));
-        mma_commit(&mbar_dr);
+    if (warp == 0) {
+        if (lane == 0) {
+            if (timed_out) atomicOr(plan.err, KDA_DEVERR_TIMEOUT);
+            // tile loads and tensor-core work this block started have finished
+            // before the block leaves or frees its TMEM (no-ops after a full run)
+            if (tiles_issued > tiles_landed) mbar_wait(&mbar_in, (uint32_t)((tiles_issued - 1) & 1));
+        }
+        __syncwarp();
+        mma_commit_w(&mbar_dr);
         mbar_wait(&mbar_dr, 0);
     }
     tc_fence_before();

@@ -373,66 +373,65 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
                 go = false;
             }
             bar_sync(OPERAND_BAR, CF::OPERAND_BAR_THREADS);
-            if (*abort || !__shfl_sync(0xffffffffu, (int)go, 0)) break;
-            if (lane == 0) {
-                {
-                    tc_fence_after();
-                    constexpr uint32_t IDESC = idesc_bf16_f32_bmn(128, N);
-                    const uint64_t gd = gd0 + (uint64_t)((stage * ST::G_BYTES) >> 4);
-                    const uint64_t sd = sd0 + (uint64_t)(((i & 1) * ST::SOP) >> 4);
+            if (__shfl_sync(0xffffffffu, (int)(*abort) || !go, 0)) break;
+            {
+                // the whole warp runs the issue code (one elected lane issues)
+                tc_fence_after();
+                constexpr uint32_t IDESC = idesc_bf16_f32_bmn(128, N);
+                const uint64_t gd = gd0 + (uint64_t)((stage * ST::G_BYTES) >> 4);
+                const uint64_t sd = sd0 + (uint64_t)(((i & 1) * ST::SOP) >> 4);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        mma_bf16(tmem_g, gd + (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
-                                 sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDESC, k > 0);
-                    mma_commit(&g_bar);
-                    if (EMIT_O) mbar_arrive(&sop_bar[i & 1]);
-                    issued_any = true;
-                }
+                for (int k = 0; k < 8; ++k)
+                    mma_bf16_w(tmem_g, gd + (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                               sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDESC, k > 0);
+                mma_commit_w(&g_bar);
+                __syncwarp();
+                if (EMIT_O && lane == 0) mbar_arrive(&sop_bar[i & 1]);
+                issued_any = true;
             }
-            __syncwarp();
             if (++stage == STAGES) {
                 stage = 0;
                 ph ^= 1u;
             }
         }
-        if (lane == 0 && issued_any) {
+        if (issued_any) {
             // every chain MMA has completed before TMEM is freed, also when the
             // block stopped early
-            mma_commit(&drain_bar);
+            mma_commit_w(&drain_bar);
             mbar_wait(&drain_bar, 0);
         }
     } else if (EMIT_O && warp == CF::OMMA_WARP) {
         // ------------------------------------------------------------ output MMAs
-        if (lane == 0) {
-            const uint64_t sd0 = sop_desc<N>(sop0);
-            for (int i = 0; i < nchunks; ++i) {
-                const int b = i & 1, qs = i % ST::QSTAGES;
-                // chunk i's chain MMA is issued (so its S operand is complete), the
-                // output warps have read what chunk i - 2 left in accumulator b, and
-                // chunk i's Q' has landed
-                if (!mbar_wait_ab(&sop_bar[b], (uint32_t)((i >> 1) & 1), abort) ||
-                    (i >= 2 && !mbar_wait_ab(&oempty_bar[b], (uint32_t)(((i - 2) >> 1) & 1), abort)) ||
-                    !mbar_wait_ab(&qfull_bar[qs], (uint32_t)((i / ST::QSTAGES) & 1), abort)) {
-                    abort_flag = 1;
-                    break;
-                }
-                tc_fence_after();
-                constexpr uint32_t IDO = idesc_bf16_f32_bmn(64, N);
-                const uint64_t qd = sdesc_sw128(smem_u32(qring + qs * ST::QBYTES));
-                const uint64_t sd = sd0 + (uint64_t)((b * ST::SOP) >> 4);
+        // (the whole warp: one elected lane issues)
+        const uint64_t sd0 = sop_desc<N>(sop0);
+        for (int i = 0; i < nchunks; ++i) {
+            const int b = i & 1, qs = i % ST::QSTAGES;
+            // chunk i's chain MMA is issued (so its S operand is complete), the
+            // output warps have read what chunk i - 2 left in accumulator b, and
+            // chunk i's Q' has landed
+            const bool fail = !mbar_wait_ab(&sop_bar[b], (uint32_t)((i >> 1) & 1), abort) ||
+                              (i >= 2 && !mbar_wait_ab(&oempty_bar[b], (uint32_t)(((i - 2) >> 1) & 1), abort)) ||
+                              !mbar_wait_ab(&qfull_bar[qs], (uint32_t)((i / ST::QSTAGES) & 1), abort);
+            if (__any_sync(0xffffffffu, fail)) {
+                if (lane == 0) abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            constexpr uint32_t IDO = idesc_bf16_f32_bmn(64, N);
+            const uint64_t qd = sdesc_sw128(smem_u32(qring + qs * ST::QBYTES));
+            const uint64_t sd = sd0 + (uint64_t)((b * ST::SOP) >> 4);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    mma_bf16(tmem_g + ST::OCOL + b * N, qd + (uint64_t)(((k >> 2) * 8192 + (k & 3) * 32) >> 4),
-                             sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDO, k > 0);
-                mma_commit(&o_bar[b]);
-                mma_commit(&qfree_bar[qs]);  // Q' read
-            }
-            // every output MMA has completed before TMEM is freed, also when the
-            // block stopped early
-            if (nchunks > 0) {
-                mma_commit(&odrain_bar);
-                mbar_wait(&odrain_bar, 0);
-            }
+            for (int k = 0; k < 8; ++k)
+                mma_bf16_w(tmem_g + ST::OCOL + b * N, qd + (uint64_t)(((k >> 2) * 8192 + (k & 3) * 32) >> 4),
+                           sd + (uint64_t)((k * SOp<N>::KSTEP) >> 4), IDO, k > 0);
+            mma_commit_w(&o_bar[b]);
+            mma_commit_w(&qfree_bar[qs]);  // Q' read
+        }
+        // every output MMA has completed before TMEM is freed, also when the
+        // block stopped early
+        if (nchunks > 0) {
+            mma_commit_w(&odrain_bar);
+            mbar_wait(&odrain_bar, 0);
         }
     } else if (warp < CF::CHAIN_WARPS) {
         // ------------------------------------------------------------ chain warps
