@@ -180,18 +180,34 @@ __device__ __forceinline__ uint64_t sop_desc(const uint8_t *sop) {
     return sdesc_mn(smem_u32(sop), N == 128 ? SOp<N>::BLOCK : SOp<N>::SBO, SOp<N>::SBO, SOp<N>::MODE);
 }
 
+// The two 16-byte halves of row r of a 16-column slice (32-byte rows), in
+// the order a thread reads them: rows r with (r >> 2) odd read the upper half
+// first, so that the eight rows a quarter-warp reads at once cover all 32
+// banks instead of half of them twice.  lo = columns 0-7, hi = 8-15.
+__device__ __forceinline__ void slice_row_halves(const uint8_t *row, int r, uint4 &lo, uint4 &hi) {
+    const int sw = (r & 4) << 2;  // 0 or 16
+    const uint4 a = *reinterpret_cast<const uint4 *>(row + sw);
+    const uint4 b = *reinterpret_cast<const uint4 *>(row + (sw ^ 16));
+    lo = sw ? b : a;
+    hi = sw ? a : b;
+}
+
 // N bf16 values of row r from consecutive 16-column slices of `rows` rows each
 template <int N>
 __device__ __forceinline__ void load_slices(const uint8_t *base, int r, int rows, float *out) {
 #pragma unroll
-    for (int j = 0; j < N; j += 8) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(base + slice_offset(r, j, rows));
-        const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u);
+    for (int j = 0; j < N; j += 16) {
+        uint4 u[2];
+        slice_row_halves(base + slice_offset(r, j, rows), r, u[0], u[1]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(p[e]);
-            out[j + 2 * e] = f.x;
-            out[j + 2 * e + 1] = f.y;
+        for (int hf = 0; hf < 2; ++hf) {
+            const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u[hf]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(p[e]);
+                out[j + 8 * hf + 2 * e] = f.x;
+                out[j + 8 * hf + 2 * e + 1] = f.y;
+            }
         }
     }
 }
@@ -610,10 +626,7 @@ __device__ __forceinline__ void scan_block(const ScanArgs &a, int unit, int h, i
             if (okw && mine) {
                 const uint8_t *o0 = qring + qs * ST::QBYTES + ST::QO0 + r * 32;
 #pragma unroll
-                for (int sl = 0; sl < ST::NS; ++sl) {
-                    o0v[2 * sl] = *reinterpret_cast<const uint4 *>(o0 + sl * REC_BF16_OSLICE);
-                    o0v[2 * sl + 1] = *reinterpret_cast<const uint4 *>(o0 + sl * REC_BF16_OSLICE + 16);
-                }
+                for (int sl = 0; sl < ST::NS; ++sl) slice_row_halves(o0 + sl * REC_BF16_OSLICE, r, o0v[2 * sl], o0v[2 * sl + 1]);
             }
             __syncwarp();
             if (okw && lane == 0) mbar_arrive(&qfree_bar[qs]);
