@@ -25,15 +25,19 @@
 //     the key side k_j exp(Delta_q) / e_j, with F_pp = exp(-Delta_p) <= e^80 and
 //     F_pq = prod_{q<t<p} exp(Delta_t) <= 1; Q_decay; and the token-contiguous
 //     Diag(beta) K_decay, Diag(beta) V, K_restore^T;
-//  2. four block-column MMAs (M = 128 for key tiles 0 and 1, M = 64 for tiles 2
-//     and 3, whose images have at most 64 rows) give M_qk and A_kk, from which
+//  2. block-column MMAs, M = 128: per k-step one N = 16 product for key tile 0,
+//     one for key tile 1, and one N = 32 product over the adjacent images of
+//     tiles 2 and 3, give M_qk and A_kk, from which
 //     L = StrictTril(Diag(beta) A_kk) (fp32) and the bf16 operand M_qk;
-//  3. INV = (I + L)^-1 in fp32 CUDA cores ("UT 变换"), written as a bf16 operand;
+//  3. INV = (I + L)^-1 ("UT 变换"): the 16 x 16 diagonal blocks by forward
+//     substitution in fp32, the block products as split-tf32 mma.sync tiles
+//     (kda_tri.cuh), written as a bf16 operand;
 //  4. two M = 128, N = 64, K = 64 MMAs: [Diag(beta) K_decay | Diag(beta) V]^T
 //     INV^T = [W | U0]^T (a channel per TMEM lane);
 //  5. [W | U0]^T becomes the K-major B operand of the MMAs issued together:
 //     K_restore^T [W | U0] = [G | H] (M = 128) and, with M = 64,
 //     Q' = I Q_decay + (-M_qk) W and O0 = M_qk U0; G, H, Q', O0 go to the record.
+// Warp 0 runs the tcgen05 issue code as a whole warp, one elected lane issuing.
 // The record is staged in shared memory, in the operand areas the last
 // products have finished reading, and written with bulk copies that overlap
 // the next unit's first phases.  Where chain blocks consume the records as

@@ -25,7 +25,8 @@
 //   After writing their rows of that operand the chain warps arrive at a named
 //   barrier and go on.
 // MMA warp: waits at that barrier (a hardware barrier wakes it at once),
-//   checks the chunk's stage and issues the chain's MMA.
+//   checks the chunk's stage and issues the chain's MMA (the whole warp runs
+//   the issue code, one elected lane issuing, as the output-MMA warp does).
 // Output-MMA warp (EMIT_O): once a chunk's chain MMA is issued, issues its
 //   output MMA O = Q' S_enter (M = 64) into one of two TMEM accumulators, so
 //   that the chain never waits for the output path.
