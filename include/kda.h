@@ -48,7 +48,7 @@ typedef struct CUstream_st *kda_stream_t;
 enum kda_status {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer   */
-    KDA_ERR_UNSUPPORTED = 2,   /* D != 128, or a mode this build does not have */
+    KDA_ERR_UNSUPPORTED = 2,   /* D != 128, or a mode the library does not implement */
     KDA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or launch failed   */
     KDA_ERR_TIMEOUT = 4,       /* a bounded device wait gave up                 */
     KDA_ERR_WORKSPACE = 5,     /* workspace missing or smaller than required    */
