@@ -7,9 +7,10 @@ its inputs untouched, and must give bit for bit the result of the same call on
 plain buffers (the kernels are deterministic).  The shapes are ragged on
 purpose: documents of 1 and 63 tokens, chunk tails, a segment split that does
 not divide the chunks, decode windows with replays.  Every path the calls
-choose between is taken: the fused launch, the three-kernel path of many
-chains, the automatic segments, the fp32 path, the segment scan with its
-pairs, and both decode steps."""
+choose between is taken: the fused launch and its input-option
+instantiation, the three-kernel path of many chains, the automatic segments,
+the fp32 path, the checkpoint pages, the segment scan with its pairs, and
+both decode steps."""
 import pytest
 import torch
 
@@ -198,3 +199,83 @@ def test_decode_writes_only_its_buffers(fused):
     assert all(torch.equal(g.t, c) for g, c in zip(cg, cache_r))
     if fused:
         assert torch.equal(cs.t, cs_r)
+
+
+def test_chunk_fwd_ckpt_writes_only_its_buffers():
+    """Checkpoint pages: the marked ones written, the skipped ones (-1, and
+    positions past a document's end) left as they were, nothing outside."""
+    lens, H, interval = [100, 700], 2, 128
+    cu = kda_synth.cu_from_lengths(lens)
+    n, T = len(lens), int(cu[-1])
+    inp = kda_synth.prefill_inputs(T, H, "bf16", seed=31, cu_seqlens=cu, init_std=0.05)
+    d = to_dev(inp, DEV)
+    Dm = d["q"].shape[2]
+    per_seq = max(lens) // interval + 1
+    slot = torch.full((n, per_seq), -1, dtype=torch.int32)
+    nxt = 0
+    for doc in range(n):
+        for j in range(per_seq):
+            if j % 3 != 1:
+                slot[doc, j] = nxt
+                nxt += 1
+    slot = slot.to(DEV)
+    before = _snapshot(dict(d, slot=slot))
+    ws_bytes = kda.chunk_fwd_workspace_size(T, H, n)
+    o = Guarded(d["q"].shape, d["q"].dtype)
+    fin = Guarded((n, H, Dm, Dm), torch.float32)
+    ck = Guarded((nxt, H, Dm, Dm), torch.float32)
+    ws = Guarded((ws_bytes,), torch.uint8)
+    lib = kda.load()
+    p = kmod._p
+    rc = lib.kda_chunk_fwd_ckpt(p(d["q"]), p(d["k"]), p(d["v"]), p(d["z"]), p(d["A"]), p(d["beta"]),
+                                p(d["cu_seqlens"]), n, T, H, Dm, kmod._dtype_code(d["q"]), float(kmod.G_MIN),
+                                p(d["init_state"]), p(o.t), p(fin.t), interval, p(slot), per_seq, p(ck.t), nxt,
+                                p(ws.t), ws_bytes, 0, kmod._stream(d["q"].device))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert kda.read_device_error(ws.t) == 0
+    assert all(g.intact() for g in (o, fin, ck, ws))
+    _inputs_unchanged(before, dict(d, slot=slot))
+    ck_r = torch.empty_like(ck.t)
+    ck_r.view(torch.uint8).fill_(PATTERN)
+    o_r, f_r = kda.chunk_fwd_ckpt(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], interval, slot, ck_r,
+                                  cu_seqlens=d["cu_seqlens"], init_state=d["init_state"], n_seqs=n)
+    torch.cuda.synchronize()
+    assert torch.equal(o.t, o_r) and torch.equal(fin.t, f_r)
+    assert torch.equal(ck.t.view(torch.uint8), ck_r.view(torch.uint8))
+
+
+def test_chunk_fwd_input_options_writes_only_its_buffers():
+    """The input-option instantiation (L2 norm of q and k, beta's sigmoid, the q
+    scale) on raw inputs, on the fused launch."""
+    lens, H = [1, 63, 65, 200], 3
+    cu = kda_synth.cu_from_lengths(lens)
+    n, T = len(lens), int(cu[-1])
+    inp = kda_synth.prefill_inputs(T, H, "bf16", seed=41, cu_seqlens=cu, init_std=0.05)
+    d = to_dev(inp, DEV)
+    g = torch.Generator(device=DEV).manual_seed(41)
+    d["q"] = (d["q"].float() * (0.5 + torch.rand(T, H, 1, generator=g, device=DEV) * 4)).to(torch.bfloat16)
+    d["k"] = (d["k"].float() * (0.5 + torch.rand(T, H, 1, generator=g, device=DEV) * 4)).to(torch.bfloat16)
+    d["beta"] = torch.randn(T, H, generator=g, device=DEV)  # logits
+    Dm = d["q"].shape[2]
+    flags = kmod.KDA_FLAG_QK_L2NORM | kmod.KDA_FLAG_BETA_SIGMOID | kmod.KDA_FLAG_Q_SCALE
+    before = _snapshot(d)
+    ws_bytes = kda.chunk_fwd_workspace_size(T, H, n)
+    o = Guarded(d["q"].shape, d["q"].dtype)
+    fin = Guarded((n, H, Dm, Dm), torch.float32)
+    ws = Guarded((ws_bytes,), torch.uint8)
+    lib = kda.load()
+    p = kmod._p
+    rc = lib.kda_chunk_fwd(p(d["q"]), p(d["k"]), p(d["v"]), p(d["z"]), p(d["A"]), p(d["beta"]),
+                           p(d["cu_seqlens"]), n, T, H, Dm, kmod._dtype_code(d["q"]), float(kmod.G_MIN),
+                           p(d["init_state"]), p(o.t), p(fin.t), p(ws.t), ws_bytes, flags,
+                           kmod._stream(d["q"].device))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert kda.read_device_error(ws.t) == 0
+    assert o.intact() and fin.intact() and ws.intact()
+    _inputs_unchanged(before, d)
+    o_r, f_r = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["A"], d["beta"], cu_seqlens=d["cu_seqlens"],
+                             init_state=d["init_state"], qk_l2norm=True, beta_sigmoid=True, q_scale=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o.t, o_r) and torch.equal(fin.t, f_r)
